@@ -1,0 +1,163 @@
+"""Python access to the CPU oracle (``gqmm_oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the test suite, ``__graft_entry__.smoke()`` and the benchmark's
+CPU-baseline / reference leg are the only callers.  The product package never imports
+this module.  The oracle follows the pages' statement of the quantized MoE gather matmul;
+the C file's header lists each step and the passage it follows.
+
+Arrays cross the boundary as numpy arrays: bfloat16 tensors as their raw uint16 bit
+patterns, indices as uint32, results as float64.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gqmm_oracle.c")
+_LIB = os.path.join(_HERE, "libgqmm_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# -O2 for speed, but no fast-math and no floating-point contraction, so every operation
+# is the IEEE operation the C source spells out.
+CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (a second of work); returns the library path."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            P = ctypes.c_void_p
+            I64 = ctypes.c_int64
+            I = ctypes.c_int
+            lib.oracle_nthreads_default.restype = I
+            lib.oracle_quantize.argtypes = [P, I64, I64, I, I, P, P, P, I]
+            lib.oracle_quantize.restype = I
+            lib.oracle_dequantize.argtypes = [P, P, P, I64, I64, I, P]
+            lib.oracle_dequantize.restype = I
+            lib.oracle_route_sort.argtypes = [P, I64, I, P, P]
+            lib.oracle_route_sort.restype = I64
+            lib.oracle_gather_qmm.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I, I, P, I]
+            lib.oracle_gather_qmm.restype = I
+            lib.oracle_gather_qmm_rows.argtypes = [P, P, P, P, P, I64, I64, I64, I, I, P, I64, P, I]
+            lib.oracle_gather_qmm_rows.restype = I
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    """Accepts a uint16 numpy array or a bfloat16 torch CPU tensor."""
+    if isinstance(a, np.ndarray):
+        assert a.dtype == np.uint16
+        return np.ascontiguousarray(a)
+    import torch  # only for the dtype view
+
+    assert a.dtype == torch.bfloat16
+    return a.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def nthreads_default() -> int:
+    return int(_load().oracle_nthreads_default())
+
+
+def quantize(w, group_size: int = 64, bits: int = 4, nthreads: int = 0):
+    """w: bf16 [..., H] -> (wq u8 [..., H/2], scales u16 [..., H/gs], biases u16 [..., H/gs])."""
+    w16 = _u16(w)
+    H = w16.shape[-1]
+    lead = w16.shape[:-1]
+    rows = int(np.prod(lead)) if lead else 1
+    if H % group_size or group_size % 2:
+        raise ValueError("H must be a multiple of group_size")
+    wq = np.empty(lead + (H // 2,), np.uint8)
+    sc = np.empty(lead + (H // group_size,), np.uint16)
+    bs = np.empty(lead + (H // group_size,), np.uint16)
+    rc = _load().oracle_quantize(_ptr(w16), rows, H, group_size, bits, _ptr(wq), _ptr(sc), _ptr(bs), nthreads)
+    if rc != 0:
+        raise ValueError("oracle_quantize rejected its arguments")
+    return wq, sc, bs
+
+
+def dequantize(wq: np.ndarray, scales: np.ndarray, biases: np.ndarray, group_size: int = 64) -> np.ndarray:
+    """-> float64 [..., H]."""
+    wq = np.ascontiguousarray(wq, np.uint8)
+    scales = _u16(scales)
+    biases = _u16(biases)
+    H = wq.shape[-1] * 2
+    rows = int(np.prod(wq.shape[:-1])) if wq.ndim > 1 else 1
+    out = np.empty(wq.shape[:-1] + (H,), np.float64)
+    rc = _load().oracle_dequantize(_ptr(wq), _ptr(scales), _ptr(biases), rows, H, group_size, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_dequantize rejected its arguments")
+    return out
+
+
+def route_sort(idx: np.ndarray, E: int):
+    """idx: uint32 [...] -> (perm int32 [n], offsets int32 [E+1], n_bad)."""
+    flat = np.ascontiguousarray(np.asarray(idx, np.uint32).reshape(-1))
+    n = flat.size
+    perm = np.empty(n, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    bad = _load().oracle_route_sort(_ptr(flat), n, E, _ptr(perm), _ptr(offsets))
+    if bad < 0:
+        raise ValueError("oracle_route_sort rejected its arguments")
+    return perm, offsets, int(bad)
+
+
+def gather_qmm(x, wq, scales, biases, idx, E: int, group_size: int = 64, bits: int = 4,
+               nthreads: int = 0, rows=None):
+    """x: bf16 [..., H] (flattened to n rows); wq u8 [E, F, H/2]; scales/biases [E, F, H/gs];
+    idx: uint32 [...] with n entries, or None for the dense case (E == 1).
+    Returns float64 [n, F] (or [len(rows), F] when ``rows`` lists flat rows)."""
+    x16 = _u16(x)
+    H = x16.shape[-1]
+    x16 = x16.reshape(-1, H)
+    n = x16.shape[0]
+    wq = np.ascontiguousarray(wq, np.uint8)
+    scales = _u16(scales)
+    biases = _u16(biases)
+    F = wq.shape[-2]
+    if wq.shape[-1] * 2 != H:
+        raise ValueError("wq last dim must be H/2")
+    idx_p = None
+    if idx is not None:
+        flat = np.ascontiguousarray(np.asarray(idx, np.uint32).reshape(-1))
+        if flat.size != n:
+            raise ValueError("idx must have one entry per row of x")
+        idx_p = _ptr(flat)
+    lib = _load()
+    if rows is None:
+        y = np.empty((n, F), np.float64)
+        used = lib.oracle_gather_qmm(_ptr(x16), _ptr(wq), _ptr(scales), _ptr(biases), idx_p,
+                                     n, H, F, E, group_size, bits, _ptr(y), nthreads)
+    else:
+        r = np.ascontiguousarray(np.asarray(rows, np.int64))
+        y = np.empty((r.size, F), np.float64)
+        used = lib.oracle_gather_qmm_rows(_ptr(x16), _ptr(wq), _ptr(scales), _ptr(biases), idx_p,
+                                          H, F, E, group_size, bits, _ptr(r), r.size, _ptr(y), nthreads)
+    if used < 0:
+        raise ValueError("oracle_gather_qmm rejected its arguments")
+    gather_qmm.last_threads = int(used)
+    return y
+
+
+gather_qmm.last_threads = 0
