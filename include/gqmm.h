@@ -1,0 +1,199 @@
+/*
+ * gqmm.h -- C ABI of libgqmm, the affine-4-bit quantized mixture-of-experts gather matmul
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the one the mlx issue "[CUDA] gather_qmm ~24x slower than equal-FLOPs
+ * quantized_matmul on GB10 (sm_121)" (ml-explore/mlx #4339) benchmarks in its section
+ * "Kernel microbenchmark":
+ *
+ *     wq, sc, bs = mx.quantize(w, group_size=64, bits=4)
+ *     y = mx.gather_qmm(x, wq, sc, bs, rhs_indices=idx, transpose=True,
+ *                       group_size=64, bits=4, mode="affine", sorted_indices=...)
+ *
+ * i.e. for every routed row (t, a):  y[t, a, :] = x[t, a, :] . deq(W[idx[t, a]])^T.
+ *
+ * Conventions shared by every entry point
+ *  - All tensor arguments are DEVICE pointers on the current CUDA device, except where a
+ *    comment says otherwise.  The caller allocates and owns every buffer (outputs and the
+ *    workspace included); the library allocates no device memory, keeps no pointer after
+ *    a call returns, and never synchronizes the stream (gqmm_device_status excepted).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Work is enqueued on it
+ *    asynchronously; results are valid once the stream reaches that point.
+ *  - bfloat16 tensors are passed as void* holding IEEE bfloat16 values.  All tensors are
+ *    dense and row-major (last dimension contiguous).
+ *  - Return value: GQMM_OK (0) or a positive GQMM_ERR_* code from argument validation or
+ *    from the CUDA launch; nothing is enqueued when validation fails.  Conditions only the
+ *    device can see (an expert index >= E, a false `sorted` promise, a wait that timed
+ *    out) set bits in a status word inside the workspace; gqmm_device_status reads them.
+ *  - gqmm_last_error() returns a short human-readable message for the calling thread's
+ *    most recent non-OK return.
+ *
+ * Quantized weight format (the reading this library takes of mx.quantize(..., 64, 4); the
+ * pages name the call but do not print its formula): for each group of 64 consecutive
+ * weights along H,
+ *     scale = bf16((max - min) / 15)  (IEEE float32 division, round to nearest even)
+ *     bias  = min                     (exact)
+ *     q     = clamp(round_half_even((w - bias) / scale), 0, 15)  using the stored scale
+ *             and bias as float32; q = 0 for a constant group (scale 0)
+ *     byte j of a row = q[2j] | (q[2j + 1] << 4)
+ * and deq(q) = scale * q + bias.  Shapes for E experts of F x H weights:
+ *     wq      uint8     [E, F, H/2]
+ *     scales  bfloat16  [E, F, H/64]
+ *     biases  bfloat16  [E, F, H/64]
+ */
+#ifndef GQMM_H
+#define GQMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define GQMM_API __attribute__((visibility("default")))
+#else
+#define GQMM_API
+#endif
+
+typedef struct CUstream_st* gqmm_stream_t; /* identical to cudaStream_t */
+
+/* Synchronous return codes. */
+#define GQMM_OK 0
+#define GQMM_ERR_NULL 1         /* a required pointer is NULL */
+#define GQMM_ERR_SHAPE 2        /* a size is out of range (see each entry point) */
+#define GQMM_ERR_UNSUPPORTED 3  /* group_size != 64, bits != 4, or E above GQMM_MAX_EXPERTS */
+#define GQMM_ERR_ALIGN 4        /* a pointer is not aligned as required */
+#define GQMM_ERR_WORKSPACE 5    /* workspace too small or misaligned */
+#define GQMM_ERR_CUDA 6         /* a CUDA runtime/driver call or a kernel launch failed */
+#define GQMM_ERR_DEVICE 7       /* the current device is not an sm_103 (GB300-class) GPU */
+
+/* Device-side status bits (returned by gqmm_device_status, OR-ed across calls). */
+#define GQMM_STATUS_BAD_INDEX 0x100u  /* some idx value was >= E; those rows of y are zero */
+#define GQMM_STATUS_NOT_SORTED 0x200u /* sorted=1 but idx decreased somewhere: y unspecified */
+#define GQMM_STATUS_TIMEOUT 0x400u    /* a bounded device-side wait gave up: y unspecified */
+
+#define GQMM_MAX_EXPERTS 1024
+
+/*
+ * gqmm_quantize -- affine 4-bit group quantization (mx.quantize(w, group_size=64, bits=4)
+ * in mlx #4339 "Kernel microbenchmark"), format as stated at the top of this header.
+ *
+ *  w       bfloat16 [rows, H] (for E experts of F x H weights, rows = E*F), 16-byte aligned
+ *  rows    >= 0;  H > 0 and H % 64 == 0
+ *  group_size must be 64, bits must be 4
+ *  wq      out: uint8 [rows, H/2], 16-byte aligned
+ *  scales  out: bfloat16 [rows, H/64];  biases  out: bfloat16 [rows, H/64]
+ * Results are bit-identical to the float32 reference formula above (no fast math).
+ * Errors: GQMM_ERR_NULL, GQMM_ERR_SHAPE, GQMM_ERR_UNSUPPORTED, GQMM_ERR_ALIGN, GQMM_ERR_CUDA.
+ */
+GQMM_API int gqmm_quantize(const void* w, int64_t rows, int64_t H, int group_size, int bits, void* wq,
+                  void* scales, void* biases, gqmm_stream_t stream);
+
+/*
+ * gqmm_workspace_size -- bytes of device workspace gqmm_gather_qmm and gqmm_route_sort
+ * need for n = T*A routed rows, F output columns and E experts.  The workspace must be
+ * 256-byte aligned and MUST BE ZERO-FILLED ONCE before its first use (it carries the
+ * device status word, which gqmm_device_status clears after reading); afterwards it can
+ * be reused by any number of calls on the same stream.  Returns 0 for invalid sizes.
+ */
+GQMM_API size_t gqmm_workspace_size(int64_t n, int F, int E);
+
+/*
+ * gqmm_route_sort -- on-device stable counting sort of the routing entries by expert
+ * (mlxcel #629 "perf(cuda/moe): fix MoE prefill collapse", implementation plan item 4b:
+ * token sorting by expert on device so each expert owns one contiguous block).
+ *
+ *  idx      uint32 [n] expert index of each flat row i = t*A + a
+ *  n        number of rows, 0 <= n <= 2^31 - 1;  E in [1, GQMM_MAX_EXPERTS]
+ *  perm     out: int32 [n]; perm[offsets[e] + k] is the k-th smallest row routed to e;
+ *           rows with idx >= E follow all valid rows, in row order
+ *  offsets  out: int32 [E + 1]; offsets[e] = number of valid rows with expert < e,
+ *           offsets[E] = number of valid rows (n when the routing is valid)
+ *  ws       workspace of at least gqmm_workspace_size(n, 1, E) bytes (see above)
+ * Two kernels (tile histograms; scan + stable scatter), no host round trip.  The output
+ * is unique (stable order).
+ * Errors: GQMM_ERR_NULL, GQMM_ERR_SHAPE, GQMM_ERR_UNSUPPORTED, GQMM_ERR_WORKSPACE,
+ * GQMM_ERR_CUDA; idx >= E sets GQMM_STATUS_BAD_INDEX.
+ */
+GQMM_API int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* perm, int32_t* offsets,
+                    void* ws, size_t ws_bytes, gqmm_stream_t stream);
+
+/*
+ * gqmm_gather_qmm -- y[t, a, :] = x[t, a, :] . deq(W[idx[t, a]])^T  (mx.gather_qmm with
+ * transpose=True, mode="affine", mlx #4339 "Kernel microbenchmark"), float32
+ * accumulation, bfloat16 output rounded to nearest even once.
+ *
+ *  x        bfloat16 [T, A, H] (the issue's (T, A, 1, H)), 16-byte aligned
+ *  wq, scales, biases   the quantized weights of E experts, [E, F, ...] as above;
+ *           wq, scales and biases 16-byte aligned
+ *  idx      uint32 [T, A] expert per row, or NULL for the dense quantized matmul
+ *           (mx.quantized_matmul, same issue), which requires E == 1
+ *  T, A     T >= 1, A >= 1, T*A <= 2^31 - 1
+ *  H        > 0, multiple of 64;   F > 0, multiple of 16;   E in [1, GQMM_MAX_EXPERTS]
+ *  group_size 64, bits 4
+ *  sorted   0: idx in any order (the library sorts rows by expert on device);
+ *           1: the caller promises idx is nondecreasing in flat order (the issue's
+ *              sorted_indices=True).  The result is identical either way; a broken
+ *              promise sets GQMM_STATUS_NOT_SORTED.
+ *  y        out: bfloat16 [T, A, F] in (t, a) order, 16-byte aligned
+ *  ws       workspace of at least gqmm_workspace_size(T*A, F, E) bytes (see above)
+ * Rows whose idx is >= E are written as zeros and set GQMM_STATUS_BAD_INDEX.
+ * Errors: GQMM_ERR_NULL, GQMM_ERR_SHAPE, GQMM_ERR_UNSUPPORTED, GQMM_ERR_ALIGN,
+ * GQMM_ERR_WORKSPACE, GQMM_ERR_DEVICE, GQMM_ERR_CUDA.
+ */
+GQMM_API int gqmm_gather_qmm(const void* x, const void* wq, const void* scales, const void* biases,
+                    const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size,
+                    int bits, int sorted, void* y, void* ws, size_t ws_bytes,
+                    gqmm_stream_t stream);
+
+/*
+ * gqmm_gather_qmm_simt -- the same operation computed on CUDA cores, one thread per output
+ * element with float32 accumulation; needs no workspace.  A slow, independent GPU
+ * cross-check of gqmm_gather_qmm's data handling, never used by it.  Same argument rules
+ * (sorted is not needed: each row reads its own index).  Rows with idx >= E are zero.
+ */
+GQMM_API int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* scales, const void* biases,
+                         const uint32_t* idx, int64_t T, int A, int H, int F, int E,
+                         int group_size, int bits, void* y, gqmm_stream_t stream);
+
+/*
+ * gqmm_device_status -- synchronizes `stream`, returns the device status bits
+ * (GQMM_STATUS_*) accumulated in workspace `ws` since the last call, and clears them.
+ * Returns a negative value if the synchronization or the copy fails.
+ */
+GQMM_API int gqmm_device_status(void* ws, gqmm_stream_t stream);
+
+/* Short description of a return code or status bit. Never NULL. */
+GQMM_API const char* gqmm_status_string(int status);
+
+/* Message describing the calling thread's most recent failing call ("" if none). */
+GQMM_API const char* gqmm_last_error(void);
+
+/*
+ * Instrumentation (host side only; nothing here changes what the kernels compute).
+ *  gqmm_launch_count      kernels this library has launched in this process.
+ *  gqmm_kernel_timer      enable (1) / disable (0) CUDA-event timing of the grouped GEMM
+ *                         kernel launched by gqmm_gather_qmm (events on the call's stream;
+ *                         not for use during stream capture).
+ *  gqmm_kernel_timer_read synchronizes the recorded events and returns the number of timed
+ *                         launches and their total duration in milliseconds, then resets.
+ *  gqmm_dispatch_count    how many times each internal variant ran (GQMM_VARIANT_*).
+ */
+GQMM_API int64_t gqmm_launch_count(void);
+GQMM_API void gqmm_kernel_timer(int enable);
+GQMM_API int gqmm_kernel_timer_read(int64_t* launches, double* total_ms);
+
+#define GQMM_VARIANT_ROUTE_UNSORTED 0 /* histogram + scatter route sort */
+#define GQMM_VARIANT_ROUTE_SORTED 1   /* segment boundaries from caller-sorted idx */
+#define GQMM_VARIANT_ROUTE_DENSE 2    /* idx == NULL, E == 1 */
+#define GQMM_VARIANT_GEMM_TC 3        /* tcgen05 grouped GEMM, direct bf16 epilogue */
+#define GQMM_VARIANT_COUNT 8
+GQMM_API int64_t gqmm_dispatch_count(int variant);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GQMM_H */

@@ -1,0 +1,244 @@
+"""Thin Python binding of libgqmm, the GB300 (sm_103a) quantized MoE gather matmul.
+
+Every function here marshals torch tensors into the C ABI declared in include/gqmm.h
+(device pointers, sizes, the current CUDA stream) and raises on a non-zero return code.
+All arithmetic runs in the library's CUDA kernels; there is no fallback of any kind.  The
+shared library is loaded on first use and its absence is an error.
+
+Names follow the C ABI: gqmm_quantize, gqmm_route_sort, gqmm_gather_qmm, ...
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import torch
+
+__all__ = [
+    "GqmmError", "library_path", "load_library", "gqmm_quantize", "gqmm_workspace_size",
+    "new_workspace", "gqmm_route_sort", "gqmm_gather_qmm", "gqmm_gather_qmm_simt",
+    "gqmm_device_status", "gqmm_status_string", "launch_count", "kernel_timer",
+    "kernel_timer_read", "dispatch_count", "STATUS_BAD_INDEX", "STATUS_NOT_SORTED",
+    "STATUS_TIMEOUT", "VARIANTS", "MAX_EXPERTS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libgqmm.so")
+_lock = threading.Lock()
+_lib = None
+
+ERR_NAMES = {0: "OK", 1: "ERR_NULL", 2: "ERR_SHAPE", 3: "ERR_UNSUPPORTED", 4: "ERR_ALIGN",
+             5: "ERR_WORKSPACE", 6: "ERR_CUDA", 7: "ERR_DEVICE"}
+STATUS_BAD_INDEX = 0x100
+STATUS_NOT_SORTED = 0x200
+STATUS_TIMEOUT = 0x400
+MAX_EXPERTS = 1024
+VARIANTS = {"route_unsorted": 0, "route_sorted": 1, "route_dense": 2, "gemm_tc": 3}
+
+
+class GqmmError(RuntimeError):
+    def __init__(self, code: int, where: str, message: str):
+        self.code = code
+        super().__init__(f"{where}: {ERR_NAMES.get(code, code)}: {message}")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load_library():
+    """Loads libgqmm.so (built by quantized_moe_expert_device_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"libgqmm.so is missing ({_LIB_PATH}); build it with "
+                "`python -m quantized_moe_expert_device_gb300.build` (needs nvcc for sm_103a)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+        sig = {
+            "gqmm_quantize": ([P, I64, I64, I, I, P, P, P, P], I),
+            "gqmm_workspace_size": ([I64, I, I], SZ),
+            "gqmm_route_sort": ([P, I64, I, P, P, P, SZ, P], I),
+            "gqmm_gather_qmm": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P, SZ, P], I),
+            "gqmm_gather_qmm_simt": ([P, P, P, P, P, I64, I, I, I, I, I, I, P, P], I),
+            "gqmm_device_status": ([P, P], I),
+            "gqmm_status_string": ([I], ctypes.c_char_p),
+            "gqmm_last_error": ([], ctypes.c_char_p),
+            "gqmm_launch_count": ([], I64),
+            "gqmm_kernel_timer": ([I], None),
+            "gqmm_kernel_timer_read": ([ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)], I),
+            "gqmm_dispatch_count": ([I], I64),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        lib = load_library()
+        raise GqmmError(rc, where, lib.gqmm_last_error().decode())
+
+
+def _stream(stream, device) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must have dtype {dtype} (got {t.dtype})")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def gqmm_quantize(w: torch.Tensor, group_size: int = 64, bits: int = 4, stream=None
+                  ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """w bf16 [..., H] -> (wq uint8 [..., H/2], scales bf16 [..., H/64], biases bf16 [..., H/64])."""
+    _need(w, "w", torch.bfloat16)
+    H = w.shape[-1]
+    lead = tuple(w.shape[:-1])
+    rows = 1
+    for s in lead:
+        rows *= s
+    wq = torch.empty(lead + (H // 2,), dtype=torch.uint8, device=w.device)
+    sc = torch.empty(lead + (max(H // max(group_size, 1), 0),), dtype=torch.bfloat16, device=w.device)
+    bs = torch.empty_like(sc)
+    lib = load_library()
+    _check(lib.gqmm_quantize(_ptr(w), rows, H, group_size, bits, _ptr(wq), _ptr(sc), _ptr(bs),
+                             _stream(stream, w.device)), "gqmm_quantize")
+    return wq, sc, bs
+
+
+def gqmm_workspace_size(n: int, F: int, E: int) -> int:
+    return int(load_library().gqmm_workspace_size(n, F, E))
+
+
+def new_workspace(n: int, F: int, E: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace of the size gqmm_workspace_size asks for."""
+    size = gqmm_workspace_size(n, F, E)
+    if size == 0:
+        raise ValueError(f"no workspace size for n={n}, F={F}, E={E}")
+    return torch.zeros(size, dtype=torch.uint8, device=device)
+
+
+def gqmm_route_sort(idx: torch.Tensor, E: int, ws: Optional[torch.Tensor] = None, stream=None
+                    ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """idx uint32 (or int32 holding the same bits) [...] -> (perm int32 [n], offsets int32 [E+1])."""
+    if idx.dtype not in (torch.int32, getattr(torch, "uint32", torch.int32)):
+        raise TypeError("idx must be int32/uint32")
+    if not idx.is_cuda or not idx.is_contiguous():
+        raise ValueError("idx must be a contiguous CUDA tensor")
+    n = idx.numel()
+    if ws is None:
+        ws = new_workspace(n, 1, E, idx.device)
+    perm = torch.empty(max(n, 1), dtype=torch.int32, device=idx.device)[:n]
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=idx.device)
+    lib = load_library()
+    _check(lib.gqmm_route_sort(_ptr(idx), n, E, _ptr(perm) if n else _ptr(offsets), _ptr(offsets), _ptr(ws),
+                               ws.numel(), _stream(stream, idx.device)), "gqmm_route_sort")
+    return perm, offsets
+
+
+def _gather_shapes(x: torch.Tensor, idx: Optional[torch.Tensor], wq: torch.Tensor):
+    H = x.shape[-1]
+    if idx is None:
+        T, A = x.numel() // H, 1
+    elif idx.dim() >= 2:
+        T, A = idx.shape[0], idx.numel() // idx.shape[0]
+    else:
+        T, A = idx.numel(), 1
+    if T * A * H != x.numel():
+        raise ValueError(f"x has {x.numel()} elements, expected T*A*H = {T}*{A}*{H}")
+    E, F = wq.shape[0], wq.shape[1]
+    return T, A, H, F, E
+
+
+def gqmm_gather_qmm(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
+                    idx: Optional[torch.Tensor], group_size: int = 64, bits: int = 4,
+                    sorted_indices: bool = False, y: Optional[torch.Tensor] = None,
+                    ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y[t, a, :] = x[t, a, :] . deq(W[idx[t, a]])^T.
+
+    x bf16 [T, A, H] (or [T, A, 1, H], or [n, H]); wq uint8 [E, F, H/2]; scales/biases bf16
+    [E, F, H/64]; idx uint32/int32 [T, A] or None (dense, E == 1).  Returns y bf16 with
+    x's leading shape and last dimension F.
+    """
+    _need(x, "x", torch.bfloat16)
+    _need(wq, "wq", torch.uint8)
+    _need(scales, "scales", torch.bfloat16)
+    _need(biases, "biases", torch.bfloat16)
+    if idx is not None and (not idx.is_cuda or not idx.is_contiguous() or idx.element_size() != 4):
+        raise ValueError("idx must be a contiguous 32-bit CUDA tensor")
+    T, A, H, F, E = _gather_shapes(x, idx, wq)
+    if y is None:
+        y = torch.empty(tuple(x.shape[:-1]) + (F,), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(y, "y", torch.bfloat16)
+    if ws is None:
+        ws = new_workspace(T * A, F, E, x.device)
+    lib = load_library()
+    _check(lib.gqmm_gather_qmm(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(idx), T, A, H, F, E,
+                               group_size, bits, 1 if sorted_indices else 0, _ptr(y), _ptr(ws), ws.numel(),
+                               _stream(stream, x.device)), "gqmm_gather_qmm")
+    return y
+
+
+def gqmm_gather_qmm_simt(x, wq, scales, biases, idx, group_size: int = 64, bits: int = 4,
+                         y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """CUDA-core cross-check of gqmm_gather_qmm (same arguments, no workspace)."""
+    _need(x, "x", torch.bfloat16)
+    T, A, H, F, E = _gather_shapes(x, idx, wq)
+    if y is None:
+        y = torch.empty(tuple(x.shape[:-1]) + (F,), dtype=torch.bfloat16, device=x.device)
+    lib = load_library()
+    _check(lib.gqmm_gather_qmm_simt(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(idx), T, A, H, F, E,
+                                    group_size, bits, _ptr(y), _stream(stream, x.device)), "gqmm_gather_qmm_simt")
+    return y
+
+
+def gqmm_device_status(ws: torch.Tensor, stream=None) -> int:
+    """Synchronizes the stream, returns and clears the device status bits in ws."""
+    lib = load_library()
+    rc = lib.gqmm_device_status(_ptr(ws), _stream(stream, ws.device))
+    if rc < 0:
+        _check(-rc, "gqmm_device_status")
+    return rc
+
+
+def gqmm_status_string(code: int) -> str:
+    return load_library().gqmm_status_string(code).decode()
+
+
+def launch_count() -> int:
+    return int(load_library().gqmm_launch_count())
+
+
+def kernel_timer(enable: bool) -> None:
+    load_library().gqmm_kernel_timer(1 if enable else 0)
+
+
+def kernel_timer_read() -> Tuple[int, float]:
+    n = ctypes.c_int64(0)
+    ms = ctypes.c_double(0.0)
+    _check(load_library().gqmm_kernel_timer_read(ctypes.byref(n), ctypes.byref(ms)), "gqmm_kernel_timer_read")
+    return int(n.value), float(ms.value)
+
+
+def dispatch_count(variant: str) -> int:
+    return int(load_library().gqmm_dispatch_count(VARIANTS[variant]))

@@ -1,0 +1,321 @@
+// C ABI of libgqmm (declared in include/gqmm.h): argument validation, workspace layout,
+// kernel launches on the caller's stream, device status, instrumentation.
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "gqmm_internal.cuh"
+
+using namespace gqmm;
+
+namespace {
+
+thread_local std::string t_last_error;
+std::atomic<int64_t> g_launches{0};
+std::atomic<int64_t> g_dispatch[GQMM_VARIANT_COUNT];
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
+int ok() {
+  t_last_error.clear();
+  return GQMM_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+bool log_dispatch() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = std::getenv("GQMM_LOG_DISPATCH");
+    v = (e && e[0] && e[0] != '0') ? 1 : 0;
+  }
+  return v == 1;
+}
+
+void count_variant(int v) {
+  g_dispatch[v].fetch_add(1, std::memory_order_relaxed);
+}
+
+// Device check: the library is built for sm_103a only.
+int check_device(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  static int cached_ok[64] = {0};
+  if (dev >= 0 && dev < 64 && cached_ok[dev] == 1) return GQMM_OK;
+  int major = 0, minor = 0;
+  cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+  cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+  if (!(major == 10 && minor == 3))
+    return fail(GQMM_ERR_DEVICE, "device %d is sm_%d%d; libgqmm is built for sm_103a only", dev, major, minor);
+  if (sms) cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64) cached_ok[dev] = 1;
+  return GQMM_OK;
+}
+
+// ---- GEMM kernel timer -------------------------------------------------------------------
+std::mutex g_timer_mu;
+bool g_timer_on = false;
+std::vector<std::pair<cudaEvent_t, cudaEvent_t>> g_events;
+size_t g_events_used = 0;
+
+bool timer_begin(cudaStream_t s, size_t* slot) {
+  std::lock_guard<std::mutex> lk(g_timer_mu);
+  if (!g_timer_on) return false;
+  if (g_events_used == g_events.size()) {
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess) return false;
+    if (cudaEventCreate(&b) != cudaSuccess) {
+      cudaEventDestroy(a);
+      return false;
+    }
+    g_events.emplace_back(a, b);
+  }
+  *slot = g_events_used++;
+  cudaEventRecord(g_events[*slot].first, s);
+  return true;
+}
+
+void timer_end(cudaStream_t s, size_t slot) {
+  std::lock_guard<std::mutex> lk(g_timer_mu);
+  cudaEventRecord(g_events[slot].second, s);
+}
+
+int validate_gather(const void* x, const void* wq, const void* scales, const void* biases,
+                    const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size,
+                    int bits, const void* y) {
+  if (!x || !wq || !scales || !biases || !y) return fail(GQMM_ERR_NULL, "x, wq, scales, biases and y must be non-NULL");
+  if (group_size != 64 || bits != 4)
+    return fail(GQMM_ERR_UNSUPPORTED, "only group_size=64, bits=4 are supported (got %d, %d)", group_size, bits);
+  if (T < 1 || A < 1 || T * (int64_t)A > 2147483647LL)
+    return fail(GQMM_ERR_SHAPE, "need T >= 1, A >= 1, T*A < 2^31 (got T=%lld A=%d)", (long long)T, A);
+  if (H <= 0 || H % 64) return fail(GQMM_ERR_SHAPE, "H must be a positive multiple of 64 (got %d)", H);
+  if (F <= 0 || F % 16) return fail(GQMM_ERR_SHAPE, "F must be a positive multiple of 16 (got %d)", F);
+  if (E < 1) return fail(GQMM_ERR_SHAPE, "E must be >= 1 (got %d)", E);
+  if (E > GQMM_MAX_EXPERTS) return fail(GQMM_ERR_UNSUPPORTED, "E=%d exceeds %d", E, GQMM_MAX_EXPERTS);
+  if ((int64_t)E * F > 2147483647LL) return fail(GQMM_ERR_SHAPE, "E*F must be < 2^31");
+  if (!idx && E != 1) return fail(GQMM_ERR_NULL, "idx may be NULL only for the dense case E == 1");
+  if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(scales, 16) || !aligned(biases, 16) || !aligned(y, 16))
+    return fail(GQMM_ERR_ALIGN, "x, wq, scales, biases and y must be 16-byte aligned");
+  if (idx && !aligned(idx, 4)) return fail(GQMM_ERR_ALIGN, "idx must be 4-byte aligned");
+  return GQMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gqmm_quantize(const void* w, int64_t rows, int64_t H, int group_size, int bits, void* wq,
+                  void* scales, void* biases, gqmm_stream_t stream) {
+  if (!w || !wq || !scales || !biases) return fail(GQMM_ERR_NULL, "w, wq, scales, biases must be non-NULL");
+  if (group_size != 64 || bits != 4)
+    return fail(GQMM_ERR_UNSUPPORTED, "only group_size=64, bits=4 are supported (got %d, %d)", group_size, bits);
+  if (rows < 0 || H <= 0 || H % 64) return fail(GQMM_ERR_SHAPE, "need rows >= 0 and H a positive multiple of 64");
+  if (!aligned(w, 16) || !aligned(wq, 16)) return fail(GQMM_ERR_ALIGN, "w and wq must be 16-byte aligned");
+  if (!aligned(scales, 2) || !aligned(biases, 2)) return fail(GQMM_ERR_ALIGN, "scales and biases must be 2-byte aligned");
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  cudaError_t e = launch_quantize(static_cast<const __nv_bfloat16*>(w), rows, H, static_cast<uint8_t*>(wq),
+                                  static_cast<__nv_bfloat16*>(scales), static_cast<__nv_bfloat16*>(biases),
+                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(e));
+  if (rows * (H / 64) > 0) g_launches.fetch_add(1);
+  return ok();
+}
+
+size_t gqmm_workspace_size(int64_t n, int F, int E) {
+  if (n < 0 || n > 2147483647LL || F < 0 || E < 1 || E > GQMM_MAX_EXPERTS) return 0;
+  return ws_layout(n, E).total;
+}
+
+int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* perm, int32_t* offsets, void* ws,
+                    size_t ws_bytes, gqmm_stream_t stream) {
+  if (!idx || !perm || !offsets || !ws) return fail(GQMM_ERR_NULL, "idx, perm, offsets and ws must be non-NULL");
+  if (n < 0 || n > 2147483647LL) return fail(GQMM_ERR_SHAPE, "n must be in [0, 2^31)");
+  if (E < 1) return fail(GQMM_ERR_SHAPE, "E must be >= 1");
+  if (E > GQMM_MAX_EXPERTS) return fail(GQMM_ERR_UNSUPPORTED, "E=%d exceeds %d", E, GQMM_MAX_EXPERTS);
+  const WsLayout L = ws_layout(n, E);
+  if (!aligned(ws, 256) || ws_bytes < L.total)
+    return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  RouteArgs a;
+  a.idx = idx;
+  a.n = n;
+  a.E = E;
+  a.sorted = 0;
+  a.perm = perm;
+  a.offsets = offsets;
+  a.tile_hist = reinterpret_cast<uint32_t*>(w + L.tile_hist);
+  a.chunks = nullptr;
+  a.header = reinterpret_cast<WsHeader*>(w);
+  a.y = nullptr;
+  a.F = 0;
+  a.n_tiles = L.n_tiles;
+  int launched = 0;
+  cudaError_t e = launch_route(a, reinterpret_cast<cudaStream_t>(stream), &launched);
+  g_launches.fetch_add(launched);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "route sort launch: %s", cudaGetErrorString(e));
+  count_variant(GQMM_VARIANT_ROUTE_UNSORTED);
+  return ok();
+}
+
+int gqmm_gather_qmm(const void* x, const void* wq, const void* scales, const void* biases, const uint32_t* idx,
+                    int64_t T, int A, int H, int F, int E, int group_size, int bits, int sorted, void* y,
+                    void* ws, size_t ws_bytes, gqmm_stream_t stream) {
+  int rc = validate_gather(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y);
+  if (rc) return rc;
+  if (sorted != 0 && sorted != 1) return fail(GQMM_ERR_SHAPE, "sorted must be 0 or 1");
+  if (!ws) return fail(GQMM_ERR_NULL, "ws must be non-NULL");
+  const int64_t n = T * (int64_t)A;
+  const WsLayout L = ws_layout(n, E);
+  if (!aligned(ws, 256) || ws_bytes < L.total)
+    return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
+  rc = check_device(nullptr);
+  if (rc) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  WsHeader* header = reinterpret_cast<WsHeader*>(w);
+
+  RouteArgs ra;
+  ra.idx = idx;
+  ra.n = n;
+  ra.E = E;
+  ra.sorted = sorted;
+  ra.perm = reinterpret_cast<int32_t*>(w + L.perm);
+  ra.offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+  ra.tile_hist = reinterpret_cast<uint32_t*>(w + L.tile_hist);
+  ra.chunks = reinterpret_cast<Chunk*>(w + L.chunks);
+  ra.header = header;
+  ra.y = static_cast<__nv_bfloat16*>(y);
+  ra.F = F;
+  ra.n_tiles = L.n_tiles;
+  const bool permuted = idx != nullptr && !sorted;
+  int launched = 0;
+  cudaError_t e = launch_route(ra, s, &launched);
+  g_launches.fetch_add(launched);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
+  const int route_variant = idx == nullptr ? GQMM_VARIANT_ROUTE_DENSE
+                                           : (sorted ? GQMM_VARIANT_ROUTE_SORTED : GQMM_VARIANT_ROUTE_UNSORTED);
+  count_variant(route_variant);
+
+  GemmArgs ga;
+  ga.x = static_cast<const __nv_bfloat16*>(x);
+  ga.wq = static_cast<const uint8_t*>(wq);
+  ga.scales = static_cast<const __nv_bfloat16*>(scales);
+  ga.biases = static_cast<const __nv_bfloat16*>(biases);
+  ga.y = static_cast<__nv_bfloat16*>(y);
+  ga.perm = permuted ? ra.perm : nullptr;
+  ga.chunks = ra.chunks;
+  ga.header = header;
+  ga.H = H;
+  ga.F = F;
+  ga.E = E;
+  size_t slot = 0;
+  const bool timed = timer_begin(s, &slot);
+  e = launch_gemm_tc(ga, s);
+  if (timed) timer_end(s, slot);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "grouped GEMM launch: %s", cudaGetErrorString(e));
+  g_launches.fetch_add(1);
+  count_variant(GQMM_VARIANT_GEMM_TC);
+  if (log_dispatch())
+    std::fprintf(stderr, "[gqmm] gather_qmm n=%lld H=%d F=%d E=%d route=%s gemm=tc\n", (long long)n, H, F, E,
+                 route_variant == GQMM_VARIANT_ROUTE_DENSE ? "dense"
+                 : route_variant == GQMM_VARIANT_ROUTE_SORTED ? "sorted" : "unsorted");
+  return ok();
+}
+
+int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* scales, const void* biases,
+                         const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size, int bits,
+                         void* y, gqmm_stream_t stream) {
+  int rc = validate_gather(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y);
+  if (rc) return rc;
+  rc = check_device(nullptr);
+  if (rc) return rc;
+  cudaError_t e = launch_gemm_simt(static_cast<const __nv_bfloat16*>(x), static_cast<const uint8_t*>(wq),
+                                   static_cast<const __nv_bfloat16*>(scales), static_cast<const __nv_bfloat16*>(biases),
+                                   idx, T * (int64_t)A, H, F, E, static_cast<__nv_bfloat16*>(y),
+                                   reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "simt launch: %s", cudaGetErrorString(e));
+  g_launches.fetch_add(1);
+  return ok();
+}
+
+int gqmm_device_status(void* ws, gqmm_stream_t stream) {
+  if (!ws) return -fail(GQMM_ERR_NULL, "ws must be non-NULL");
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return -fail(GQMM_ERR_CUDA, "stream sync: %s", cudaGetErrorString(e));
+  uint32_t st = 0;
+  e = cudaMemcpy(&st, ws, sizeof st, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return -fail(GQMM_ERR_CUDA, "status read: %s", cudaGetErrorString(e));
+  e = cudaMemset(ws, 0, sizeof(uint32_t));
+  if (e != cudaSuccess) return -fail(GQMM_ERR_CUDA, "status clear: %s", cudaGetErrorString(e));
+  ok();
+  return (int)st;
+}
+
+const char* gqmm_status_string(int status) {
+  switch (status) {
+    case GQMM_OK: return "ok";
+    case GQMM_ERR_NULL: return "a required pointer is NULL";
+    case GQMM_ERR_SHAPE: return "a size argument is out of range";
+    case GQMM_ERR_UNSUPPORTED: return "unsupported group_size, bits or expert count";
+    case GQMM_ERR_ALIGN: return "a pointer is not aligned as required";
+    case GQMM_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case GQMM_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case GQMM_ERR_DEVICE: return "current device is not sm_103";
+    case (int)GQMM_STATUS_BAD_INDEX: return "device: an expert index was >= E (rows zeroed)";
+    case (int)GQMM_STATUS_NOT_SORTED: return "device: sorted=1 but the indices decrease";
+    case (int)GQMM_STATUS_TIMEOUT: return "device: a bounded wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* gqmm_last_error(void) { return t_last_error.c_str(); }
+
+int64_t gqmm_launch_count(void) { return g_launches.load(); }
+
+void gqmm_kernel_timer(int enable) {
+  std::lock_guard<std::mutex> lk(g_timer_mu);
+  g_timer_on = enable != 0;
+  g_events_used = 0;
+}
+
+int gqmm_kernel_timer_read(int64_t* launches, double* total_ms) {
+  std::lock_guard<std::mutex> lk(g_timer_mu);
+  double tot = 0.0;
+  for (size_t i = 0; i < g_events_used; ++i) {
+    cudaError_t e = cudaEventSynchronize(g_events[i].second);
+    if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "event sync: %s", cudaGetErrorString(e));
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, g_events[i].first, g_events[i].second);
+    if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "event elapsed: %s", cudaGetErrorString(e));
+    tot += ms;
+  }
+  if (launches) *launches = (int64_t)g_events_used;
+  if (total_ms) *total_ms = tot;
+  g_events_used = 0;
+  return ok();
+}
+
+int64_t gqmm_dispatch_count(int variant) {
+  if (variant < 0 || variant >= GQMM_VARIANT_COUNT) return -1;
+  return g_dispatch[variant].load();
+}
+
+}  // extern "C"

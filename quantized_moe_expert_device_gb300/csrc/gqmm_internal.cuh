@@ -1,0 +1,290 @@
+// Internal declarations shared by the libgqmm translation units (sm_103a only).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "gqmm.h"
+
+namespace gqmm {
+
+// ------------------------------------------------------------------------------------------
+// Workspace layout.  Every section starts on a 256-byte boundary.
+//   [0, 256)        header: status word, counters written by the route/plan kernels
+//   perm            int32 [n]                    sorted position -> flat row
+//   offsets         int32 [E + 1]                expert segment starts
+//   tile_hist       uint32 [(E + 1) * n_tiles]   per-tile key counts, key-major
+//   chunks          Chunk [max_chunks]           work list of (expert, row range)
+// ------------------------------------------------------------------------------------------
+struct WsHeader {
+  uint32_t status;    // GQMM_STATUS_* bits, OR-ed by kernels, cleared by gqmm_device_status
+  int32_t n_chunks;   // number of valid entries in the chunk list (written by the plan step)
+  int32_t pad[62];
+};
+static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
+
+struct Chunk {
+  int32_t expert;  // expert id
+  int32_t start;   // first sorted position of the chunk
+  int32_t rows;    // rows in the chunk, 1..kChunkMaxRows
+  int32_t pad;
+};
+
+constexpr int kRouteThreads = 256;            // threads per route-sort block
+constexpr int kRouteTile = 2048;              // routing entries per route-sort block
+constexpr int kChunkMaxRows = 256;            // tokens per work unit = largest UMMA N
+constexpr int kMaxExperts = GQMM_MAX_EXPERTS;
+
+struct WsLayout {
+  size_t perm, offsets, tile_hist, chunks, total;
+  int64_t n_tiles, max_chunks;
+};
+
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+inline WsLayout ws_layout(int64_t n, int E) {
+  WsLayout L;
+  L.n_tiles = (n + kRouteTile - 1) / kRouteTile;
+  if (L.n_tiles < 1) L.n_tiles = 1;
+  L.max_chunks = E + n / kChunkMaxRows + 1;
+  size_t off = sizeof(WsHeader);
+  L.perm = off;
+  off = align256(off + sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+  L.offsets = off;
+  off = align256(off + sizeof(int32_t) * (size_t)(E + 1));
+  L.tile_hist = off;
+  off = align256(off + sizeof(uint32_t) * (size_t)(E + 1) * (size_t)L.n_tiles);
+  L.chunks = off;
+  off = align256(off + sizeof(Chunk) * (size_t)L.max_chunks);
+  L.total = off;
+  return L;
+}
+
+// ------------------------------------------------------------------------------------------
+// Kernel launchers (defined in the .cu files).  All return cudaError_t of the launch.
+// ------------------------------------------------------------------------------------------
+cudaError_t launch_quantize(const __nv_bfloat16* w, int64_t rows, int64_t H, uint8_t* wq,
+                            __nv_bfloat16* scales, __nv_bfloat16* biases, cudaStream_t s);
+
+struct RouteArgs {
+  const uint32_t* idx;  // NULL: dense (E == 1, every row in expert 0)
+  int64_t n;
+  int E;
+  int sorted;           // 1: caller promises nondecreasing idx
+  int32_t* perm;        // sorted position -> flat row (unused when rows keep their order)
+  int32_t* offsets;     // [E + 1]
+  uint32_t* tile_hist;
+  Chunk* chunks;        // NULL: no work list wanted (standalone route sort)
+  WsHeader* header;
+  __nv_bfloat16* y;     // rows with an invalid index are zero-filled here (may be NULL)
+  int F;
+  int64_t n_tiles;
+};
+// Unsorted: histogram kernel + scan/scatter/plan kernel.  Sorted or dense: one plan kernel.
+cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int* kernels_launched);
+
+struct GemmArgs {
+  const __nv_bfloat16* x;
+  const uint8_t* wq;
+  const __nv_bfloat16* scales;
+  const __nv_bfloat16* biases;
+  __nv_bfloat16* y;
+  const int32_t* perm;  // NULL: sorted position == flat row
+  const Chunk* chunks;
+  WsHeader* header;
+  int H, F, E;
+};
+cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s);
+
+cudaError_t launch_gemm_simt(const __nv_bfloat16* x, const uint8_t* wq,
+                             const __nv_bfloat16* scales, const __nv_bfloat16* biases,
+                             const uint32_t* idx, int64_t n, int H, int F, int E,
+                             __nv_bfloat16* y, cudaStream_t s);
+
+// ------------------------------------------------------------------------------------------
+// Device helpers: PTX wrappers for mbarrier, TMA, cp.async and tcgen05.
+// ------------------------------------------------------------------------------------------
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Upper bound on any single wait inside a kernel.  A correct launch never gets near it;
+// hitting it means a producer is missing, and the kernel then unwinds instead of hanging.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Bounded wait for the phase of parity `parity` of barrier `bar` to complete.  Returns
+// false if the CTA-wide abort flag is raised or the limit passes (which raises the flag and
+// records GQMM_STATUS_TIMEOUT).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          uint32_t* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(status, GQMM_STATUS_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Wait used only while unwinding after an abort: bounded, ignores the abort flag.
+__device__ __forceinline__ bool mbar_wait_unwind(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async proxy
+// (the tensor core reads its operands through the async proxy).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 2-D tiled TMA load global -> shared, completion counted on an mbarrier in bytes.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int32_t c0, int32_t c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---- tcgen05 (5th-generation tensor core, accumulators in tensor memory) ----
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T, bf16 inputs, f32 accumulate.
+__device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on `bar` when every tcgen05 operation this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// Each thread of the warp reads 16 consecutive 32-bit columns of its own TMEM lane.
+__device__ __forceinline__ void tc_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Shared-memory matrix descriptor for a K-major operand in the 128-byte-swizzle canonical
+// layout: rows of 64 bf16 (128 bytes), 8-row groups 1024 bytes apart, 16-byte chunks of
+// row r stored at chunk position (c ^ (r % 8)).  The tile must start 1024-byte aligned.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);       // start address, bits 0-13
+  d |= (uint64_t)(16u >> 4) << 16;                    // leading byte offset (unused here)
+  d |= (uint64_t)(1024u >> 4) << 32;                  // stride byte offset: 8-row group pitch
+  d |= (uint64_t)1 << 46;                             // descriptor version (tcgen05)
+  d |= (uint64_t)2 << 61;                             // layout: 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor for kind::f16 with bf16 A/B, f32 D, both operands K-major.
+__device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N) {
+  uint32_t d = 0;
+  d |= 1u << 4;                          // D format: f32
+  d |= 1u << 7;                          // A format: bf16
+  d |= 1u << 10;                         // B format: bf16
+  d |= (uint32_t)(N >> 3) << 17;         // N / 8
+  d |= (uint32_t)(M >> 4) << 24;         // M / 16
+  return d;
+}
+
+#endif  // __CUDACC__
+
+}  // namespace gqmm

@@ -1,0 +1,92 @@
+"""CPU checks of the C ABI: the library builds, loads, and exports every function that
+include/gqmm.h declares; argument validation rejects bad calls before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "gqmm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w \*]*?\b(gqmm_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_moe_expert_device_gb300 import build
+
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("gqmm_quantize", "gqmm_route_sort", "gqmm_gather_qmm", "gqmm_workspace_size",
+                     "gqmm_device_status", "gqmm_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in gqmm.h but not exported"
+
+
+def test_binding_covers_the_boundary():
+    import quantized_moe_expert_device_gb300 as g
+
+    lib = g.load_library()
+    for name in ("gqmm_quantize", "gqmm_route_sort", "gqmm_gather_qmm", "gqmm_workspace_size",
+                 "gqmm_device_status", "gqmm_gather_qmm_simt"):
+        assert hasattr(g, name)
+        assert getattr(lib, name).argtypes is not None
+
+
+def test_workspace_size_is_positive_and_monotone(lib):
+    import quantized_moe_expert_device_gb300 as g
+
+    a = g.gqmm_workspace_size(32, 128, 8)
+    b = g.gqmm_workspace_size(16384, 768, 64)
+    assert 0 < a < b
+    assert a % 256 == 0 and b % 256 == 0
+    assert g.gqmm_workspace_size(10, 128, 0) == 0
+    assert g.gqmm_workspace_size(10, 128, 4096) == 0
+
+
+def test_validation_rejects_bad_arguments_without_a_gpu(lib):
+    # Validation runs before any CUDA call, so these return codes are exact on any host.
+    P = ctypes.c_void_p
+    f = lib.gqmm_gather_qmm
+    f.argtypes = [P, P, P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_size_t, P]
+    f.restype = ctypes.c_int
+    fake = P(0x10000)  # never dereferenced: every call below fails validation first
+    args = dict(x=fake, wq=fake, sc=fake, bs=fake, idx=fake, T=16, A=2, H=256, F=128, E=8, gs=64, bits=4,
+                sorted=0, y=fake, ws=fake, wsb=1 << 20, s=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return f(a["x"], a["wq"], a["sc"], a["bs"], a["idx"], a["T"], a["A"], a["H"], a["F"], a["E"], a["gs"],
+                 a["bits"], a["sorted"], a["y"], a["ws"], a["wsb"], a["s"])
+
+    assert call(x=None) == 1                  # ERR_NULL
+    assert call(gs=32) == 3                   # ERR_UNSUPPORTED
+    assert call(bits=8) == 3
+    assert call(H=100) == 2                   # ERR_SHAPE
+    assert call(F=120) == 2
+    assert call(T=0) == 2
+    assert call(E=0) == 2
+    assert call(E=4096) == 3
+    assert call(idx=None) == 1                # dense needs E == 1
+    assert call(x=P(0x10008)) == 4            # ERR_ALIGN
+    assert call(sorted=2) == 2
+    assert call(wsb=16) == 5                  # ERR_WORKSPACE
+    lib.gqmm_last_error.restype = ctypes.c_char_p
+    assert b"workspace" in lib.gqmm_last_error()
+    lib.gqmm_status_string.restype = ctypes.c_char_p
+    assert lib.gqmm_status_string(0) == b"ok"

@@ -1,0 +1,172 @@
+"""gqmm_gather_qmm (tcgen05 grouped GEMM) on the GPU vs the CPU oracle.
+
+Inputs: seeded workloads (x, W ~ N(0, 1) bf16, quantized by the oracle; idx per case).
+Criteria: relative Frobenius error <= 5e-3 and every element within 2e-2 * max|y_ref|
+(tests/helpers.py states the derivation)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from helpers import assert_parity, to_dev_idx
+
+pytestmark = pytest.mark.gpu
+
+
+def _weights(E, F, H, seed=wl.SEED_W, std=1.0):
+    w = wl.normal_bf16((E, F, H), seed, std=std, chunk_rows=1)
+    wq, sc, bs = oracle.quantize(w)
+    dev = (torch.from_numpy(wq).cuda(), torch.from_numpy(sc.view(np.int16)).cuda().view(torch.bfloat16),
+           torch.from_numpy(bs.view(np.int16)).cuda().view(torch.bfloat16))
+    return (wq, sc, bs), dev
+
+
+def _run(x_cpu, idx, E, host_w, dev_w, sorted_indices=False, simt=False):
+    import quantized_moe_expert_device_gb300 as g
+
+    x = x_cpu.cuda()
+    d_idx = None if idx is None else to_dev_idx(idx)
+    if simt:
+        y = g.gqmm_gather_qmm_simt(x, *dev_w, d_idx)
+        status = 0
+    else:
+        F = dev_w[0].shape[1]
+        ws = g.new_workspace(x.numel() // x.shape[-1], F, E)
+        y = g.gqmm_gather_qmm(x, *dev_w, d_idx, sorted_indices=sorted_indices, ws=ws)
+        status = g.gqmm_device_status(ws)
+    torch.cuda.synchronize()
+    y_ref = oracle.gather_qmm(x_cpu, *host_w, idx, E)
+    return y, y_ref, status
+
+
+@pytest.mark.parametrize("simt", [False, True])
+@pytest.mark.parametrize("sorted_indices", [False, True])
+def test_tiny_config(sorted_indices, simt):
+    w = wl.workloads()["tiny"]
+    host_w, dev_w = _weights(w.E, w.F, w.H)
+    inp = wl.make_inputs(w)
+    x, idx = inp["x"], inp["idx"]
+    if sorted_indices:
+        x, idx, _ = wl.sorted_by_expert(x, idx)
+    y, y_ref, status = _run(x, idx, w.E, host_w, dev_w, sorted_indices, simt)
+    assert status == 0
+    assert_parity(y.reshape(-1, w.F), y_ref, f"tiny sorted={sorted_indices} simt={simt}")
+
+
+@pytest.mark.parametrize("rows_per_expert", [1, 2, 3, 4, 5, 8, 16, 17, 64, 255, 256, 257, 300, 513])
+def test_rows_per_expert_regimes(rows_per_expert):
+    # The pages' test regimes (mlx PR #4023 coverage discussion: 16 and 64 rows per expert and
+    # a 78-row unaligned batch) plus the small-M decode range and chunk boundaries at 256.
+    E, F, H = 4, 256, 512
+    host_w, dev_w = _weights(E, F, H)
+    n = rows_per_expert * E
+    idx = wl.idx_balanced(rows_per_expert, E, 1).reshape(-1)
+    x = wl.normal_bf16((n, H), wl.SEED_X)
+    y, y_ref, status = _run(x, idx, E, host_w, dev_w)
+    assert status == 0
+    assert_parity(y, y_ref, f"r={rows_per_expert}")
+
+
+def test_unaligned_78_row_batch_sorted_and_unsorted():
+    E, F, H = 4, 128, 1024
+    host_w, dev_w = _weights(E, F, H)
+    idx = np.random.default_rng(78).integers(0, E, size=78, dtype=np.uint32)
+    x = wl.normal_bf16((78, H), wl.SEED_X)
+    y, y_ref, _ = _run(x, idx, E, host_w, dev_w)
+    assert_parity(y, y_ref, "78 unsorted")
+    xs, idx_s, _ = wl.sorted_by_expert(x.reshape(78, 1, H), idx.reshape(78, 1))
+    ys, ys_ref, _ = _run(xs, idx_s, E, host_w, dev_w, sorted_indices=True)
+    assert_parity(ys, ys_ref, "78 sorted")
+
+
+@pytest.mark.parametrize("F", [16, 144, 400])
+def test_f_not_a_multiple_of_the_tile(F):
+    E, H = 3, 256
+    host_w, dev_w = _weights(E, F, H)
+    idx = np.random.default_rng(F).integers(0, E, size=100, dtype=np.uint32)
+    x = wl.normal_bf16((100, H), wl.SEED_X)
+    y, y_ref, _ = _run(x, idx, E, host_w, dev_w)
+    assert_parity(y, y_ref, f"F={F}")
+
+
+@pytest.mark.parametrize("H", [64, 192, 448, 4096])
+def test_h_sizes_scalar_and_vector_scale_paths(H):
+    # H % 512 != 0 takes the per-group scale fetch, H % 512 == 0 the 8-group one
+    E, F = 2, 128
+    host_w, dev_w = _weights(E, F, H)
+    idx = np.random.default_rng(H).integers(0, E, size=40, dtype=np.uint32)
+    x = wl.normal_bf16((40, H), wl.SEED_X)
+    y, y_ref, _ = _run(x, idx, E, host_w, dev_w)
+    assert_parity(y, y_ref, f"H={H}")
+
+
+def test_dense_e1_matches_gather_with_zero_index_bitwise():
+    E, F, H = 1, 256, 1024
+    host_w, dev_w = _weights(E, F, H)
+    x = wl.normal_bf16((300, H), wl.SEED_X)
+    yd, y_ref, _ = _run(x, None, 1, host_w, dev_w)
+    assert_parity(yd, y_ref, "dense")
+    y0, _, _ = _run(x, np.zeros(300, np.uint32), 1, host_w, dev_w)
+    assert torch.equal(yd, y0)
+
+
+def test_sorted_equals_unsorted_bitwise():
+    w = wl.workloads()["tiny"]
+    E, F, H = 16, 256, 512
+    host_w, dev_w = _weights(E, F, H)
+    idx = wl.idx_uniform(200, 4, E)
+    x = wl.normal_bf16((200, 4, H), wl.SEED_X)
+    y, y_ref, _ = _run(x, idx, E, host_w, dev_w)
+    assert_parity(y.reshape(-1, F), y_ref, "unsorted")
+    xs, idx_s, order = wl.sorted_by_expert(x, idx)
+    ys, _, _ = _run(xs, idx_s, E, host_w, dev_w, sorted_indices=True)
+    assert torch.equal(ys.cpu(), y.reshape(-1, F).cpu()[torch.from_numpy(order)])
+    del w
+
+
+def test_invalid_index_rows_are_zero_and_flagged():
+    import quantized_moe_expert_device_gb300 as g
+
+    E, F, H = 4, 128, 256
+    host_w, dev_w = _weights(E, F, H)
+    idx = np.random.default_rng(3).integers(0, E, size=64, dtype=np.uint32)
+    idx[5] = E
+    idx[40] = 2**32 - 1
+    x = wl.normal_bf16((64, H), wl.SEED_X)
+    for sorted_indices in (False, True):
+        xi, ii = x, idx
+        if sorted_indices:
+            xi, ii, _ = wl.sorted_by_expert(x.reshape(64, 1, H), idx.reshape(64, 1))
+        y, y_ref, status = _run(xi, ii, E, host_w, dev_w, sorted_indices)
+        assert status & g.STATUS_BAD_INDEX
+        assert_parity(y.reshape(64, F), y_ref, f"bad index sorted={sorted_indices}")
+        bad_rows = np.nonzero(np.asarray(ii).reshape(-1) >= E)[0]
+        assert (y.reshape(64, F)[torch.from_numpy(bad_rows).cuda()] == 0).all()
+
+
+def test_false_sorted_promise_is_flagged():
+    import quantized_moe_expert_device_gb300 as g
+
+    E, F, H = 4, 128, 256
+    _, dev_w = _weights(E, F, H)
+    idx = to_dev_idx(np.array([3, 2, 1, 0] * 8, np.uint32))
+    x = wl.normal_bf16((32, H), wl.SEED_X).cuda()
+    ws = g.new_workspace(32, F, E)
+    g.gqmm_gather_qmm(x, *dev_w, idx, sorted_indices=True, ws=ws)
+    assert g.gqmm_device_status(ws) & g.STATUS_NOT_SORTED
+    assert g.gqmm_device_status(ws) == 0  # reading clears
+
+
+def test_workspace_reuse_across_shapes_and_calls():
+    import quantized_moe_expert_device_gb300 as g
+
+    E, F, H = 8, 256, 512
+    host_w, dev_w = _weights(E, F, H)
+    ws = g.new_workspace(4096, F, E)
+    for n in (1000, 17, 4096, 256):
+        idx = np.random.default_rng(n).integers(0, E, size=n, dtype=np.uint32)
+        x = wl.normal_bf16((n, H), n)
+        y = g.gqmm_gather_qmm(x.cuda(), *dev_w, to_dev_idx(idx), ws=ws)
+        assert_parity(y, oracle.gather_qmm(x, *host_w, idx, E), f"n={n}")
+    assert g.gqmm_device_status(ws) == 0
