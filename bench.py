@@ -1,0 +1,399 @@
+"""Benchmark of the quantized MoE gather matmul (gqmm_gather_qmm) on GB300.
+
+Default workload: the MoE prefill microbenchmark shape of the mlx issue "[CUDA] gather_qmm
+~24x slower than equal-FLOPs quantized_matmul on GB10" (section "Kernel microbenchmark"):
+T=2048 tokens, A=8 active experts, H=2048, F=768, E=64, affine 4-bit weights with 64-wide
+groups, x ~ N(0, 1) bf16, idx uniform (unsorted).  One step = one gqmm_gather_qmm call
+(on-device route sort + work-list plan + grouped tcgen05 GEMM + scatter epilogue) on inputs
+already resident in HBM.  Metric: effective TFLOP/s = 2*T*A*H*F / step time.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs an independent replica of the
+workload on its own GPU (the op has no cross-GPU exchange); value = total FLOPs of all ranks /
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def algorithmic_bytes(w: wl.Workload, idx: np.ndarray | None) -> int:
+    """Packed codes + scales/biases of the experts actually hit, x, y and idx, each once."""
+    hit = w.E if idx is None else len(np.unique(idx))
+    G = w.H // 64
+    weights = hit * w.F * (w.H // 2 + 4 * G)
+    return int(weights + w.n * w.H * 2 + w.n * w.F * 2 + (0 if idx is None else w.n * 4))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------------------------
+# CPU oracle legs (the only places this script runs the oracle)
+# ----------------------------------------------------------------------------------------------
+
+def oracle_rate(w: wl.Workload, x_cpu, qw, idx, target_s: float, max_rows: int | None = None):
+    """Times the oracle on a bounded sample of rows; returns (TFLOP/s, rows, seconds, threads)."""
+    import oracle
+
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(w.n, size=min(w.n, 32), replace=False))
+    t0 = time.perf_counter()
+    oracle.gather_qmm(x_cpu, *qw, idx, w.E, rows=probe)
+    dt = time.perf_counter() - t0
+    rows = int(max(1, min(w.n, len(probe) * target_s / max(dt, 1e-6))))
+    if max_rows:
+        rows = min(rows, max_rows)
+    sample = np.sort(rng.choice(w.n, size=rows, replace=False))
+    t0 = time.perf_counter()
+    oracle.gather_qmm(x_cpu, *qw, idx, w.E, rows=sample)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows * w.H * w.F
+    return flops / dt / 1e12, rows, dt, oracle.gather_qmm.last_threads
+
+
+def run_reference(args, w: wl.Workload, world: int, rank: int):
+    """The oracle, as it stands, on the host cores: each step computes a bounded sample of rows."""
+    if rank != 0:
+        return
+    import oracle
+
+    inp = wl.make_inputs(w)
+    qw = oracle.quantize(inp["w"])
+    idx = inp["idx"]
+    budget_s = 90.0
+    rng = np.random.default_rng(1)
+    probe = np.sort(rng.choice(w.n, size=min(w.n, 16), replace=False))
+    t0 = time.perf_counter()
+    oracle.gather_qmm(inp["x"], *qw, idx, w.E, rows=probe)
+    per_row = (time.perf_counter() - t0) / len(probe)
+    rows_per_step = int(max(1, min(w.n, budget_s / (args.steps + args.warmup) / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        oracle.gather_qmm(inp["x"], *qw, idx, w.E, rows=rng.choice(w.n, rows_per_step, replace=False))
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.gather_qmm(inp["x"], *qw, idx, w.E, rows=rng.choice(w.n, rows_per_step, replace=False))
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * w.H * w.F * args.steps
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": "gather_qmm TFLOPs (2*T*A*H*F/time)", "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "A": w.A, "H": w.H, "F": w.F, "E": w.E, "group_size": 64,
+                   "bits": 4, "routing": w.routing},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.gather_qmm.last_threads,
+                         "kind": "oracle",
+                         "sample": f"{rows_per_step} random rows of the workload per step (of {w.n})"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------------------------
+
+def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
+    import quantized_moe_expert_device_gb300 as g
+
+    lib = g.load_library()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    inp = wl.make_inputs(w)
+    idx_np = inp["idx"]
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+
+    # Rotate enough distinct copies of every input that the working set exceeds 3x L2.
+    per_copy = algorithmic_bytes(w, idx_np)
+    copies = int(max(2, min(16, np.ceil(3 * l2 / max(per_copy, 1)))))
+    w_dev = inp["w"].to(dev)
+    wq0, sc0, bs0 = g.gqmm_quantize(w_dev)
+    del w_dev
+    x0 = inp["x"].to(dev)
+    idx0 = None if idx_np is None else torch.from_numpy(np.ascontiguousarray(idx_np).view(np.int32)).to(dev)
+    sets = []
+    for c in range(copies):
+        s = dict(x=x0.clone(), wq=wq0.clone(), sc=sc0.clone(), bs=bs0.clone(),
+                 idx=None if idx0 is None else idx0.clone(),
+                 y=torch.empty(w.T, w.A, w.F, dtype=torch.bfloat16, device=dev),
+                 ws=g.new_workspace(w.n, w.F, w.E, dev))
+        sets.append(s)
+    del x0, wq0, sc0, bs0, idx0
+    torch.cuda.synchronize(dev)
+
+    fn = lib.gqmm_gather_qmm
+    sptr = ctypes.c_void_p(stream.cuda_stream)
+
+    def argv(s, sorted_flag=0):
+        P = ctypes.c_void_p
+        return (P(s["x"].data_ptr()), P(s["wq"].data_ptr()), P(s["sc"].data_ptr()), P(s["bs"].data_ptr()),
+                None if s["idx"] is None else P(s["idx"].data_ptr()), w.T, w.A, w.H, w.F, w.E, 64, 4,
+                sorted_flag, P(s["y"].data_ptr()), P(s["ws"].data_ptr()), s["ws"].numel(), sptr)
+
+    calls = [argv(s) for s in sets]
+
+    def step(i):
+        rc = fn(*calls[i % copies])
+        if rc != 0:
+            raise RuntimeError(f"gqmm_gather_qmm failed: {rc} {lib.gqmm_last_error().decode()}")
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    launches0 = g.launch_count()
+    g.kernel_timer(True)
+    t_host0 = time.perf_counter()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    t_host_enqueue = time.perf_counter() - t_host0
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    n_timed, gemm_ms_total = g.kernel_timer_read()
+    g.kernel_timer(False)
+    launches = g.launch_count() - launches0
+    status = 0
+    for s in sets:
+        status |= g.gqmm_device_status(s["ws"])
+    if status:
+        raise RuntimeError(f"device status after timed region: {status:#x}")
+
+    ms_max = max_over_ranks(ms_total, world)
+    ms_per_step = ms_max / args.steps
+    flops = float(w.flops)
+    value = flops * world * args.steps / (ms_max * 1e-3) / 1e12
+
+    peaks, peaks_src = load_peaks()
+    alg_bytes = algorithmic_bytes(w, idx_np)
+    gemm_ms = gemm_ms_total / max(n_timed, 1)
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if flops / alg_bytes >= ridge else "hbm"
+    if bound == "tensor":
+        achieved = flops / (gemm_ms * 1e-3) / 1e12
+        peak = peaks["bf16_tflops"]
+        unit = "TFLOP/s"
+    else:
+        achieved = alg_bytes / (gemm_ms * 1e-3) / 1e9
+        peak = peaks["hbm_gbs"]
+        unit = "GB/s"
+    t_roof_s = max(flops / (peaks["bf16_tflops"] * 1e12), alg_bytes / (peaks["hbm_gbs"] * 1e9))
+
+    # ---- end to end: host-resident inputs, pinned, copied in and out every step ----
+    e2e_steps = max(3, min(args.steps, 200))
+    x_h = inp["x"].pin_memory()
+    idx_h = None if idx_np is None else torch.from_numpy(np.ascontiguousarray(idx_np).view(np.int32)).pin_memory()
+    y_h = torch.empty(w.T, w.A, w.F, dtype=torch.bfloat16).pin_memory()
+    s0 = sets[0]
+    h2d = x_h.numel() * 2 + (0 if idx_h is None else idx_h.numel() * 4)
+    d2h = y_h.numel() * 2
+    for _ in range(2):
+        s0["x"].copy_(x_h, non_blocking=True)
+        if idx_h is not None:
+            s0["idx"].copy_(idx_h, non_blocking=True)
+        step(0)
+        y_h.copy_(s0["y"], non_blocking=True)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        s0["x"].copy_(x_h, non_blocking=True)
+        if idx_h is not None:
+            s0["idx"].copy_(idx_h, non_blocking=True)
+        step(0)
+        y_h.copy_(s0["y"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
+    e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        qw = oracle.quantize(inp["w"])
+        rate, rows, secs, threads = oracle_rate(w, inp["x"], qw, idx_np, target_s=12.0)
+        cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"{rows} random rows of the workload ({rows * 2 * w.H * w.F / 1e9:.2f} GFLOP, {secs:.1f} s)"}
+
+    if rank != 0:
+        return
+    line = {
+        "metric": "gather_qmm TFLOPs (2*T*A*H*F/time)",
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "T": w.T, "A": w.A, "H": w.H, "F": w.F, "E": w.E, "group_size": 64,
+                   "bits": 4, "routing": w.routing, "sorted_indices": False,
+                   "rows_per_expert": w.n / w.E,
+                   "l2": f"inputs rotate over {copies} copies ({copies * per_copy / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+                     "traffic": None, "kernel": "gemm_tc_kernel", "kernel_ms": gemm_ms,
+                     "peak_source": f"{peaks_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"},
+        "op_roofline": {"t_min_us": t_roof_s * 1e6, "frac": t_roof_s / (ms_per_step * 1e-3),
+                        "algorithmic_bytes": alg_bytes, "flops": flops},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_ms, "steps": e2e_steps},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "host_enqueue_ms_per_step": t_host_enqueue / args.steps * 1e3,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="prefill_e64", choices=sorted(wl.workloads()))
+    ap.add_argument("--impl", default="gqmm", choices=["gqmm", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    w = wl.workloads()[args.workload]
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, w, world, rank)
+    else:
+        run_gpu(args, w, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -307,7 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint4 val;
             asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                          : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                         : "r"(epi_addr + (uint32_t)(jj * 64 + q * 16)));
+                         : "r"(epi_addr + (uint32_t)(jj * 64 + q * 16))
+                         : "memory");
             *reinterpret_cast<uint4*>(p.y + (int64_t)row * F + fcol) = val;
           }
         }
@@ -369,8 +370,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint4 nib;
       asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                    : "=r"(nib.x), "=r"(nib.y), "=r"(nib.z), "=r"(nib.w)
-                   : "r"(sbase + OFF_NIB + s * NIB_BYTES + r * 32 + half * 16));
-      mbar_arrive(bar(b_nib_empty(s)));
+                   : "r"(sbase + OFF_NIB + s * NIB_BYTES + r * 32 + half * 16)
+                   : "memory");
+      // The nibble stage is released only after the proxy fence below: the next TMA into
+      // it is an async-proxy write, which is not ordered after these generic-proxy reads
+      // by the mbarrier alone.
       const uint4 o0 = deq8(nib.x, s2, b2);
       const uint4 o1 = deq8(nib.y, s2, b2);
       const uint4 o2 = deq8(nib.z, s2, b2);
@@ -386,8 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    "r"(o2.x), "r"(o2.y), "r"(o2.z), "r"(o2.w) : "memory");
       asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_tile + swz128(r, c0 + 3)),
                    "r"(o3.x), "r"(o3.y), "r"(o3.z), "r"(o3.w) : "memory");
-      fence_proxy_async_smem();
+      fence_proxy_async_smem();  // orders the A writes and the nibble reads before async-proxy use
       mbar_arrive(bar(b_a_full(s)));
+      mbar_arrive(bar(b_nib_empty(s)));
       ++it;
 
       ++kb;

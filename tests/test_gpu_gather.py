@@ -170,3 +170,29 @@ def test_workspace_reuse_across_shapes_and_calls():
         y = g.gqmm_gather_qmm(x.cuda(), *dev_w, to_dev_idx(idx), ws=ws)
         assert_parity(y, oracle.gather_qmm(x, *host_w, idx, E), f"n={n}")
     assert g.gqmm_device_status(ws) == 0
+
+
+def test_repeated_calls_many_units_per_cta_match_oracle_every_time():
+    """Regression test for cross-stage races: with T*A=16384, E=64, F=768 every CTA runs
+    several work units, and each call starts with a cold pipeline.  Every one of 30 calls
+    (with a device synchronization before each) must match the oracle."""
+    import quantized_moe_expert_device_gb300 as g
+
+    w = wl.workloads()["prefill_e64"]
+    host_w, dev_w = _weights(w.E, w.F, w.H)
+    inp = wl.make_inputs(w)
+    x_cpu, idx = inp["x"], inp["idx"]
+    y_ref = oracle.gather_qmm(x_cpu, *host_w, idx, w.E)
+    x = x_cpu.cuda()
+    d_idx = to_dev_idx(idx)
+    ws = g.new_workspace(w.n, w.F, w.E)
+    first = None
+    for rep in range(30):
+        torch.cuda.synchronize()
+        y = g.gqmm_gather_qmm(x, *dev_w, d_idx, ws=ws).reshape(w.n, w.F)
+        assert_parity(y, y_ref, f"rep {rep}")
+        if first is None:
+            first = y.clone()
+        else:
+            assert torch.equal(y, first), f"rep {rep} differs from rep 0"
+    assert g.gqmm_device_status(ws) == 0
