@@ -174,15 +174,16 @@ GQMM_API const char* gqmm_last_error(void);
 /*
  * Instrumentation (host side only; nothing here changes what the kernels compute).
  *  gqmm_launch_count      kernels this library has launched in this process.
- *  gqmm_kernel_timer      enable (1) / disable (0) CUDA-event timing of the grouped GEMM
- *                         kernel launched by gqmm_gather_qmm (events on the call's stream;
- *                         not for use during stream capture).
+ *  gqmm_kernel_timer      capacity > 0: time the next `capacity` grouped-GEMM launches of
+ *                         gqmm_gather_qmm with CUDA events on the call's stream (events are
+ *                         created by this call; not for use during stream capture);
+ *                         capacity 0: stop timing.
  *  gqmm_kernel_timer_read synchronizes the recorded events and returns the number of timed
  *                         launches and their total duration in milliseconds, then resets.
  *  gqmm_dispatch_count    how many times each internal variant ran (GQMM_VARIANT_*).
  */
 GQMM_API int64_t gqmm_launch_count(void);
-GQMM_API void gqmm_kernel_timer(int enable);
+GQMM_API void gqmm_kernel_timer(int capacity);
 GQMM_API int gqmm_kernel_timer_read(int64_t* launches, double* total_ms);
 
 #define GQMM_VARIANT_ROUTE_UNSORTED 0 /* histogram + scatter route sort */

@@ -229,8 +229,9 @@ def launch_count() -> int:
     return int(load_library().gqmm_launch_count())
 
 
-def kernel_timer(enable: bool) -> None:
-    load_library().gqmm_kernel_timer(1 if enable else 0)
+def kernel_timer(capacity: int) -> None:
+    """capacity > 0: time the next `capacity` grouped-GEMM launches; 0: stop."""
+    load_library().gqmm_kernel_timer(int(capacity))
 
 
 def kernel_timer_read() -> Tuple[int, float]:

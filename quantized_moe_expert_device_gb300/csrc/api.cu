@@ -74,16 +74,7 @@ size_t g_events_used = 0;
 
 bool timer_begin(cudaStream_t s, size_t* slot) {
   std::lock_guard<std::mutex> lk(g_timer_mu);
-  if (!g_timer_on) return false;
-  if (g_events_used == g_events.size()) {
-    cudaEvent_t a, b;
-    if (cudaEventCreate(&a) != cudaSuccess) return false;
-    if (cudaEventCreate(&b) != cudaSuccess) {
-      cudaEventDestroy(a);
-      return false;
-    }
-    g_events.emplace_back(a, b);
-  }
+  if (!g_timer_on || g_events_used >= g_events.size()) return false;  // capacity is set up front
   *slot = g_events_used++;
   cudaEventRecord(g_events[*slot].first, s);
   return true;
@@ -215,6 +206,7 @@ int gqmm_gather_qmm(const void* x, const void* wq, const void* scales, const voi
 
   GemmArgs ga;
   ga.x = static_cast<const __nv_bfloat16*>(x);
+  ga.n = n;
   ga.wq = static_cast<const uint8_t*>(wq);
   ga.scales = static_cast<const __nv_bfloat16*>(scales);
   ga.biases = static_cast<const __nv_bfloat16*>(biases);
@@ -290,10 +282,20 @@ const char* gqmm_last_error(void) { return t_last_error.c_str(); }
 
 int64_t gqmm_launch_count(void) { return g_launches.load(); }
 
-void gqmm_kernel_timer(int enable) {
+void gqmm_kernel_timer(int capacity) {
   std::lock_guard<std::mutex> lk(g_timer_mu);
-  g_timer_on = enable != 0;
+  g_timer_on = capacity > 0;
   g_events_used = 0;
+  // Events are created here, outside any timed region.
+  while (g_events.size() < (size_t)(capacity > 0 ? capacity : 0)) {
+    cudaEvent_t a, b;
+    if (cudaEventCreate(&a) != cudaSuccess) break;
+    if (cudaEventCreate(&b) != cudaSuccess) {
+      cudaEventDestroy(a);
+      break;
+    }
+    g_events.emplace_back(a, b);
+  }
 }
 
 int gqmm_kernel_timer_read(int64_t* launches, double* total_ms) {

@@ -1,26 +1,36 @@
 // Persistent grouped GEMM for the quantized MoE gather matmul on tcgen05 tensor cores.
 //
-// Work unit = (chunk of one expert's sorted rows, 128-row tile of the expert's F outputs).
-// The product is computed transposed ("swap A/B"): the UMMA M slot (128) holds weight rows
-// f, the N slot holds the chunk's tokens, so N = round_up(rows, 16) follows the rows per
-// expert.  This is the tensor-core form of the lesson in mlx PR #4023 "Pick BM from rows
-// per expert in gather_qmm_rhs_nax" (useful arithmetic ~ min(1, run / BM)): a 4-row run
-// costs an N=16 MMA instead of most of a 64- or 128-row tile, and each expert's weight
-// tile is read and dequantized once per chunk of up to 256 rows instead of once per row
-// (mlx #4339 comment by manunicholasjacob: one CTA per token-expert pair, 15 of 16 tile
-// rows empty, the 4-bit slab dequantized once per row).
+// Work unit = (chunk of one expert's sorted rows, pair of 128-row tiles of the expert's F
+// outputs).  The product is computed transposed ("swap A/B"): the UMMA M slot (128) holds
+// weight rows f, the N slot holds the chunk's tokens, so N = round_up(rows, 16) follows the
+// rows per expert.  This is the tensor-core form of the lesson in mlx PR #4023 "Pick BM from
+// rows per expert in gather_qmm_rhs_nax" (useful arithmetic ~ min(1, run / BM)): a 4-row run
+// costs an N=16 MMA instead of most of a 64- or 128-row tile, and each expert's weight tile is
+// read and dequantized once per chunk of up to 256 rows instead of once per row (mlx #4339,
+// comment by manunicholasjacob: one CTA per token-expert pair, 15 of 16 tile rows empty, the
+// 4-bit slab dequantized once per row).  The two tiles of a unit share every x tile, which
+// halves the x bytes moved per FLOP compared with one tile per unit.
 //
 // Per CTA (one per SM, persistent, static round-robin over units), warp roles:
-//   warps 0-7   dequant:  read packed nibbles from shared memory, w = scale*q + bias in
-//                         bf16x2, write the bf16 A tile in the 128-byte-swizzle K-major layout
-//   warps 8-11  epilogue: TMEM -> registers -> bf16 -> shared transpose -> 16-byte stores
-//                         to y rows perm[j] (the scatter back to (t, a) order)
-//   warp 12     TMA:      one thread streams 128 x 32-byte nibble tiles (one 64-wide group)
-//   warp 13     MMA:      allocates TMEM (2 x 256 columns), one thread issues
-//                         tcgen05.mma 128xNx16 x4 per stage, commits to mbarriers
-//   warps 14-15 gather:   cp.async 16-byte copies of x rows perm[j] into the swizzled B tile
-// Pipeline depth: 4 stages of (A 16 KB, B 32 KB, nibbles 4 KB).  TMEM accumulators are double
-// buffered so the epilogue of unit i overlaps the mainloop of unit i+1.
+//   warps 0-15  dequant:  two groups of 256 threads take alternate k-blocks; a thread owns one
+//                         of the unit's 256 weight rows: reads its 32 bytes of codes, computes
+//                         w = scale*q + bias in bf16x2 and writes the 64 bf16 in the
+//                         128-byte-swizzle K-major A layout
+//   warps 16-23 epilogue: warp 16+e drains TMEM lanes 32(e%4).. of tile e/4: TMEM -> registers
+//                         -> bf16 -> shared transpose -> 16-byte stores to y rows perm[j]
+//   warp 24     TMA:      one thread streams the unit's 256 x 32-byte nibble tile per k-block
+//   warp 25     MMA:      allocates TMEM (two 256-column fp32 accumulators), one thread issues
+//                         tcgen05.mma 128xNx16, four per tile per k-block, commits to mbarriers
+//   warps 26-31 gather:   warps 26+2s and 27+2s own pipeline stage s: whenever the stage is free
+//                         they copy the chunk's x rows perm[j] (128 bytes each) with 16-byte
+//                         cp.async into the swizzled B tile, wait for their own copies, fence
+//                         them for the tensor core and mark the stage full.  Each lane keeps its
+//                         32 source rows in registers for the whole unit, so a stage's copies
+//                         issue back to back.  (TMA tile::gather4 was measured at ~80 cycles per
+//                         512-byte gather per SM: too slow for 128-byte rows.)
+// Pipeline depth: 3 stages of (A 2 x 16 KB, B 32 KB, nibbles 8 KB).  The accumulators use all
+// 512 TMEM columns, so the MMA of a unit starts once the epilogue has drained the previous one;
+// the producers keep filling stages meanwhile.
 //
 // Every wait is bounded (mbar_wait): on expiry the CTA raises GQMM_STATUS_TIMEOUT, unwinds,
 // waits (bounded) for its own copies and MMAs in flight and frees its TMEM.
@@ -29,31 +39,36 @@
 namespace gqmm {
 namespace {
 
-constexpr int BM = 128;                 // weight rows per tile (UMMA M)
-constexpr int BK = 64;                  // K per stage = one quantization group
-constexpr int NMAX = kChunkMaxRows;     // tokens per unit, UMMA N <= 256
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;    // 16 KB bf16
-constexpr int B_BYTES = NMAX * BK * 2;  // 32 KB bf16
-constexpr int NIB_BYTES = BM * BK / 2;  // 4 KB packed codes
+constexpr int BM = 128;                  // weight rows per tile (UMMA M)
+constexpr int NT = 2;                    // tiles per unit
+constexpr int UM = BM * NT;              // weight rows per unit
+constexpr int BK = 64;                   // K per stage = one quantization group
+constexpr int NMAX = kChunkMaxRows;      // tokens per unit, UMMA N <= 256
+constexpr int STAGES = 3;
+constexpr int A_TILE_BYTES = BM * BK * 2;      // 16 KB bf16
+constexpr int A_BYTES = NT * A_TILE_BYTES;     // 32 KB
+constexpr int B_BYTES = NMAX * BK * 2;         // 32 KB bf16
+constexpr int NIB_BYTES = UM * BK / 2;         // 8 KB packed codes
 constexpr int EPI_WARP_BYTES = 16 * 32 * 2;
 
-constexpr int kThreads = 512;
-constexpr int kDeqThreads = 256;        // warps 0-7
-constexpr int kEpiWarp0 = 8;            // warps 8-11
-constexpr int kTmaWarp = 12;
-constexpr int kMmaWarp = 13;
-constexpr int kGatherWarp0 = 14;        // warps 14-15
-constexpr int kGatherThreads = 64;
-constexpr int kGatherLag = 2;           // cp.async groups kept in flight per gather thread
-constexpr uint32_t kTmemCols = 512;     // two 256-column fp32 accumulators
+constexpr int kThreads = 1024;
+constexpr int kDeqGroup = UM;            // threads per dequant group (one per weight row)
+constexpr int kDeqGroups = 2;            // warps 0-15
+constexpr int kEpiWarp0 = 16;            // warps 16-23
+constexpr int kEpiWarps = 4 * NT;
+constexpr int kTmaWarp = 24;
+constexpr int kMmaWarp = 25;
+constexpr int kGatherWarp0 = 26;         // warps 26 .. 31, a pair per stage
+constexpr uint32_t kTmemCols = 512;      // NT accumulators of NMAX fp32 columns
+static_assert(kGatherWarp0 + 2 * STAGES == kThreads / 32, "warp roles fill the block");
+static_assert(kDeqGroup * kDeqGroups == kEpiWarp0 * 32, "dequant warps");
 
 constexpr int OFF_A = 0;
 constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
 constexpr int OFF_NIB = OFF_B + STAGES * B_BYTES;
 constexpr int OFF_EPI = OFF_NIB + STAGES * NIB_BYTES;
-constexpr int OFF_BAR = OFF_EPI + 4 * EPI_WARP_BYTES;
-constexpr int NUM_BARS = 5 * STAGES + 5;
+constexpr int OFF_BAR = OFF_EPI + kEpiWarps * EPI_WARP_BYTES;
+constexpr int NUM_BARS = 5 * STAGES + 3;
 constexpr int OFF_MISC = OFF_BAR + ((NUM_BARS * 8 + 127) / 128) * 128;
 constexpr int SMEM_USED = OFF_MISC + 16;
 constexpr int SMEM_DYN = SMEM_USED + 1024;  // room to align the base to 1024 bytes
@@ -65,23 +80,23 @@ __device__ __forceinline__ int b_nib_empty(int s) { return STAGES + s; }
 __device__ __forceinline__ int b_a_full(int s) { return 2 * STAGES + s; }
 __device__ __forceinline__ int b_b_full(int s) { return 3 * STAGES + s; }
 __device__ __forceinline__ int b_ab_empty(int s) { return 4 * STAGES + s; }
-__device__ __forceinline__ int b_tmem_full(int b) { return 5 * STAGES + b; }
-__device__ __forceinline__ int b_tmem_empty(int b) { return 5 * STAGES + 2 + b; }
-__device__ __forceinline__ int b_unwind() { return 5 * STAGES + 4; }
+__device__ __forceinline__ int b_tmem_full() { return 5 * STAGES; }
+__device__ __forceinline__ int b_tmem_empty() { return 5 * STAGES + 1; }
+__device__ __forceinline__ int b_unwind() { return 5 * STAGES + 2; }
 
 struct Unit {
   int expert, start, rows, f0;
 };
 
-__device__ __forceinline__ Unit decode_unit(const Chunk* chunks, int u, int n_ftiles) {
-  const int c = u / n_ftiles;
-  const int ft = u - c * n_ftiles;
+__device__ __forceinline__ Unit decode_unit(const Chunk* chunks, int u, int n_fpairs) {
+  const int c = u / n_fpairs;
+  const int fp = u - c * n_fpairs;
   const int4 ch = __ldg(reinterpret_cast<const int4*>(chunks) + c);
   Unit U;
   U.expert = ch.x;
   U.start = ch.y;
   U.rows = ch.z;
-  U.f0 = ft * BM;
+  U.f0 = fp * UM;
   return U;
 }
 
@@ -112,16 +127,6 @@ __device__ __forceinline__ uint4 deq8(uint32_t w, uint32_t s2, uint32_t b2) {
   return o;
 }
 
-// Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled K-major tile.
-__device__ __forceinline__ uint32_t swz128(int r, int c) {
-  return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
-}
-
-__device__ __forceinline__ uint16_t pick16(const uint4& v, int g) {
-  const uint32_t w = (g & 4) ? ((g & 2) ? v.w : v.z) : ((g & 2) ? v.y : v.x);
-  return (uint16_t)((g & 1) ? (w >> 16) : (w & 0xFFFFu));
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_wq, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
@@ -138,15 +143,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(bar(b_nib_full(s)), 1);
-      mbar_init(bar(b_nib_empty(s)), kDeqThreads);
-      mbar_init(bar(b_a_full(s)), kDeqThreads);
-      mbar_init(bar(b_b_full(s)), kGatherThreads);
+      mbar_init(bar(b_nib_empty(s)), kDeqGroup);  // the dequant group that consumed it
+      mbar_init(bar(b_a_full(s)), kDeqGroup);
+      mbar_init(bar(b_b_full(s)), 64);            // every lane of the stage's two gather warps
       mbar_init(bar(b_ab_empty(s)), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(b_tmem_full(b)), 1);
-      mbar_init(bar(b_tmem_empty(b)), 128);
-    }
+    mbar_init(bar(b_tmem_full()), 1);
+    mbar_init(bar(b_tmem_empty()), kEpiWarps * 32);
     mbar_init(bar(b_unwind()), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -164,18 +167,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int H = p.H, F = p.F;
   const int G = H / BK;
   const int num_kb = G;
-  const int n_ftiles = (F + BM - 1) / BM;
-  const int n_units = p.header->n_chunks * n_ftiles;
+  const int n_fpairs = (F + UM - 1) / UM;
+  const int n_units = p.header->n_chunks * n_fpairs;
 
   if (warp == kTmaWarp) {
-    // ---------------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------------- TMA producer (nibbles)
+    // Besides the stage loads, the tile kPrefetchAhead k-blocks ahead (possibly in the next
+    // unit) is prefetched into L2, so stage loads see L2 rather than HBM latency: with only
+    // three stages the loads themselves cannot run far enough ahead.
     if (lane == 0) {
+      constexpr int kPrefetchAhead = 6;
+      auto prefetch = [&](int u, int kb) {
+        while (kb >= num_kb && u < n_units) {
+          kb -= num_kb;
+          u += gridDim.x;
+        }
+        if (u < n_units) {
+          const Unit V = decode_unit(p.chunks, u, n_fpairs);
+          tma_prefetch_l2_2d(&tmap_wq, kb * (BK / 2), V.expert * F + V.f0);
+        }
+      };
+      for (int j = 0; j < kPrefetchAhead; ++j) prefetch(blockIdx.x, j);
       uint32_t it = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const Unit U = decode_unit(p.chunks, u, n_ftiles);
+        const Unit U = decode_unit(p.chunks, u, n_fpairs);
         const int row0 = U.expert * F + U.f0;
         for (int kb = 0; kb < num_kb; ++kb) {
+          prefetch(u, kb + kPrefetchAhead);
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait(bar(b_nib_empty(s)), ph ^ 1u, abort_flag, status)) {
             ok = false;
@@ -198,13 +217,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, lu = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++lu) {
-        const Unit U = decode_unit(p.chunks, u, n_ftiles);
+        const Unit U = decode_unit(p.chunks, u, n_fpairs);
         const int N = (U.rows + 15) & ~15;
         const uint32_t idesc = umma_idesc_bf16(BM, N);
-        const uint32_t ab = lu & 1u, aph = (lu >> 1) & 1u;
-        if (!mbar_wait(bar(b_tmem_empty(ab)), aph ^ 1u, abort_flag, status)) break;
+        if (!mbar_wait(bar(b_tmem_empty()), (lu & 1u) ^ 1u, abort_flag, status)) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + ab * 256u;
         for (int kb = 0; kb < num_kb; ++kb) {
           const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
           if (!mbar_wait(bar(b_a_full(s)), ph, abort_flag, status) ||
@@ -213,16 +230,20 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint64_t adesc = umma_desc_sw128(sbase + OFF_A + s * A_BYTES);
           const uint64_t bdesc = umma_desc_sw128(sbase + OFF_B + s * B_BYTES);
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)  // advance 16 elements = 32 bytes along K
-            tc_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+          for (int t = 0; t < NT; ++t) {
+            const uint64_t adesc = umma_desc_sw128(sbase + OFF_A + s * A_BYTES + t * A_TILE_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)  // advance 16 elements = 32 bytes along K
+              tc_mma_bf16(tmem_base + (uint32_t)(t * NMAX), adesc + 2u * k, bdesc + 2u * k, idesc,
+                          (kb > 0 || k > 0) ? 1u : 0u);
+          }
           tc_commit(bar(b_ab_empty(s)));
           ++it;
         }
         if (!ok) break;
-        tc_commit(bar(b_tmem_full(ab)));
+        tc_commit(bar(b_tmem_full()));
       }
       // every MMA issued above completes before this barrier's phase 0 completes
       tc_commit(bar(b_unwind()));
@@ -234,62 +255,58 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kGatherWarp0) {
     // ---------------------------------------------------------------- x row gather
-    const int g = threadIdx.x - kGatherWarp0 * 32;
-    const int cidx = g & 7;    // 16-byte chunk of the 128-byte row slice
-    const int jrow0 = g >> 3;  // this thread handles rows jrow0 + 8 m
-    uint32_t it = 0, issued = 0;
+    const uint32_t gs = (uint32_t)(warp - kGatherWarp0) >> 1;  // the stage this warp pair fills
+    const int h = (warp - kGatherWarp0) & 1;
+    const int cidx = lane & 7;                 // 16-byte chunk of a 128-byte row slice
+    const int rlow = 4 * h + (lane >> 3);      // rows 8 q + rlow, q = 0..31
+    const uint32_t dst_lane = (uint32_t)(rlow * 128 + ((cidx ^ rlow) << 4));
+    uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-      const Unit U = decode_unit(p.chunks, u, n_ftiles);
-      int src_row[NMAX / 8];
+      const Unit U = decode_unit(p.chunks, u, n_fpairs);
+      int src[NMAX / 8];
 #pragma unroll
-      for (int m = 0; m < NMAX / 8; ++m) {
-        const int j = jrow0 + 8 * m;
-        src_row[m] = j < U.rows ? (p.perm ? __ldg(p.perm + U.start + j) : U.start + j) : -1;
+      for (int q = 0; q < NMAX / 8; ++q) {
+        const int row = 8 * q + rlow;
+        src[q] = row < U.rows ? (p.perm ? __ldg(p.perm + U.start + row) : U.start + row) : -1;
       }
-      for (int kb = 0; kb < num_kb; ++kb) {
-        const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-        if (!mbar_wait(bar(b_ab_empty(s)), ph ^ 1u, abort_flag, status)) {
+      for (int kb = 0; kb < num_kb; ++kb, ++it) {
+        if (it % STAGES != gs) continue;
+        const uint32_t ph = (it / STAGES) & 1u;
+        const bool okl = mbar_wait(bar(b_ab_empty(gs)), ph ^ 1u, abort_flag, status);
+        if (!__all_sync(0xffffffffu, okl)) {
           ok = false;
           break;
         }
-        const uint32_t bs = sbase + OFF_B + s * B_BYTES + jrow0 * 128 + ((cidx ^ jrow0) << 4);
+        const uint32_t b_lane = sbase + OFF_B + gs * B_BYTES + dst_lane;
         const __nv_bfloat16* xk = p.x + kb * BK + cidx * 8;
 #pragma unroll
-        for (int m = 0; m < NMAX / 8; ++m)
-          if (src_row[m] >= 0) cp_async_16(bs + m * 1024, xk + (int64_t)src_row[m] * H);
+        for (int q = 0; q < NMAX / 8; ++q)
+          if (src[q] >= 0) cp_async_16(b_lane + q * 1024, xk + (int64_t)src[q] * H);
         cp_async_commit();
-        ++it;
-        ++issued;
-        if (issued > kGatherLag) {
-          cp_async_wait<kGatherLag>();
-          fence_proxy_async_smem();
-          mbar_arrive(bar(b_b_full((it - 1 - kGatherLag) % STAGES)));
-        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();  // this lane's copies, made visible to the tensor core
+        mbar_arrive(bar(b_b_full(gs)));
       }
     }
     cp_async_wait<0>();
-    fence_proxy_async_smem();
-    if (ok) {
-      const uint32_t first = it > (uint32_t)kGatherLag ? it - kGatherLag : 0;
-      for (uint32_t j = first; j < it; ++j) mbar_arrive(bar(b_b_full(j % STAGES)));
-    }
   } else if (warp >= kEpiWarp0) {
     // ---------------------------------------------------------------- epilogue
-    const int ew = warp - kEpiWarp0;  // TMEM lanes 32 ew .. 32 ew + 31
+    const int ew = warp - kEpiWarp0;
+    const int tile = ew >> 2;          // accumulator (weight-row tile) this warp drains
+    const int quarter = ew & 3;        // TMEM lanes 32 quarter .. 32 quarter + 31 (= warp % 4)
     uint16_t* epi = reinterpret_cast<uint16_t*>(smem + OFF_EPI + ew * EPI_WARP_BYTES);
     const uint32_t epi_addr = sbase + OFF_EPI + ew * EPI_WARP_BYTES;
     uint32_t lu = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++lu) {
-      const Unit U = decode_unit(p.chunks, u, n_ftiles);
+      const Unit U = decode_unit(p.chunks, u, n_fpairs);
       const int N = (U.rows + 15) & ~15;
-      const uint32_t ab = lu & 1u, aph = (lu >> 1) & 1u;
-      const bool okl = mbar_wait(bar(b_tmem_full(ab)), aph, abort_flag, status);
+      const bool okl = mbar_wait(bar(b_tmem_full()), lu & 1u, abort_flag, status);
       if (!__all_sync(0xffffffffu, okl)) break;
       tc_fence_after();
-      const uint32_t trow = tmem_base + ((uint32_t)(ew * 32) << 16) + ab * 256u;
+      const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(tile * NMAX);
       const int q = lane & 3;
-      const int fcol = U.f0 + ew * 32 + q * 8;
+      const int fcol = U.f0 + tile * BM + quarter * 32 + q * 8;
       for (int c0 = 0; c0 < N; c0 += 16) {
         uint32_t v[16];
         tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
@@ -299,8 +316,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           epi[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
         __syncwarp();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int jj = (lane >> 2) + 8 * h;
+        for (int hh = 0; hh < 2; ++hh) {
+          const int jj = (lane >> 2) + 8 * hh;
           const int tok = c0 + jj;
           if (tok < U.rows && fcol < F) {
             const int row = p.perm ? __ldg(p.perm + U.start + tok) : U.start + tok;
@@ -315,96 +332,96 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
       }
       tc_fence_before();
-      mbar_arrive(bar(b_tmem_empty(ab)));
+      mbar_arrive(bar(b_tmem_empty()));
     }
   } else {
     // ---------------------------------------------------------------- dequant
-    const int t = threadIdx.x;  // 0..255
-    const int r = t & (BM - 1);  // weight row within the tile
-    const int half = t >> 7;     // which 32 of the 64 codes of the group
-    const bool vec8 = (G & 7) == 0;  // scales/biases fetched 8 groups (16 bytes) at a time
-    const int blk = vec8 ? 8 : 1;
-    uint32_t it = 0;
-
-    auto load_sb = [&](const Unit& U, int kb, uint4& s_out, uint4& b_out) {
-      s_out = make_uint4(0, 0, 0, 0);
-      b_out = make_uint4(0, 0, 0, 0);
-      if (U.f0 + r < F) {
-        const int64_t off = ((int64_t)U.expert * F + U.f0 + r) * G + kb;
-        if (vec8) {
-          s_out = __ldg(reinterpret_cast<const uint4*>(p.scales + off));
-          b_out = __ldg(reinterpret_cast<const uint4*>(p.biases + off));
-        } else {
-          s_out.x = __ldg(reinterpret_cast<const uint16_t*>(p.scales) + off);
-          b_out.x = __ldg(reinterpret_cast<const uint16_t*>(p.biases) + off);
-        }
+    const int t = threadIdx.x;                   // 0 .. 2 * UM - 1
+    const int r = t % UM;                        // weight row within the unit
+    const uint32_t grp = (uint32_t)(t / UM);     // handles the steps with it % 2 == grp
+    const int tile = r >> 7, rr = r & (BM - 1);
+    // nibble tile rows are 32 bytes, TMA-swizzled in 32-byte mode: 16-byte chunk c of row r
+    // sits at chunk position c ^ ((r >> 2) & 1)
+    const uint32_t nib_row = (uint32_t)(r * 32);
+    const uint32_t nib_c0 = (uint32_t)(((r >> 2) & 1) << 4), nib_c1 = nib_c0 ^ 16u;
+    const uint32_t a_off = (uint32_t)(tile * A_TILE_BYTES + (rr >> 3) * 1024 + (rr & 7) * 128);
+    const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(p.scales);
+    const uint16_t* bs16 = reinterpret_cast<const uint16_t*>(p.biases);
+    // Flat walk over (unit, k-block); this group processes every second step.  The scale and
+    // bias of the next step it processes are loaded one processed step ahead.
+    struct Step {
+      int u, kb;
+      Unit U;
+    };
+    auto advance = [&](Step& st, int by) {
+      st.kb += by;
+      while (st.kb >= num_kb && st.u < n_units) {
+        st.kb -= num_kb;
+        st.u += gridDim.x;
+        if (st.u < n_units) st.U = decode_unit(p.chunks, st.u, n_fpairs);
       }
     };
-
-    int u = blockIdx.x;
-    Unit U;
-    uint4 s_cur, b_cur, s_nxt = make_uint4(0, 0, 0, 0), b_nxt = make_uint4(0, 0, 0, 0);
-    if (u < n_units) {
-      U = decode_unit(p.chunks, u, n_ftiles);
-      load_sb(U, 0, s_cur, b_cur);
-    }
-    int kb = 0;
-    while (u < n_units) {
-      if (kb % blk == 0) {  // prefetch the next block of scales/biases
-        int nkb = kb + blk, nu = u;
-        if (nkb >= num_kb) {
-          nkb = 0;
-          nu = u + gridDim.x;
-        }
-        if (nu < n_units) {
-          const Unit NU = (nu == u) ? U : decode_unit(p.chunks, nu, n_ftiles);
-          load_sb(NU, nkb, s_nxt, b_nxt);
-        }
+    auto load_sb = [&](const Step& st, uint32_t& sv, uint32_t& bv) {
+      sv = 0;
+      bv = 0;
+      if (st.u < n_units && st.U.f0 + r < F) {
+        const int64_t off = ((int64_t)st.U.expert * F + st.U.f0 + r) * G + st.kb;
+        sv = __ldg(sc16 + off);
+        bv = __ldg(bs16 + off);
       }
-      const int gsel = vec8 ? (kb & 7) : 0;
-      const uint32_t s2 = splat16(pick16(s_cur, gsel));
-      const uint32_t b2 = splat16(pick16(b_cur, gsel));
-
+    };
+    Step cur;
+    cur.u = blockIdx.x;
+    cur.kb = 0;
+    if (cur.u < n_units) cur.U = decode_unit(p.chunks, cur.u, n_fpairs);
+    advance(cur, (int)grp);
+    uint32_t it = grp;  // global step index of cur
+    uint32_t s_cur, b_cur;
+    load_sb(cur, s_cur, b_cur);
+    while (cur.u < n_units) {
+      Step nxt = cur;
+      advance(nxt, kDeqGroups);
+      uint32_t s_nxt, b_nxt;
+      load_sb(nxt, s_nxt, b_nxt);
+      const uint32_t s2 = splat16(s_cur), b2 = splat16(b_cur);
       const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
       if (!mbar_wait(bar(b_nib_full(s)), ph, abort_flag, status)) break;
-      uint4 nib;
+      const uint32_t nib_tile = sbase + OFF_NIB + s * NIB_BYTES + nib_row;
+      uint4 n0, n1;
       asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(nib.x), "=r"(nib.y), "=r"(nib.z), "=r"(nib.w)
-                   : "r"(sbase + OFF_NIB + s * NIB_BYTES + r * 32 + half * 16)
+                   : "=r"(n0.x), "=r"(n0.y), "=r"(n0.z), "=r"(n0.w)
+                   : "r"(nib_tile + nib_c0)
+                   : "memory");
+      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                   : "=r"(n1.x), "=r"(n1.y), "=r"(n1.z), "=r"(n1.w)
+                   : "r"(nib_tile + nib_c1)
                    : "memory");
       // The nibble stage is released only after the proxy fence below: the next TMA into
       // it is an async-proxy write, which is not ordered after these generic-proxy reads
       // by the mbarrier alone.
-      const uint4 o0 = deq8(nib.x, s2, b2);
-      const uint4 o1 = deq8(nib.y, s2, b2);
-      const uint4 o2 = deq8(nib.z, s2, b2);
-      const uint4 o3 = deq8(nib.w, s2, b2);
+      uint4 o[8];
+      o[0] = deq8(n0.x, s2, b2);
+      o[1] = deq8(n0.y, s2, b2);
+      o[2] = deq8(n0.z, s2, b2);
+      o[3] = deq8(n0.w, s2, b2);
+      o[4] = deq8(n1.x, s2, b2);
+      o[5] = deq8(n1.y, s2, b2);
+      o[6] = deq8(n1.z, s2, b2);
+      o[7] = deq8(n1.w, s2, b2);
       if (!mbar_wait(bar(b_ab_empty(s)), ph ^ 1u, abort_flag, status)) break;
-      const uint32_t a_tile = sbase + OFF_A + s * A_BYTES;
-      const int c0 = half * 4;
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_tile + swz128(r, c0 + 0)),
-                   "r"(o0.x), "r"(o0.y), "r"(o0.z), "r"(o0.w) : "memory");
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_tile + swz128(r, c0 + 1)),
-                   "r"(o1.x), "r"(o1.y), "r"(o1.z), "r"(o1.w) : "memory");
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_tile + swz128(r, c0 + 2)),
-                   "r"(o2.x), "r"(o2.y), "r"(o2.z), "r"(o2.w) : "memory");
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_tile + swz128(r, c0 + 3)),
-                   "r"(o3.x), "r"(o3.y), "r"(o3.z), "r"(o3.w) : "memory");
+      const uint32_t a_row = sbase + OFF_A + s * A_BYTES + a_off;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row + (uint32_t)((c ^ (rr & 7)) << 4)),
+                     "r"(o[c].x), "r"(o[c].y), "r"(o[c].z), "r"(o[c].w)
+                     : "memory");
       fence_proxy_async_smem();  // orders the A writes and the nibble reads before async-proxy use
       mbar_arrive(bar(b_a_full(s)));
       mbar_arrive(bar(b_nib_empty(s)));
-      ++it;
-
-      ++kb;
-      if (kb % blk == 0) {
-        s_cur = s_nxt;
-        b_cur = b_nxt;
-      }
-      if (kb == num_kb) {
-        kb = 0;
-        u += gridDim.x;
-        if (u < n_units) U = decode_unit(p.chunks, u, n_ftiles);
-      }
+      cur = nxt;
+      s_cur = s_nxt;
+      b_cur = b_nxt;
+      it += kDeqGroups;
     }
   }
 
@@ -447,17 +464,18 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
     if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
     encode = reinterpret_cast<decltype(&cuTensorMapEncodeTiled)>(fn);
   }
-  CUtensorMap map;
+  // Packed codes as a [E*F, H/2] byte matrix; one box = the unit's 256 rows x 32 bytes (one
+  // 64-wide group), 32-byte swizzled so the dequant threads read it without bank conflicts.
+  CUtensorMap map_wq;
   const cuuint64_t dims[2] = {(cuuint64_t)(a.H / 2), (cuuint64_t)a.E * (cuuint64_t)a.F};
   const cuuint64_t strides[1] = {(cuuint64_t)(a.H / 2)};
-  const cuuint32_t box[2] = {BK / 2, BM};
+  const cuuint32_t box[2] = {BK / 2, UM};
   const cuuint32_t estr[2] = {1, 1};
-  CUresult cr = encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.wq),
-                                       dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                       CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult cr = encode(&map_wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.wq), dims, strides, box,
+                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  gemm_tc_kernel<<<di.sms, kThreads, SMEM_DYN, s>>>(map, a);
+  gemm_tc_kernel<<<di.sms, kThreads, SMEM_DYN, s>>>(map_wq, a);
   return cudaGetLastError();
 }
 

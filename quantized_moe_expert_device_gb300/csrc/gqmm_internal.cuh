@@ -87,6 +87,7 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int* kernels_launch
 
 struct GemmArgs {
   const __nv_bfloat16* x;
+  int64_t n;            // rows of x
   const uint8_t* wq;
   const __nv_bfloat16* scales;
   const __nv_bfloat16* biases;
@@ -194,6 +195,14 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
+}
+
+// Prefetch a 2-D TMA box into L2 (no shared-memory destination, no completion signal).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
