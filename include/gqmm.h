@@ -159,6 +159,32 @@ GQMM_API int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* sca
                          int group_size, int bits, void* y, gqmm_stream_t stream);
 
 /*
+ * gqmm_gather_qmm_noalloc -- the pages have no counterpart to this entry point; it is a
+ * convenience of this library.  Same operation, arguments and results as gqmm_gather_qmm,
+ * but without a workspace argument: the scratch it needs is a fixed array of
+ * GQMM_NOALLOC_SCRATCH_BYTES inside the library's device code, and the call allocates
+ * nothing (no cudaMalloc, no cudaFree, no allocating library routine).  It is meant for
+ * callers that cannot allocate device memory or keep a workspace: a plugin whose host
+ * framework owns all device memory, or a latency-critical path that must not call
+ * cudaMalloc (which can synchronize the device).
+ *  - The scratch covers any call with T*A <= 131072 rows (and E <= GQMM_MAX_EXPERTS); larger
+ *    calls return GQMM_ERR_WORKSPACE with a message and enqueue nothing.
+ *  - The array occupies device memory on every GPU that loads the library, until exit.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress); make that first call before any stream capture.
+ *  - Every call on a device shares the one array: calls whose GPU work overlaps (different
+ *    streams, no ordering between them) race and give undefined results.  Calls on one
+ *    stream are ordered and safe.
+ *  - Each call clears the scratch's status word; device-detected conditions are not
+ *    reported (rows with an index >= E are still zeroed).  Use gqmm_gather_qmm with
+ *    gqmm_device_status when the status is needed.
+ */
+#define GQMM_NOALLOC_SCRATCH_BYTES (1u << 20)
+GQMM_API int gqmm_gather_qmm_noalloc(const void* x, const void* wq, const void* scales, const void* biases,
+                                     const uint32_t* idx, int64_t T, int A, int H, int F, int E,
+                                     int group_size, int bits, int sorted, void* y, gqmm_stream_t stream);
+
+/*
  * gqmm_device_status -- synchronizes `stream`, returns the device status bits
  * (GQMM_STATUS_*) accumulated in workspace `ws` since the last call, and clears them.
  * Returns a negative value if the synchronization or the copy fails.

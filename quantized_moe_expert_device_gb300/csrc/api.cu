@@ -107,6 +107,16 @@ int validate_gather(const void* x, const void* wq, const void* scales, const voi
 
 }  // namespace
 
+int gqmm::report_error(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_last_error = buf;
+  return code;
+}
+
 extern "C" {
 
 int gqmm_quantize(const void* w, int64_t rows, int64_t H, int group_size, int bits, void* wq,

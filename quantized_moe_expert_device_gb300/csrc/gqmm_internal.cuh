@@ -62,6 +62,9 @@ inline WsLayout ws_layout(int64_t n, int E) {
   return L;
 }
 
+// Records a printf-style message as the calling thread's gqmm_last_error() and returns code.
+int report_error(int code, const char* fmt, ...);
+
 // ------------------------------------------------------------------------------------------
 // Kernel launchers (defined in the .cu files).  All return cudaError_t of the launch.
 // ------------------------------------------------------------------------------------------
