@@ -95,8 +95,12 @@ GQMM_API int gqmm_quantize(const void* w, int64_t rows, int64_t H, int group_siz
  * gqmm_workspace_size -- bytes of device workspace gqmm_gather_qmm and gqmm_route_sort
  * need for n = T*A routed rows, F output columns and E experts.  The workspace must be
  * 256-byte aligned and MUST BE ZERO-FILLED ONCE before its first use (it carries the
- * device status word, which gqmm_device_status clears after reading); afterwards it can
- * be reused by any number of calls on the same stream.  Returns 0 for invalid sizes.
+ * device status word, which gqmm_device_status clears after reading); afterwards it can be
+ * reused by any number of calls on the same stream whose own gqmm_workspace_size is at
+ * most its size.  For decode-sized calls with few work units the size includes float32
+ * planes for split-K partial sums (ksplit x n x F, ksplit <= 16), so it is not monotone
+ * in n: a workspace shared by several shapes takes the maximum over them.
+ * Returns 0 for invalid sizes.
  */
 GQMM_API size_t gqmm_workspace_size(int64_t n, int F, int E);
 
@@ -168,7 +172,10 @@ GQMM_API int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* sca
  * framework owns all device memory, or a latency-critical path that must not call
  * cudaMalloc (which can synchronize the device).
  *  - The scratch covers any call with T*A <= 131072 rows (and E <= GQMM_MAX_EXPERTS); larger
- *    calls return GQMM_ERR_WORKSPACE with a message and enqueue nothing.
+ *    calls return GQMM_ERR_WORKSPACE with a message and enqueue nothing.  Calls with few
+ *    work units, which gqmm_gather_qmm runs with K split into slices, are split here only
+ *    when the float32 partial-sum planes also fit; otherwise they run unsplit (equal
+ *    within rounding, less parallelism).
  *  - The array occupies device memory on every GPU that loads the library, until exit.
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress); make that first call before any stream capture.
@@ -215,7 +222,9 @@ GQMM_API int gqmm_kernel_timer_read(int64_t* launches, double* total_ms);
 #define GQMM_VARIANT_ROUTE_UNSORTED 0 /* histogram + scatter route sort */
 #define GQMM_VARIANT_ROUTE_SORTED 1   /* segment boundaries from caller-sorted idx */
 #define GQMM_VARIANT_ROUTE_DENSE 2    /* idx == NULL, E == 1 */
-#define GQMM_VARIANT_GEMM_TC 3        /* tcgen05 grouped GEMM, direct bf16 epilogue */
+#define GQMM_VARIANT_GEMM_TC 3        /* tcgen05 grouped GEMM, chunks of up to 256 rows */
+#define GQMM_VARIANT_GEMM_NARROW 4    /* tcgen05 grouped GEMM, chunks of up to 32 rows */
+#define GQMM_VARIANT_SPLIT_K 5        /* K split into slices, fp32 partial sums + finalize */
 #define GQMM_VARIANT_COUNT 8
 GQMM_API int64_t gqmm_dispatch_count(int variant);
 

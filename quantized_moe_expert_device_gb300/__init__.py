@@ -35,7 +35,8 @@ STATUS_BAD_INDEX = 0x100
 STATUS_NOT_SORTED = 0x200
 STATUS_TIMEOUT = 0x400
 MAX_EXPERTS = 1024
-VARIANTS = {"route_unsorted": 0, "route_sorted": 1, "route_dense": 2, "gemm_tc": 3}
+VARIANTS = {"route_unsorted": 0, "route_sorted": 1, "route_dense": 2, "gemm_tc": 3, "gemm_narrow": 4,
+            "split_k": 5}
 
 
 class GqmmError(RuntimeError):
@@ -129,10 +130,14 @@ def gqmm_workspace_size(n: int, F: int, E: int) -> int:
     return int(load_library().gqmm_workspace_size(n, F, E))
 
 
-def new_workspace(n: int, F: int, E: int, device="cuda") -> torch.Tensor:
-    """A zero-filled workspace of the size gqmm_workspace_size asks for."""
-    size = gqmm_workspace_size(n, F, E)
-    if size == 0:
+def new_workspace(n, F: int, E: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace of the size gqmm_workspace_size asks for.  n may be a list of
+    row counts the workspace will serve; it is then sized for the largest need among them
+    (the size is not monotone in n: decode-sized calls add split-K partial-sum planes)."""
+    ns = list(n) if isinstance(n, (list, tuple)) else [n]
+    sizes = [gqmm_workspace_size(int(k), F, E) for k in ns]
+    size = max(sizes) if sizes else 0
+    if not sizes or min(sizes) == 0:
         raise ValueError(f"no workspace size for n={n}, F={F}, E={E}")
     return torch.zeros(size, dtype=torch.uint8, device=device)
 

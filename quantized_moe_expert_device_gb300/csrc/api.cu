@@ -117,6 +117,84 @@ int gqmm::report_error(int code, const char* fmt, ...) {
   return code;
 }
 
+int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, const void* biases,
+                          const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size, int bits,
+                          int sorted, void* y, void* ws, size_t ws_bytes, cudaStream_t s, bool allow_split) {
+  int rc = validate_gather(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y);
+  if (rc) return rc;
+  if (sorted != 0 && sorted != 1) return fail(GQMM_ERR_SHAPE, "sorted must be 0 or 1");
+  if (!ws) return fail(GQMM_ERR_NULL, "ws must be non-NULL");
+  const int64_t n = T * (int64_t)A;
+  const WsLayout L = ws_layout(n, F, E, allow_split);
+  UnitShape shape = unit_shape(n, H, F, E);
+  if (!allow_split) shape.ksplit = 1;
+  if (!aligned(ws, 256) || ws_bytes < L.total)
+    return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
+  rc = check_device(nullptr);
+  if (rc) return rc;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  WsHeader* header = reinterpret_cast<WsHeader*>(w);
+
+  RouteArgs ra;
+  ra.idx = idx;
+  ra.n = n;
+  ra.E = E;
+  ra.sorted = sorted;
+  ra.perm = reinterpret_cast<int32_t*>(w + L.perm);
+  ra.offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+  ra.tile_hist = reinterpret_cast<uint32_t*>(w + L.tile_hist);
+  ra.chunks = reinterpret_cast<Chunk*>(w + L.chunks);
+  ra.header = header;
+  ra.y = static_cast<__nv_bfloat16*>(y);
+  ra.F = F;
+  ra.n_tiles = L.n_tiles;
+  ra.chunk_rows = shape.chunk_rows;
+  const bool permuted = idx != nullptr && !sorted;
+  int launched = 0;
+  cudaError_t e = launch_route(ra, s, &launched);
+  g_launches.fetch_add(launched);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
+  const int route_variant = idx == nullptr ? GQMM_VARIANT_ROUTE_DENSE
+                                           : (sorted ? GQMM_VARIANT_ROUTE_SORTED : GQMM_VARIANT_ROUTE_UNSORTED);
+  count_variant(route_variant);
+
+  GemmArgs ga;
+  ga.x = static_cast<const __nv_bfloat16*>(x);
+  ga.n = n;
+  ga.wq = static_cast<const uint8_t*>(wq);
+  ga.scales = static_cast<const __nv_bfloat16*>(scales);
+  ga.biases = static_cast<const __nv_bfloat16*>(biases);
+  ga.y = static_cast<__nv_bfloat16*>(y);
+  ga.perm = permuted ? ra.perm : nullptr;
+  ga.chunks = ra.chunks;
+  ga.header = header;
+  ga.H = H;
+  ga.F = F;
+  ga.E = E;
+  ga.chunk_rows = shape.chunk_rows;
+  ga.ksplit = shape.ksplit;
+  ga.acc = L.has_acc ? reinterpret_cast<float*>(w + L.acc) : nullptr;
+  ga.offsets = ra.offsets;
+  if (shape.ksplit > 1 && !L.has_acc) return fail(GQMM_ERR_WORKSPACE, "internal: split-K without a buffer");
+  size_t slot = 0;
+  const bool timed = timer_begin(s, &slot);
+  int gemm_launched = 0;
+  e = launch_gemm_tc(ga, s, &gemm_launched);
+  if (timed) timer_end(s, slot);
+  g_launches.fetch_add(gemm_launched);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "grouped GEMM launch: %s", cudaGetErrorString(e));
+  count_variant(shape.chunk_rows == kChunkRowsNarrow ? GQMM_VARIANT_GEMM_NARROW : GQMM_VARIANT_GEMM_TC);
+  if (shape.ksplit > 1) count_variant(GQMM_VARIANT_SPLIT_K);
+  if (log_dispatch())
+    std::fprintf(stderr, "[gqmm] gather_qmm n=%lld H=%d F=%d E=%d route=%s gemm=%s ksplit=%d\n", (long long)n, H,
+                 F, E,
+                 route_variant == GQMM_VARIANT_ROUTE_DENSE ? "dense"
+                 : route_variant == GQMM_VARIANT_ROUTE_SORTED ? "sorted" : "unsorted",
+                 shape.chunk_rows == kChunkRowsNarrow ? "narrow" : "wide", shape.ksplit);
+  return ok();
+}
+
+
 extern "C" {
 
 int gqmm_quantize(const void* w, int64_t rows, int64_t H, int group_size, int bits, void* wq,
@@ -139,7 +217,7 @@ int gqmm_quantize(const void* w, int64_t rows, int64_t H, int group_size, int bi
 
 size_t gqmm_workspace_size(int64_t n, int F, int E) {
   if (n < 0 || n > 2147483647LL || F < 0 || E < 1 || E > GQMM_MAX_EXPERTS) return 0;
-  return ws_layout(n, E).total;
+  return ws_layout(n, F, E).total;
 }
 
 int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* perm, int32_t* offsets, void* ws,
@@ -148,13 +226,14 @@ int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* perm, int32_
   if (n < 0 || n > 2147483647LL) return fail(GQMM_ERR_SHAPE, "n must be in [0, 2^31)");
   if (E < 1) return fail(GQMM_ERR_SHAPE, "E must be >= 1");
   if (E > GQMM_MAX_EXPERTS) return fail(GQMM_ERR_UNSUPPORTED, "E=%d exceeds %d", E, GQMM_MAX_EXPERTS);
-  const WsLayout L = ws_layout(n, E);
+  const WsLayout L = ws_layout(n, 1, E);
   if (!aligned(ws, 256) || ws_bytes < L.total)
     return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
   int rc = check_device(nullptr);
   if (rc) return rc;
   uint8_t* w = static_cast<uint8_t*>(ws);
   RouteArgs a;
+  a.chunk_rows = kChunkRowsWide;
   a.idx = idx;
   a.n = n;
   a.E = E;
@@ -178,67 +257,8 @@ int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* perm, int32_
 int gqmm_gather_qmm(const void* x, const void* wq, const void* scales, const void* biases, const uint32_t* idx,
                     int64_t T, int A, int H, int F, int E, int group_size, int bits, int sorted, void* y,
                     void* ws, size_t ws_bytes, gqmm_stream_t stream) {
-  int rc = validate_gather(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y);
-  if (rc) return rc;
-  if (sorted != 0 && sorted != 1) return fail(GQMM_ERR_SHAPE, "sorted must be 0 or 1");
-  if (!ws) return fail(GQMM_ERR_NULL, "ws must be non-NULL");
-  const int64_t n = T * (int64_t)A;
-  const WsLayout L = ws_layout(n, E);
-  if (!aligned(ws, 256) || ws_bytes < L.total)
-    return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
-  rc = check_device(nullptr);
-  if (rc) return rc;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  uint8_t* w = static_cast<uint8_t*>(ws);
-  WsHeader* header = reinterpret_cast<WsHeader*>(w);
-
-  RouteArgs ra;
-  ra.idx = idx;
-  ra.n = n;
-  ra.E = E;
-  ra.sorted = sorted;
-  ra.perm = reinterpret_cast<int32_t*>(w + L.perm);
-  ra.offsets = reinterpret_cast<int32_t*>(w + L.offsets);
-  ra.tile_hist = reinterpret_cast<uint32_t*>(w + L.tile_hist);
-  ra.chunks = reinterpret_cast<Chunk*>(w + L.chunks);
-  ra.header = header;
-  ra.y = static_cast<__nv_bfloat16*>(y);
-  ra.F = F;
-  ra.n_tiles = L.n_tiles;
-  const bool permuted = idx != nullptr && !sorted;
-  int launched = 0;
-  cudaError_t e = launch_route(ra, s, &launched);
-  g_launches.fetch_add(launched);
-  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
-  const int route_variant = idx == nullptr ? GQMM_VARIANT_ROUTE_DENSE
-                                           : (sorted ? GQMM_VARIANT_ROUTE_SORTED : GQMM_VARIANT_ROUTE_UNSORTED);
-  count_variant(route_variant);
-
-  GemmArgs ga;
-  ga.x = static_cast<const __nv_bfloat16*>(x);
-  ga.n = n;
-  ga.wq = static_cast<const uint8_t*>(wq);
-  ga.scales = static_cast<const __nv_bfloat16*>(scales);
-  ga.biases = static_cast<const __nv_bfloat16*>(biases);
-  ga.y = static_cast<__nv_bfloat16*>(y);
-  ga.perm = permuted ? ra.perm : nullptr;
-  ga.chunks = ra.chunks;
-  ga.header = header;
-  ga.H = H;
-  ga.F = F;
-  ga.E = E;
-  size_t slot = 0;
-  const bool timed = timer_begin(s, &slot);
-  e = launch_gemm_tc(ga, s);
-  if (timed) timer_end(s, slot);
-  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "grouped GEMM launch: %s", cudaGetErrorString(e));
-  g_launches.fetch_add(1);
-  count_variant(GQMM_VARIANT_GEMM_TC);
-  if (log_dispatch())
-    std::fprintf(stderr, "[gqmm] gather_qmm n=%lld H=%d F=%d E=%d route=%s gemm=tc\n", (long long)n, H, F, E,
-                 route_variant == GQMM_VARIANT_ROUTE_DENSE ? "dense"
-                 : route_variant == GQMM_VARIANT_ROUTE_SORTED ? "sorted" : "unsorted");
-  return ok();
+  return gqmm::gather_qmm_impl(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, sorted, y, ws, ws_bytes,
+                               reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* scales, const void* biases,

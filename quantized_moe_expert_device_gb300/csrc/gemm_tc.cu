@@ -1,15 +1,26 @@
 // Persistent grouped GEMM for the quantized MoE gather matmul on tcgen05 tensor cores.
 //
 // Work unit = (chunk of one expert's sorted rows, pair of 128-row tiles of the expert's F
-// outputs).  The product is computed transposed ("swap A/B"): the UMMA M slot (128) holds
-// weight rows f, the N slot holds the chunk's tokens, so N = round_up(rows, 16) follows the
-// rows per expert.  This is the tensor-core form of the lesson in mlx PR #4023 "Pick BM from
-// rows per expert in gather_qmm_rhs_nax" (useful arithmetic ~ min(1, run / BM)): a 4-row run
-// costs an N=16 MMA instead of most of a 64- or 128-row tile, and each expert's weight tile is
-// read and dequantized once per chunk of up to 256 rows instead of once per row (mlx #4339,
-// comment by manunicholasjacob: one CTA per token-expert pair, 15 of 16 tile rows empty, the
-// 4-bit slab dequantized once per row).  The two tiles of a unit share every x tile, which
-// halves the x bytes moved per FLOP compared with one tile per unit.
+// outputs, K slice).  The product is computed transposed ("swap A/B"): the UMMA M slot (128)
+// holds weight rows f, the N slot holds the chunk's tokens, so N = round_up(rows, 16) follows
+// the rows per expert.  This is the tensor-core form of the lesson in mlx PR #4023 "Pick BM
+// from rows per expert in gather_qmm_rhs_nax" (useful arithmetic ~ min(1, run / BM)): a 4-row
+// run costs an N=16 MMA instead of most of a 64- or 128-row tile, and each expert's weight
+// tile is read and dequantized once per chunk instead of once per row (mlx #4339, comment by
+// manunicholasjacob: one CTA per token-expert pair, 15 of 16 tile rows empty, the 4-bit slab
+// dequantized once per row).  The two tiles of a unit share every x tile, which halves the x
+// bytes moved per FLOP compared with one tile per unit.  For decode-sized calls (mlxcel #725
+// "amortizing small-M quantized GEMM": per-row qmv re-reads the weights, a 128-wide tile is
+// 94% wasted) the same kernel reads each weight tile once per call for all of its M <= 8 rows.
+//
+// Two variants (template Cfg), chosen on the host from the rows per expert:
+//   wide    chunks of <= 256 rows; 3 stages of (A 2 x 16 KB, x 32 KB, codes 8 KB)
+//   narrow  chunks of <= 32 rows; 3 stages of (A 2 x 16 KB, x 4 KB) and 13 stages of codes:
+//           with few rows the weight-code stream from HBM is the bottleneck, so the smem the
+//           x tiles do not need goes to a deeper code ring.
+// Calls with too few units for the GPU (dense decode: F/256 units) split K into slices; each
+// slice stores its fp32 partial sums in its own plane of a workspace buffer, and a second
+// kernel adds the planes in slice order (so results are deterministic) into bf16 y.
 //
 // Per CTA (one per SM, persistent, static round-robin over units), warp roles:
 //   warps 0-15  dequant:  two groups of 256 threads take alternate k-blocks; a thread owns one
@@ -18,19 +29,18 @@
 //                         128-byte-swizzle K-major A layout
 //   warps 16-23 epilogue: warp 16+e drains TMEM lanes 32(e%4).. of tile e/4: TMEM -> registers
 //                         -> bf16 -> shared transpose -> 16-byte stores to y rows perm[j]
-//   warp 24     TMA:      one thread streams the unit's 256 x 32-byte nibble tile per k-block
+//                         (or fp32 stores into the slice's plane of the split-K sums)
+//   warp 24     TMA:      one thread streams the unit's 256 x 32-byte code tile per k-block
 //   warp 25     MMA:      allocates TMEM (two 256-column fp32 accumulators), one thread issues
 //                         tcgen05.mma 128xNx16, four per tile per k-block, commits to mbarriers
-//   warps 26-31 gather:   warps 26+2s and 27+2s own pipeline stage s: whenever the stage is free
-//                         they copy the chunk's x rows perm[j] (128 bytes each) with 16-byte
-//                         cp.async into the swizzled B tile, wait for their own copies, fence
-//                         them for the tensor core and mark the stage full.  Each lane keeps its
-//                         32 source rows in registers for the whole unit, so a stage's copies
-//                         issue back to back.  (TMA tile::gather4 was measured at ~80 cycles per
-//                         512-byte gather per SM: too slow for 128-byte rows.)
-// Pipeline depth: 3 stages of (A 2 x 16 KB, B 32 KB, nibbles 8 KB).  The accumulators use all
-// 512 TMEM columns, so the MMA of a unit starts once the epilogue has drained the previous one;
-// the producers keep filling stages meanwhile.
+//   warps 26-31 gather:   warps 26+2s and 27+2s own A/x stage s: whenever the stage is free they
+//                         copy the chunk's x rows perm[j] (128 bytes each) with 16-byte cp.async
+//                         into the swizzled x tile, wait for their own copies, fence them for the
+//                         tensor core and mark the stage full.  Each lane keeps its source rows in
+//                         registers for the whole unit.  (TMA tile::gather4 was measured at ~80
+//                         cycles per 512-byte gather per SM: too slow for 128-byte rows.)
+// The accumulators use all 512 TMEM columns, so the MMA of a unit starts once the epilogue has
+// drained the previous one; the producers keep filling stages meanwhile.
 //
 // Every wait is bounded (mbar_wait): on expiry the CTA raises GQMM_STATUS_TIMEOUT, unwinds,
 // waits (bounded) for its own copies and MMAs in flight and frees its TMEM.
@@ -42,12 +52,10 @@ namespace {
 constexpr int BM = 128;                  // weight rows per tile (UMMA M)
 constexpr int NT = 2;                    // tiles per unit
 constexpr int UM = BM * NT;              // weight rows per unit
+static_assert(UM == kUnitRows, "unit height");
 constexpr int BK = 64;                   // K per stage = one quantization group
-constexpr int NMAX = kChunkMaxRows;      // tokens per unit, UMMA N <= 256
-constexpr int STAGES = 3;
 constexpr int A_TILE_BYTES = BM * BK * 2;      // 16 KB bf16
 constexpr int A_BYTES = NT * A_TILE_BYTES;     // 32 KB
-constexpr int B_BYTES = NMAX * BK * 2;         // 32 KB bf16
 constexpr int NIB_BYTES = UM * BK / 2;         // 8 KB packed codes
 constexpr int EPI_WARP_BYTES = 16 * 32 * 2;
 
@@ -58,45 +66,60 @@ constexpr int kEpiWarp0 = 16;            // warps 16-23
 constexpr int kEpiWarps = 4 * NT;
 constexpr int kTmaWarp = 24;
 constexpr int kMmaWarp = 25;
-constexpr int kGatherWarp0 = 26;         // warps 26 .. 31, a pair per stage
-constexpr uint32_t kTmemCols = 512;      // NT accumulators of NMAX fp32 columns
-static_assert(kGatherWarp0 + 2 * STAGES == kThreads / 32, "warp roles fill the block");
+constexpr int kGatherWarp0 = 26;         // warps 26 .. 31, a pair per A/x stage
+constexpr int kAbStages = 3;
+constexpr uint32_t kTmemCols = 512;      // NT accumulators of 256 fp32 columns
+static_assert(kGatherWarp0 + 2 * kAbStages == kThreads / 32, "warp roles fill the block");
 static_assert(kDeqGroup * kDeqGroups == kEpiWarp0 * 32, "dequant warps");
 
-constexpr int OFF_A = 0;
-constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
-constexpr int OFF_NIB = OFF_B + STAGES * B_BYTES;
-constexpr int OFF_EPI = OFF_NIB + STAGES * NIB_BYTES;
-constexpr int OFF_BAR = OFF_EPI + kEpiWarps * EPI_WARP_BYTES;
-constexpr int NUM_BARS = 5 * STAGES + 3;
-constexpr int OFF_MISC = OFF_BAR + ((NUM_BARS * 8 + 127) / 128) * 128;
-constexpr int SMEM_USED = OFF_MISC + 16;
-constexpr int SMEM_DYN = SMEM_USED + 1024;  // room to align the base to 1024 bytes
-static_assert(SMEM_DYN <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
-
-// barrier slots
-__device__ __forceinline__ int b_nib_full(int s) { return s; }
-__device__ __forceinline__ int b_nib_empty(int s) { return STAGES + s; }
-__device__ __forceinline__ int b_a_full(int s) { return 2 * STAGES + s; }
-__device__ __forceinline__ int b_b_full(int s) { return 3 * STAGES + s; }
-__device__ __forceinline__ int b_ab_empty(int s) { return 4 * STAGES + s; }
-__device__ __forceinline__ int b_tmem_full() { return 5 * STAGES; }
-__device__ __forceinline__ int b_tmem_empty() { return 5 * STAGES + 1; }
-__device__ __forceinline__ int b_unwind() { return 5 * STAGES + 2; }
+template <int NMAX_, int NIB_STAGES_>
+struct Cfg {
+  static constexpr int NMAX = NMAX_;              // rows per chunk = largest UMMA N
+  static constexpr int NIB_STAGES = NIB_STAGES_;  // code ring depth
+  static constexpr int B_BYTES = NMAX * BK * 2;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + kAbStages * A_BYTES;
+  static constexpr int OFF_NIB = OFF_B + kAbStages * B_BYTES;
+  static constexpr int OFF_EPI = OFF_NIB + NIB_STAGES * NIB_BYTES;
+  static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * EPI_WARP_BYTES;
+  static constexpr int NUM_BARS = 2 * NIB_STAGES + 2 * kAbStages + 3;
+  static constexpr int OFF_MISC = OFF_BAR + ((NUM_BARS * 8 + 127) / 128) * 128;
+  static constexpr int SMEM_DYN = OFF_MISC + 16 + 1024;  // room to align the base to 1024 bytes
+  static_assert(SMEM_DYN <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
+  static_assert(B_BYTES % 1024 == 0, "x tiles stay 1024-byte aligned");
+  // barrier slots
+  __device__ static int nib_full(int s) { return s; }
+  __device__ static int nib_empty(int s) { return NIB_STAGES + s; }
+  // A tile and x tile of a stage are both written: the stage's dequant group (256 arrivals)
+  // and the two gather warps (64) arrive on one barrier, so the MMA thread probes once per
+  // k-block (a probe costs ~160 cycles even when the phase is already complete, which at
+  // N=16 is more than half the MMA time of the k-block).
+  __device__ static int ab_full(int s) { return 2 * NIB_STAGES + s; }
+  __device__ static int ab_empty(int s) { return 2 * NIB_STAGES + kAbStages + s; }
+  __device__ static int tmem_full() { return 2 * NIB_STAGES + 2 * kAbStages; }
+  __device__ static int tmem_empty() { return 2 * NIB_STAGES + 2 * kAbStages + 1; }
+  __device__ static int unwind() { return 2 * NIB_STAGES + 2 * kAbStages + 2; }
+};
+using CfgWide = Cfg<kChunkRowsWide, 3>;
+using CfgNarrow = Cfg<kChunkRowsNarrow, 13>;
 
 struct Unit {
-  int expert, start, rows, f0;
+  int expert, start, rows, f0, kb0, kb1;
 };
 
-__device__ __forceinline__ Unit decode_unit(const Chunk* chunks, int u, int n_fpairs) {
-  const int c = u / n_fpairs;
-  const int fp = u - c * n_fpairs;
+__device__ __forceinline__ Unit decode_unit(const Chunk* chunks, int u, int n_fpairs, int ksplit, int num_kb) {
+  const int ks = u % ksplit;
+  const int t = u / ksplit;
+  const int c = t / n_fpairs;
+  const int fp = t - c * n_fpairs;
   const int4 ch = __ldg(reinterpret_cast<const int4*>(chunks) + c);
   Unit U;
   U.expert = ch.x;
   U.start = ch.y;
   U.rows = ch.z;
   U.f0 = fp * UM;
+  U.kb0 = (int)((int64_t)num_kb * ks / ksplit);
+  U.kb1 = (int)((int64_t)num_kb * (ks + 1) / ksplit);
   return U;
 }
 
@@ -127,30 +150,34 @@ __device__ __forceinline__ uint4 deq8(uint32_t w, uint32_t s2, uint32_t b2) {
   return o;
 }
 
+template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_wq, const GemmArgs p) {
+  constexpr int NMAX = C::NMAX;
+  constexpr int NIB_STAGES = C::NIB_STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + OFF_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + OFF_MISC + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   uint32_t* status = &p.header->status;
-  auto bar = [&](int i) -> uint32_t { return sbase + OFF_BAR + 8u * (uint32_t)i; };
+  auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(b_nib_full(s)), 1);
-      mbar_init(bar(b_nib_empty(s)), kDeqGroup);  // the dequant group that consumed it
-      mbar_init(bar(b_a_full(s)), kDeqGroup);
-      mbar_init(bar(b_b_full(s)), 64);            // every lane of the stage's two gather warps
-      mbar_init(bar(b_ab_empty(s)), 1);
+    for (int s = 0; s < NIB_STAGES; ++s) {
+      mbar_init(bar(C::nib_full(s)), 1);
+      mbar_init(bar(C::nib_empty(s)), kDeqGroup);  // the dequant group that consumed it
     }
-    mbar_init(bar(b_tmem_full()), 1);
-    mbar_init(bar(b_tmem_empty()), kEpiWarps * 32);
-    mbar_init(bar(b_unwind()), 1);
+    for (int s = 0; s < kAbStages; ++s) {
+      mbar_init(bar(C::ab_full(s)), kDeqGroup + 64);  // dequant group + both gather warps' lanes
+      mbar_init(bar(C::ab_empty(s)), 1);
+    }
+    mbar_init(bar(C::tmem_full()), 1);
+    mbar_init(bar(C::tmem_empty()), kEpiWarps * 32);
+    mbar_init(bar(C::unwind()), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -167,48 +194,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int H = p.H, F = p.F;
   const int G = H / BK;
   const int num_kb = G;
+  const int ksplit = p.ksplit;
   const int n_fpairs = (F + UM - 1) / UM;
-  const int n_units = p.header->n_chunks * n_fpairs;
+  const int n_units = p.header->n_chunks * n_fpairs * ksplit;
 
   if (warp == kTmaWarp) {
-    // ---------------------------------------------------------------- TMA producer (nibbles)
-    // Besides the stage loads, the tile kPrefetchAhead k-blocks ahead (possibly in the next
-    // unit) is prefetched into L2, so stage loads see L2 rather than HBM latency: with only
-    // three stages the loads themselves cannot run far enough ahead.
+    // ---------------------------------------------------------------- TMA producer (codes)
+    // (An L2 prefetch of the tile several k-blocks ahead was measured: no gain with three
+    // stages, a loss with thirteen, so there is none.)
     if (lane == 0) {
-      constexpr int kPrefetchAhead = 6;
-      auto prefetch = [&](int u, int kb) {
-        while (kb >= num_kb && u < n_units) {
-          kb -= num_kb;
-          u += gridDim.x;
-        }
-        if (u < n_units) {
-          const Unit V = decode_unit(p.chunks, u, n_fpairs);
-          tma_prefetch_l2_2d(&tmap_wq, kb * (BK / 2), V.expert * F + V.f0);
-        }
-      };
-      for (int j = 0; j < kPrefetchAhead; ++j) prefetch(blockIdx.x, j);
-      uint32_t it = 0;
+      uint32_t itn = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const Unit U = decode_unit(p.chunks, u, n_fpairs);
+        const Unit U = decode_unit(p.chunks, u, n_fpairs, ksplit, num_kb);
         const int row0 = U.expert * F + U.f0;
-        for (int kb = 0; kb < num_kb; ++kb) {
-          prefetch(u, kb + kPrefetchAhead);
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-          if (!mbar_wait(bar(b_nib_empty(s)), ph ^ 1u, abort_flag, status)) {
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
+          const uint32_t s = itn % NIB_STAGES, ph = (itn / NIB_STAGES) & 1u;
+          if (!mbar_wait(bar(C::nib_empty(s)), ph ^ 1u, abort_flag, status)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(b_nib_full(s)), NIB_BYTES);
-          tma_load_2d(sbase + OFF_NIB + s * NIB_BYTES, &tmap_wq, bar(b_nib_full(s)), kb * (BK / 2), row0);
-          ++it;
+          mbar_arrive_expect_tx(bar(C::nib_full(s)), NIB_BYTES);
+          tma_load_2d(sbase + C::OFF_NIB + s * NIB_BYTES, &tmap_wq, bar(C::nib_full(s)), kb * (BK / 2), row0);
+          ++itn;
         }
       }
       if (!ok) {  // unwinding: let the copies already issued land before the CTA exits
-        const uint32_t first = it > STAGES ? it - STAGES : 0;
-        for (uint32_t j = first; j < it; ++j)
-          mbar_wait_unwind(bar(b_nib_full(j % STAGES)), (j / STAGES) & 1u, 100000000ull);
+        const uint32_t first = itn > NIB_STAGES ? itn - NIB_STAGES : 0;
+        for (uint32_t j = first; j < itn; ++j)
+          mbar_wait_unwind(bar(C::nib_full(j % NIB_STAGES)), (j / NIB_STAGES) & 1u, 100000000ull);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -217,76 +231,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, lu = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++lu) {
-        const Unit U = decode_unit(p.chunks, u, n_fpairs);
+        const Unit U = decode_unit(p.chunks, u, n_fpairs, ksplit, num_kb);
         const int N = (U.rows + 15) & ~15;
         const uint32_t idesc = umma_idesc_bf16(BM, N);
-        if (!mbar_wait(bar(b_tmem_empty()), (lu & 1u) ^ 1u, abort_flag, status)) break;
+        if (!mbar_wait(bar(C::tmem_empty()), (lu & 1u) ^ 1u, abort_flag, status)) break;
         tc_fence_after();
-        for (int kb = 0; kb < num_kb; ++kb) {
-          const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-          if (!mbar_wait(bar(b_a_full(s)), ph, abort_flag, status) ||
-              !mbar_wait(bar(b_b_full(s)), ph, abort_flag, status)) {
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
+          const uint32_t s = it % kAbStages, ph = (it / kAbStages) & 1u;
+          if (!mbar_wait(bar(C::ab_full(s)), ph, abort_flag, status)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t bdesc = umma_desc_sw128(sbase + OFF_B + s * B_BYTES);
+          const uint64_t bdesc = umma_desc_sw128(sbase + C::OFF_B + s * C::B_BYTES);
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            const uint64_t adesc = umma_desc_sw128(sbase + OFF_A + s * A_BYTES + t * A_TILE_BYTES);
+            const uint64_t adesc = umma_desc_sw128(sbase + C::OFF_A + s * A_BYTES + t * A_TILE_BYTES);
 #pragma unroll
             for (int k = 0; k < BK / 16; ++k)  // advance 16 elements = 32 bytes along K
-              tc_mma_bf16(tmem_base + (uint32_t)(t * NMAX), adesc + 2u * k, bdesc + 2u * k, idesc,
-                          (kb > 0 || k > 0) ? 1u : 0u);
+              tc_mma_bf16(tmem_base + (uint32_t)(t * 256), adesc + 2u * k, bdesc + 2u * k, idesc,
+                          (kb > U.kb0 || k > 0) ? 1u : 0u);
           }
-          tc_commit(bar(b_ab_empty(s)));
+          tc_commit(bar(C::ab_empty(s)));
           ++it;
         }
         if (!ok) break;
-        tc_commit(bar(b_tmem_full()));
+        tc_commit(bar(C::tmem_full()));
       }
       // every MMA issued above completes before this barrier's phase 0 completes
-      tc_commit(bar(b_unwind()));
-      mbar_wait_unwind(bar(b_unwind()), 0, 100000000ull);
-      // and the stage-release arrivals of the last STAGES iterations have landed
-      const uint32_t first = it > STAGES ? it - STAGES : 0;
+      tc_commit(bar(C::unwind()));
+      mbar_wait_unwind(bar(C::unwind()), 0, 100000000ull);
+      // and the stage-release arrivals of the last stages have landed
+      const uint32_t first = it > kAbStages ? it - kAbStages : 0;
       for (uint32_t j = first; j < it; ++j)
-        mbar_wait_unwind(bar(b_ab_empty(j % STAGES)), (j / STAGES) & 1u, 100000000ull);
+        mbar_wait_unwind(bar(C::ab_empty(j % kAbStages)), (j / kAbStages) & 1u, 100000000ull);
     }
   } else if (warp >= kGatherWarp0) {
     // ---------------------------------------------------------------- x row gather
+    constexpr int Q = NMAX / 8;                // rows per lane
     const uint32_t gs = (uint32_t)(warp - kGatherWarp0) >> 1;  // the stage this warp pair fills
     const int h = (warp - kGatherWarp0) & 1;
     const int cidx = lane & 7;                 // 16-byte chunk of a 128-byte row slice
-    const int rlow = 4 * h + (lane >> 3);      // rows 8 q + rlow, q = 0..31
+    const int rlow = 4 * h + (lane >> 3);      // rows 8 q + rlow
     const uint32_t dst_lane = (uint32_t)(rlow * 128 + ((cidx ^ rlow) << 4));
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-      const Unit U = decode_unit(p.chunks, u, n_fpairs);
-      int src[NMAX / 8];
+      const Unit U = decode_unit(p.chunks, u, n_fpairs, ksplit, num_kb);
+      int src[Q];
 #pragma unroll
-      for (int q = 0; q < NMAX / 8; ++q) {
+      for (int q = 0; q < Q; ++q) {
         const int row = 8 * q + rlow;
         src[q] = row < U.rows ? (p.perm ? __ldg(p.perm + U.start + row) : U.start + row) : -1;
       }
-      for (int kb = 0; kb < num_kb; ++kb, ++it) {
-        if (it % STAGES != gs) continue;
-        const uint32_t ph = (it / STAGES) & 1u;
-        const bool okl = mbar_wait(bar(b_ab_empty(gs)), ph ^ 1u, abort_flag, status);
+      for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
+        if (it % kAbStages != gs) continue;
+        const uint32_t ph = (it / kAbStages) & 1u;
+        const bool okl = mbar_wait(bar(C::ab_empty(gs)), ph ^ 1u, abort_flag, status);
         if (!__all_sync(0xffffffffu, okl)) {
           ok = false;
           break;
         }
-        const uint32_t b_lane = sbase + OFF_B + gs * B_BYTES + dst_lane;
+        const uint32_t b_lane = sbase + C::OFF_B + gs * C::B_BYTES + dst_lane;
         const __nv_bfloat16* xk = p.x + kb * BK + cidx * 8;
 #pragma unroll
-        for (int q = 0; q < NMAX / 8; ++q)
+        for (int q = 0; q < Q; ++q)
           if (src[q] >= 0) cp_async_16(b_lane + q * 1024, xk + (int64_t)src[q] * H);
         cp_async_commit();
         cp_async_wait<0>();
         fence_proxy_async_smem();  // this lane's copies, made visible to the tensor core
-        mbar_arrive(bar(b_b_full(gs)));
+        mbar_arrive(bar(C::ab_full(gs)));
       }
     }
     cp_async_wait<0>();
@@ -295,44 +309,61 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - kEpiWarp0;
     const int tile = ew >> 2;          // accumulator (weight-row tile) this warp drains
     const int quarter = ew & 3;        // TMEM lanes 32 quarter .. 32 quarter + 31 (= warp % 4)
-    uint16_t* epi = reinterpret_cast<uint16_t*>(smem + OFF_EPI + ew * EPI_WARP_BYTES);
-    const uint32_t epi_addr = sbase + OFF_EPI + ew * EPI_WARP_BYTES;
+    uint16_t* epi = reinterpret_cast<uint16_t*>(smem + C::OFF_EPI + ew * EPI_WARP_BYTES);
+    const uint32_t epi_addr = sbase + C::OFF_EPI + ew * EPI_WARP_BYTES;
     uint32_t lu = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++lu) {
-      const Unit U = decode_unit(p.chunks, u, n_fpairs);
+      const Unit U = decode_unit(p.chunks, u, n_fpairs, ksplit, num_kb);
       const int N = (U.rows + 15) & ~15;
-      const bool okl = mbar_wait(bar(b_tmem_full()), lu & 1u, abort_flag, status);
+      const bool okl = mbar_wait(bar(C::tmem_full()), lu & 1u, abort_flag, status);
       if (!__all_sync(0xffffffffu, okl)) break;
       tc_fence_after();
-      const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(tile * NMAX);
-      const int q = lane & 3;
-      const int fcol = U.f0 + tile * BM + quarter * 32 + q * 8;
-      for (int c0 = 0; c0 < N; c0 += 16) {
-        uint32_t v[16];
-        tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
-        tc_wait_ld();
+      const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(tile * 256);
+      if (ksplit > 1) {
+        // partial sums of this K slice into its own plane: thread = weight row f, 16 tokens
+        // per TMEM load; a warp's stores for one token are 32 consecutive f (128 bytes)
+        const int f = U.f0 + tile * BM + quarter * 32 + lane;
+        float* plane = p.acc + (int64_t)(u % ksplit) * p.n * F;
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          uint32_t v[16];
+          tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
+          tc_wait_ld();
+          if (f < F) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-          epi[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
-        __syncwarp();
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int jj = (lane >> 2) + 8 * hh;
-          const int tok = c0 + jj;
-          if (tok < U.rows && fcol < F) {
-            const int row = p.perm ? __ldg(p.perm + U.start + tok) : U.start + tok;
-            uint4 val;
-            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                         : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                         : "r"(epi_addr + (uint32_t)(jj * 64 + q * 16))
-                         : "memory");
-            *reinterpret_cast<uint4*>(p.y + (int64_t)row * F + fcol) = val;
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < U.rows) plane[(int64_t)(U.start + c0 + j) * F + f] = __uint_as_float(v[j]);
           }
         }
-        __syncwarp();
+      } else {
+        const int q = lane & 3;
+        const int fcol = U.f0 + tile * BM + quarter * 32 + q * 8;
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          uint32_t v[16];
+          tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            epi[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+          __syncwarp();
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int jj = (lane >> 2) + 8 * hh;
+            const int tok = c0 + jj;
+            if (tok < U.rows && fcol < F) {
+              const int row = p.perm ? __ldg(p.perm + U.start + tok) : U.start + tok;
+              uint4 val;
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                           : "r"(epi_addr + (uint32_t)(jj * 64 + q * 16))
+                           : "memory");
+              *reinterpret_cast<uint4*>(p.y + (int64_t)row * F + fcol) = val;
+            }
+          }
+          __syncwarp();
+        }
       }
       tc_fence_before();
-      mbar_arrive(bar(b_tmem_empty()));
+      mbar_arrive(bar(C::tmem_empty()));
     }
   } else {
     // ---------------------------------------------------------------- dequant
@@ -340,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = t % UM;                        // weight row within the unit
     const uint32_t grp = (uint32_t)(t / UM);     // handles the steps with it % 2 == grp
     const int tile = r >> 7, rr = r & (BM - 1);
-    // nibble tile rows are 32 bytes, TMA-swizzled in 32-byte mode: 16-byte chunk c of row r
+    // code tile rows are 32 bytes, TMA-swizzled in 32-byte mode: 16-byte chunk c of row r
     // sits at chunk position c ^ ((r >> 2) & 1)
     const uint32_t nib_row = (uint32_t)(r * 32);
     const uint32_t nib_c0 = (uint32_t)(((r >> 2) & 1) << 4), nib_c1 = nib_c0 ^ 16u;
@@ -353,12 +384,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int u, kb;
       Unit U;
     };
-    auto advance = [&](Step& st, int by) {
-      st.kb += by;
-      while (st.kb >= num_kb && st.u < n_units) {
-        st.kb -= num_kb;
+    auto normalize = [&](Step& st) {  // carry kb past the unit's end into the following units
+      while (st.u < n_units && st.kb >= st.U.kb1) {
+        const int over = st.kb - st.U.kb1;
         st.u += gridDim.x;
-        if (st.u < n_units) st.U = decode_unit(p.chunks, st.u, n_fpairs);
+        if (st.u >= n_units) break;
+        st.U = decode_unit(p.chunks, st.u, n_fpairs, ksplit, num_kb);
+        st.kb = st.U.kb0 + over;
       }
     };
     auto load_sb = [&](const Step& st, uint32_t& sv, uint32_t& bv) {
@@ -372,21 +404,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     Step cur;
     cur.u = blockIdx.x;
-    cur.kb = 0;
-    if (cur.u < n_units) cur.U = decode_unit(p.chunks, cur.u, n_fpairs);
-    advance(cur, (int)grp);
+    if (cur.u < n_units) {
+      cur.U = decode_unit(p.chunks, cur.u, n_fpairs, ksplit, num_kb);
+      cur.kb = cur.U.kb0 + (int)grp;
+      normalize(cur);
+    }
     uint32_t it = grp;  // global step index of cur
-    uint32_t s_cur, b_cur;
+    uint32_t s_cur = 0, b_cur = 0;
     load_sb(cur, s_cur, b_cur);
     while (cur.u < n_units) {
       Step nxt = cur;
-      advance(nxt, kDeqGroups);
+      nxt.kb += kDeqGroups;
+      normalize(nxt);
       uint32_t s_nxt, b_nxt;
       load_sb(nxt, s_nxt, b_nxt);
       const uint32_t s2 = splat16(s_cur), b2 = splat16(b_cur);
-      const uint32_t s = it % STAGES, ph = (it / STAGES) & 1u;
-      if (!mbar_wait(bar(b_nib_full(s)), ph, abort_flag, status)) break;
-      const uint32_t nib_tile = sbase + OFF_NIB + s * NIB_BYTES + nib_row;
+      const uint32_t sn = it % NIB_STAGES, phn = (it / NIB_STAGES) & 1u;
+      const uint32_t sa = it % kAbStages, pha = (it / kAbStages) & 1u;
+      if (!mbar_wait(bar(C::nib_full(sn)), phn, abort_flag, status)) break;
+      const uint32_t nib_tile = sbase + C::OFF_NIB + sn * NIB_BYTES + nib_row;
       uint4 n0, n1;
       asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                    : "=r"(n0.x), "=r"(n0.y), "=r"(n0.z), "=r"(n0.w)
@@ -396,9 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                    : "=r"(n1.x), "=r"(n1.y), "=r"(n1.z), "=r"(n1.w)
                    : "r"(nib_tile + nib_c1)
                    : "memory");
-      // The nibble stage is released only after the proxy fence below: the next TMA into
-      // it is an async-proxy write, which is not ordered after these generic-proxy reads
-      // by the mbarrier alone.
+      // The code stage is released only after the proxy fence below: the next TMA into it
+      // is an async-proxy write, which is not ordered after these generic-proxy reads by the
+      // mbarrier alone.
       uint4 o[8];
       o[0] = deq8(n0.x, s2, b2);
       o[1] = deq8(n0.y, s2, b2);
@@ -408,16 +444,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       o[5] = deq8(n1.y, s2, b2);
       o[6] = deq8(n1.z, s2, b2);
       o[7] = deq8(n1.w, s2, b2);
-      if (!mbar_wait(bar(b_ab_empty(s)), ph ^ 1u, abort_flag, status)) break;
-      const uint32_t a_row = sbase + OFF_A + s * A_BYTES + a_off;
+      if (!mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status)) break;
+      const uint32_t a_row = sbase + C::OFF_A + sa * A_BYTES + a_off;
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row + (uint32_t)((c ^ (rr & 7)) << 4)),
                      "r"(o[c].x), "r"(o[c].y), "r"(o[c].z), "r"(o[c].w)
                      : "memory");
-      fence_proxy_async_smem();  // orders the A writes and the nibble reads before async-proxy use
-      mbar_arrive(bar(b_a_full(s)));
-      mbar_arrive(bar(b_nib_empty(s)));
+      fence_proxy_async_smem();  // orders the A writes and the code reads before async-proxy use
+      mbar_arrive(bar(C::ab_full(sa)));
+      mbar_arrive(bar(C::nib_empty(sn)));
       cur = nxt;
       s_cur = s_nxt;
       b_cur = b_nxt;
@@ -432,6 +468,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) tmem_dealloc(tmem_base, kTmemCols);
 }
 
+// Split-K epilogue: y[row(p), f] = bf16(sum over slices ks of acc[ks, p, f]), added in slice
+// order, for every valid sorted position p (rows with an invalid index keep the zeros the
+// route step wrote).  One thread per 8 consecutive outputs.
+__global__ void __launch_bounds__(256) splitk_finalize(const GemmArgs p) {
+  int64_t n_valid = __ldg(p.offsets + p.E);
+  n_valid = n_valid < 0 ? 0 : (n_valid > p.n ? p.n : n_valid);
+  const int oct = p.F / 8;
+  const int64_t n_oct = n_valid * oct;
+  const int64_t plane = p.n * (int64_t)p.F;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_oct; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t pos = i / oct;
+    const int f = (int)(i - pos * oct) * 8;
+    const float4* a = reinterpret_cast<const float4*>(p.acc + pos * p.F + f);
+    float4 s0 = __ldg(a), s1 = __ldg(a + 1);
+    for (int ks = 1; ks < p.ksplit; ++ks) {
+      const float4* b = reinterpret_cast<const float4*>(p.acc + ks * plane + pos * p.F + f);
+      const float4 t0 = __ldg(b), t1 = __ldg(b + 1);
+      s0.x += t0.x; s0.y += t0.y; s0.z += t0.z; s0.w += t0.w;
+      s1.x += t1.x; s1.y += t1.y; s1.z += t1.z; s1.w += t1.w;
+    }
+    const int row = p.perm ? __ldg(p.perm + pos) : (int)pos;
+    uint4 o;
+    o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s0.x)) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s0.y)) << 16);
+    o.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s0.z)) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s0.w)) << 16);
+    o.z = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s1.x)) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s1.y)) << 16);
+    o.w = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s1.z)) |
+          ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s1.w)) << 16);
+    *reinterpret_cast<uint4*>(p.y + (int64_t)row * p.F + f) = o;
+  }
+}
+
 struct DeviceInfo {
   int sms = 0;
   bool configured = false;
@@ -439,9 +509,15 @@ struct DeviceInfo {
 
 DeviceInfo g_dev[64];
 
+template <class C>
+cudaError_t configure() {
+  return cudaFuncSetAttribute(gemm_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DYN);
+}
+
 }  // namespace
 
-cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
+cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
+  *launched = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -450,8 +526,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
   if (!di.configured) {
     e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_DYN);
-    if (e != cudaSuccess) return e;
+    if ((e = configure<CfgWide>()) != cudaSuccess) return e;
+    if ((e = configure<CfgNarrow>()) != cudaSuccess) return e;
     di.configured = true;
   }
 
@@ -475,8 +551,22 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s) {
                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  gemm_tc_kernel<<<di.sms, kThreads, SMEM_DYN, s>>>(map_wq, a);
-  return cudaGetLastError();
+  if (a.chunk_rows == kChunkRowsNarrow)
+    gemm_tc_kernel<CfgNarrow><<<di.sms, kThreads, CfgNarrow::SMEM_DYN, s>>>(map_wq, a);
+  else
+    gemm_tc_kernel<CfgWide><<<di.sms, kThreads, CfgWide::SMEM_DYN, s>>>(map_wq, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  *launched = 1;
+  if (a.ksplit > 1) {
+    const int64_t n_oct = a.n * (a.F / 8);
+    const int64_t blocks = (n_oct + 255) / 256;
+    splitk_finalize<<<(unsigned)(blocks < 4 * di.sms ? blocks : 4 * di.sms), 256, 0, s>>>(a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    *launched = 2;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace gqmm

@@ -17,6 +17,9 @@ namespace gqmm {
 //   offsets         int32 [E + 1]                expert segment starts
 //   tile_hist       uint32 [(E + 1) * n_tiles]   per-tile key counts, key-major
 //   chunks          Chunk [max_chunks]           work list of (expert, row range)
+//   acc             float [ksplit, n, F]         split-K partial sums, one plane per K slice
+//                                                (only when split-K can be chosen for these
+//                                                sizes; every entry read is written first)
 // ------------------------------------------------------------------------------------------
 struct WsHeader {
   uint32_t status;    // GQMM_STATUS_* bits, OR-ed by kernels, cleared by gqmm_device_status
@@ -28,27 +31,65 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 struct Chunk {
   int32_t expert;  // expert id
   int32_t start;   // first sorted position of the chunk
-  int32_t rows;    // rows in the chunk, 1..kChunkMaxRows
+  int32_t rows;    // rows in the chunk, 1..chunk_max_rows
   int32_t pad;
 };
 
 constexpr int kRouteThreads = 256;            // threads per route-sort block
 constexpr int kRouteTile = 2048;              // routing entries per route-sort block
-constexpr int kChunkMaxRows = 256;            // tokens per work unit = largest UMMA N
+constexpr int kChunkRowsWide = 256;           // tokens per work unit, wide GEMM variant
+constexpr int kChunkRowsNarrow = 32;          // tokens per work unit, narrow GEMM variant
 constexpr int kMaxExperts = GQMM_MAX_EXPERTS;
+constexpr int kUnitRows = 256;                // weight rows per work unit (two 128-row tiles)
+constexpr int kTargetUnits = 2 * 152;         // split K until about this many units exist
+constexpr int64_t kSplitMaxRows = 1024;       // split K only for decode-sized calls: the fp32
+                                              // partial sums cost n*F*4 bytes per slice
+
+// How a call is split into work units.  A pure function of the sizes, so the workspace size
+// (which depends on it) is known before any device work.
+struct UnitShape {
+  int chunk_rows;  // kChunkRowsWide or kChunkRowsNarrow
+  int ksplit;      // K slices per (chunk, F pair); 1 = no split
+};
+
+// K slices chosen before the per-H cap (which only lowers it): ceil(kTargetUnits / units) for
+// decode-sized calls with too few units, at most 16.
+inline int ksplit_bound(int64_t n, int F, int E, int* chunk_rows_out) {
+  const int64_t busy = n < E ? n : E;                  // experts that can have rows
+  const int64_t avg = busy > 0 ? (n + busy - 1) / busy : 0;
+  const int rows = avg <= kChunkRowsNarrow ? kChunkRowsNarrow : kChunkRowsWide;
+  if (chunk_rows_out) *chunk_rows_out = rows;
+  const int64_t units = (busy + n / rows) * ((F + kUnitRows - 1) / kUnitRows);  // upper bound
+  if (n > kSplitMaxRows || units <= 0 || units >= kTargetUnits) return 1;
+  const int64_t ks = (kTargetUnits + units - 1) / units;
+  return (int)(ks < 16 ? ks : 16);
+}
+
+inline UnitShape unit_shape(int64_t n, int H, int F, int E) {
+  UnitShape u;
+  const int ks = ksplit_bound(n, F, E, &u.chunk_rows);
+  const int G = H / 64;
+  const int ks_max = G / 4 > 1 ? (G / 4 < 16 ? G / 4 : 16) : 1;  // keep >= 4 K blocks per slice
+  u.ksplit = ks < ks_max ? ks : ks_max;
+  return u;
+}
 
 struct WsLayout {
-  size_t perm, offsets, tile_hist, chunks, total;
+  size_t perm, offsets, tile_hist, chunks, acc, total;
   int64_t n_tiles, max_chunks;
+  bool has_acc;
 };
 
 inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-inline WsLayout ws_layout(int64_t n, int E) {
+// allow_split = false lays out a workspace for calls that never split K (no sum buffer).
+inline WsLayout ws_layout(int64_t n, int F, int E, bool allow_split = true) {
   WsLayout L;
   L.n_tiles = (n + kRouteTile - 1) / kRouteTile;
   if (L.n_tiles < 1) L.n_tiles = 1;
-  L.max_chunks = E + n / kChunkMaxRows + 1;
+  L.max_chunks = E + n / kChunkRowsNarrow + 1;
+  const int ks = allow_split ? ksplit_bound(n, F, E, nullptr) : 1;
+  L.has_acc = ks > 1;
   size_t off = sizeof(WsHeader);
   L.perm = off;
   off = align256(off + sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
@@ -58,12 +99,20 @@ inline WsLayout ws_layout(int64_t n, int E) {
   off = align256(off + sizeof(uint32_t) * (size_t)(E + 1) * (size_t)L.n_tiles);
   L.chunks = off;
   off = align256(off + sizeof(Chunk) * (size_t)L.max_chunks);
+  L.acc = off;
+  if (L.has_acc) off = align256(off + sizeof(float) * (size_t)ks * (size_t)n * (size_t)F);
   L.total = off;
   return L;
 }
 
 // Records a printf-style message as the calling thread's gqmm_last_error() and returns code.
 int report_error(int code, const char* fmt, ...);
+
+// gqmm_gather_qmm with a switch: allow_split = false never splits K, so its workspace needs no
+// split-K sum buffer (ws_layout(n, F, E, false)).
+int gather_qmm_impl(const void* x, const void* wq, const void* scales, const void* biases, const uint32_t* idx,
+                    int64_t T, int A, int H, int F, int E, int group_size, int bits, int sorted, void* y, void* ws,
+                    size_t ws_bytes, cudaStream_t s, bool allow_split);
 
 // ------------------------------------------------------------------------------------------
 // Kernel launchers (defined in the .cu files).  All return cudaError_t of the launch.
@@ -84,6 +133,7 @@ struct RouteArgs {
   __nv_bfloat16* y;     // rows with an invalid index are zero-filled here (may be NULL)
   int F;
   int64_t n_tiles;
+  int chunk_rows;       // longest chunk of the work list
 };
 // Unsorted: histogram kernel + scan/scatter/plan kernel.  Sorted or dense: one plan kernel.
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int* kernels_launched);
@@ -98,9 +148,15 @@ struct GemmArgs {
   const int32_t* perm;  // NULL: sorted position == flat row
   const Chunk* chunks;
   WsHeader* header;
+  float* acc;           // [ksplit, n, F] split-K partial sums (ksplit > 1)
+  const int32_t* offsets;  // [E + 1]; offsets[E] = valid sorted positions (split-K finalize)
   int H, F, E;
+  int chunk_rows;       // kChunkRowsWide or kChunkRowsNarrow: selects the kernel variant
+  int ksplit;
 };
-cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s);
+// Launches the grouped GEMM (and, when ksplit > 1, the kernel that turns the partial sums into
+// y).  *launched gets the number of kernels enqueued.
+cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched);
 
 cudaError_t launch_gemm_simt(const __nv_bfloat16* x, const uint8_t* wq,
                              const __nv_bfloat16* scales, const __nv_bfloat16* biases,
@@ -198,14 +254,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
-}
-
-// Prefetch a 2-D TMA box into L2 (no shared-memory destination, no completion signal).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t c0, int32_t c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1)
-               : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

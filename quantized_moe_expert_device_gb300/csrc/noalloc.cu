@@ -49,22 +49,33 @@ int scratch_for_current_device(void** out) {
 extern "C" int gqmm_gather_qmm_noalloc(const void* x, const void* wq, const void* scales, const void* biases,
                                        const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size,
                                        int bits, int sorted, void* y, gqmm_stream_t stream) {
-  if (T >= 1 && A >= 1) {
-    const size_t need = gqmm_workspace_size(T * (int64_t)A, F, E);
-    if (need > kScratchBytes)
-      return gqmm::report_error(GQMM_ERR_WORKSPACE,
-                                "gqmm_gather_qmm_noalloc: T*A=%lld rows with E=%d need %zu bytes of scratch, "
-                                "more than the built-in %zu bytes (GQMM_NOALLOC_SCRATCH_BYTES); "
-                                "use gqmm_gather_qmm with a caller workspace",
-                                (long long)(T * (int64_t)A), E, need, kScratchBytes);
+  // Split K (used when a call has too few work units for the GPU) needs partial-sum planes
+  // in the scratch; it is used only when those fit too, else the call runs unsplit.
+  // Sizes the C ABI rejects anyway are passed through for gather_qmm_impl to report.
+  bool allow_split = true;
+  const bool sizes_ok = T >= 1 && A >= 1 && T * (int64_t)A <= 2147483647LL && F > 0 && E >= 1 &&
+                        E <= GQMM_MAX_EXPERTS;
+  if (sizes_ok) {
+    const int64_t n = T * (int64_t)A;
+    if (gqmm::ws_layout(n, F, E, true).total > kScratchBytes) {
+      allow_split = false;
+      const size_t need = gqmm::ws_layout(n, F, E, false).total;
+      if (need > kScratchBytes)
+        return gqmm::report_error(GQMM_ERR_WORKSPACE,
+                                  "gqmm_gather_qmm_noalloc: T*A=%lld rows with E=%d need %zu bytes of scratch, "
+                                  "more than the built-in %zu bytes (GQMM_NOALLOC_SCRATCH_BYTES); "
+                                  "use gqmm_gather_qmm with a caller workspace",
+                                  (long long)n, E, need, kScratchBytes);
+    }
   }
   void* ws = nullptr;
   int rc = scratch_for_current_device(&ws);
   if (rc != GQMM_OK) return rc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // The status word at the start of the scratch is cleared on every call: nothing reads it
   // back through this entry point, and it must not carry bits from earlier calls.
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(gqmm::WsHeader), reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(gqmm::WsHeader), s);
   if (e != cudaSuccess) return gqmm::report_error(GQMM_ERR_CUDA, "gqmm_gather_qmm_noalloc: clearing scratch failed");
-  return gqmm_gather_qmm(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, sorted, y, ws, kScratchBytes,
-                         stream);
+  return gqmm::gather_qmm_impl(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, sorted, y, ws,
+                               kScratchBytes, s, allow_split);
 }

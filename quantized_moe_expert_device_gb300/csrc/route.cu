@@ -53,22 +53,22 @@ __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* warp
 }
 
 // Writes the chunk list for experts [0, E) whose segment e is [seg_start[e], seg_start[e] +
-// seg_len[e]).  A segment longer than kChunkMaxRows is split into equal chunks (sizes differ
-// by at most one row) so no chunk leaves most of an MMA tile empty.  Called by one block.
+// seg_len[e]).  A segment longer than max_rows is split into equal chunks (sizes differ by at
+// most one row) so no chunk leaves most of an MMA tile empty.  Called by one block.
 template <int NT>
-__device__ void write_plan(const int32_t* seg_start, const int32_t* seg_len, int E, Chunk* chunks,
+__device__ void write_plan(const int32_t* seg_start, const int32_t* seg_len, int E, int max_rows, Chunk* chunks,
                            WsHeader* header, int64_t* warp_tot) {
   // Each thread owns a contiguous run of experts so one scan orders all chunks by expert.
   const int per = (E + NT - 1) / NT;
   const int e0 = threadIdx.x * per;
   const int e1 = min(E, e0 + per);
   int64_t my = 0;
-  for (int e = e0; e < e1; ++e) my += (seg_len[e] + kChunkMaxRows - 1) / kChunkMaxRows;
+  for (int e = e0; e < e1; ++e) my += (seg_len[e] + max_rows - 1) / max_rows;
   int64_t total;
   int64_t at = block_exclusive_scan<NT>(my, warp_tot, &total);
   for (int e = e0; e < e1; ++e) {
     const int len = seg_len[e];
-    const int nch = (len + kChunkMaxRows - 1) / kChunkMaxRows;
+    const int nch = (len + max_rows - 1) / max_rows;
     if (nch == 0) continue;
     const int base = len / nch, rem = len % nch;
     for (int k = 0; k < nch; ++k) {
@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter(RouteArgs a) {
   }
 
   // 3. work list (block 0)
-  if (tile == 0 && a.chunks != nullptr) write_plan<kRouteThreads>(seg_start, seg_len, E, a.chunks, a.header, warp_tot);
+  if (tile == 0 && a.chunks != nullptr) write_plan<kRouteThreads>(seg_start, seg_len, E, a.chunk_rows, a.chunks, a.header, warp_tot);
 }
 
 constexpr int kPlanThreads = 1024;
@@ -216,6 +216,7 @@ __global__ void __launch_bounds__(kPlanThreads) route_plan_sorted(RouteArgs a) {
     if (bits) atomicOr(&a.header->status, bits);
   }
   if (unsorted) {  // the promise is broken: no segments can be trusted, compute nothing
+    for (int e = threadIdx.x; e <= E; e += kPlanThreads) a.offsets[e] = 0;
     if (threadIdx.x == 0) a.header->n_chunks = 0;
     return;
   }
@@ -238,7 +239,7 @@ __global__ void __launch_bounds__(kPlanThreads) route_plan_sorted(RouteArgs a) {
   for (int e = threadIdx.x; e < E; e += kPlanThreads) seg_len[e] = seg_start[e + 1] - seg_start[e];
   for (int e = threadIdx.x; e <= E; e += kPlanThreads) a.offsets[e] = seg_start[e];
   __syncthreads();
-  if (a.chunks != nullptr) write_plan<kPlanThreads>(seg_start, seg_len, E, a.chunks, a.header, warp_tot);
+  if (a.chunks != nullptr) write_plan<kPlanThreads>(seg_start, seg_len, E, a.chunk_rows, a.chunks, a.header, warp_tot);
 }
 
 }  // namespace

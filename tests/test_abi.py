@@ -49,10 +49,14 @@ def test_binding_covers_the_boundary():
 def test_workspace_size_is_positive_and_monotone(lib):
     import quantized_moe_expert_device_gb300 as g
 
-    a = g.gqmm_workspace_size(32, 128, 8)
+    # above the split-K size limit the workspace grows with the number of rows
+    a = g.gqmm_workspace_size(2048, 768, 64)
     b = g.gqmm_workspace_size(16384, 768, 64)
     assert 0 < a < b
     assert a % 256 == 0 and b % 256 == 0
+    # a decode-sized call (9 work units at most) has room for 16 split-K float32 planes
+    c = g.gqmm_workspace_size(32, 128, 8)
+    assert c % 256 == 0 and c >= 16 * 32 * 128 * 4
     assert g.gqmm_workspace_size(10, 128, 0) == 0
     assert g.gqmm_workspace_size(10, 128, 4096) == 0
 

@@ -163,8 +163,9 @@ def test_workspace_reuse_across_shapes_and_calls():
 
     E, F, H = 8, 256, 512
     host_w, dev_w = _weights(E, F, H)
-    ws = g.new_workspace(4096, F, E)
-    for n in (1000, 17, 4096, 256):
+    shapes = (1000, 17, 4096, 256)
+    ws = g.new_workspace(list(shapes), F, E)
+    for n in shapes:
         idx = np.random.default_rng(n).integers(0, E, size=n, dtype=np.uint32)
         x = wl.normal_bf16((n, H), n)
         y = g.gqmm_gather_qmm(x.cuda(), *dev_w, to_dev_idx(idx), ws=ws)
@@ -196,3 +197,31 @@ def test_repeated_calls_many_units_per_cta_match_oracle_every_time():
         else:
             assert torch.equal(y, first), f"rep {rep} differs from rep 0"
     assert g.gqmm_device_status(ws) == 0
+
+
+def test_dispatch_coverage_every_variant_runs_and_matches():
+    """Each internal variant (wide and narrow GEMM, split-K, the three routing paths) is
+    exercised and checked here, in the manner of the pages' coverage check (mlx PR #4023:
+    log each dispatched kernel while running the suite, count the distinct ones)."""
+    import quantized_moe_expert_device_gb300 as g
+
+    before = {k: g.dispatch_count(k) for k in g.VARIANTS}
+    E, F, H = 8, 512, 1024
+    host_w, dev_w = _weights(E, F, H)
+    cases = [
+        (wl.idx_uniform(512, 8, E), False),            # 512 rows/expert: wide, no split
+        (wl.idx_uniform(4, 2, E), False),              # 1 row/expert: narrow + split-K
+        (np.sort(wl.idx_uniform(64, 4, E).reshape(-1)).reshape(64, 4), True),  # caller-sorted
+    ]
+    for idx, srt in cases:
+        x = wl.normal_bf16(idx.shape + (H,), wl.SEED_X)
+        y, y_ref, status = _run(x, idx, E, host_w, dev_w, sorted_indices=srt)
+        assert status == 0
+        assert_parity(y.reshape(-1, F), y_ref, f"coverage {idx.shape} sorted={srt}")
+    host1, dev1 = _weights(1, F, H)
+    x = wl.normal_bf16((3, H), wl.SEED_X)
+    yd, yd_ref, _ = _run(x, None, 1, host1, dev1)   # dense decode: narrow + split-K
+    assert_parity(yd, yd_ref, "coverage dense")
+    after = {k: g.dispatch_count(k) for k in g.VARIANTS}
+    for k in g.VARIANTS:
+        assert after[k] > before[k], f"variant {k} never dispatched"
