@@ -149,9 +149,15 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   ra.F = F;
   ra.n_tiles = L.n_tiles;
   ra.chunk_rows = shape.chunk_rows;
+  ra.n_fpairs = (F + kUnitRows - 1) / kUnitRows;
+  ra.ks_cap = L.has_acc ? shape.ksplit : 1;
+  int sms = 0;
+  cudaError_t e = device_sm_count(&sms);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+  ra.sms = sms;
   const bool permuted = idx != nullptr && !sorted;
   int launched = 0;
-  cudaError_t e = launch_route(ra, s, &launched);
+  e = launch_route(ra, s, &launched);
   g_launches.fetch_add(launched);
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
   const int route_variant = idx == nullptr ? GQMM_VARIANT_ROUTE_DENSE
@@ -172,10 +178,9 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   ga.F = F;
   ga.E = E;
   ga.chunk_rows = shape.chunk_rows;
-  ga.ksplit = shape.ksplit;
+  ga.ks_cap = ra.ks_cap;
   ga.acc = L.has_acc ? reinterpret_cast<float*>(w + L.acc) : nullptr;
   ga.offsets = ra.offsets;
-  if (shape.ksplit > 1 && !L.has_acc) return fail(GQMM_ERR_WORKSPACE, "internal: split-K without a buffer");
   size_t slot = 0;
   const bool timed = timer_begin(s, &slot);
   int gemm_launched = 0;
@@ -184,13 +189,13 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   g_launches.fetch_add(gemm_launched);
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "grouped GEMM launch: %s", cudaGetErrorString(e));
   count_variant(shape.chunk_rows == kChunkRowsNarrow ? GQMM_VARIANT_GEMM_NARROW : GQMM_VARIANT_GEMM_TC);
-  if (shape.ksplit > 1) count_variant(GQMM_VARIANT_SPLIT_K);
+  if (ga.ks_cap > 1) count_variant(GQMM_VARIANT_SPLIT_K);
   if (log_dispatch())
-    std::fprintf(stderr, "[gqmm] gather_qmm n=%lld H=%d F=%d E=%d route=%s gemm=%s ksplit=%d\n", (long long)n, H,
+    std::fprintf(stderr, "[gqmm] gather_qmm n=%lld H=%d F=%d E=%d route=%s gemm=%s ks_cap=%d\n", (long long)n, H,
                  F, E,
                  route_variant == GQMM_VARIANT_ROUTE_DENSE ? "dense"
                  : route_variant == GQMM_VARIANT_ROUTE_SORTED ? "sorted" : "unsorted",
-                 shape.chunk_rows == kChunkRowsNarrow ? "narrow" : "wide", shape.ksplit);
+                 shape.chunk_rows == kChunkRowsNarrow ? "narrow" : "wide", ga.ks_cap);
   return ok();
 }
 
@@ -246,6 +251,9 @@ int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* perm, int32_
   a.y = nullptr;
   a.F = 0;
   a.n_tiles = L.n_tiles;
+  a.n_fpairs = 1;
+  a.ks_cap = 1;
+  a.sms = 1;
   int launched = 0;
   cudaError_t e = launch_route(a, reinterpret_cast<cudaStream_t>(stream), &launched);
   g_launches.fetch_add(launched);

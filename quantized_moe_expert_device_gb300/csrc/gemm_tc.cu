@@ -22,7 +22,7 @@
 // slice stores its fp32 partial sums in its own plane of a workspace buffer, and a second
 // kernel adds the planes in slice order (so results are deterministic) into bf16 y.
 //
-// Per CTA (one per SM, persistent, static round-robin over units), warp roles:
+// Per CTA (one per SM, persistent; units taken from a call-wide counter), warp roles:
 //   warps 0-15  dequant:  two groups of 256 threads take alternate k-blocks; a thread owns one
 //                         of the unit's 256 weight rows: reads its 32 bytes of codes, computes
 //                         w = scale*q + bias in bf16x2 and writes the 64 bf16 in the
@@ -30,7 +30,9 @@
 //   warps 16-23 epilogue: warp 16+e drains TMEM lanes 32(e%4).. of tile e/4: TMEM -> registers
 //                         -> bf16 -> shared transpose -> 16-byte stores to y rows perm[j]
 //                         (or fp32 stores into the slice's plane of the split-K sums)
-//   warp 24     TMA:      one thread streams the unit's 256 x 32-byte code tile per k-block
+//   warp 24     scheduler + TMA: one thread takes the next unit from the call-wide counter,
+//                         pushes it into the CTA's unit queue (read by every other warp) and
+//                         streams the unit's 256 x 32-byte code tile per k-block
 //   warp 25     MMA:      allocates TMEM (two 256-column fp32 accumulators), one thread issues
 //                         tcgen05.mma 128xNx16, four per tile per k-block, commits to mbarriers
 //   warps 26-31 gather:   warps 26+2s and 27+2s own A/x stage s: whenever the stage is free they
@@ -72,6 +74,19 @@ constexpr uint32_t kTmemCols = 512;      // NT accumulators of 256 fp32 columns
 static_assert(kGatherWarp0 + 2 * kAbStages == kThreads / 32, "warp roles fill the block");
 static_assert(kDeqGroup * kDeqGroups == kEpiWarp0 * 32, "dequant warps");
 
+// A work unit as the scheduler hands it to the CTA's roles (one entry of the unit queue), or
+// the end of the work (valid == 0).
+struct UnitEntry {
+  int expert, start, rows;  // chunk: expert id, first sorted position, rows
+  int f0;                   // first weight row (output column) of the unit's 256
+  int kb0, kb1;             // k-blocks [kb0, kb1) of the unit's K slice
+  int ks;                   // K slice index when K is split, else -1
+  int valid;
+};
+constexpr int kUnitQ = 8;  // queue depth: how far the scheduler may run ahead of the epilogue
+constexpr int kUnitConsumerWarps = kEpiWarp0 + kEpiWarps + 2 * kAbStages + 1;  // dequant, epilogue, gather, MMA
+static_assert(kUnitConsumerWarps == 31, "every warp but the scheduler's pops each unit");
+
 template <int NMAX_, int NIB_STAGES_>
 struct Cfg {
   static constexpr int NMAX = NMAX_;              // rows per chunk = largest UMMA N
@@ -82,9 +97,10 @@ struct Cfg {
   static constexpr int OFF_NIB = OFF_B + kAbStages * B_BYTES;
   static constexpr int OFF_EPI = OFF_NIB + NIB_STAGES * NIB_BYTES;
   static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * EPI_WARP_BYTES;
-  static constexpr int NUM_BARS = 2 * NIB_STAGES + 2 * kAbStages + 3;
+  static constexpr int NUM_BARS = 2 * NIB_STAGES + 2 * kAbStages + 3 + 2 * kUnitQ;
   static constexpr int OFF_MISC = OFF_BAR + ((NUM_BARS * 8 + 127) / 128) * 128;
-  static constexpr int SMEM_DYN = OFF_MISC + 16 + 1024;  // room to align the base to 1024 bytes
+  static constexpr int OFF_UQ = OFF_MISC + 16;
+  static constexpr int SMEM_DYN = OFF_UQ + kUnitQ * 32 + 1024;  // room to align the base to 1024 bytes
   static_assert(SMEM_DYN <= 232448, "fits the 227 KB opt-in shared memory of one CTA");
   static_assert(B_BYTES % 1024 == 0, "x tiles stay 1024-byte aligned");
   // barrier slots
@@ -99,27 +115,27 @@ struct Cfg {
   __device__ static int tmem_full() { return 2 * NIB_STAGES + 2 * kAbStages; }
   __device__ static int tmem_empty() { return 2 * NIB_STAGES + 2 * kAbStages + 1; }
   __device__ static int unwind() { return 2 * NIB_STAGES + 2 * kAbStages + 2; }
+  __device__ static int uq_full(int q) { return 2 * NIB_STAGES + 2 * kAbStages + 3 + q; }
+  __device__ static int uq_empty(int q) { return 2 * NIB_STAGES + 2 * kAbStages + 3 + kUnitQ + q; }
 };
 using CfgWide = Cfg<kChunkRowsWide, 3>;
 using CfgNarrow = Cfg<kChunkRowsNarrow, 13>;
 
-struct Unit {
-  int expert, start, rows, f0, kb0, kb1;
-};
-
-__device__ __forceinline__ Unit decode_unit(const Chunk* chunks, int u, int n_fpairs, int ksplit, int num_kb) {
+__device__ __forceinline__ UnitEntry decode_unit(const Chunk* chunks, int u, int n_fpairs, int ksplit, int num_kb) {
   const int ks = u % ksplit;
   const int t = u / ksplit;
   const int c = t / n_fpairs;
   const int fp = t - c * n_fpairs;
   const int4 ch = __ldg(reinterpret_cast<const int4*>(chunks) + c);
-  Unit U;
+  UnitEntry U;
   U.expert = ch.x;
   U.start = ch.y;
   U.rows = ch.z;
   U.f0 = fp * UM;
   U.kb0 = (int)((int64_t)num_kb * ks / ksplit);
   U.kb1 = (int)((int64_t)num_kb * (ks + 1) / ksplit);
+  U.ks = ksplit > 1 ? ks : -1;
+  U.valid = 1;
   return U;
 }
 
@@ -161,6 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile UnitEntry* uq = reinterpret_cast<volatile UnitEntry*>(smem + C::OFF_UQ);
   uint32_t* status = &p.header->status;
   auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
 
@@ -174,6 +191,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kAbStages; ++s) {
       mbar_init(bar(C::ab_full(s)), kDeqGroup + 64);  // dequant group + both gather warps' lanes
       mbar_init(bar(C::ab_empty(s)), 1);
+    }
+    for (int q = 0; q < kUnitQ; ++q) {
+      mbar_init(bar(C::uq_full(q)), 1);
+      mbar_init(bar(C::uq_empty(q)), kUnitConsumerWarps);
     }
     mbar_init(bar(C::tmem_full()), 1);
     mbar_init(bar(C::tmem_empty()), kEpiWarps * 32);
@@ -194,19 +215,65 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int H = p.H, F = p.F;
   const int G = H / BK;
   const int num_kb = G;
-  const int ksplit = p.ksplit;
-  const int n_fpairs = (F + UM - 1) / UM;
-  const int n_units = p.header->n_chunks * n_fpairs * ksplit;
+
+  // Unit queue: the scheduler (TMA thread) pushes decoded units; every consumer warp pops
+  // each entry in order and releases it once its lanes hold a copy.
+  auto pop = [&](uint32_t qi, UnitEntry& U) -> bool {
+    const uint32_t slot = qi % kUnitQ;
+    if (!mbar_wait(bar(C::uq_full(slot)), (qi / kUnitQ) & 1u, abort_flag, status)) return false;
+    U.expert = uq[slot].expert;
+    U.start = uq[slot].start;
+    U.rows = uq[slot].rows;
+    U.f0 = uq[slot].f0;
+    U.kb0 = uq[slot].kb0;
+    U.kb1 = uq[slot].kb1;
+    U.ks = uq[slot].ks;
+    U.valid = uq[slot].valid;
+    return true;
+  };
+  auto release_warp = [&](uint32_t qi) {  // all 32 lanes of the warp call this
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(C::uq_empty(qi % kUnitQ)));
+  };
 
   if (warp == kTmaWarp) {
-    // ---------------------------------------------------------------- TMA producer (codes)
-    // (An L2 prefetch of the tile several k-blocks ahead was measured: no gain with three
-    // stages, a loss with thirteen, so there is none.)
+    // ---------------------------------------------------------------- scheduler + TMA (codes)
+    // Units are taken from the call-wide counter one at a time, largest first (the plan
+    // orders chunks by size), so CTAs that finish early take more.  (An L2 prefetch of the
+    // code tiles several k-blocks ahead was measured: no gain with three stages, a loss with
+    // thirteen, so there is none.)
     if (lane == 0) {
-      uint32_t itn = 0;
+      const int ksplit = p.header->ksplit;
+      const int n_fpairs = (F + UM - 1) / UM;
+      const int n_units = p.header->n_chunks * n_fpairs * ksplit;
+      uint32_t itn = 0, qi = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-        const Unit U = decode_unit(p.chunks, u, n_fpairs, ksplit, num_kb);
+      for (;;) {
+        const uint32_t slot = qi % kUnitQ;
+        if (!mbar_wait(bar(C::uq_empty(slot)), ((qi / kUnitQ) & 1u) ^ 1u, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        const int u = atomicAdd(&p.header->next_unit, 1);
+        UnitEntry U;
+        U.valid = u < n_units ? 1 : 0;
+        if (U.valid) {
+          U = decode_unit(p.chunks, u, n_fpairs, ksplit, num_kb);
+        } else {
+          U.expert = U.start = U.rows = U.f0 = U.kb0 = U.kb1 = 0;
+          U.ks = -1;
+        }
+        uq[slot].expert = U.expert;
+        uq[slot].start = U.start;
+        uq[slot].rows = U.rows;
+        uq[slot].f0 = U.f0;
+        uq[slot].kb0 = U.kb0;
+        uq[slot].kb1 = U.kb1;
+        uq[slot].ks = U.ks;
+        uq[slot].valid = U.valid;
+        mbar_arrive(bar(C::uq_full(slot)));  // release: the entry is visible to the waiters
+        ++qi;
+        if (!U.valid) break;
         const int row0 = U.expert * F + U.f0;
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
           const uint32_t s = itn % NIB_STAGES, ph = (itn / NIB_STAGES) & 1u;
@@ -218,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_2d(sbase + C::OFF_NIB + s * NIB_BYTES, &tmap_wq, bar(C::nib_full(s)), kb * (BK / 2), row0);
           ++itn;
         }
+        if (!ok) break;
       }
       if (!ok) {  // unwinding: let the copies already issued land before the CTA exits
         const uint32_t first = itn > NIB_STAGES ? itn - NIB_STAGES : 0;
@@ -228,10 +296,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, lu = 0;
+      uint32_t it = 0, lu = 0, qi = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x, ++lu) {
-        const Unit U = decode_unit(p.chunks, u, n_fpairs, ksplit, num_kb);
+      for (;; ++lu) {
+        UnitEntry U;
+        if (!pop(qi, U)) break;
+        mbar_arrive(bar(C::uq_empty(qi % kUnitQ)));  // the only lane of this role
+        ++qi;
+        if (!U.valid) break;
         const int N = (U.rows + 15) & ~15;
         const uint32_t idesc = umma_idesc_bf16(BM, N);
         if (!mbar_wait(bar(C::tmem_empty()), (lu & 1u) ^ 1u, abort_flag, status)) break;
@@ -274,10 +346,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int cidx = lane & 7;                 // 16-byte chunk of a 128-byte row slice
     const int rlow = 4 * h + (lane >> 3);      // rows 8 q + rlow
     const uint32_t dst_lane = (uint32_t)(rlow * 128 + ((cidx ^ rlow) << 4));
-    uint32_t it = 0;
+    uint32_t it = 0, qi = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < n_units; u += gridDim.x) {
-      const Unit U = decode_unit(p.chunks, u, n_fpairs, ksplit, num_kb);
+    while (ok) {
+      UnitEntry U;
+      if (!pop(qi, U)) break;
+      release_warp(qi);
+      ++qi;
+      if (!U.valid) break;
       int src[Q];
 #pragma unroll
       for (int q = 0; q < Q; ++q) {
@@ -311,19 +387,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = ew & 3;        // TMEM lanes 32 quarter .. 32 quarter + 31 (= warp % 4)
     uint16_t* epi = reinterpret_cast<uint16_t*>(smem + C::OFF_EPI + ew * EPI_WARP_BYTES);
     const uint32_t epi_addr = sbase + C::OFF_EPI + ew * EPI_WARP_BYTES;
-    uint32_t lu = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++lu) {
-      const Unit U = decode_unit(p.chunks, u, n_fpairs, ksplit, num_kb);
+    uint32_t lu = 0, qi = 0;
+    for (;; ++lu) {
+      UnitEntry U;
+      if (!pop(qi, U)) break;
+      release_warp(qi);
+      ++qi;
+      if (!U.valid) break;
       const int N = (U.rows + 15) & ~15;
       const bool okl = mbar_wait(bar(C::tmem_full()), lu & 1u, abort_flag, status);
       if (!__all_sync(0xffffffffu, okl)) break;
       tc_fence_after();
       const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(tile * 256);
-      if (ksplit > 1) {
+      if (U.ks >= 0) {
         // partial sums of this K slice into its own plane: thread = weight row f, 16 tokens
         // per TMEM load; a warp's stores for one token are 32 consecutive f (128 bytes)
         const int f = U.f0 + tile * BM + quarter * 32 + lane;
-        float* plane = p.acc + (int64_t)(u % ksplit) * p.n * F;
+        float* plane = p.acc + (int64_t)U.ks * p.n * F;
         for (int c0 = 0; c0 < N; c0 += 16) {
           uint32_t v[16];
           tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
@@ -378,46 +458,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t a_off = (uint32_t)(tile * A_TILE_BYTES + (rr >> 3) * 1024 + (rr & 7) * 128);
     const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(p.scales);
     const uint16_t* bs16 = reinterpret_cast<const uint16_t*>(p.biases);
-    // Flat walk over (unit, k-block); this group processes every second step.  The scale and
-    // bias of the next step it processes are loaded one processed step ahead.
-    struct Step {
-      int u, kb;
-      Unit U;
+    // Flat walk over (unit, k-block) steps in queue order; this group processes every second
+    // step.  The scale and bias of the next step it processes are loaded one step ahead.
+    uint32_t qi = 0;
+    bool ok = true;
+    auto next_unit = [&](UnitEntry& U) {
+      if (!pop(qi, U)) {
+        ok = false;
+        U.valid = 0;
+      }
+      release_warp(qi);
+      ++qi;
     };
-    auto normalize = [&](Step& st) {  // carry kb past the unit's end into the following units
-      while (st.u < n_units && st.kb >= st.U.kb1) {
-        const int over = st.kb - st.U.kb1;
-        st.u += gridDim.x;
-        if (st.u >= n_units) break;
-        st.U = decode_unit(p.chunks, st.u, n_fpairs, ksplit, num_kb);
-        st.kb = st.U.kb0 + over;
+    // carry kb past the unit's end into the following units
+    auto normalize = [&](UnitEntry& U, int& kb) {
+      while (U.valid && kb >= U.kb1) {
+        const int over = kb - U.kb1;
+        next_unit(U);
+        kb = U.kb0 + over;
       }
     };
-    auto load_sb = [&](const Step& st, uint32_t& sv, uint32_t& bv) {
+    auto load_sb = [&](const UnitEntry& U, int kb, uint32_t& sv, uint32_t& bv) {
       sv = 0;
       bv = 0;
-      if (st.u < n_units && st.U.f0 + r < F) {
-        const int64_t off = ((int64_t)st.U.expert * F + st.U.f0 + r) * G + st.kb;
+      if (U.valid && U.f0 + r < F) {
+        const int64_t off = ((int64_t)U.expert * F + U.f0 + r) * G + kb;
         sv = __ldg(sc16 + off);
         bv = __ldg(bs16 + off);
       }
     };
-    Step cur;
-    cur.u = blockIdx.x;
-    if (cur.u < n_units) {
-      cur.U = decode_unit(p.chunks, cur.u, n_fpairs, ksplit, num_kb);
-      cur.kb = cur.U.kb0 + (int)grp;
-      normalize(cur);
-    }
+    UnitEntry cur;
+    next_unit(cur);
+    int kb_cur = cur.kb0 + (int)grp;
+    normalize(cur, kb_cur);
     uint32_t it = grp;  // global step index of cur
     uint32_t s_cur = 0, b_cur = 0;
-    load_sb(cur, s_cur, b_cur);
-    while (cur.u < n_units) {
-      Step nxt = cur;
-      nxt.kb += kDeqGroups;
-      normalize(nxt);
+    load_sb(cur, kb_cur, s_cur, b_cur);
+    while (ok && cur.valid) {
+      UnitEntry nxt = cur;
+      int kb_nxt = kb_cur + kDeqGroups;
+      normalize(nxt, kb_nxt);
       uint32_t s_nxt, b_nxt;
-      load_sb(nxt, s_nxt, b_nxt);
+      load_sb(nxt, kb_nxt, s_nxt, b_nxt);
       const uint32_t s2 = splat16(s_cur), b2 = splat16(b_cur);
       const uint32_t sn = it % NIB_STAGES, phn = (it / NIB_STAGES) & 1u;
       const uint32_t sa = it % kAbStages, pha = (it / kAbStages) & 1u;
@@ -455,6 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(C::ab_full(sa)));
       mbar_arrive(bar(C::nib_empty(sn)));
       cur = nxt;
+      kb_cur = kb_nxt;
       s_cur = s_nxt;
       b_cur = b_nxt;
       it += kDeqGroups;
@@ -472,6 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // order, for every valid sorted position p (rows with an invalid index keep the zeros the
 // route step wrote).  One thread per 8 consecutive outputs.
 __global__ void __launch_bounds__(256) splitk_finalize(const GemmArgs p) {
+  const int ksplit = p.header->ksplit;  // chosen by the plan step; 1: the GEMM wrote y itself
+  if (ksplit <= 1) return;
   int64_t n_valid = __ldg(p.offsets + p.E);
   n_valid = n_valid < 0 ? 0 : (n_valid > p.n ? p.n : n_valid);
   const int oct = p.F / 8;
@@ -482,7 +567,7 @@ __global__ void __launch_bounds__(256) splitk_finalize(const GemmArgs p) {
     const int f = (int)(i - pos * oct) * 8;
     const float4* a = reinterpret_cast<const float4*>(p.acc + pos * p.F + f);
     float4 s0 = __ldg(a), s1 = __ldg(a + 1);
-    for (int ks = 1; ks < p.ksplit; ++ks) {
+    for (int ks = 1; ks < ksplit; ++ks) {
       const float4* b = reinterpret_cast<const float4*>(p.acc + ks * plane + pos * p.F + f);
       const float4 t0 = __ldg(b), t1 = __ldg(b + 1);
       s0.x += t0.x; s0.y += t0.y; s0.z += t0.z; s0.w += t0.w;
@@ -515,6 +600,20 @@ cudaError_t configure() {
 }
 
 }  // namespace
+
+cudaError_t device_sm_count(int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  DeviceInfo& di = g_dev[dev];
+  if (di.sms == 0) {
+    e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  *sms = di.sms;
+  return cudaSuccess;
+}
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   *launched = 0;
@@ -558,7 +657,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   *launched = 1;
-  if (a.ksplit > 1) {
+  if (a.ks_cap > 1) {
     const int64_t n_oct = a.n * (a.F / 8);
     const int64_t blocks = (n_oct + 255) / 256;
     splitk_finalize<<<(unsigned)(blocks < 4 * di.sms ? blocks : 4 * di.sms), 256, 0, s>>>(a);

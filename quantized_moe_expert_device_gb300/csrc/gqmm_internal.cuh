@@ -24,7 +24,9 @@ namespace gqmm {
 struct WsHeader {
   uint32_t status;    // GQMM_STATUS_* bits, OR-ed by kernels, cleared by gqmm_device_status
   int32_t n_chunks;   // number of valid entries in the chunk list (written by the plan step)
-  int32_t pad[62];
+  int32_t ksplit;     // K slices per (chunk, F pair) chosen by the plan step (1 = no split)
+  int32_t next_unit;  // work counter of the grouped GEMM's schedulers (zeroed by the plan step)
+  int32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
@@ -36,7 +38,10 @@ struct Chunk {
 };
 
 constexpr int kRouteThreads = 256;            // threads per route-sort block
-constexpr int kRouteTile = 2048;              // routing entries per route-sort block
+constexpr int kRouteTileSmall = 1024;         // routing entries per route-sort block, n <= 65536
+constexpr int kRouteTileLarge = 2048;         // and above (keeps the tile table at (E+1)*n/2048)
+inline int route_tile(int64_t n) { return n <= 65536 ? kRouteTileSmall : kRouteTileLarge; }
+constexpr int64_t kSmallMaxN = 4096;          // unsorted calls up to this size: one route block
 constexpr int kChunkRowsWide = 256;           // tokens per work unit, wide GEMM variant
 constexpr int kChunkRowsNarrow = 32;          // tokens per work unit, narrow GEMM variant
 constexpr int kMaxExperts = GQMM_MAX_EXPERTS;
@@ -52,8 +57,10 @@ struct UnitShape {
   int ksplit;      // K slices per (chunk, F pair); 1 = no split
 };
 
-// K slices chosen before the per-H cap (which only lowers it): ceil(kTargetUnits / units) for
-// decode-sized calls with too few units, at most 16.
+// Largest K split a call of these sizes may use before the per-H cap (which only lowers it):
+// for decode-sized calls with fewer than kTargetUnits units, ceil(2 kTargetUnits / units), at
+// most 16; the plan step picks the split within this bound from the actual chunk count.
+// The workspace holds this many partial-sum planes.
 inline int ksplit_bound(int64_t n, int F, int E, int* chunk_rows_out) {
   const int64_t busy = n < E ? n : E;                  // experts that can have rows
   const int64_t avg = busy > 0 ? (n + busy - 1) / busy : 0;
@@ -61,7 +68,7 @@ inline int ksplit_bound(int64_t n, int F, int E, int* chunk_rows_out) {
   if (chunk_rows_out) *chunk_rows_out = rows;
   const int64_t units = (busy + n / rows) * ((F + kUnitRows - 1) / kUnitRows);  // upper bound
   if (n > kSplitMaxRows || units <= 0 || units >= kTargetUnits) return 1;
-  const int64_t ks = (kTargetUnits + units - 1) / units;
+  const int64_t ks = (2 * kTargetUnits + units - 1) / units;
   return (int)(ks < 16 ? ks : 16);
 }
 
@@ -85,7 +92,7 @@ inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 // allow_split = false lays out a workspace for calls that never split K (no sum buffer).
 inline WsLayout ws_layout(int64_t n, int F, int E, bool allow_split = true) {
   WsLayout L;
-  L.n_tiles = (n + kRouteTile - 1) / kRouteTile;
+  L.n_tiles = (n + route_tile(n) - 1) / route_tile(n);
   if (L.n_tiles < 1) L.n_tiles = 1;
   L.max_chunks = E + n / kChunkRowsNarrow + 1;
   const int ks = allow_split ? ksplit_bound(n, F, E, nullptr) : 1;
@@ -134,6 +141,9 @@ struct RouteArgs {
   int F;
   int64_t n_tiles;
   int chunk_rows;       // longest chunk of the work list
+  int n_fpairs;         // 256-row output tiles per expert (work units per chunk and K slice)
+  int ks_cap;           // largest K split the workspace and H allow (1: never split)
+  int sms;              // streaming multiprocessors the grouped GEMM runs on
 };
 // Unsorted: histogram kernel + scan/scatter/plan kernel.  Sorted or dense: one plan kernel.
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int* kernels_launched);
@@ -148,15 +158,17 @@ struct GemmArgs {
   const int32_t* perm;  // NULL: sorted position == flat row
   const Chunk* chunks;
   WsHeader* header;
-  float* acc;           // [ksplit, n, F] split-K partial sums (ksplit > 1)
+  float* acc;           // [ksplit, n, F] split-K partial sums (ks_cap > 1)
   const int32_t* offsets;  // [E + 1]; offsets[E] = valid sorted positions (split-K finalize)
   int H, F, E;
   int chunk_rows;       // kChunkRowsWide or kChunkRowsNarrow: selects the kernel variant
-  int ksplit;
+  int ks_cap;           // > 1: the plan step may split K (header->ksplit) and the finalize runs
 };
-// Launches the grouped GEMM (and, when ksplit > 1, the kernel that turns the partial sums into
+// Launches the grouped GEMM (and, when ks_cap > 1, the kernel that turns the partial sums into
 // y).  *launched gets the number of kernels enqueued.
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched);
+// Streaming multiprocessors of the current device (queried once per device).
+cudaError_t device_sm_count(int* sms);
 
 cudaError_t launch_gemm_simt(const __nv_bfloat16* x, const uint8_t* wq,
                              const __nv_bfloat16* scales, const __nv_bfloat16* biases,

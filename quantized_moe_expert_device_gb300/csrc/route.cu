@@ -6,13 +6,19 @@
 // expert on the device gives every expert one contiguous block of rows for a single grouped
 // GEMM launch.
 //
-// Unsorted idx (two kernels, no host round trip):
-//   1. route_hist:     one block per tile of kRouteTile entries; per-key counts in shared
+// Unsorted idx, small calls (n <= kSmallMaxN, E <= kSmallMaxE): route_small, one block of
+// 1024 threads.  Each warp owns a contiguous range of entries and holds its keys in registers;
+// pass 1 counts keys per warp (warp match, no atomics), one scan over (key, warp) gives every
+// warp its first position per key, and pass 2 ranks the warp's entries in order.  Three block
+// barriers in all, and the index array is read once.
+// Unsorted idx, larger calls (two kernels, no host round trip):
+//   1. route_hist:     one block per tile of TILE entries; per-key counts in shared
 //                      memory (keys >= E are folded into an extra key E) written key-major.
 //   2. route_scatter:  every block scans the key-major table itself (warp-shuffle scan), so
-//                      no block waits on another; then it ranks its tile's entries stably
-//                      (warp match + per-warp counts) and writes perm.  Block 0 also writes
-//                      offsets and the work list.
+//                      no block waits on another; then it ranks its tile's entries stably with
+//                      the same per-warp scheme and writes perm.  Block 0 also writes offsets
+//                      and the work list.
+// The sort is stable: entries of one expert keep their order of flat index.
 // Caller-sorted or dense idx: route_plan_sorted finds segment boundaries by binary search,
 // checks the sorted promise and writes the work list (one kernel).
 #include "gqmm_internal.cuh"
@@ -52,20 +58,53 @@ __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* warp
   return warp_prefix + inc - v;
 }
 
+// K slices per (chunk, F pair) for n_units0 = chunks x F pairs work units on `sms` CTAs:
+// the split (at most ks_cap) that minimises the waves of units per CTA per unit of work,
+// ceil(n_units0 * ks / sms) / ks, taken only when it saves at least a tenth.
+__device__ __forceinline__ int choose_ksplit(int64_t n_units0, int ks_cap, int sms) {
+  if (n_units0 <= 0 || ks_cap <= 1 || sms <= 0) return 1;
+  int best = 1;
+  int64_t best_w = (n_units0 + sms - 1) / sms;
+  for (int ks = 2; ks <= ks_cap; ++ks) {
+    const int64_t w = (n_units0 * ks + sms - 1) / sms;
+    if (w * best * 10 <= best_w * ks * 9) {  // w / ks <= 0.9 * best_w / best
+      best = ks;
+      best_w = w;
+    }
+  }
+  return best;
+}
+
 // Writes the chunk list for experts [0, E) whose segment e is [seg_start[e], seg_start[e] +
 // seg_len[e]).  A segment longer than max_rows is split into equal chunks (sizes differ by at
-// most one row) so no chunk leaves most of an MMA tile empty.  Called by one block.
+// most one row) so no chunk leaves most of an MMA tile empty.  Chunks are stored largest
+// first (a counting sort on the row count; the order among chunks of one size is arbitrary
+// and does not affect any result), so the GEMM's schedulers hand out the big units first.
+// Also writes the header fields the GEMM reads: chunk count, K split, zeroed work counter.
+// Called by one whole block of NT threads.
 template <int NT>
 __device__ void write_plan(const int32_t* seg_start, const int32_t* seg_len, int E, int max_rows, Chunk* chunks,
-                           WsHeader* header, int64_t* warp_tot) {
-  // Each thread owns a contiguous run of experts so one scan orders all chunks by expert.
+                           WsHeader* header, int64_t* warp_tot, int n_fpairs, int ks_cap, int sms) {
+  static_assert(NT >= kChunkRowsWide, "one thread per size bucket");
+  __shared__ int32_t bucket[kChunkRowsWide];  // chunks with max_rows - b rows, then cursors
+  for (int b = threadIdx.x; b < kChunkRowsWide; b += NT) bucket[b] = 0;
+  __syncthreads();
   const int per = (E + NT - 1) / NT;
   const int e0 = threadIdx.x * per;
   const int e1 = min(E, e0 + per);
-  int64_t my = 0;
-  for (int e = e0; e < e1; ++e) my += (seg_len[e] + max_rows - 1) / max_rows;
+  for (int e = e0; e < e1; ++e) {
+    const int len = seg_len[e];
+    const int nch = (len + max_rows - 1) / max_rows;
+    if (nch == 0) continue;
+    const int base = len / nch, rem = len % nch;  // rem chunks of base + 1 rows, the rest base
+    if (rem) atomicAdd(&bucket[max_rows - (base + 1)], rem);
+    if (nch > rem) atomicAdd(&bucket[max_rows - base], nch - rem);
+  }
+  __syncthreads();
   int64_t total;
-  int64_t at = block_exclusive_scan<NT>(my, warp_tot, &total);
+  const int64_t at = block_exclusive_scan<NT>(threadIdx.x < max_rows ? bucket[threadIdx.x] : 0, warp_tot, &total);
+  if (threadIdx.x < max_rows) bucket[threadIdx.x] = (int32_t)at;
+  __syncthreads();
   for (int e = e0; e < e1; ++e) {
     const int len = seg_len[e];
     const int nch = (len + max_rows - 1) / max_rows;
@@ -77,10 +116,14 @@ __device__ void write_plan(const int32_t* seg_start, const int32_t* seg_len, int
       c.start = seg_start[e] + k * base + min(k, rem);
       c.rows = base + (k < rem ? 1 : 0);
       c.pad = 0;
-      chunks[at++] = c;
+      chunks[atomicAdd(&bucket[max_rows - c.rows], 1)] = c;
     }
   }
-  if (threadIdx.x == 0) header->n_chunks = (int32_t)total;
+  if (threadIdx.x == 0) {
+    header->n_chunks = (int32_t)total;
+    header->ksplit = choose_ksplit(total * (int64_t)n_fpairs, ks_cap, sms);
+    header->next_unit = 0;
+  }
 }
 
 __device__ __forceinline__ void zero_row(__nv_bfloat16* y, int64_t row, int F) {
@@ -88,13 +131,159 @@ __device__ __forceinline__ void zero_row(__nv_bfloat16* y, int64_t row, int F) {
   for (int c = 0; c < F / 8; ++c) p[c] = make_uint4(0, 0, 0, 0);
 }
 
+// Per-warp stable ranking over a contiguous range [w_begin, w_end) of entries, S rounds of
+// 32 (S <= MAXS).  Keys (clamped to E; entries past the range get the sentinel E + 1, which
+// is never counted or stored) are loaded once into registers, two 16-bit keys per register
+// when PACK (E + 1 < 65536).
+template <int MAXS, bool PACK>
+struct WarpKeys {
+  static constexpr int R = PACK ? (MAXS + 1) / 2 : MAXS;
+  uint32_t k[R];
+  __device__ __forceinline__ uint32_t get(int j) const {
+    return PACK ? (k[j >> 1] >> ((j & 1) * 16)) & 0xFFFFu : k[j];
+  }
+};
+
+template <int MAXS, bool PACK>
+__device__ __forceinline__ WarpKeys<MAXS, PACK> load_warp_keys(const uint32_t* idx, int64_t w_begin,
+                                                               int64_t w_end, int S, int E, int* bad) {
+  const int lane = threadIdx.x & 31;
+  WarpKeys<MAXS, PACK> K;
+#pragma unroll
+  for (int r = 0; r < WarpKeys<MAXS, PACK>::R; ++r) K.k[r] = 0;
+#pragma unroll
+  for (int j = 0; j < MAXS; ++j) {
+    const int64_t i = w_begin + (int64_t)j * 32 + lane;
+    uint32_t key = (uint32_t)E + 1u;
+    if (j < S && i < w_end) {
+      key = __ldg(idx + i);
+      if (key >= (uint32_t)E) {
+        key = (uint32_t)E;
+        *bad = 1;
+      }
+    }
+    if (PACK)
+      K.k[j >> 1] |= key << ((j & 1) * 16);
+    else
+      K.k[j] = key;
+  }
+  return K;
+}
+
+// Lanes of the warp whose key equals this lane's key, from one ballot per key bit (keys
+// below 2^nbits).  Cheaper than a warp match, which is a slow instruction when many warps
+// of one SM use it.
+__device__ __forceinline__ unsigned warp_peers(uint32_t key, int nbits) {
+  unsigned m = 0xffffffffu;
+  for (int b = 0; b < nbits; ++b) {
+    const uint32_t bit = (key >> b) & 1u;
+    const unsigned bb = __ballot_sync(0xffffffffu, bit != 0u);
+    m &= bit ? bb : ~bb;
+  }
+  return m;
+}
+
+// bits that hold every key including the sentinel E + 1
+__device__ __forceinline__ int key_bits(int E) { return 32 - __clz(E + 1); }
+
+// Pass 1: cnt[key] += entries of this warp with that key (cnt is this warp's private row).
+template <int MAXS, bool PACK>
+__device__ __forceinline__ void warp_count(const WarpKeys<MAXS, PACK>& K, int S, int E, int32_t* cnt) {
+  const int nbits = key_bits(E);
+#pragma unroll
+  for (int j = 0; j < MAXS; ++j) {
+    if (j < S) {
+      const uint32_t key = K.get(j);
+      const unsigned peers = warp_peers(key, nbits);
+      if (key <= (uint32_t)E && (threadIdx.x & 31) == __ffs(peers) - 1) cnt[key] += __popc(peers);
+      __syncwarp();
+    }
+  }
+}
+
+// Pass 2: next[key] holds this warp's next perm position for each key.
+template <int MAXS, bool PACK>
+__device__ __forceinline__ void warp_scatter(const WarpKeys<MAXS, PACK>& K, int S, int E, int64_t w_begin, int32_t* next,
+                                             int32_t* perm, __nv_bfloat16* y, int F) {
+  const int nbits = key_bits(E);
+  const int lane = threadIdx.x & 31;
+  const unsigned lt_mask = (1u << lane) - 1u;
+#pragma unroll
+  for (int j = 0; j < MAXS; ++j) {
+    if (j < S) {
+      const uint32_t key = K.get(j);
+      const unsigned peers = warp_peers(key, nbits);
+      const bool valid = key <= (uint32_t)E;
+      if (valid) {
+        const int64_t i = w_begin + (int64_t)j * 32 + lane;
+        perm[next[key] + __popc(peers & lt_mask)] = (int32_t)i;
+        if (key == (uint32_t)E && y != nullptr) zero_row(y, i, F);
+      }
+      __syncwarp();
+      if (valid && lane == __ffs(peers) - 1) next[key] += __popc(peers);
+      __syncwarp();
+    }
+  }
+}
+
+constexpr int kSmallThreads = 1024;
+constexpr int kSmallWarps = kSmallThreads / 32;
+constexpr int kSmallMaxS = 4;                                   // rounds of 32 per warp
+constexpr int kSmallMaxE = 256;
+static_assert(kSmallMaxN == (int64_t)kSmallWarps * 32 * kSmallMaxS, "small-route capacity");
+
+__global__ void __launch_bounds__(kSmallThreads) route_small(RouteArgs a) {
+  __shared__ int32_t wc[kSmallWarps][kSmallMaxE + 2];  // per-warp counts, then next positions
+  __shared__ int32_t seg_start[kSmallMaxE + 1];
+  __shared__ int32_t seg_len[kSmallMaxE + 1];
+  __shared__ int64_t warp_tot[32];
+  const int E = a.E;
+  const int64_t n = a.n;
+  const int warp = threadIdx.x >> 5;
+  for (int i = threadIdx.x; i < kSmallWarps * (kSmallMaxE + 2); i += kSmallThreads) (&wc[0][0])[i] = 0;
+  // warp ranges: L entries each, a multiple of 32
+  const int64_t L = ((n + kSmallWarps - 1) / kSmallWarps + 31) / 32 * 32;
+  const int S = (int)(L / 32);
+  const int64_t w_begin = (int64_t)warp * L;
+  const int64_t w_end = min(n, w_begin + L);
+  int bad = 0;
+  const WarpKeys<kSmallMaxS, true> K = load_warp_keys<kSmallMaxS, true>(a.idx, w_begin, w_end, S, E, &bad);
+  __syncthreads();
+  warp_count(K, S, E, wc[warp]);
+  bad = __syncthreads_or(bad);
+  // key totals, segment starts (block scan over keys), then per-warp first positions
+  const int key = threadIdx.x;
+  int64_t tot = 0;
+  if (key <= E)
+    for (int w = 0; w < kSmallWarps; ++w) tot += wc[w][key];
+  int64_t total;
+  const int64_t start = block_exclusive_scan<kSmallThreads>(tot, warp_tot, &total);
+  if (key <= E) {
+    seg_start[key] = (int32_t)start;
+    seg_len[key] = (int32_t)tot;
+    int32_t run = (int32_t)start;
+    for (int w = 0; w < kSmallWarps; ++w) {
+      const int32_t c = wc[w][key];
+      wc[w][key] = run;
+      run += c;
+    }
+    a.offsets[key] = (int32_t)start;
+  }
+  if (threadIdx.x == 0 && bad) atomicOr(&a.header->status, GQMM_STATUS_BAD_INDEX);
+  __syncthreads();
+  warp_scatter(K, S, E, w_begin, wc[warp], a.perm, a.y, a.F);
+  if (a.chunks != nullptr) write_plan<kSmallThreads>(seg_start, seg_len, E, a.chunk_rows, a.chunks, a.header, warp_tot,
+                                 a.n_fpairs, a.ks_cap, a.sms);
+}
+
+template <int TILE>
 __global__ void __launch_bounds__(kRouteThreads) route_hist(RouteArgs a) {
   __shared__ uint32_t h[kMaxExperts + 1];
   const int E = a.E;
   for (int k = threadIdx.x; k <= E; k += kRouteThreads) h[k] = 0;
   __syncthreads();
-  const int64_t begin = (int64_t)blockIdx.x * kRouteTile;
-  const int64_t end = min(a.n, begin + kRouteTile);
+  const int64_t begin = (int64_t)blockIdx.x * TILE;
+  const int64_t end = min(a.n, begin + TILE);
   int bad = 0;
   for (int64_t i = begin + threadIdx.x; i < end; i += kRouteThreads) {
     uint32_t key = __ldg(a.idx + i);
@@ -110,16 +299,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_hist(RouteArgs a) {
   if (bad && threadIdx.x == 0) atomicOr(&a.header->status, GQMM_STATUS_BAD_INDEX);
 }
 
+template <int TILE>
 __global__ void __launch_bounds__(kRouteThreads) route_scatter(RouteArgs a) {
   __shared__ int32_t base[kMaxExperts + 1];      // next perm position for each key, this tile
   __shared__ int32_t seg_start[kMaxExperts + 1]; // first perm position of each key
   __shared__ int32_t seg_len[kMaxExperts + 1];   // rows of each key
-  __shared__ int32_t wc[kWarps][kMaxExperts + 2];  // per-warp counts in the current round
+  __shared__ int32_t wc[kWarps][kMaxExperts + 2];  // per-warp counts, then next positions
   __shared__ int64_t warp_tot[32];
 
   const int E = a.E;
   const int tile = blockIdx.x;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int warp = threadIdx.x >> 5;
 
   // 1. key totals over all tiles and this tile's preceding count, one contiguous key run
   //    per thread, then a block scan over keys gives each key's segment start.
@@ -148,45 +338,35 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter(RouteArgs a) {
   }
   for (int w = 0; w < kWarps; ++w)
     for (int k = threadIdx.x; k <= E + 1; k += kRouteThreads) wc[w][k] = 0;
-  __syncthreads();
 
+  // 2. stable scatter: warp w ranks the tile's entries [w * kWarpRange, (w + 1) * kWarpRange)
+  //    in order; the per-warp counts of pass 1 give each warp its first position per key.
+  constexpr int kWarpRange = TILE / kWarps;
+  constexpr int kS = kWarpRange / 32;
+  const int64_t w_begin = (int64_t)tile * TILE + (int64_t)warp * kWarpRange;
+  const int64_t w_end = min(a.n, w_begin + kWarpRange);
+  int bad = 0;  // already reported by route_hist
+  const WarpKeys<kS, false> K = load_warp_keys<kS, false>(a.idx, w_begin, w_end, kS, E, &bad);
+  __syncthreads();
   if (tile == 0) {
     for (int k = threadIdx.x; k <= E; k += kRouteThreads) a.offsets[k] = seg_start[k];
   }
-
-  // 2. stable scatter: rounds of kRouteThreads consecutive entries.  Within a warp the rank
-  //    comes from the match mask; across warps from the per-warp counts of earlier warps.
-  const int64_t tile_begin = (int64_t)tile * kRouteTile;
-  const unsigned lt_mask = (1u << lane) - 1u;
-  for (int r = 0; r < kRouteTile / kRouteThreads; ++r) {
-    const int64_t i = tile_begin + (int64_t)r * kRouteThreads + threadIdx.x;
-    const bool valid = i < a.n;
-    uint32_t key = (uint32_t)E + 1u;  // sentinel for entries past n: never stored
-    if (valid) {
-      key = __ldg(a.idx + i);
-      if (key > (uint32_t)E) key = (uint32_t)E;
+  warp_count(K, kS, E, wc[warp]);
+  __syncthreads();
+  for (int k = threadIdx.x; k <= E; k += kRouteThreads) {
+    int32_t run = base[k];
+    for (int w = 0; w < kWarps; ++w) {
+      const int32_t c = wc[w][k];
+      wc[w][k] = run;
+      run += c;
     }
-    const unsigned peers = __match_any_sync(0xffffffffu, key);
-    const int rank = __popc(peers & lt_mask);
-    const int cnt = __popc(peers);
-    if (valid && rank == 0) wc[warp][key] = cnt;
-    __syncthreads();
-    if (valid) {
-      int pre = 0;
-      for (int w = 0; w < warp; ++w) pre += wc[w][key];
-      a.perm[base[key] + pre + rank] = (int32_t)i;
-      if (key == (uint32_t)E && a.y != nullptr) zero_row(a.y, i, a.F);
-    }
-    __syncthreads();
-    if (valid && rank == 0) {
-      atomicAdd(&base[key], cnt);
-      wc[warp][key] = 0;
-    }
-    __syncthreads();
   }
+  __syncthreads();
+  warp_scatter(K, kS, E, w_begin, wc[warp], a.perm, a.y, a.F);
 
   // 3. work list (block 0)
-  if (tile == 0 && a.chunks != nullptr) write_plan<kRouteThreads>(seg_start, seg_len, E, a.chunk_rows, a.chunks, a.header, warp_tot);
+  if (tile == 0 && a.chunks != nullptr) write_plan<kRouteThreads>(seg_start, seg_len, E, a.chunk_rows, a.chunks, a.header, warp_tot,
+                                 a.n_fpairs, a.ks_cap, a.sms);
 }
 
 constexpr int kPlanThreads = 1024;
@@ -217,7 +397,11 @@ __global__ void __launch_bounds__(kPlanThreads) route_plan_sorted(RouteArgs a) {
   }
   if (unsorted) {  // the promise is broken: no segments can be trusted, compute nothing
     for (int e = threadIdx.x; e <= E; e += kPlanThreads) a.offsets[e] = 0;
-    if (threadIdx.x == 0) a.header->n_chunks = 0;
+    if (threadIdx.x == 0) {
+      a.header->n_chunks = 0;
+      a.header->ksplit = 1;
+      a.header->next_unit = 0;
+    }
     return;
   }
   // Segment starts: first row whose (clamped) key is >= e.
@@ -239,19 +423,32 @@ __global__ void __launch_bounds__(kPlanThreads) route_plan_sorted(RouteArgs a) {
   for (int e = threadIdx.x; e < E; e += kPlanThreads) seg_len[e] = seg_start[e + 1] - seg_start[e];
   for (int e = threadIdx.x; e <= E; e += kPlanThreads) a.offsets[e] = seg_start[e];
   __syncthreads();
-  if (a.chunks != nullptr) write_plan<kPlanThreads>(seg_start, seg_len, E, a.chunk_rows, a.chunks, a.header, warp_tot);
+  if (a.chunks != nullptr) write_plan<kPlanThreads>(seg_start, seg_len, E, a.chunk_rows, a.chunks, a.header, warp_tot,
+                                 a.n_fpairs, a.ks_cap, a.sms);
 }
 
 }  // namespace
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int* kernels_launched) {
   *kernels_launched = 0;
+  if (a.idx != nullptr && !a.sorted && a.n <= kSmallMaxN && a.E <= kSmallMaxE) {
+    route_small<<<1, kSmallThreads, 0, s>>>(a);
+    *kernels_launched = 1;
+    return cudaGetLastError();
+  }
   if (a.idx != nullptr && !a.sorted) {
     const unsigned tiles = (unsigned)a.n_tiles;
-    route_hist<<<tiles, kRouteThreads, 0, s>>>(a);
+    const bool small = route_tile(a.n) == kRouteTileSmall;
+    if (small)
+      route_hist<kRouteTileSmall><<<tiles, kRouteThreads, 0, s>>>(a);
+    else
+      route_hist<kRouteTileLarge><<<tiles, kRouteThreads, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    route_scatter<<<tiles, kRouteThreads, 0, s>>>(a);
+    if (small)
+      route_scatter<kRouteTileSmall><<<tiles, kRouteThreads, 0, s>>>(a);
+    else
+      route_scatter<kRouteTileLarge><<<tiles, kRouteThreads, 0, s>>>(a);
     *kernels_launched = 2;
     return cudaGetLastError();
   }
