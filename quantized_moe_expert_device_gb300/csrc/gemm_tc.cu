@@ -35,12 +35,13 @@
 //                         streams the unit's 256 x 32-byte code tile per k-block
 //   warp 25     MMA:      allocates TMEM (two 256-column fp32 accumulators), one thread issues
 //                         tcgen05.mma 128xNx16, four per tile per k-block, commits to mbarriers
-//   warps 26-31 gather:   warps 26+2s and 27+2s own A/x stage s: whenever the stage is free they
-//                         copy the chunk's x rows perm[j] (128 bytes each) with 16-byte cp.async
-//                         into the swizzled x tile, wait for their own copies, fence them for the
-//                         tensor core and mark the stage full.  Each lane keeps its source rows in
-//                         registers for the whole unit.  (TMA tile::gather4 was measured at ~80
-//                         cycles per 512-byte gather per SM: too slow for 128-byte rows.)
+//   warps 26-31 gather:   the chunk's x rows perm[j] (128 bytes per k-block) come by TMA
+//                         tile::gather4, four rows per copy, into the 128-byte-swizzled x tile;
+//                         the copies of a stage are spread over the six warps (one per lane), so
+//                         the TMA engine gets many issuers, and no warp waits for its data: the
+//                         copies complete the stage's full barrier.  (Measured on all SMs with
+//                         random 128-byte rows: cp.async from 2 warps moves ~9 B/clk/SM and from
+//                         16 warps ~23; gather4 from one thread ~7, from 8 warps ~26.)
 // The accumulators use all 512 TMEM columns, so the MMA of a unit starts once the epilogue has
 // drained the previous one; the producers keep filling stages meanwhile.
 //
@@ -68,10 +69,11 @@ constexpr int kEpiWarp0 = 16;            // warps 16-23
 constexpr int kEpiWarps = 4 * NT;
 constexpr int kTmaWarp = 24;
 constexpr int kMmaWarp = 25;
-constexpr int kGatherWarp0 = 26;         // warps 26 .. 31, a pair per A/x stage
+constexpr int kGatherWarp0 = 26;         // warps 26 .. 31: x rows by TMA gather
+constexpr int kGatherWarps = 6;
 constexpr int kAbStages = 3;
 constexpr uint32_t kTmemCols = 512;      // NT accumulators of 256 fp32 columns
-static_assert(kGatherWarp0 + 2 * kAbStages == kThreads / 32, "warp roles fill the block");
+static_assert(kGatherWarp0 + kGatherWarps == kThreads / 32, "warp roles fill the block");
 static_assert(kDeqGroup * kDeqGroups == kEpiWarp0 * 32, "dequant warps");
 
 // A work unit as the scheduler hands it to the CTA's roles (one entry of the unit queue), or
@@ -84,7 +86,7 @@ struct UnitEntry {
   int valid;
 };
 constexpr int kUnitQ = 8;  // queue depth: how far the scheduler may run ahead of the epilogue
-constexpr int kUnitConsumerWarps = kEpiWarp0 + kEpiWarps + 2 * kAbStages + 1;  // dequant, epilogue, gather, MMA
+constexpr int kUnitConsumerWarps = kEpiWarp0 + kEpiWarps + kGatherWarps + 1;  // dequant, epilogue, gather, MMA
 static_assert(kUnitConsumerWarps == 31, "every warp but the scheduler's pops each unit");
 
 template <int NMAX_, int NIB_STAGES_>
@@ -107,7 +109,8 @@ struct Cfg {
   __device__ static int nib_full(int s) { return s; }
   __device__ static int nib_empty(int s) { return NIB_STAGES + s; }
   // A tile and x tile of a stage are both written: the stage's dequant group (256 arrivals)
-  // and the two gather warps (64) arrive on one barrier, so the MMA thread probes once per
+  // and the six gather warps (one arrival with their byte count each, plus the copies'
+  // completed bytes) arrive on one barrier, so the MMA thread probes once per
   // k-block (a probe costs ~160 cycles even when the phase is already complete, which at
   // N=16 is more than half the MMA time of the k-block).
   __device__ static int ab_full(int s) { return 2 * NIB_STAGES + s; }
@@ -168,8 +171,8 @@ __device__ __forceinline__ uint4 deq8(uint32_t w, uint32_t s2, uint32_t b2) {
 
 template <class C>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_wq, const GemmArgs p) {
-  constexpr int NMAX = C::NMAX;
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_wq, const __grid_constant__ CUtensorMap tmap_x,
+                   const GemmArgs p) {
   constexpr int NIB_STAGES = C::NIB_STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::nib_empty(s)), kDeqGroup);  // the dequant group that consumed it
     }
     for (int s = 0; s < kAbStages; ++s) {
-      mbar_init(bar(C::ab_full(s)), kDeqGroup + 64);  // dequant group + both gather warps' lanes
+      mbar_init(bar(C::ab_full(s)), kDeqGroup + kGatherWarps);  // dequant group + one arrival per gather warp
       mbar_init(bar(C::ab_empty(s)), 1);
     }
     for (int q = 0; q < kUnitQ; ++q) {
@@ -203,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_barrier_init();
   }
   if (warp == kTmaWarp && lane == 0) prefetch_tensormap(&tmap_wq);
+  if (warp == kGatherWarp0 && lane == 0) prefetch_tensormap(&tmap_x);
   if (warp == kMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
@@ -339,13 +343,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_unwind(bar(C::ab_empty(j % kAbStages)), (j / kAbStages) & 1u, 100000000ull);
     }
   } else if (warp >= kGatherWarp0) {
-    // ---------------------------------------------------------------- x row gather
-    constexpr int Q = NMAX / 8;                // rows per lane
-    const uint32_t gs = (uint32_t)(warp - kGatherWarp0) >> 1;  // the stage this warp pair fills
-    const int h = (warp - kGatherWarp0) & 1;
-    const int cidx = lane & 7;                 // 16-byte chunk of a 128-byte row slice
-    const int rlow = 4 * h + (lane >> 3);      // rows 8 q + rlow
-    const uint32_t dst_lane = (uint32_t)(rlow * 128 + ((cidx ^ rlow) << 4));
+    // ---------------------------------------------------------------- x row gather (TMA)
+    // The unit's x tile (N rows x 64 columns per k-block) is fetched with tile::gather4, four
+    // rows per copy, straight into the 128-byte-swizzled K-major layout the MMA reads.  Copy g
+    // (rows 4g .. 4g+3 of the tile) belongs to lane g / 6 of gather warp g % 6, so every warp
+    // issues a few copies per stage and none waits for its data: each warp's lane 0 arrives on
+    // the stage's full barrier with the bytes its lanes will deliver.  Rows past the chunk's
+    // end (up to N) repeat its first row; the MMA columns they feed are never stored.
+    const int gw = warp - kGatherWarp0;
+    const int g = lane * kGatherWarps + gw;
     uint32_t it = 0, qi = 0;
     bool ok = true;
     while (ok) {
@@ -354,32 +360,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       release_warp(qi);
       ++qi;
       if (!U.valid) break;
-      int src[Q];
+      const int nops = ((U.rows + 15) & ~15) / 4;
+      const bool mine = g < nops;
+      int rr[4];
 #pragma unroll
-      for (int q = 0; q < Q; ++q) {
-        const int row = 8 * q + rlow;
-        src[q] = row < U.rows ? (p.perm ? __ldg(p.perm + U.start + row) : U.start + row) : -1;
+      for (int j = 0; j < 4; ++j) {
+        const int pos = 4 * g + j < U.rows ? 4 * g + j : 0;
+        rr[j] = mine ? (p.perm ? __ldg(p.perm + U.start + pos) : U.start + pos) : 0;
       }
+      const int wops = nops > gw ? min(32, (nops - gw + kGatherWarps - 1) / kGatherWarps) : 0;
       for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
-        if (it % kAbStages != gs) continue;
-        const uint32_t ph = (it / kAbStages) & 1u;
-        const bool okl = mbar_wait(bar(C::ab_empty(gs)), ph ^ 1u, abort_flag, status);
+        const uint32_t s = it % kAbStages, ph = (it / kAbStages) & 1u;
+        const bool okl = mbar_wait(bar(C::ab_empty(s)), ph ^ 1u, abort_flag, status);
         if (!__all_sync(0xffffffffu, okl)) {
           ok = false;
           break;
         }
-        const uint32_t b_lane = sbase + C::OFF_B + gs * C::B_BYTES + dst_lane;
-        const __nv_bfloat16* xk = p.x + kb * BK + cidx * 8;
-#pragma unroll
-        for (int q = 0; q < Q; ++q)
-          if (src[q] >= 0) cp_async_16(b_lane + q * 1024, xk + (int64_t)src[q] * H);
-        cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async_smem();  // this lane's copies, made visible to the tensor core
-        mbar_arrive(bar(C::ab_full(gs)));
+        if (lane == 0) mbar_arrive_expect_tx(bar(C::ab_full(s)), (uint32_t)wops * 512u);
+        __syncwarp();
+        if (mine)
+          tma_gather4(sbase + C::OFF_B + s * C::B_BYTES + (uint32_t)g * 512u, &tmap_x, bar(C::ab_full(s)), kb * BK,
+                      rr[0], rr[1], rr[2], rr[3]);
       }
     }
-    cp_async_wait<0>();
+    if (!ok && lane == 0) {  // unwinding: let this warp's copies of the last stages land
+      const uint32_t first = it > kAbStages ? it - kAbStages : 0;
+      for (uint32_t j = first; j < it; ++j)
+        mbar_wait_unwind(bar(C::ab_full(j % kAbStages)), (j / kAbStages) & 1u, 100000000ull);
+    }
   } else if (warp >= kEpiWarp0) {
     // ---------------------------------------------------------------- epilogue
     const int ew = warp - kEpiWarp0;
@@ -650,10 +658,20 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  // x as a [n, H] bf16 matrix; one box = 64 columns (one k-block, 128 bytes) of one row, for
+  // tile::gather4 into the 128-byte-swizzled B tile.
+  CUtensorMap map_x;
+  const cuuint64_t xdims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.n};
+  const cuuint64_t xstrides[1] = {(cuuint64_t)a.H * 2};
+  const cuuint32_t xbox[2] = {BK, 1};
+  cr = encode(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(a.x), xdims, xstrides, xbox,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
   if (a.chunk_rows == kChunkRowsNarrow)
-    gemm_tc_kernel<CfgNarrow><<<di.sms, kThreads, CfgNarrow::SMEM_DYN, s>>>(map_wq, a);
+    gemm_tc_kernel<CfgNarrow><<<di.sms, kThreads, CfgNarrow::SMEM_DYN, s>>>(map_wq, map_x, a);
   else
-    gemm_tc_kernel<CfgWide><<<di.sms, kThreads, CfgWide::SMEM_DYN, s>>>(map_wq, a);
+    gemm_tc_kernel<CfgWide><<<di.sms, kThreads, CfgWide::SMEM_DYN, s>>>(map_wq, map_x, a);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   *launched = 1;
