@@ -258,7 +258,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const int u = atomicAdd(&p.header->next_unit, 1);
+        // the first unit is the CTA's own (the counter starts at the grid size), which saves
+        // the counter's round trip on the way to the first MMA
+        const int u = qi == 0 ? (int)blockIdx.x : atomicAdd(&p.header->next_unit, 1);
         UnitEntry U;
         U.valid = u < n_units ? 1 : 0;
         if (U.valid) {
@@ -278,6 +280,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(C::uq_full(slot)));  // release: the entry is visible to the waiters
         ++qi;
         if (!U.valid) break;
+        {
+          // The unit's scales and biases (its rows are contiguous, rows x H/64 bf16 each) are
+          // pulled into L2 now, so the dequant threads' loads a step ahead hit L2 rather
+          // than HBM when they reach this unit.
+          const int rows = F - U.f0 < UM ? F - U.f0 : UM;  // a multiple of 16 (F is)
+          const int64_t off = ((int64_t)U.expert * F + U.f0) * G;
+          prefetch_l2_bulk(p.scales + off, (uint32_t)(rows * G * 2));
+          prefetch_l2_bulk(p.biases + off, (uint32_t)(rows * G * 2));
+        }
         const int row0 = U.expert * F + U.f0;
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
           const uint32_t s = itn % NIB_STAGES, ph = (itn / NIB_STAGES) & 1u;
@@ -403,6 +414,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++qi;
       if (!U.valid) break;
       const int N = (U.rows + 15) & ~15;
+      // destination rows of the unit's tokens, loaded before the accumulator is ready: lane l
+      // holds the rows of tokens l, l + 32, ...; an iteration's 16 tokens share one register
+      int prow[C::NMAX / 32];
+#pragma unroll
+      for (int q = 0; q < C::NMAX / 32; ++q) {
+        const int tok = q * 32 + lane;
+        prow[q] = tok < U.rows ? (p.perm ? __ldg(p.perm + U.start + tok) : U.start + tok) : 0;
+      }
       const bool okl = mbar_wait(bar(C::tmem_full()), lu & 1u, abort_flag, status);
       if (!__all_sync(0xffffffffu, okl)) break;
       tc_fence_after();
@@ -425,7 +444,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         const int q = lane & 3;
         const int fcol = U.f0 + tile * BM + quarter * 32 + q * 8;
-        for (int c0 = 0; c0 < N; c0 += 16) {
+#pragma unroll
+        for (int c0 = 0; c0 < C::NMAX; c0 += 16) {
+          if (c0 >= N) break;
           uint32_t v[16];
           tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
           tc_wait_ld();
@@ -437,8 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int hh = 0; hh < 2; ++hh) {
             const int jj = (lane >> 2) + 8 * hh;
             const int tok = c0 + jj;
+            const int row = __shfl_sync(0xffffffffu, prow[c0 >> 5], (c0 & 16) + jj);
             if (tok < U.rows && fcol < F) {
-              const int row = p.perm ? __ldg(p.perm + U.start + tok) : U.start + tok;
               uint4 val;
               asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                            : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
@@ -467,7 +488,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(p.scales);
     const uint16_t* bs16 = reinterpret_cast<const uint16_t*>(p.biases);
     // Flat walk over (unit, k-block) steps in queue order; this group processes every second
-    // step.  The scale and bias of the next step it processes are loaded one step ahead.
+    // step.  Scales and biases come one step ahead: when H/64 is a multiple of 8, as one
+    // 16-byte load each covering eight groups of the thread's row (reused for the next steps
+    // in that block of eight; a scattered 2-byte load per step and row cost ~14% of the
+    // kernel on the Mixtral-like shape), else one 2-byte load each per step.
+    const bool sb_vec = (G & 7) == 0;
     uint32_t qi = 0;
     bool ok = true;
     auto next_unit = [&](UnitEntry& U) {
@@ -486,29 +511,48 @@ __global__ void __launch_bounds__(kThreads, 1)
         kb = U.kb0 + over;
       }
     };
-    auto load_sb = [&](const UnitEntry& U, int kb, uint32_t& sv, uint32_t& bv) {
-      sv = 0;
-      bv = 0;
-      if (U.valid && U.f0 + r < F) {
-        const int64_t off = ((int64_t)U.expert * F + U.f0 + r) * G + kb;
-        sv = __ldg(sc16 + off);
-        bv = __ldg(bs16 + off);
+    // scale / bias block of the thread's row: eight bf16 (sb_vec) or one (low half of .x)
+    uint4 sblk = make_uint4(0, 0, 0, 0), bblk = make_uint4(0, 0, 0, 0);
+    int blk_row = -1, blk_b = -1;  // (expert row block E*F index of f0, k block) the registers hold
+    auto load_sb = [&](const UnitEntry& U, int kb) {
+      if (!U.valid || U.f0 + r >= F) {  // rows past F: zero weights (their outputs are dropped)
+        sblk = bblk = make_uint4(0, 0, 0, 0);
+        blk_row = -1;
+        return;
       }
+      const int b = sb_vec ? (kb >> 3) : kb;
+      const int row0 = U.expert * F + U.f0;  // < E * F, which fits in int
+      if (row0 == blk_row && b == blk_b) return;
+      blk_row = row0;
+      blk_b = b;
+      const int64_t row = (int64_t)row0 + r;
+      if (sb_vec) {
+        sblk = __ldg(reinterpret_cast<const uint4*>(sc16 + row * G) + b);
+        bblk = __ldg(reinterpret_cast<const uint4*>(bs16 + row * G) + b);
+      } else {
+        sblk.x = __ldg(sc16 + row * G + kb);
+        bblk.x = __ldg(bs16 + row * G + kb);
+      }
+    };
+    // (v, v) as bf16x2 for the block's element of k-block kb
+    auto pick = [&](const uint4& blk, int kb) -> uint32_t {
+      if (!sb_vec) return splat16(blk.x);
+      const int j = kb & 7;
+      const uint32_t w = (j & 4) ? ((j & 2) ? blk.w : blk.z) : ((j & 2) ? blk.y : blk.x);
+      return __byte_perm(w, 0, (j & 1) ? 0x3232 : 0x1010);
     };
     UnitEntry cur;
     next_unit(cur);
     int kb_cur = cur.kb0 + (int)grp;
     normalize(cur, kb_cur);
     uint32_t it = grp;  // global step index of cur
-    uint32_t s_cur = 0, b_cur = 0;
-    load_sb(cur, kb_cur, s_cur, b_cur);
+    load_sb(cur, kb_cur);
     while (ok && cur.valid) {
+      const uint32_t s2 = pick(sblk, kb_cur), b2 = pick(bblk, kb_cur);
       UnitEntry nxt = cur;
       int kb_nxt = kb_cur + kDeqGroups;
       normalize(nxt, kb_nxt);
-      uint32_t s_nxt, b_nxt;
-      load_sb(nxt, kb_nxt, s_nxt, b_nxt);
-      const uint32_t s2 = splat16(s_cur), b2 = splat16(b_cur);
+      load_sb(nxt, kb_nxt);  // the block for the next step (s2 and b2 are already taken)
       const uint32_t sn = it % NIB_STAGES, phn = (it / NIB_STAGES) & 1u;
       const uint32_t sa = it % kAbStages, pha = (it / kAbStages) & 1u;
       if (!mbar_wait(bar(C::nib_full(sn)), phn, abort_flag, status)) break;
@@ -546,8 +590,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(C::nib_empty(sn)));
       cur = nxt;
       kb_cur = kb_nxt;
-      s_cur = s_nxt;
-      b_cur = b_nxt;
       it += kDeqGroups;
     }
   }

@@ -25,7 +25,8 @@ struct WsHeader {
   uint32_t status;    // GQMM_STATUS_* bits, OR-ed by kernels, cleared by gqmm_device_status
   int32_t n_chunks;   // number of valid entries in the chunk list (written by the plan step)
   int32_t ksplit;     // K slices per (chunk, F pair) chosen by the plan step (1 = no split)
-  int32_t next_unit;  // work counter of the grouped GEMM's schedulers (zeroed by the plan step)
+  int32_t next_unit;  // work counter of the grouped GEMM's schedulers; the plan step sets it to
+                      // the grid size (CTA b takes unit b first)
   int32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
@@ -143,7 +144,7 @@ struct RouteArgs {
   int chunk_rows;       // longest chunk of the work list
   int n_fpairs;         // 256-row output tiles per expert (work units per chunk and K slice)
   int ks_cap;           // largest K split the workspace and H allow (1: never split)
-  int sms;              // streaming multiprocessors the grouped GEMM runs on
+  int sms;              // streaming multiprocessors = CTAs of the grouped GEMM
 };
 // Unsorted: histogram kernel + scan/scatter/plan kernel.  Sorted or dense: one plan kernel.
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int* kernels_launched);
@@ -277,6 +278,12 @@ __device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
+}
+
+// Bulk prefetch of [src, src + bytes) into L2 (src 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
+               : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {

@@ -122,7 +122,7 @@ __device__ void write_plan(const int32_t* seg_start, const int32_t* seg_len, int
   if (threadIdx.x == 0) {
     header->n_chunks = (int32_t)total;
     header->ksplit = choose_ksplit(total * (int64_t)n_fpairs, ks_cap, sms);
-    header->next_unit = 0;
+    header->next_unit = sms;  // units below the grid size go to the CTA of that index first
   }
 }
 
@@ -400,7 +400,7 @@ __global__ void __launch_bounds__(kPlanThreads) route_plan_sorted(RouteArgs a) {
     if (threadIdx.x == 0) {
       a.header->n_chunks = 0;
       a.header->ksplit = 1;
-      a.header->next_unit = 0;
+      a.header->next_unit = a.sms;
     }
     return;
   }
