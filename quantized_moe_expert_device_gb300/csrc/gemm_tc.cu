@@ -215,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dependents_launch();  // the split-K finalize may be scheduled; it waits for this grid
 
   const int H = p.H, F = p.F;
   const int G = H / BK;
@@ -247,6 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // code tiles several k-blocks ahead was measured: no gain with three stages, a loss with
     // thirteen, so there is none.)
     if (lane == 0) {
+      // The kernel may start while the route step that wrote the plan is still running
+      // (programmatic dependent launch).  Only this thread reads the plan directly; every
+      // other read of routing output (perm) follows a pop from the unit queue, so it comes
+      // after this wait.
+      grid_dependency_wait();
       const int ksplit = p.header->ksplit;
       const int n_fpairs = (F + UM - 1) / UM;
       const int n_units = p.header->n_chunks * n_fpairs * ksplit;
@@ -482,16 +488,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tile = r >> 7, rr = r & (BM - 1);
     // code tile rows are 32 bytes, TMA-swizzled in 32-byte mode: 16-byte chunk c of row r
     // sits at chunk position c ^ ((r >> 2) & 1)
-    const uint32_t nib_row = (uint32_t)(r * 32);
+    const uint32_t nib_row = sbase + C::OFF_NIB + (uint32_t)(r * 32);
     const uint32_t nib_c0 = (uint32_t)(((r >> 2) & 1) << 4), nib_c1 = nib_c0 ^ 16u;
-    const uint32_t a_off = (uint32_t)(tile * A_TILE_BYTES + (rr >> 3) * 1024 + (rr & 7) * 128);
+    // the row in A stage 0, with its 128-byte-swizzle XOR folded in: chunk c of the row is at
+    // a_row ^ (c << 4) (the unswizzled row address has bits 4-6 clear)
+    const uint32_t a_row0 = sbase + C::OFF_A +
+                            (uint32_t)(tile * A_TILE_BYTES + (rr >> 3) * 1024 + (rr & 7) * 128 + ((rr & 7) << 4));
     const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(p.scales);
     const uint16_t* bs16 = reinterpret_cast<const uint16_t*>(p.biases);
     // Flat walk over (unit, k-block) steps in queue order; this group processes every second
     // step.  Scales and biases come one step ahead: when H/64 is a multiple of 8, as one
-    // 16-byte load each covering eight groups of the thread's row (reused for the next steps
-    // in that block of eight; a scattered 2-byte load per step and row cost ~14% of the
-    // kernel on the Mixtral-like shape), else one 2-byte load each per step.
+    // 16-byte load each covering eight groups of the thread's row (reloaded when the step
+    // leaves the block of eight); else one 2-byte load each per step.
     const bool sb_vec = (G & 7) == 0;
     uint32_t qi = 0;
     bool ok = true;
@@ -511,24 +519,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         kb = U.kb0 + over;
       }
     };
-    // scale / bias block of the thread's row: eight bf16 (sb_vec) or one (low half of .x)
+    // scale / bias block of the thread's row in unit U: eight bf16 (sb_vec) or one (low half
+    // of .x); zero for rows past F (their outputs are dropped)
     uint4 sblk = make_uint4(0, 0, 0, 0), bblk = make_uint4(0, 0, 0, 0);
-    int blk_row = -1, blk_b = -1;  // (expert row block E*F index of f0, k block) the registers hold
     auto load_sb = [&](const UnitEntry& U, int kb) {
-      if (!U.valid || U.f0 + r >= F) {  // rows past F: zero weights (their outputs are dropped)
+      if (!U.valid || U.f0 + r >= F) {
         sblk = bblk = make_uint4(0, 0, 0, 0);
-        blk_row = -1;
         return;
       }
-      const int b = sb_vec ? (kb >> 3) : kb;
-      const int row0 = U.expert * F + U.f0;  // < E * F, which fits in int
-      if (row0 == blk_row && b == blk_b) return;
-      blk_row = row0;
-      blk_b = b;
-      const int64_t row = (int64_t)row0 + r;
+      const int64_t row = (int64_t)(U.expert * F + U.f0) + r;  // E * F fits in int
       if (sb_vec) {
-        sblk = __ldg(reinterpret_cast<const uint4*>(sc16 + row * G) + b);
-        bblk = __ldg(reinterpret_cast<const uint4*>(bs16 + row * G) + b);
+        sblk = __ldg(reinterpret_cast<const uint4*>(sc16 + row * G) + (kb >> 3));
+        bblk = __ldg(reinterpret_cast<const uint4*>(bs16 + row * G) + (kb >> 3));
       } else {
         sblk.x = __ldg(sc16 + row * G + kb);
         bblk.x = __ldg(bs16 + row * G + kb);
@@ -541,22 +543,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t w = (j & 4) ? ((j & 2) ? blk.w : blk.z) : ((j & 2) ? blk.y : blk.x);
       return __byte_perm(w, 0, (j & 1) ? 0x3232 : 0x1010);
     };
-    UnitEntry cur;
-    next_unit(cur);
-    int kb_cur = cur.kb0 + (int)grp;
-    normalize(cur, kb_cur);
-    uint32_t it = grp;  // global step index of cur
-    load_sb(cur, kb_cur);
-    while (ok && cur.valid) {
-      const uint32_t s2 = pick(sblk, kb_cur), b2 = pick(bblk, kb_cur);
-      UnitEntry nxt = cur;
-      int kb_nxt = kb_cur + kDeqGroups;
-      normalize(nxt, kb_nxt);
-      load_sb(nxt, kb_nxt);  // the block for the next step (s2 and b2 are already taken)
-      const uint32_t sn = it % NIB_STAGES, phn = (it / NIB_STAGES) & 1u;
-      const uint32_t sa = it % kAbStages, pha = (it / kAbStages) & 1u;
+    UnitEntry U;
+    next_unit(U);
+    int kb = U.kb0 + (int)grp;
+    normalize(U, kb);
+    load_sb(U, kb);
+    // stage indices and phase parities of the current step (global step index grp, grp+2, ...)
+    uint32_t sn = grp, phn = 0, sa = grp, pha = 0;
+    while (ok && U.valid) {
+      const uint32_t s2 = pick(sblk, kb), b2 = pick(bblk, kb);
+      // the next step of this group: same unit, or carried into the following ones
+      int kbn = kb + kDeqGroups;
+      UnitEntry Un;
+      const bool cross = kbn >= U.kb1;
+      if (cross) {
+        Un = U;
+        normalize(Un, kbn);
+        load_sb(Un, kbn);
+      } else if (!sb_vec || (kbn >> 3) != (kb >> 3)) {
+        load_sb(U, kbn);
+      }
       if (!mbar_wait(bar(C::nib_full(sn)), phn, abort_flag, status)) break;
-      const uint32_t nib_tile = sbase + C::OFF_NIB + sn * NIB_BYTES + nib_row;
+      const uint32_t nib_tile = nib_row + sn * NIB_BYTES;
       uint4 n0, n1;
       asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                    : "=r"(n0.x), "=r"(n0.y), "=r"(n0.z), "=r"(n0.w)
@@ -579,18 +587,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       o[6] = deq8(n1.z, s2, b2);
       o[7] = deq8(n1.w, s2, b2);
       if (!mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status)) break;
-      const uint32_t a_row = sbase + C::OFF_A + sa * A_BYTES + a_off;
+      const uint32_t a_row = a_row0 + sa * A_BYTES;
 #pragma unroll
       for (int c = 0; c < 8; ++c)
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row + (uint32_t)((c ^ (rr & 7)) << 4)),
-                     "r"(o[c].x), "r"(o[c].y), "r"(o[c].z), "r"(o[c].w)
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row ^ (uint32_t)(c << 4)), "r"(o[c].x),
+                     "r"(o[c].y), "r"(o[c].z), "r"(o[c].w)
                      : "memory");
       fence_proxy_async_smem();  // orders the A writes and the code reads before async-proxy use
       mbar_arrive(bar(C::ab_full(sa)));
       mbar_arrive(bar(C::nib_empty(sn)));
-      cur = nxt;
-      kb_cur = kb_nxt;
-      it += kDeqGroups;
+      if (cross) U = Un;
+      kb = kbn;
+      sn += kDeqGroups;
+      if (sn >= (uint32_t)NIB_STAGES) {
+        sn -= NIB_STAGES;
+        phn ^= 1u;
+      }
+      sa += kDeqGroups;
+      if (sa >= (uint32_t)kAbStages) {
+        sa -= kAbStages;
+        pha ^= 1u;
+      }
     }
   }
 
@@ -605,6 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // order, for every valid sorted position p (rows with an invalid index keep the zeros the
 // route step wrote).  One thread per 8 consecutive outputs.
 __global__ void __launch_bounds__(256) splitk_finalize(const GemmArgs p) {
+  grid_dependency_wait();  // launched to overlap the GEMM's tail; the planes are complete here
   const int ksplit = p.header->ksplit;  // chosen by the plan step; 1: the GEMM wrote y itself
   if (ksplit <= 1) return;
   int64_t n_valid = __ldg(p.offsets + p.E);
@@ -710,18 +728,34 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
-  if (a.chunk_rows == kChunkRowsNarrow)
-    gemm_tc_kernel<CfgNarrow><<<di.sms, kThreads, CfgNarrow::SMEM_DYN, s>>>(map_wq, map_x, a);
-  else
-    gemm_tc_kernel<CfgWide><<<di.sms, kThreads, CfgWide::SMEM_DYN, s>>>(map_wq, map_x, a);
-  e = cudaGetLastError();
+  // Both kernels are launched with programmatic stream serialization: the GEMM's prologue
+  // (barriers, TMEM, tensor maps) overlaps the route step, and the finalize's launch the
+  // GEMM's tail.  Each waits (griddepcontrol.wait) before reading its predecessor's output.
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)di.sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = s;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
+  if (a.chunk_rows == kChunkRowsNarrow) {
+    cfg.dynamicSmemBytes = CfgNarrow::SMEM_DYN;
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CfgNarrow>, map_wq, map_x, a);
+  } else {
+    cfg.dynamicSmemBytes = CfgWide::SMEM_DYN;
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CfgWide>, map_wq, map_x, a);
+  }
   if (e != cudaSuccess) return e;
   *launched = 1;
   if (a.ks_cap > 1) {
     const int64_t n_oct = a.n * (a.F / 8);
     const int64_t blocks = (n_oct + 255) / 256;
-    splitk_finalize<<<(unsigned)(blocks < 4 * di.sms ? blocks : 4 * di.sms), 256, 0, s>>>(a);
-    e = cudaGetLastError();
+    cfg.gridDim = dim3((unsigned)(blocks < 4 * di.sms ? blocks : 4 * di.sms));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    e = cudaLaunchKernelEx(&cfg, splitk_finalize, a);
     if (e != cudaSuccess) return e;
     *launched = 2;
   }

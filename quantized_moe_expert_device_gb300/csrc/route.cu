@@ -233,6 +233,7 @@ constexpr int kSmallMaxE = 256;
 static_assert(kSmallMaxN == (int64_t)kSmallWarps * 32 * kSmallMaxS, "small-route capacity");
 
 __global__ void __launch_bounds__(kSmallThreads) route_small(RouteArgs a) {
+  grid_dependents_launch();  // the GEMM may start its prologue; it waits before reading the plan
   __shared__ int32_t wc[kSmallWarps][kSmallMaxE + 2];  // per-warp counts, then next positions
   __shared__ int32_t seg_start[kSmallMaxE + 1];
   __shared__ int32_t seg_len[kSmallMaxE + 1];
@@ -301,6 +302,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_hist(RouteArgs a) {
 
 template <int TILE>
 __global__ void __launch_bounds__(kRouteThreads) route_scatter(RouteArgs a) {
+  grid_dependents_launch();  // the GEMM may start its prologue; it waits before reading the plan
   __shared__ int32_t base[kMaxExperts + 1];      // next perm position for each key, this tile
   __shared__ int32_t seg_start[kMaxExperts + 1]; // first perm position of each key
   __shared__ int32_t seg_len[kMaxExperts + 1];   // rows of each key
@@ -372,6 +374,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter(RouteArgs a) {
 constexpr int kPlanThreads = 1024;
 
 __global__ void __launch_bounds__(kPlanThreads) route_plan_sorted(RouteArgs a) {
+  grid_dependents_launch();  // the GEMM may start its prologue; it waits before reading the plan
   __shared__ int32_t seg_start[kMaxExperts + 1];
   __shared__ int32_t seg_len[kMaxExperts + 1];
   __shared__ int64_t warp_tot[32];
