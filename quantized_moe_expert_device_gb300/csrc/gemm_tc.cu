@@ -22,7 +22,9 @@
 // slice stores its fp32 partial sums in its own plane of a workspace buffer, and a second
 // kernel adds the planes in slice order (so results are deterministic) into bf16 y.
 //
-// Per CTA (one per SM, persistent; units taken from a call-wide counter), warp roles:
+// Per CTA (one per SM, persistent; units taken from a call-wide counter), warp roles (the
+// warp numbers are the wide variant's; the narrow one has 3 dequant groups, warps 0-23, 4
+// epilogue warps that drain both tiles, and 2 gather warps):
 //   warps 0-15  dequant:  two groups of 256 threads take alternate k-blocks; a thread owns one
 //                         of the unit's 256 weight rows: reads its 32 bytes of codes, computes
 //                         w = scale*q + bias in bf16x2 and writes the 64 bf16 in the
@@ -64,17 +66,7 @@ constexpr int EPI_WARP_BYTES = 16 * 32 * 2;
 
 constexpr int kThreads = 1024;
 constexpr int kDeqGroup = UM;            // threads per dequant group (one per weight row)
-constexpr int kDeqGroups = 2;            // warps 0-15
-constexpr int kEpiWarp0 = 16;            // warps 16-23
-constexpr int kEpiWarps = 4 * NT;
-constexpr int kTmaWarp = 24;
-constexpr int kMmaWarp = 25;
-constexpr int kGatherWarp0 = 26;         // warps 26 .. 31: x rows by TMA gather
-constexpr int kGatherWarps = 6;
-constexpr int kAbStages = 3;
-constexpr uint32_t kTmemCols = 512;      // NT accumulators of 256 fp32 columns
-static_assert(kGatherWarp0 + kGatherWarps == kThreads / 32, "warp roles fill the block");
-static_assert(kDeqGroup * kDeqGroups == kEpiWarp0 * 32, "dequant warps");
+constexpr uint32_t kTmemCols = 512;      // the whole tensor memory of the SM
 
 // A work unit as the scheduler hands it to the CTA's roles (one entry of the unit queue), or
 // the end of the work (valid == 0).
@@ -86,20 +78,43 @@ struct UnitEntry {
   int valid;
 };
 constexpr int kUnitQ = 8;  // queue depth: how far the scheduler may run ahead of the epilogue
-constexpr int kUnitConsumerWarps = kEpiWarp0 + kEpiWarps + kGatherWarps + 1;  // dequant, epilogue, gather, MMA
-static_assert(kUnitConsumerWarps == 31, "every warp but the scheduler's pops each unit");
 
-template <int NMAX_, int NIB_STAGES_>
+// Variant: largest chunk (UMMA N), code ring depth, and the warp roles: DEQ_GROUPS groups of 8
+// dequant warps (warps 0 ..), EPI_WARPS epilogue warps, then the scheduler/TMA warp, the MMA
+// warp and the gather warps.
+template <int NMAX_, int NIB_STAGES_, int DEQ_GROUPS_, int EPI_WARPS_, bool A_TMEM_, int AB_STAGES_>
 struct Cfg {
   static constexpr int NMAX = NMAX_;              // rows per chunk = largest UMMA N
   static constexpr int NIB_STAGES = NIB_STAGES_;  // code ring depth
+  // A (dequantized weights) in tensor memory instead of shared memory; AB_STAGES = depth of
+  // the A / x ring.  Tensor memory: accumulators of NMAX columns per tile at column
+  // tile * ACC_COLS, then (A_TMEM) the A stages, NT * 32 columns each (64 bf16 per row).
+  static constexpr bool A_TMEM = A_TMEM_;
+  static constexpr int AB_STAGES = AB_STAGES_;
+  static constexpr int ACC_COLS = NMAX;
+  static constexpr int A_COL0 = NT * ACC_COLS;
+  static_assert(!A_TMEM || A_COL0 + AB_STAGES * NT * 32 <= (int)kTmemCols, "A stages fit in tensor memory");
+  static_assert(A_TMEM || NT * ACC_COLS <= (int)kTmemCols, "accumulators fit in tensor memory");
+  static constexpr int DEQ_GROUPS = DEQ_GROUPS_;  // dequant groups of kDeqGroup threads, alternate steps
+  static constexpr int EPI_WARPS = EPI_WARPS_;    // 4 * NT (one tile each) or 4 (both tiles each)
+  static constexpr int EPI_WARP0 = DEQ_GROUPS * kDeqGroup / 32;
+  static constexpr int TMA_WARP = EPI_WARP0 + EPI_WARPS;
+  static constexpr int MMA_WARP = TMA_WARP + 1;
+  static constexpr int GATHER_WARP0 = MMA_WARP + 1;
+  static constexpr int GATHER_WARPS = kThreads / 32 - GATHER_WARP0;
+  static constexpr int TILES_PER_EPI_WARP = NT * 4 / EPI_WARPS;
+  // warps that pop every unit: all but the scheduler's
+  static constexpr int UNIT_CONSUMER_WARPS = EPI_WARP0 + EPI_WARPS + GATHER_WARPS + 1;
+  static_assert(GATHER_WARPS >= 1 && UNIT_CONSUMER_WARPS == kThreads / 32 - 1, "warp roles fill the block");
+  static_assert(EPI_WARPS % 4 == 0 && (NT * 4) % EPI_WARPS == 0, "epilogue warps cover the TMEM lane quarters");
+  static_assert(NIB_STAGES > DEQ_GROUPS && AB_STAGES >= DEQ_GROUPS, "a step advances the rings by DEQ_GROUPS");
   static constexpr int B_BYTES = NMAX * BK * 2;
   static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + kAbStages * A_BYTES;
-  static constexpr int OFF_NIB = OFF_B + kAbStages * B_BYTES;
+  static constexpr int OFF_B = OFF_A + (A_TMEM ? 0 : AB_STAGES * A_BYTES);
+  static constexpr int OFF_NIB = OFF_B + AB_STAGES * B_BYTES;
   static constexpr int OFF_EPI = OFF_NIB + NIB_STAGES * NIB_BYTES;
-  static constexpr int OFF_BAR = OFF_EPI + kEpiWarps * EPI_WARP_BYTES;
-  static constexpr int NUM_BARS = 2 * NIB_STAGES + 2 * kAbStages + 3 + 2 * kUnitQ;
+  static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_WARP_BYTES;
+  static constexpr int NUM_BARS = 2 * NIB_STAGES + 2 * AB_STAGES + 3 + 2 * kUnitQ;
   static constexpr int OFF_MISC = OFF_BAR + ((NUM_BARS * 8 + 127) / 128) * 128;
   static constexpr int OFF_UQ = OFF_MISC + 16;
   static constexpr int SMEM_DYN = OFF_UQ + kUnitQ * 32 + 1024;  // room to align the base to 1024 bytes
@@ -114,15 +129,20 @@ struct Cfg {
   // k-block (a probe costs ~160 cycles even when the phase is already complete, which at
   // N=16 is more than half the MMA time of the k-block).
   __device__ static int ab_full(int s) { return 2 * NIB_STAGES + s; }
-  __device__ static int ab_empty(int s) { return 2 * NIB_STAGES + kAbStages + s; }
-  __device__ static int tmem_full() { return 2 * NIB_STAGES + 2 * kAbStages; }
-  __device__ static int tmem_empty() { return 2 * NIB_STAGES + 2 * kAbStages + 1; }
-  __device__ static int unwind() { return 2 * NIB_STAGES + 2 * kAbStages + 2; }
-  __device__ static int uq_full(int q) { return 2 * NIB_STAGES + 2 * kAbStages + 3 + q; }
-  __device__ static int uq_empty(int q) { return 2 * NIB_STAGES + 2 * kAbStages + 3 + kUnitQ + q; }
+  __device__ static int ab_empty(int s) { return 2 * NIB_STAGES + AB_STAGES + s; }
+  __device__ static int tmem_full() { return 2 * NIB_STAGES + 2 * AB_STAGES; }
+  __device__ static int tmem_empty() { return 2 * NIB_STAGES + 2 * AB_STAGES + 1; }
+  __device__ static int unwind() { return 2 * NIB_STAGES + 2 * AB_STAGES + 2; }
+  __device__ static int uq_full(int q) { return 2 * NIB_STAGES + 2 * AB_STAGES + 3 + q; }
+  __device__ static int uq_empty(int q) { return 2 * NIB_STAGES + 2 * AB_STAGES + 3 + kUnitQ + q; }
 };
-using CfgWide = Cfg<kChunkRowsWide, 3>;
-using CfgNarrow = Cfg<kChunkRowsNarrow, 13>;
+// wide: 2 dequant groups, 8 epilogue warps, 6 gather warps (x tiles of up to 256 rows need
+// many TMA issuers).  narrow: the x tile is at most 32 rows and the accumulators 32 columns,
+// so 2 gather warps and 4 epilogue warps suffice and a third dequant group takes the rest.
+// The narrow variant keeps A in tensor memory (its accumulators need only 64 columns), which
+// gives it a 7-deep A / x ring next to a 13-deep code ring.
+using CfgWide = Cfg<kChunkRowsWide, 3, 2, 8, false, 3>;
+using CfgNarrow = Cfg<kChunkRowsNarrow, 13, 3, 4, true, 7>;
 
 __device__ __forceinline__ UnitEntry decode_unit(const Chunk* chunks, int u, int n_fpairs, int ksplit, int num_kb) {
   const int ks = u % ksplit;
@@ -189,25 +209,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < NIB_STAGES; ++s) {
       mbar_init(bar(C::nib_full(s)), 1);
-      mbar_init(bar(C::nib_empty(s)), kDeqGroup);  // the dequant group that consumed it
+      mbar_init(bar(C::nib_empty(s)), kDeqGroup / 32);  // one arrival per warp of the group that consumed it
     }
-    for (int s = 0; s < kAbStages; ++s) {
-      mbar_init(bar(C::ab_full(s)), kDeqGroup + kGatherWarps);  // dequant group + one arrival per gather warp
+    for (int s = 0; s < C::AB_STAGES; ++s) {
+      // one arrival per warp of the dequant group that wrote A and per gather warp
+      mbar_init(bar(C::ab_full(s)), kDeqGroup / 32 + C::GATHER_WARPS);
       mbar_init(bar(C::ab_empty(s)), 1);
     }
     for (int q = 0; q < kUnitQ; ++q) {
       mbar_init(bar(C::uq_full(q)), 1);
-      mbar_init(bar(C::uq_empty(q)), kUnitConsumerWarps);
+      mbar_init(bar(C::uq_empty(q)), C::UNIT_CONSUMER_WARPS);
     }
     mbar_init(bar(C::tmem_full()), 1);
-    mbar_init(bar(C::tmem_empty()), kEpiWarps * 32);
+    mbar_init(bar(C::tmem_empty()), C::EPI_WARPS);  // one arrival per epilogue warp
     mbar_init(bar(C::unwind()), 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == kTmaWarp && lane == 0) prefetch_tensormap(&tmap_wq);
-  if (warp == kGatherWarp0 && lane == 0) prefetch_tensormap(&tmap_x);
-  if (warp == kMmaWarp) {
+  if (warp == C::TMA_WARP && lane == 0) prefetch_tensormap(&tmap_wq);
+  if (warp == C::GATHER_WARP0 && lane == 0) prefetch_tensormap(&tmap_x);
+  if (warp == C::MMA_WARP) {
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
@@ -241,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) mbar_arrive(bar(C::uq_empty(qi % kUnitQ)));
   };
 
-  if (warp == kTmaWarp) {
+  if (warp == C::TMA_WARP) {
     // ---------------------------------------------------------------- scheduler + TMA (codes)
     // Units are taken from the call-wide counter one at a time, largest first (the plan
     // orders chunks by size), so CTAs that finish early take more.  (An L2 prefetch of the
@@ -314,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_unwind(bar(C::nib_full(j % NIB_STAGES)), (j / NIB_STAGES) & 1u, 100000000ull);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::MMA_WARP) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t it = 0, lu = 0, qi = 0;
@@ -330,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(bar(C::tmem_empty()), (lu & 1u) ^ 1u, abort_flag, status)) break;
         tc_fence_after();
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
-          const uint32_t s = it % kAbStages, ph = (it / kAbStages) & 1u;
+          const uint32_t s = it % C::AB_STAGES, ph = (it / C::AB_STAGES) & 1u;
           if (!mbar_wait(bar(C::ab_full(s)), ph, abort_flag, status)) {
             ok = false;
             break;
@@ -339,11 +360,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bdesc = umma_desc_sw128(sbase + C::OFF_B + s * C::B_BYTES);
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            const uint64_t adesc = umma_desc_sw128(sbase + C::OFF_A + s * A_BYTES + t * A_TILE_BYTES);
+            const uint32_t d_tmem = tmem_base + (uint32_t)(t * C::ACC_COLS);
+            if (C::A_TMEM) {
+              const uint32_t a_tmem = tmem_base + (uint32_t)(C::A_COL0 + (int)s * NT * 32 + t * 32);
 #pragma unroll
-            for (int k = 0; k < BK / 16; ++k)  // advance 16 elements = 32 bytes along K
-              tc_mma_bf16(tmem_base + (uint32_t)(t * 256), adesc + 2u * k, bdesc + 2u * k, idesc,
-                          (kb > U.kb0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < BK / 16; ++k)  // 16 elements = 8 columns of A, 32 bytes of B
+                tc_mma_bf16_ta(d_tmem, a_tmem + 8u * k, bdesc + 2u * k, idesc, (kb > U.kb0 || k > 0) ? 1u : 0u);
+            } else {
+              const uint64_t adesc = umma_desc_sw128(sbase + C::OFF_A + s * A_BYTES + t * A_TILE_BYTES);
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k)  // advance 16 elements = 32 bytes along K
+                tc_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb > U.kb0 || k > 0) ? 1u : 0u);
+            }
           }
           tc_commit(bar(C::ab_empty(s)));
           ++it;
@@ -355,11 +383,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_commit(bar(C::unwind()));
       mbar_wait_unwind(bar(C::unwind()), 0, 100000000ull);
       // and the stage-release arrivals of the last stages have landed
-      const uint32_t first = it > kAbStages ? it - kAbStages : 0;
+      const uint32_t first = it > C::AB_STAGES ? it - C::AB_STAGES : 0;
       for (uint32_t j = first; j < it; ++j)
-        mbar_wait_unwind(bar(C::ab_empty(j % kAbStages)), (j / kAbStages) & 1u, 100000000ull);
+        mbar_wait_unwind(bar(C::ab_empty(j % C::AB_STAGES)), (j / C::AB_STAGES) & 1u, 100000000ull);
     }
-  } else if (warp >= kGatherWarp0) {
+  } else if (warp >= C::GATHER_WARP0) {
     // ---------------------------------------------------------------- x row gather (TMA)
     // The unit's x tile (N rows x 64 columns per k-block) is fetched with tile::gather4, four
     // rows per copy, straight into the 128-byte-swizzled K-major layout the MMA reads.  Copy g
@@ -367,13 +395,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // issues a few copies per stage and none waits for its data: each warp's lane 0 arrives on
     // the stage's full barrier with the bytes its lanes will deliver.  Rows past the chunk's
     // end (up to N) repeat its first row; the MMA columns they feed are never stored.
-    const int gw = warp - kGatherWarp0;
-    const int g = lane * kGatherWarps + gw;
+    const int gw = warp - C::GATHER_WARP0;
+    const int g = lane * C::GATHER_WARPS + gw;
     uint32_t it = 0, qi = 0;
     bool ok = true;
     while (ok) {
       UnitEntry U;
-      if (!pop(qi, U)) break;
+      // a warp-uniform decision: lanes whose bounded wait ran out must not leave the others
+      // waiting in the warp synchronization below
+      if (!__all_sync(0xffffffffu, pop(qi, U))) break;
       release_warp(qi);
       ++qi;
       if (!U.valid) break;
@@ -385,9 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pos = 4 * g + j < U.rows ? 4 * g + j : 0;
         rr[j] = mine ? (p.perm ? __ldg(p.perm + U.start + pos) : U.start + pos) : 0;
       }
-      const int wops = nops > gw ? min(32, (nops - gw + kGatherWarps - 1) / kGatherWarps) : 0;
+      const int wops = nops > gw ? min(32, (nops - gw + C::GATHER_WARPS - 1) / C::GATHER_WARPS) : 0;
       for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
-        const uint32_t s = it % kAbStages, ph = (it / kAbStages) & 1u;
+        const uint32_t s = it % C::AB_STAGES, ph = (it / C::AB_STAGES) & 1u;
         const bool okl = mbar_wait(bar(C::ab_empty(s)), ph ^ 1u, abort_flag, status);
         if (!__all_sync(0xffffffffu, okl)) {
           ok = false;
@@ -401,21 +431,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     if (!ok && lane == 0) {  // unwinding: let this warp's copies of the last stages land
-      const uint32_t first = it > kAbStages ? it - kAbStages : 0;
+      const uint32_t first = it > C::AB_STAGES ? it - C::AB_STAGES : 0;
       for (uint32_t j = first; j < it; ++j)
-        mbar_wait_unwind(bar(C::ab_full(j % kAbStages)), (j / kAbStages) & 1u, 100000000ull);
+        mbar_wait_unwind(bar(C::ab_full(j % C::AB_STAGES)), (j / C::AB_STAGES) & 1u, 100000000ull);
     }
-  } else if (warp >= kEpiWarp0) {
+  } else if (warp >= C::EPI_WARP0) {
     // ---------------------------------------------------------------- epilogue
-    const int ew = warp - kEpiWarp0;
-    const int tile = ew >> 2;          // accumulator (weight-row tile) this warp drains
+    const int ew = warp - C::EPI_WARP0;
     const int quarter = ew & 3;        // TMEM lanes 32 quarter .. 32 quarter + 31 (= warp % 4)
     uint16_t* epi = reinterpret_cast<uint16_t*>(smem + C::OFF_EPI + ew * EPI_WARP_BYTES);
     const uint32_t epi_addr = sbase + C::OFF_EPI + ew * EPI_WARP_BYTES;
     uint32_t lu = 0, qi = 0;
     for (;; ++lu) {
       UnitEntry U;
-      if (!pop(qi, U)) break;
+      // a warp-uniform decision: lanes whose bounded wait ran out must not leave the others
+      // waiting in the warp synchronization below
+      if (!__all_sync(0xffffffffu, pop(qi, U))) break;
       release_warp(qi);
       ++qi;
       if (!U.valid) break;
@@ -431,60 +462,64 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool okl = mbar_wait(bar(C::tmem_full()), lu & 1u, abort_flag, status);
       if (!__all_sync(0xffffffffu, okl)) break;
       tc_fence_after();
-      const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(tile * 256);
-      if (U.ks >= 0) {
-        // partial sums of this K slice into its own plane: thread = weight row f, 16 tokens
-        // per TMEM load; a warp's stores for one token are 32 consecutive f (128 bytes)
-        const int f = U.f0 + tile * BM + quarter * 32 + lane;
-        float* plane = p.acc + (int64_t)U.ks * p.n * F;
-        for (int c0 = 0; c0 < N; c0 += 16) {
-          uint32_t v[16];
-          tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
-          tc_wait_ld();
-          if (f < F) {
+      for (int tt = 0; tt < C::TILES_PER_EPI_WARP; ++tt) {
+        const int tile = (ew >> 2) * C::TILES_PER_EPI_WARP + tt;  // accumulator (weight-row tile)
+        const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(tile * C::ACC_COLS);
+        if (U.ks >= 0) {
+          // partial sums of this K slice into its own plane: thread = weight row f, 16 tokens
+          // per TMEM load; a warp's stores for one token are 32 consecutive f (128 bytes)
+          const int f = U.f0 + tile * BM + quarter * 32 + lane;
+          float* plane = p.acc + (int64_t)U.ks * p.n * F;
+          for (int c0 = 0; c0 < N; c0 += 16) {
+            uint32_t v[16];
+            tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
+            tc_wait_ld();
+            if (f < F) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < U.rows) plane[(int64_t)(U.start + c0 + j) * F + f] = __uint_as_float(v[j]);
-          }
-        }
-      } else {
-        const int q = lane & 3;
-        const int fcol = U.f0 + tile * BM + quarter * 32 + q * 8;
-#pragma unroll
-        for (int c0 = 0; c0 < C::NMAX; c0 += 16) {
-          if (c0 >= N) break;
-          uint32_t v[16];
-          tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
-          tc_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            epi[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
-          __syncwarp();
-#pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const int jj = (lane >> 2) + 8 * hh;
-            const int tok = c0 + jj;
-            const int row = __shfl_sync(0xffffffffu, prow[c0 >> 5], (c0 & 16) + jj);
-            if (tok < U.rows && fcol < F) {
-              uint4 val;
-              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                           : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
-                           : "r"(epi_addr + (uint32_t)(jj * 64 + q * 16))
-                           : "memory");
-              *reinterpret_cast<uint4*>(p.y + (int64_t)row * F + fcol) = val;
+              for (int j = 0; j < 16; ++j)
+                if (c0 + j < U.rows) plane[(int64_t)(U.start + c0 + j) * F + f] = __uint_as_float(v[j]);
             }
           }
-          __syncwarp();
+        } else {
+          const int q = lane & 3;
+          const int fcol = U.f0 + tile * BM + quarter * 32 + q * 8;
+#pragma unroll
+          for (int c0 = 0; c0 < C::NMAX; c0 += 16) {
+            if (c0 >= N) break;
+            uint32_t v[16];
+            tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
+            tc_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              epi[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
+            __syncwarp();
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+              const int jj = (lane >> 2) + 8 * hh;
+              const int tok = c0 + jj;
+              const int row = __shfl_sync(0xffffffffu, prow[c0 >> 5], (c0 & 16) + jj);
+              if (tok < U.rows && fcol < F) {
+                uint4 val;
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                             : "=r"(val.x), "=r"(val.y), "=r"(val.z), "=r"(val.w)
+                             : "r"(epi_addr + (uint32_t)(jj * 64 + q * 16))
+                             : "memory");
+                *reinterpret_cast<uint4*>(p.y + (int64_t)row * F + fcol) = val;
+              }
+            }
+            __syncwarp();
+          }
         }
       }
       tc_fence_before();
-      mbar_arrive(bar(C::tmem_empty()));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::tmem_empty()));
     }
   } else {
     // ---------------------------------------------------------------- dequant
-    const int t = threadIdx.x;                   // 0 .. 2 * UM - 1
+    const int t = threadIdx.x;                   // 0 .. DEQ_GROUPS * UM - 1
     const int r = t % UM;                        // weight row within the unit
-    const uint32_t grp = (uint32_t)(t / UM);     // handles the steps with it % 2 == grp
+    const uint32_t grp = (uint32_t)(t / UM);     // handles the steps with it % DEQ_GROUPS == grp
     const int tile = r >> 7, rr = r & (BM - 1);
     // code tile rows are 32 bytes, TMA-swizzled in 32-byte mode: 16-byte chunk c of row r
     // sits at chunk position c ^ ((r >> 2) & 1)
@@ -496,15 +531,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (uint32_t)(tile * A_TILE_BYTES + (rr >> 3) * 1024 + (rr & 7) * 128 + ((rr & 7) << 4));
     const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(p.scales);
     const uint16_t* bs16 = reinterpret_cast<const uint16_t*>(p.biases);
-    // Flat walk over (unit, k-block) steps in queue order; this group processes every second
-    // step.  Scales and biases come one step ahead: when H/64 is a multiple of 8, as one
+    // Flat walk over (unit, k-block) steps in queue order; this group processes every
+    // DEQ_GROUPS-th step.  Scales and biases come one step ahead: when H/64 is a multiple of 8, as one
     // 16-byte load each covering eight groups of the thread's row (reloaded when the step
     // leaves the block of eight); else one 2-byte load each per step.
     const bool sb_vec = (G & 7) == 0;
     uint32_t qi = 0;
     bool ok = true;
     auto next_unit = [&](UnitEntry& U) {
-      if (!pop(qi, U)) {
+      if (!__all_sync(0xffffffffu, pop(qi, U))) {  // warp-uniform, see the gather role
         ok = false;
         U.valid = 0;
       }
@@ -553,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && U.valid) {
       const uint32_t s2 = pick(sblk, kb), b2 = pick(bblk, kb);
       // the next step of this group: same unit, or carried into the following ones
-      int kbn = kb + kDeqGroups;
+      int kbn = kb + C::DEQ_GROUPS;
       UnitEntry Un;
       const bool cross = kbn >= U.kb1;
       if (cross) {
@@ -563,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else if (!sb_vec || (kbn >> 3) != (kb >> 3)) {
         load_sb(U, kbn);
       }
-      if (!mbar_wait(bar(C::nib_full(sn)), phn, abort_flag, status)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::nib_full(sn)), phn, abort_flag, status))) break;
       const uint32_t nib_tile = nib_row + sn * NIB_BYTES;
       uint4 n0, n1;
       asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -586,26 +621,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       o[5] = deq8(n1.y, s2, b2);
       o[6] = deq8(n1.z, s2, b2);
       o[7] = deq8(n1.w, s2, b2);
-      if (!mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status)) break;
-      const uint32_t a_row = a_row0 + sa * A_BYTES;
+      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
+      if (C::A_TMEM) {
+        // the row's 64 bf16 into the warp's TMEM lane quarter, 32 columns of the A stage
+        tc_fence_after();  // after the MMA that last read this stage (ab_empty)
+        const uint32_t taddr = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) +
+                               (uint32_t)(C::A_COL0 + (int)sa * NT * 32 + tile * 32);
+        tc_st_32x32b_x32(taddr, o);
+        tc_wait_st();
+        tc_fence_before();
+      } else {
+        const uint32_t a_row = a_row0 + sa * A_BYTES;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row ^ (uint32_t)(c << 4)), "r"(o[c].x),
-                     "r"(o[c].y), "r"(o[c].z), "r"(o[c].w)
-                     : "memory");
-      fence_proxy_async_smem();  // orders the A writes and the code reads before async-proxy use
-      mbar_arrive(bar(C::ab_full(sa)));
-      mbar_arrive(bar(C::nib_empty(sn)));
+        for (int c = 0; c < 8; ++c)
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row ^ (uint32_t)(c << 4)), "r"(o[c].x),
+                       "r"(o[c].y), "r"(o[c].z), "r"(o[c].w)
+                       : "memory");
+      }
+      // Every thread orders its A writes and code reads before async-proxy use; the warp then
+      // synchronizes and one lane arrives for it (an arrival per thread costs the barrier
+      // unit 32 updates per warp).
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar(C::ab_full(sa)));
+        mbar_arrive(bar(C::nib_empty(sn)));
+      }
       if (cross) U = Un;
       kb = kbn;
-      sn += kDeqGroups;
+      sn += C::DEQ_GROUPS;
       if (sn >= (uint32_t)NIB_STAGES) {
         sn -= NIB_STAGES;
         phn ^= 1u;
       }
-      sa += kDeqGroups;
-      if (sa >= (uint32_t)kAbStages) {
-        sa -= kAbStages;
+      sa += C::DEQ_GROUPS;
+      if (sa >= (uint32_t)C::AB_STAGES) {
+        sa -= C::AB_STAGES;
         pha ^= 1u;
       }
     }
@@ -615,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem_base, kTmemCols);
+  if (warp == C::MMA_WARP) tmem_dealloc(tmem_base, kTmemCols);
 }
 
 // Split-K epilogue: y[row(p), f] = bf16(sum over slices ks of acc[ks, p, f]), added in slice
