@@ -261,6 +261,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     barrier(world)
     torch.cuda.synchronize(dev)
     launches0 = g.launch_count()
+    variants0 = {v: g.dispatch_count(v) for v in _VARIANT_KERNEL}
     t_host0 = time.perf_counter()
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
@@ -273,6 +274,8 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     barrier(world)
     ms_total = ev0.elapsed_time(ev1)
     launches = g.launch_count() - launches0
+    ran = [v for v in _VARIANT_KERNEL if g.dispatch_count(v) > variants0[v]]
+    kernel = _VARIANT_KERNEL[ran[0]] if ran else "gemm_tc_kernel"
     # Timed pass 2, the roofline: the same K steps with CUDA events around every GEMM launch
     # on the call's stream (the library's kernel timer).
     g.kernel_timer(args.steps)
@@ -371,7 +374,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
                    "l2": f"inputs rotate over {copies} copies ({copies * per_copy / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "traffic": measured_traffic(w.name), "kernel": "gemm_tc_kernel", "kernel_ms": gemm_ms,
+                     "traffic": measured_traffic(kernel, w.name), "kernel": kernel, "kernel_ms": gemm_ms,
                      "kernel_timing": "second timed pass of the same steps, CUDA events around each GEMM launch",
                      "peak_source": f"{peaks_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"},
         "op_roofline": {"t_min_us": t_roof_s * 1e6, "frac": t_roof_s / (ms_per_step * 1e-3),
@@ -386,29 +389,37 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     print(json.dumps(line), flush=True)
 
 
-KERNEL_SOURCES = ("quantized_moe_expert_device_gb300/csrc/gemm_tc.cu",
-                  "quantized_moe_expert_device_gb300/csrc/gqmm_internal.cuh")
+_CSRC = "quantized_moe_expert_device_gb300/csrc/"
+# The sources each GEMM-step kernel is built from (a traffic record is stale once they change).
+KERNEL_SOURCES = {
+    "gemm_tc_kernel": (_CSRC + "gemm_tc.cu", _CSRC + "gqmm_internal.cuh"),
+    "gemv_fma_kernel": (_CSRC + "gemv.cu", _CSRC + "gqmm_internal.cuh"),
+    "gemv_mma_kernel": (_CSRC + "gemv_mma.cu", _CSRC + "gqmm_internal.cuh"),
+}
+# dispatch-count variant -> the kernel it launches for the GEMM step
+_VARIANT_KERNEL = {"gemv": "gemv_fma_kernel", "gemv_mma": "gemv_mma_kernel", "gemm_narrow": "gemm_tc_kernel",
+                   "gemm_tc": "gemm_tc_kernel"}
 
 
-def kernel_source_sha():
+def kernel_source_sha(kernel):
     import hashlib
 
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kernel]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def measured_traffic(workload):
-    """DRAM bytes (read + write) per GEMM launch from the committed ncu capture of this
+def measured_traffic(kernel, workload):
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu capture of this
     workload, or None when there is none or the kernel's sources changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"gemm_tc_kernel_{workload}.json")
-    if not os.path.exists(path):
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
+    if kernel not in KERNEL_SOURCES or not os.path.exists(path):
         return None
     with open(path) as f:
         prof = json.load(f)
-    if prof.get("source_sha256") != kernel_source_sha():
+    if prof.get("source_sha256") != kernel_source_sha(kernel):
         return None
     return prof.get("dram_bytes_per_launch")
 

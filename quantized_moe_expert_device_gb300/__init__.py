@@ -36,7 +36,7 @@ STATUS_NOT_SORTED = 0x200
 STATUS_TIMEOUT = 0x400
 MAX_EXPERTS = 1024
 VARIANTS = {"route_unsorted": 0, "route_sorted": 1, "route_dense": 2, "gemm_tc": 3, "gemm_narrow": 4,
-            "split_k": 5}
+            "split_k": 5, "gemv": 6, "gemv_mma": 7}
 
 
 class GqmmError(RuntimeError):

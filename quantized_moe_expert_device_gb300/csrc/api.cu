@@ -150,7 +150,7 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   ra.n_tiles = L.n_tiles;
   ra.chunk_rows = shape.chunk_rows;
   ra.n_fpairs = (F + kUnitRows - 1) / kUnitRows;
-  ra.ks_cap = L.has_acc ? shape.ksplit : 1;
+  ra.ks_cap = L.has_acc && !shape.stream ? shape.ksplit : 1;
   int sms = 0;
   cudaError_t e = device_sm_count(&sms);
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
@@ -179,23 +179,32 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   ga.E = E;
   ga.chunk_rows = shape.chunk_rows;
   ga.ks_cap = ra.ks_cap;
+  ga.dense_plan = idx == nullptr ? 1 : 0;
   ga.acc = L.has_acc ? reinterpret_cast<float*>(w + L.acc) : nullptr;
   ga.offsets = ra.offsets;
   size_t slot = 0;
   const bool timed = timer_begin(s, &slot);
   int gemm_launched = 0;
-  e = launch_gemm_tc(ga, s, &gemm_launched);
+  if (shape.stream) {
+    e = launch_gemv(ga, shape.chunk_rows, sms, s);
+    gemm_launched = 1;
+  } else {
+    e = launch_gemm_tc(ga, s, &gemm_launched);
+  }
   if (timed) timer_end(s, slot);
   g_launches.fetch_add(gemm_launched);
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "grouped GEMM launch: %s", cudaGetErrorString(e));
-  count_variant(shape.chunk_rows == kChunkRowsNarrow ? GQMM_VARIANT_GEMM_NARROW : GQMM_VARIANT_GEMM_TC);
+  count_variant(shape.stream ? (shape.chunk_rows <= 2 ? GQMM_VARIANT_GEMV : GQMM_VARIANT_GEMV_MMA)
+                : shape.chunk_rows <= kChunkRowsNarrow ? GQMM_VARIANT_GEMM_NARROW : GQMM_VARIANT_GEMM_TC);
   if (ga.ks_cap > 1) count_variant(GQMM_VARIANT_SPLIT_K);
   if (log_dispatch())
     std::fprintf(stderr, "[gqmm] gather_qmm n=%lld H=%d F=%d E=%d route=%s gemm=%s ks_cap=%d\n", (long long)n, H,
                  F, E,
                  route_variant == GQMM_VARIANT_ROUTE_DENSE ? "dense"
                  : route_variant == GQMM_VARIANT_ROUTE_SORTED ? "sorted" : "unsorted",
-                 shape.chunk_rows == kChunkRowsNarrow ? "narrow" : "wide", ga.ks_cap);
+                 shape.stream ? (shape.chunk_rows <= 2 ? "stream" : "stream-mma")
+                 : shape.chunk_rows <= kChunkRowsNarrow ? "narrow" : "wide",
+                 ga.ks_cap);
   return ok();
 }
 

@@ -791,7 +791,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   cfg.stream = s;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  if (a.chunk_rows == kChunkRowsNarrow) {
+  if (a.chunk_rows <= kChunkRowsNarrow) {
     cfg.dynamicSmemBytes = CfgNarrow::SMEM_DYN;
     e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CfgNarrow>, map_wq, map_x, a);
   } else {

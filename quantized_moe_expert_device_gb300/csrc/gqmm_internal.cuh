@@ -51,11 +51,31 @@ constexpr int kTargetUnits = 2 * 152;         // split K until about this many u
 constexpr int64_t kSplitMaxRows = 1024;       // split K only for decode-sized calls: the fp32
                                               // partial sums cost n*F*4 bytes per slice
 
-// How a call is split into work units.  A pure function of the sizes, so the workspace size
-// (which depends on it) is known before any device work.
+constexpr int kStreamMaxRows = 8;             // weight-streaming path: a dense call of <= 8 rows,
+constexpr int kStreamMoeRows = 2;             // or a routed call in chunks of <= 2 rows
+
+// Rows per chunk of the work list for n routed rows over E experts, a pure function of (n, E)
+// so the workspace size (which depends on it) is known before any device work:
+//   up to 8 for decode-sized calls (the weight-streaming path: one dense call of n <= 8 rows,
+//   or at most 1.5 rows per hit expert on average in chunks of 2, so a second row of an expert
+//   does not stream its weights again), else 32 (narrow) or 256 (wide).
+inline int chunk_rows_for(int64_t n, int E) {
+  const int64_t busy = n < E ? n : E;  // experts that can have rows
+  if (busy <= 0) return kChunkRowsWide;
+  if (E == 1) {
+    if (n <= kStreamMaxRows) return (int)n;
+  } else {
+    if (2 * n <= 3 * busy) return kStreamMoeRows;
+  }
+  const int64_t avg = (n + busy - 1) / busy;
+  return avg <= kChunkRowsNarrow ? kChunkRowsNarrow : kChunkRowsWide;
+}
+
+// How a call is split into work units.  A pure function of the sizes.
 struct UnitShape {
-  int chunk_rows;  // kChunkRowsWide or kChunkRowsNarrow
+  int chunk_rows;  // chunk_rows_for(n, E)
   int ksplit;      // K slices per (chunk, F pair); 1 = no split
+  bool stream;     // weight-streaming path (chunk_rows <= kStreamMaxRows and H supported)
 };
 
 // Largest K split a call of these sizes may use before the per-H cap (which only lowers it):
@@ -64,8 +84,7 @@ struct UnitShape {
 // The workspace holds this many partial-sum planes.
 inline int ksplit_bound(int64_t n, int F, int E, int* chunk_rows_out) {
   const int64_t busy = n < E ? n : E;                  // experts that can have rows
-  const int64_t avg = busy > 0 ? (n + busy - 1) / busy : 0;
-  const int rows = avg <= kChunkRowsNarrow ? kChunkRowsNarrow : kChunkRowsWide;
+  const int rows = chunk_rows_for(n, E);
   if (chunk_rows_out) *chunk_rows_out = rows;
   const int64_t units = (busy + n / rows) * ((F + kUnitRows - 1) / kUnitRows);  // upper bound
   if (n > kSplitMaxRows || units <= 0 || units >= kTargetUnits) return 1;
@@ -73,9 +92,12 @@ inline int ksplit_bound(int64_t n, int F, int E, int* chunk_rows_out) {
   return (int)(ks < 16 ? ks : 16);
 }
 
+bool gemv_supported(int rows, int H, int E);
+
 inline UnitShape unit_shape(int64_t n, int H, int F, int E) {
   UnitShape u;
   const int ks = ksplit_bound(n, F, E, &u.chunk_rows);
+  u.stream = u.chunk_rows <= kStreamMaxRows && gemv_supported(u.chunk_rows, H, E);
   const int G = H / 64;
   const int ks_max = G / 4 > 1 ? (G / 4 < 16 ? G / 4 : 16) : 1;  // keep >= 4 K blocks per slice
   u.ksplit = ks < ks_max ? ks : ks_max;
@@ -95,7 +117,7 @@ inline WsLayout ws_layout(int64_t n, int F, int E, bool allow_split = true) {
   WsLayout L;
   L.n_tiles = (n + route_tile(n) - 1) / route_tile(n);
   if (L.n_tiles < 1) L.n_tiles = 1;
-  L.max_chunks = E + n / kChunkRowsNarrow + 1;
+  L.max_chunks = E + n / chunk_rows_for(n, E) + 1;
   const int ks = allow_split ? ksplit_bound(n, F, E, nullptr) : 1;
   L.has_acc = ks > 1;
   size_t off = sizeof(WsHeader);
@@ -162,14 +184,23 @@ struct GemmArgs {
   float* acc;           // [ksplit, n, F] split-K partial sums (ks_cap > 1)
   const int32_t* offsets;  // [E + 1]; offsets[E] = valid sorted positions (split-K finalize)
   int H, F, E;
-  int chunk_rows;       // kChunkRowsWide or kChunkRowsNarrow: selects the kernel variant
+  int chunk_rows;       // rows per chunk: <= kChunkRowsNarrow selects the narrow variant
   int ks_cap;           // > 1: the plan step may split K (header->ksplit) and the finalize runs
+  int dense_plan;       // 1: idx is NULL, so the plan is the single chunk (expert 0, start 0, n rows)
 };
 // Launches the grouped GEMM (and, when ks_cap > 1, the kernel that turns the partial sums into
 // y).  *launched gets the number of kernels enqueued.
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched);
 // Streaming multiprocessors of the current device (queried once per device).
 cudaError_t device_sm_count(int* sms);
+
+// The weight-streaming kernels for chunks of at most `rows` rows: the CUDA-core kernel for 1 or
+// 2 rows (two blocks per SM), the MMA kernel for dense calls of 3 to 8 rows (one per SM).
+bool gemv_fma_supported(int rows, int H);
+cudaError_t launch_gemv_fma(const GemmArgs& a, int rows, int sms, cudaStream_t s);
+bool gemv_mma_supported(int rows, int H);
+cudaError_t launch_gemv_mma(const GemmArgs& a, int rows, int sms, cudaStream_t s);
+cudaError_t launch_gemv(const GemmArgs& a, int rows, int sms, cudaStream_t s);
 
 cudaError_t launch_gemm_simt(const __nv_bfloat16* x, const uint8_t* wq,
                              const __nv_bfloat16* scales, const __nv_bfloat16* biases,
@@ -292,6 +323,28 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void* src, uint32_t bytes
                : "memory");
 }
 
+// 1-D bulk copy global -> shared of `bytes` bytes (both addresses 16-byte aligned, bytes a
+// multiple of 16), completion counted on an mbarrier in bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
+}
+
+// Named barrier `id` over `nthreads` threads (a multiple of 32) that also ORs `v` over them.
+__device__ __forceinline__ bool named_barrier_or(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, %2, %3, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -303,6 +356,24 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+// Wait until at most n (0..7, clamped) of this thread's most recent cp.async groups are pending.
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+  switch (n) {
+    case 0: cp_async_wait<0>(); break;
+    case 1: cp_async_wait<1>(); break;
+    case 2: cp_async_wait<2>(); break;
+    case 3: cp_async_wait<3>(); break;
+    case 4: cp_async_wait<4>(); break;
+    case 5: cp_async_wait<5>(); break;
+    case 6: cp_async_wait<6>(); break;
+    default: cp_async_wait<7>(); break;
+  }
+}
+// Arrive (without raising the expected count) on `bar` once all of this thread's prior
+// cp.async copies have completed.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // ---- tcgen05 (5th-generation tensor core, accumulators in tensor memory) ----

@@ -200,7 +200,7 @@ def test_repeated_calls_many_units_per_cta_match_oracle_every_time():
 
 
 def test_dispatch_coverage_every_variant_runs_and_matches():
-    """Each internal variant (wide and narrow GEMM, split-K, the three routing paths) is
+    """Each internal variant (wide and narrow GEMM, split-K, weight streaming, the three routing paths) is
     exercised and checked here, in the manner of the pages' coverage check (mlx PR #4023:
     log each dispatched kernel while running the suite, count the distinct ones)."""
     import quantized_moe_expert_device_gb300 as g
@@ -210,7 +210,8 @@ def test_dispatch_coverage_every_variant_runs_and_matches():
     host_w, dev_w = _weights(E, F, H)
     cases = [
         (wl.idx_uniform(512, 8, E), False),            # 512 rows/expert: wide, no split
-        (wl.idx_uniform(4, 2, E), False),              # 1 row/expert: narrow + split-K
+        (wl.idx_uniform(16, 4, E), False),             # 8 rows/expert, few units: narrow + split-K
+        (wl.idx_uniform(4, 2, E), False),              # 1 row/expert: weight streaming
         (np.sort(wl.idx_uniform(64, 4, E).reshape(-1)).reshape(64, 4), True),  # caller-sorted
     ]
     for idx, srt in cases:
@@ -219,9 +220,83 @@ def test_dispatch_coverage_every_variant_runs_and_matches():
         assert status == 0
         assert_parity(y.reshape(-1, F), y_ref, f"coverage {idx.shape} sorted={srt}")
     host1, dev1 = _weights(1, F, H)
-    x = wl.normal_bf16((3, H), wl.SEED_X)
-    yd, yd_ref, _ = _run(x, None, 1, host1, dev1)   # dense decode: narrow + split-K
-    assert_parity(yd, yd_ref, "coverage dense")
+    for rows in (2, 3):                              # dense decode: CUDA-core and MMA streaming
+        x = wl.normal_bf16((rows, H), wl.SEED_X)
+        yd, yd_ref, _ = _run(x, None, 1, host1, dev1)
+        assert_parity(yd, yd_ref, f"coverage dense {rows} rows")
     after = {k: g.dispatch_count(k) for k in g.VARIANTS}
     for k in g.VARIANTS:
         assert after[k] > before[k], f"variant {k} never dispatched"
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 5, 8, 9])
+@pytest.mark.parametrize("H", [1024, 4096])
+def test_weight_streaming_dense_matches_oracle(M, H):
+    """Dense decode shapes: 1 or 2 rows run on the CUDA-core weight-streaming kernel, 3 to 8 on
+    the MMA one, 9 on the narrow tensor-core kernel; F is not a multiple of any row batch."""
+    import quantized_moe_expert_device_gb300 as g
+
+    F = 400
+    host_w, dev_w = _weights(1, F, H)
+    before = g.dispatch_count("gemv"), g.dispatch_count("gemv_mma")
+    x = wl.normal_bf16((M, H), wl.SEED_X + M)
+    y, y_ref, status = _run(x, None, 1, host_w, dev_w)
+    assert status == 0
+    assert (g.dispatch_count("gemv") > before[0]) == (M <= 2)
+    assert (g.dispatch_count("gemv_mma") > before[1]) == (3 <= M <= 8)
+    assert_parity(y, y_ref, f"stream dense M={M} H={H}")
+
+
+@pytest.mark.parametrize("T,A,E,H,hot", [(1, 8, 128, 2048, 1), (8, 8, 128, 2048, 1), (5, 3, 16, 1024, 1),
+                                         (32, 8, 256, 2048, 1), (32, 8, 256, 2048, 3)])
+def test_weight_streaming_moe_matches_oracle(T, A, E, H, hot):
+    """MoE decode shapes with at most 1.5 rows per hit expert on average run on the
+    weight-streaming kernel in chunks of 2 rows; an expert with more rows gets several chunks
+    (`hot` tokens send all their A rows to expert 3)."""
+    import quantized_moe_expert_device_gb300 as g
+
+    F = 272
+    host_w, dev_w = _weights(E, F, H)
+    idx = np.random.default_rng(T * 1000 + E).integers(0, E, size=(T, A), dtype=np.uint32)
+    idx[:hot, :] = 3
+    before = g.dispatch_count("gemv")
+    x = wl.normal_bf16((T, A, H), wl.SEED_X)
+    y, y_ref, status = _run(x, idx, E, host_w, dev_w)
+    assert status == 0
+    assert g.dispatch_count("gemv") > before
+    assert_parity(y.reshape(-1, F), y_ref, f"stream moe T={T} A={A} E={E}")
+
+
+def test_weight_streaming_one_item_chunks():
+    """F = 16 makes every chunk a single work item, so each block of the streaming kernel
+    moves through a new chunk (and a new copy of x) at every item."""
+    import quantized_moe_expert_device_gb300 as g
+
+    E, F, H = 512, 16, 1024
+    host_w, dev_w = _weights(E, F, H)
+    idx = np.random.default_rng(5).integers(0, E, size=(64, 8), dtype=np.uint32)
+    before = g.dispatch_count("gemv")
+    x = wl.normal_bf16((64, 8, H), wl.SEED_X)
+    y, y_ref, status = _run(x, idx, E, host_w, dev_w)
+    assert status == 0
+    assert g.dispatch_count("gemv") > before
+    assert_parity(y.reshape(-1, F), y_ref, "stream one-item chunks")
+
+
+def test_weight_streaming_invalid_indices_and_unsupported_h():
+    """Invalid indices give zero rows on the streaming path; an H the streaming kernel does
+    not take (192: not a multiple of the kernel's k slices) runs the narrow tensor-core kernel
+    with the same small chunks."""
+    import quantized_moe_expert_device_gb300 as g
+
+    E, F = 16, 144
+    for H, expect_stream in ((1024, True), (4096, True), (192, False)):
+        host_w, dev_w = _weights(E, F, H)
+        idx = np.random.default_rng(H).integers(0, E, size=(6, 2), dtype=np.uint32)
+        idx[2, 1] = E + 5
+        before = g.dispatch_count("gemv")
+        x = wl.normal_bf16((6, 2, H), wl.SEED_X)
+        y, y_ref, status = _run(x, idx, E, host_w, dev_w)
+        assert status & g.STATUS_BAD_INDEX
+        assert (g.dispatch_count("gemv") > before) == expect_stream
+        assert_parity(y.reshape(-1, F), y_ref, f"stream invalid H={H}")
