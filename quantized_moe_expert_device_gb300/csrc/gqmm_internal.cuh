@@ -43,6 +43,7 @@ constexpr int kRouteTileSmall = 1024;         // routing entries per route-sort 
 constexpr int kRouteTileLarge = 2048;         // and above (keeps the tile table at (E+1)*n/2048)
 inline int route_tile(int64_t n) { return n <= 65536 ? kRouteTileSmall : kRouteTileLarge; }
 constexpr int64_t kSmallMaxN = 4096;          // unsorted calls up to this size: one route block
+constexpr int64_t kTinyMaxN = 256;            // ... and up to this size: one entry per thread
 constexpr int kChunkRowsWide = 256;           // tokens per work unit, wide GEMM variant
 constexpr int kChunkRowsNarrow = 32;          // tokens per work unit, narrow GEMM variant
 constexpr int kMaxExperts = GQMM_MAX_EXPERTS;

@@ -6,6 +6,8 @@
 // expert on the device gives every expert one contiguous block of rows for a single grouped
 // GEMM launch.
 //
+// Unsorted idx, decode-sized calls (n <= kTinyMaxN, E <= kSmallMaxE): route_tiny, one block,
+// one entry per thread, ranks by loops over the keys in shared memory.
 // Unsorted idx, small calls (n <= kSmallMaxN, E <= kSmallMaxE): route_small, one block of
 // 1024 threads.  Each warp owns a contiguous range of entries and holds its keys in registers;
 // pass 1 counts keys per warp (warp match, no atomics), one scan over (key, warp) gives every
@@ -277,6 +279,54 @@ __global__ void __launch_bounds__(kSmallThreads) route_small(RouteArgs a) {
                                  a.n_fpairs, a.ks_cap, a.sms);
 }
 
+// Unsorted idx, decode-sized calls (n <= kTinyMaxN, E <= kSmallMaxE): one block of 256 threads,
+// one entry per thread.  Every key's count and first position, and every entry's stable rank
+// (keys below its own, plus equal keys at lower flat index), are loops over the n keys held in
+// shared memory: two block barriers before the plan, and no atomics.
+constexpr int kTinyThreads = 256;
+static_assert(kTinyMaxN <= kTinyThreads, "one entry per thread");
+
+__global__ void __launch_bounds__(kTinyThreads) route_tiny(RouteArgs a) {
+  grid_dependents_launch();  // the GEMM may start its prologue; it waits before reading the plan
+  __shared__ int32_t keys[kTinyThreads];
+  __shared__ int32_t seg_start[kSmallMaxE + 1];
+  __shared__ int32_t seg_len[kSmallMaxE + 1];
+  __shared__ int64_t warp_tot[32];
+  const int E = a.E, n = (int)a.n, t = threadIdx.x;
+  int key = E, bad = 0;
+  if (t < n) {
+    const uint32_t k = __ldg(a.idx + t);
+    bad = k >= (uint32_t)E;
+    key = bad ? E : (int)k;  // invalid indices sort last, as key E
+  }
+  keys[t] = key;
+  bad = __syncthreads_or(bad);
+  for (int e = t; e <= E; e += kTinyThreads) {
+    int cnt = 0, less = 0;
+    for (int i = 0; i < n; ++i) {
+      const int k = keys[i];
+      cnt += k == e;
+      less += k < e;
+    }
+    seg_start[e] = less;
+    seg_len[e] = cnt;
+    a.offsets[e] = less;
+  }
+  if (t < n) {
+    int rank = 0;
+    for (int i = 0; i < n; ++i) {
+      const int k = keys[i];
+      rank += k < key || (k == key && i < t);
+    }
+    a.perm[rank] = t;
+    if (key == E && a.y != nullptr) zero_row(a.y, t, a.F);
+  }
+  if (t == 0 && bad) atomicOr(&a.header->status, GQMM_STATUS_BAD_INDEX);
+  __syncthreads();
+  if (a.chunks != nullptr) write_plan<kTinyThreads>(seg_start, seg_len, E, a.chunk_rows, a.chunks, a.header, warp_tot,
+                                 a.n_fpairs, a.ks_cap, a.sms);
+}
+
 template <int TILE>
 __global__ void __launch_bounds__(kRouteThreads) route_hist(RouteArgs a) {
   __shared__ uint32_t h[kMaxExperts + 1];
@@ -434,6 +484,11 @@ __global__ void __launch_bounds__(kPlanThreads) route_plan_sorted(RouteArgs a) {
 
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int* kernels_launched) {
   *kernels_launched = 0;
+  if (a.idx != nullptr && !a.sorted && a.n <= kTinyMaxN && a.E <= kSmallMaxE) {
+    route_tiny<<<1, kTinyThreads, 0, s>>>(a);
+    *kernels_launched = 1;
+    return cudaGetLastError();
+  }
   if (a.idx != nullptr && !a.sorted && a.n <= kSmallMaxN && a.E <= kSmallMaxE) {
     route_small<<<1, kSmallThreads, 0, s>>>(a);
     *kernels_launched = 1;

@@ -30,12 +30,13 @@ def test_route_sort_workloads(name):
     _check(wl.make_idx(w), w.E)
 
 
-# sizes on both sides of the single-block route limits (4096 entries, E = 256), of the
+# sizes on both sides of the single-block route limits (256 and 4096 entries, E = 256), of the
 # 1024-entry tiles of the two-kernel route and of its switch to 2048-entry tiles (n > 65536)
 @pytest.mark.parametrize("n,E", [(1, 1), (77, 1), (78, 4), (2047, 3), (2048, 64), (2049, 64),
                                  (6000, 1024), (40000, 257), (5, 1024), (4096, 256), (4097, 256),
                                  (4096, 257), (16384, 256), (9999, 255), (33, 256), (1025, 300),
-                                 (65536, 64), (65537, 64), (70001, 1000)])
+                                 (65536, 64), (65537, 64), (70001, 1000), (255, 256), (256, 256),
+                                 (257, 256), (256, 257), (200, 3), (64, 128)])
 def test_route_sort_sizes(n, E):
     idx = np.random.default_rng(n * 7 + E).integers(0, E, size=n, dtype=np.uint32)
     _check(idx, E)
@@ -47,7 +48,7 @@ def test_route_sort_all_rows_one_expert_and_empty_experts():
     _check(idx, 64)
 
 
-@pytest.mark.parametrize("n", [4100, 20000])
+@pytest.mark.parametrize("n", [200, 4100, 20000])
 def test_route_sort_invalid_indices_go_last_and_flag(n):
     idx = np.random.default_rng(2).integers(0, 12, size=n, dtype=np.uint32)
     idx[::97] = 2**31 + 5
