@@ -39,9 +39,12 @@ struct Chunk {
 };
 
 constexpr int kRouteThreads = 256;            // threads per route-sort block
-constexpr int kRouteTileSmall = 1024;         // routing entries per route-sort block, n <= 65536
+constexpr int kRouteTileTiny = 512;          // routing entries per route-sort block, n <= 16384
+constexpr int kRouteTileSmall = 1024;         // n <= 65536
 constexpr int kRouteTileLarge = 2048;         // and above (keeps the tile table at (E+1)*n/2048)
-inline int route_tile(int64_t n) { return n <= 65536 ? kRouteTileSmall : kRouteTileLarge; }
+inline int route_tile(int64_t n) {
+  return n <= 16384 ? kRouteTileTiny : n <= 65536 ? kRouteTileSmall : kRouteTileLarge;
+}
 constexpr int64_t kSmallMaxN = 4096;          // unsorted calls up to this size: one route block
 constexpr int64_t kTinyMaxN = 256;            // ... and up to this size: one entry per thread
 constexpr int kChunkRowsWide = 256;           // tokens per work unit, wide GEMM variant

@@ -14,12 +14,13 @@
 // warp its first position per key, and pass 2 ranks the warp's entries in order.  Three block
 // barriers in all, and the index array is read once.
 // Unsorted idx, larger calls (two kernels, no host round trip):
-//   1. route_hist:     one block per tile of TILE entries; per-key counts in shared
-//                      memory (keys >= E are folded into an extra key E) written key-major.
+//   1. route_hist:     one block per tile of TILE entries (512, 1024 or 2048 by n); per-key
+//                      counts in shared memory (keys >= E are folded into an extra key E)
+//                      written key-major.
 //   2. route_scatter:  every block scans the key-major table itself (warp-shuffle scan), so
 //                      no block waits on another; then it ranks its tile's entries stably with
-//                      the same per-warp scheme and writes perm.  Block 0 also writes offsets
-//                      and the work list.
+//                      the same per-warp scheme and writes perm.  One extra block writes
+//                      offsets and the work list meanwhile.
 // The sort is stable: entries of one expert keep their order of flat index.
 // Caller-sorted or dense idx: route_plan_sorted finds segment boundaries by binary search,
 // checks the sorted promise and writes the work list (one kernel).
@@ -329,6 +330,7 @@ __global__ void __launch_bounds__(kTinyThreads) route_tiny(RouteArgs a) {
 
 template <int TILE>
 __global__ void __launch_bounds__(kRouteThreads) route_hist(RouteArgs a) {
+  grid_dependents_launch();  // route_scatter may launch now; it waits before reading the table
   __shared__ uint32_t h[kMaxExperts + 1];
   const int E = a.E;
   for (int k = threadIdx.x; k <= E; k += kRouteThreads) h[k] = 0;
@@ -362,6 +364,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter(RouteArgs a) {
   const int E = a.E;
   const int tile = blockIdx.x;
   const int warp = threadIdx.x >> 5;
+  grid_dependency_wait();  // route_hist's table is complete and visible
 
   // 1. key totals over all tiles and this tile's preceding count, one contiguous key run
   //    per thread, then a block scan over keys gives each key's segment start.
@@ -388,6 +391,14 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter(RouteArgs a) {
     base[k] += (int32_t)run;
     run += seg_len[k];
   }
+  if (tile == a.n_tiles) {
+    // the plan block (one past the tiles): offsets and the work list, while the others rank
+    __syncthreads();
+    for (int k = threadIdx.x; k <= E; k += kRouteThreads) a.offsets[k] = seg_start[k];
+    if (a.chunks != nullptr) write_plan<kRouteThreads>(seg_start, seg_len, E, a.chunk_rows, a.chunks, a.header, warp_tot,
+                                   a.n_fpairs, a.ks_cap, a.sms);
+    return;
+  }
   for (int w = 0; w < kWarps; ++w)
     for (int k = threadIdx.x; k <= E + 1; k += kRouteThreads) wc[w][k] = 0;
 
@@ -400,9 +411,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter(RouteArgs a) {
   int bad = 0;  // already reported by route_hist
   const WarpKeys<kS, false> K = load_warp_keys<kS, false>(a.idx, w_begin, w_end, kS, E, &bad);
   __syncthreads();
-  if (tile == 0) {
-    for (int k = threadIdx.x; k <= E; k += kRouteThreads) a.offsets[k] = seg_start[k];
-  }
   warp_count(K, kS, E, wc[warp]);
   __syncthreads();
   for (int k = threadIdx.x; k <= E; k += kRouteThreads) {
@@ -415,10 +423,6 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter(RouteArgs a) {
   }
   __syncthreads();
   warp_scatter(K, kS, E, w_begin, wc[warp], a.perm, a.y, a.F);
-
-  // 3. work list (block 0)
-  if (tile == 0 && a.chunks != nullptr) write_plan<kRouteThreads>(seg_start, seg_len, E, a.chunk_rows, a.chunks, a.header, warp_tot,
-                                 a.n_fpairs, a.ks_cap, a.sms);
 }
 
 constexpr int kPlanThreads = 1024;
@@ -496,17 +500,33 @@ cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int* kernels_launch
   }
   if (a.idx != nullptr && !a.sorted) {
     const unsigned tiles = (unsigned)a.n_tiles;
-    const bool small = route_tile(a.n) == kRouteTileSmall;
-    if (small)
+    const int tile = route_tile(a.n);
+    if (tile == kRouteTileTiny)
+      route_hist<kRouteTileTiny><<<tiles, kRouteThreads, 0, s>>>(a);
+    else if (tile == kRouteTileSmall)
       route_hist<kRouteTileSmall><<<tiles, kRouteThreads, 0, s>>>(a);
     else
       route_hist<kRouteTileLarge><<<tiles, kRouteThreads, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (small)
-      route_scatter<kRouteTileSmall><<<tiles, kRouteThreads, 0, s>>>(a);
+    // one block per tile, plus the plan block; launched as a programmatic dependent of
+    // route_hist (which starts only after the previous call's kernels, as a plain launch)
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles + 1);
+    cfg.blockDim = dim3(kRouteThreads);
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    if (tile == kRouteTileTiny)
+      e = cudaLaunchKernelEx(&cfg, route_scatter<kRouteTileTiny>, a);
+    else if (tile == kRouteTileSmall)
+      e = cudaLaunchKernelEx(&cfg, route_scatter<kRouteTileSmall>, a);
     else
-      route_scatter<kRouteTileLarge><<<tiles, kRouteThreads, 0, s>>>(a);
+      e = cudaLaunchKernelEx(&cfg, route_scatter<kRouteTileLarge>, a);
+    if (e != cudaSuccess) return e;
     *kernels_launched = 2;
     return cudaGetLastError();
   }
