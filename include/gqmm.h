@@ -225,8 +225,8 @@ GQMM_API int gqmm_kernel_timer_read(int64_t* launches, double* total_ms);
 #define GQMM_VARIANT_GEMM_TC 3        /* tcgen05 grouped GEMM, chunks of up to 256 rows */
 #define GQMM_VARIANT_GEMM_NARROW 4    /* tcgen05 grouped GEMM, chunks of up to 32 rows */
 #define GQMM_VARIANT_SPLIT_K 5        /* K split into slices, fp32 partial sums + finalize */
-#define GQMM_VARIANT_GEMV 6           /* weight-streaming CUDA-core kernel, chunks of 1 or 2 rows */
-#define GQMM_VARIANT_GEMV_MMA 7       /* weight-streaming MMA kernel, dense calls of 3 to 8 rows */
+#define GQMM_VARIANT_GEMV 6           /* weight-streaming CUDA-core kernel: routed chunks of 1-2 rows, dense 1 row */
+#define GQMM_VARIANT_GEMV_MMA 7       /* weight-streaming MMA kernel, dense calls of 2 to 8 rows */
 #define GQMM_VARIANT_COUNT 8
 GQMM_API int64_t gqmm_dispatch_count(int variant);
 

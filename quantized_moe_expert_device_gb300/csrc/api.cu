@@ -194,7 +194,8 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   if (timed) timer_end(s, slot);
   g_launches.fetch_add(gemm_launched);
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "grouped GEMM launch: %s", cudaGetErrorString(e));
-  count_variant(shape.stream ? (shape.chunk_rows <= 2 ? GQMM_VARIANT_GEMV : GQMM_VARIANT_GEMV_MMA)
+  const bool stream_mma = shape.stream && gemv_uses_mma(shape.chunk_rows, H, E);
+  count_variant(shape.stream ? (stream_mma ? GQMM_VARIANT_GEMV_MMA : GQMM_VARIANT_GEMV)
                 : shape.chunk_rows <= kChunkRowsNarrow ? GQMM_VARIANT_GEMM_NARROW : GQMM_VARIANT_GEMM_TC);
   if (ga.ks_cap > 1) count_variant(GQMM_VARIANT_SPLIT_K);
   if (log_dispatch())
@@ -202,7 +203,7 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
                  F, E,
                  route_variant == GQMM_VARIANT_ROUTE_DENSE ? "dense"
                  : route_variant == GQMM_VARIANT_ROUTE_SORTED ? "sorted" : "unsorted",
-                 shape.stream ? (shape.chunk_rows <= 2 ? "stream" : "stream-mma")
+                 shape.stream ? (stream_mma ? "stream-mma" : "stream")
                  : shape.chunk_rows <= kChunkRowsNarrow ? "narrow" : "wide",
                  ga.ks_cap);
   return ok();

@@ -350,16 +350,18 @@ cudaError_t launch_gemv_fma(const GemmArgs& a, int rows, int sms, cudaStream_t s
   return cudaLaunchKernelEx(&cfg, gemv_fma_kernel<2>, a);
 }
 
-// The weight-streaming path: chunks of 1 or 2 rows run on the CUDA-core kernel above, dense
-// calls of 3 to 8 rows on the MMA kernel (gemv_mma.cu), whose cost does not grow with the rows.
+// The weight-streaming path: dense calls of 2 to 8 rows run on the MMA kernel (gemv_mma.cu),
+// whose cost does not grow with the rows; single-row dense calls and routed chunks of 1 or 2
+// rows on the CUDA-core kernel above.
+bool gemv_uses_mma(int rows, int H, int E) { return E == 1 && rows >= 2 && gemv_mma_supported(rows, H); }
+
 bool gemv_supported(int rows, int H, int E) {
-  if (rows <= 2) return gemv_fma_supported(rows, H);
-  return E == 1 && gemv_mma_supported(rows, H);
+  return gemv_uses_mma(rows, H, E) || (rows <= 2 && gemv_fma_supported(rows, H));
 }
 
 cudaError_t launch_gemv(const GemmArgs& a, int rows, int sms, cudaStream_t s) {
-  if (rows <= 2) return launch_gemv_fma(a, rows, sms, s);
-  return launch_gemv_mma(a, rows, sms, s);
+  if (gemv_uses_mma(rows, a.H, a.E)) return launch_gemv_mma(a, rows, sms, s);
+  return launch_gemv_fma(a, rows, sms, s);
 }
 
 }  // namespace gqmm

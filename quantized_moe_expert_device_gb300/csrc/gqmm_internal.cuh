@@ -198,13 +198,15 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched);
 // Streaming multiprocessors of the current device (queried once per device).
 cudaError_t device_sm_count(int* sms);
 
-// The weight-streaming kernels for chunks of at most `rows` rows: the CUDA-core kernel for 1 or
-// 2 rows (two blocks per SM), the MMA kernel for dense calls of 3 to 8 rows (one per SM).
+// The weight-streaming kernels for chunks of at most `rows` rows: the CUDA-core kernel (two blocks
+// per SM) for routed chunks of 1 or 2 rows and single-row dense calls, the MMA kernel (one block
+// per SM) for dense calls of 2 to 8 rows.
 bool gemv_fma_supported(int rows, int H);
 cudaError_t launch_gemv_fma(const GemmArgs& a, int rows, int sms, cudaStream_t s);
 bool gemv_mma_supported(int rows, int H);
 cudaError_t launch_gemv_mma(const GemmArgs& a, int rows, int sms, cudaStream_t s);
 cudaError_t launch_gemv(const GemmArgs& a, int rows, int sms, cudaStream_t s);
+bool gemv_uses_mma(int rows, int H, int E);  // which of the two launch_gemv runs
 
 cudaError_t launch_gemm_simt(const __nv_bfloat16* x, const uint8_t* wq,
                              const __nv_bfloat16* scales, const __nv_bfloat16* biases,
