@@ -411,6 +411,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
                    "bits": 4, "routing": w.routing, "sorted_indices": False,
                    "rows_per_expert": w.n / w.E,
                    "l2": f"inputs rotate over {copies} copies ({copies * per_copy / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)",
+                   "gpu": torch.cuda.get_device_name(dev), "seeds": {"x": wl.SEED_X, "w": wl.SEED_W, "idx": wl.SEED_IDX},
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": measured_traffic(kernel, w.name), "kernel": kernel, "kernel_ms": gemm_ms,
