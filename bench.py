@@ -276,6 +276,19 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     launches = g.launch_count() - launches0
     ran = [v for v in _VARIANT_KERNEL if g.dispatch_count(v) > variants0[v]]
     kernel = _VARIANT_KERNEL[ran[0]] if ran else "gemm_tc_kernel"
+    # Hot pass (context only, not the metric): the same call repeated on one input set, so
+    # inputs that fit in L2 stay there between steps.
+    hot_steps = min(args.steps, 200)
+    h0 = torch.cuda.Event(enable_timing=True)
+    h1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        fn(*calls[0])
+    h0.record(stream)
+    for _ in range(hot_steps):
+        fn(*calls[0])
+    h1.record(stream)
+    torch.cuda.synchronize(dev)
+    hot_ms = max_over_ranks(h0.elapsed_time(h1), world) / hot_steps
     # Timed pass 2, the roofline: the same K steps with CUDA events around every GEMM launch
     # on the call's stream (the library's kernel timer).
     g.kernel_timer(args.steps)
@@ -412,7 +425,9 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
                    "rows_per_expert": w.n / w.E,
                    "l2": f"inputs rotate over {copies} copies ({copies * per_copy / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)",
                    "gpu": torch.cuda.get_device_name(dev), "seeds": {"x": wl.SEED_X, "w": wl.SEED_W, "idx": wl.SEED_IDX},
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}",
+                   "hot": {"ms_per_step": hot_ms, "value": flops * world / (hot_ms * 1e-3) / 1e12,
+                           "note": "one input set repeated (L2-warm where it fits); context, not the metric"}},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": measured_traffic(kernel, w.name), "kernel": kernel, "kernel_ms": gemm_ms,
                      "kernel_timing": "second timed pass of the same steps, CUDA events around each GEMM launch",
