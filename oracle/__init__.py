@@ -161,3 +161,36 @@ def gather_qmm(x, wq, scales, biases, idx, E: int, group_size: int = 64, bits: i
 
 
 gather_qmm.last_threads = 0
+
+
+def silu(v: np.ndarray) -> np.ndarray:
+    """SiLU in float64: v / (1 + exp(-v))."""
+    return v / (1.0 + np.exp(-v))
+
+
+def moe_mlp(x, q_gu, q_dn, idx, E: int, group_size: int = 64, bits: int = 4, nthreads: int = 0, rows=None):
+    """The MoE expert MLP on the routed rows, in float64:
+    y[i] = W_dn[e] (SiLU(W_g[e] x[i]) * (W_u[e] x[i])), e = idx[i], with W_gu[e] = [W_g[e]; W_u[e]]
+    (gate rows 0 .. I-1, up rows I .. 2I-1) and every weight dequantized from its 4-bit codes.
+    q_gu = (wq, scales, biases) for W_gu [E, 2I, H]; q_dn the same for W_dn [E, H, I].
+    Rows whose index is >= E are zero.  Returns float64 [n, H] (or [len(rows), H])."""
+    wq_gu, sc_gu, bs_gu = q_gu
+    wq_dn, sc_dn, bs_dn = q_dn
+    I2 = np.asarray(wq_gu).shape[-2]
+    I = I2 // 2
+    gu = gather_qmm(x, wq_gu, sc_gu, bs_gu, idx, E, group_size, bits, nthreads, rows)  # [m, 2I]
+    h = silu(gu[:, :I]) * gu[:, I:]
+    x16 = _u16(x)
+    n = x16.reshape(-1, x16.shape[-1]).shape[0]
+    r = np.arange(n) if rows is None else np.asarray(rows, np.int64)
+    e = np.zeros(r.size, np.int64) if idx is None else np.asarray(idx, np.uint32).reshape(-1)[r].astype(np.int64)
+    H_out = np.asarray(wq_dn).shape[-2]
+    y = np.zeros((r.size, H_out), np.float64)
+    for ex in np.unique(e):
+        if ex >= E:
+            continue
+        sel = np.nonzero(e == ex)[0]
+        w_dn = dequantize(np.asarray(wq_dn)[ex], _u16(sc_dn)[ex], _u16(bs_dn)[ex], group_size)  # [H, I]
+        for i in sel:  # one matrix-vector product per row: a row's result depends on that row only
+            y[i] = w_dn @ h[i]
+    return y

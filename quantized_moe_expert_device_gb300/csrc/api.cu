@@ -172,6 +172,7 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   ga.biases = static_cast<const __nv_bfloat16*>(biases);
   ga.y = static_cast<__nv_bfloat16*>(y);
   ga.perm = permuted ? ra.perm : nullptr;
+  ga.y_perm = ga.perm;
   ga.chunks = ra.chunks;
   ga.header = header;
   ga.H = H;

@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int q = 0; q < C::NMAX / 32; ++q) {
         const int tok = q * 32 + lane;
-        prow[q] = tok < U.rows ? (p.perm ? __ldg(p.perm + U.start + tok) : U.start + tok) : 0;
+        prow[q] = tok < U.rows ? (p.y_perm ? __ldg(p.y_perm + U.start + tok) : U.start + tok) : 0;
       }
       const bool okl = mbar_wait(bar(C::tmem_full()), lu & 1u, abort_flag, status);
       if (!__all_sync(0xffffffffu, okl)) break;
@@ -692,7 +692,7 @@ __global__ void __launch_bounds__(256) splitk_finalize(const GemmArgs p) {
       s0.x += t0.x; s0.y += t0.y; s0.z += t0.z; s0.w += t0.w;
       s1.x += t1.x; s1.y += t1.y; s1.z += t1.z; s1.w += t1.w;
     }
-    const int row = p.perm ? __ldg(p.perm + pos) : (int)pos;
+    const int row = p.y_perm ? __ldg(p.y_perm + pos) : (int)pos;
     uint4 o;
     o.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s0.x)) |
           ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(s0.y)) << 16);

@@ -206,7 +206,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
     if (lane == 0) {
       int prev_c = -1;
       int4 rec = make_int4(0, 0, 0, 0);
-      int trow[2] = {0, 0};
+      int trow[2] = {0, 0};  // rows of y
+      int xrow[2] = {0, 0};  // rows of x
       bool ok = true;
       int issued = 0;
       for (int j = it0; j < it1 && ok; ++j) {
@@ -220,8 +221,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
         if (newx) {
           rec = p.dense_plan ? make_int4(0, 0, (int)p.n, 0) : __ldg(reinterpret_cast<const int4*>(p.chunks) + c);
 #pragma unroll
-          for (int t = 0; t < 2; ++t)
-            trow[t] = t < M && t < rec.z ? (p.perm ? __ldg(p.perm + rec.y + t) : rec.y + t) : 0;
+          for (int t = 0; t < 2; ++t) {
+            const bool live = t < M && t < rec.z;
+            trow[t] = live ? (p.y_perm ? __ldg(p.y_perm + rec.y + t) : rec.y + t) : 0;
+            xrow[t] = live ? (p.perm ? __ldg(p.perm + rec.y + t) : rec.y + t) : 0;
+          }
           prev_c = c;
         }
         const int fb = b * RB;
@@ -244,7 +248,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
         bulk_load(base + RB * (H / 2) + RB * G * 2, p.biases + row * G, sb_bytes, bar);
         if (newx)
           for (int t = 0; t < xr; ++t)
-            bulk_load(base + RB * (H / 2 + 4 * G) + t * H * 2, p.x + (int64_t)trow[t] * H, H * 2, bar);
+            bulk_load(base + RB * (H / 2 + 4 * G) + t * H * 2, p.x + (int64_t)xrow[t] * H, H * 2, bar);
         ++issued;
         if (p.dense_plan && k == NS - 1) grid_dependency_wait();
       }

@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemmArgs
     // ---------------- producer warp (all lanes run the loop in step) ----------------
     int prev_c = -1, xq = 0, issued = 0, x_issued = 0;
     int4 rec = make_int4(0, 0, 0, 0);
-    int trow_lane = 0;
+    int trow_lane = 0, xrow_lane = 0;  // lane t < 8: row t of the chunk in y and in x
     bool ok = true;
     for (int j = it0; j < it1; ++j) {
       const int k = j - it0, s = k % NS, u = k / NS;
@@ -158,11 +158,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemmArgs
           ok = mbar_wait(smem_u32(&xempty_bar), (xq - 1) & 1, &abort_flag, status);
           if (!__all_sync(0xffffffffu, ok)) break;
         }
-        trow_lane = lane < xr ? (p.perm ? __ldg(p.perm + rec.y + lane) : rec.y + lane) : 0;
+        trow_lane = lane < xr ? (p.y_perm ? __ldg(p.y_perm + rec.y + lane) : rec.y + lane) : 0;
+        xrow_lane = lane < xr ? (p.perm ? __ldg(p.perm + rec.y + lane) : rec.y + lane) : 0;
         if (lane == 0) mbar_arrive_expect_tx(smem_u32(&xfull_bar), (uint32_t)xr * H * 2);
         __syncwarp();
         if (lane < xr)
-          bulk_load(smem_u32(xbuf + lane * XS), p.x + (int64_t)trow_lane * H, H * 2, smem_u32(&xfull_bar));
+          bulk_load(smem_u32(xbuf + lane * XS), p.x + (int64_t)xrow_lane * H, H * 2, smem_u32(&xfull_bar));
         prev_c = c;
         ++xq;
         x_issued = 1;

@@ -182,7 +182,8 @@ struct GemmArgs {
   const __nv_bfloat16* scales;
   const __nv_bfloat16* biases;
   __nv_bfloat16* y;
-  const int32_t* perm;  // NULL: sorted position == flat row
+  const int32_t* perm;  // rows of x: NULL means sorted position == row of x
+  const int32_t* y_perm;  // rows of y: NULL means sorted position == row of y
   const Chunk* chunks;
   WsHeader* header;
   float* acc;           // [ksplit, n, F] split-K partial sums (ks_cap > 1)
