@@ -153,6 +153,40 @@ GQMM_API int gqmm_gather_qmm(const void* x, const void* wq, const void* scales, 
                     gqmm_stream_t stream);
 
 /*
+ * gqmm_moe_mlp_workspace_size -- bytes of workspace for gqmm_moe_mlp with n = T*A rows,
+ * model width H, expert intermediate width I and E experts (256-byte aligned pointer
+ * required).  Holds the route sort, the work list and the two bf16 intermediates
+ * ([n, 2I] and [n, I]); 0 for invalid sizes.
+ */
+GQMM_API size_t gqmm_moe_mlp_workspace_size(int64_t n, int H, int I, int E);
+
+/*
+ * gqmm_moe_mlp -- the MoE expert MLP on the routed rows, the two quantized projections
+ * chained through one route sort (mlx PR #4023 "Pick BM from rows per expert", Measurement:
+ * chained up and down projection pairs; mlxcel #629 References: a fused switch MLP over
+ * gather_qmm):
+ *     g = x[t, a, :] . deq(W_gu[e])[0 : I]^T,   u = x[t, a, :] . deq(W_gu[e])[I : 2I]^T,
+ *     y[t, a, :] = (SiLU(g) * u) . deq(W_dn[e])^T,   e = idx[t, a],   SiLU(v) = v / (1 + e^-v).
+ * g and u are rounded to bfloat16 as the first projection writes them, SiLU(g) * u is
+ * computed in float32 and rounded to bfloat16, and each projection accumulates in float32.
+ *
+ *  x        bfloat16 [T, A, H], 16-byte aligned
+ *  wq_gu, sc_gu, bs_gu   W_gu = [W_gate; W_up] quantized, [E, 2I, ...] (gate rows 0 .. I-1,
+ *           up rows I .. 2I-1), as gqmm_quantize writes for rows = E*2I
+ *  wq_dn, sc_dn, bs_dn   W_dn quantized, [E, H, ...] with K = I
+ *  idx, T, A, E, group_size, bits, sorted   as for gqmm_gather_qmm
+ *  H        > 0, multiple of 64;   I > 0, multiple of 64 (it is the down projection's K)
+ *  y        out: bfloat16 [T, A, H] in (t, a) order, 16-byte aligned
+ *  ws       workspace of at least gqmm_moe_mlp_workspace_size(T*A, H, I, E) bytes
+ * Rows whose idx is >= E are written as zeros and set GQMM_STATUS_BAD_INDEX.
+ * Errors: as gqmm_gather_qmm, for both projections' shapes.
+ */
+GQMM_API int gqmm_moe_mlp(const void* x, const void* wq_gu, const void* sc_gu, const void* bs_gu,
+                          const void* wq_dn, const void* sc_dn, const void* bs_dn, const uint32_t* idx,
+                          int64_t T, int A, int H, int I, int E, int group_size, int bits, int sorted,
+                          void* y, void* ws, size_t ws_bytes, gqmm_stream_t stream);
+
+/*
  * gqmm_gather_qmm_simt -- the same operation computed on CUDA cores, one thread per output
  * element with float32 accumulation; needs no workspace.  A slow, independent GPU
  * cross-check of gqmm_gather_qmm's data handling, never used by it.  Same argument rules

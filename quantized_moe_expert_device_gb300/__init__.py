@@ -5,7 +5,7 @@ Every function here marshals torch tensors into the C ABI declared in include/gq
 All arithmetic runs in the library's CUDA kernels; there is no fallback of any kind.  The
 shared library is loaded on first use and its absence is an error.
 
-Names follow the C ABI: gqmm_quantize, gqmm_route_sort, gqmm_gather_qmm, ...
+Names follow the C ABI: gqmm_quantize, gqmm_route_sort, gqmm_gather_qmm, gqmm_moe_mlp, ...
 """
 from __future__ import annotations
 
@@ -19,6 +19,7 @@ import torch
 __all__ = [
     "GqmmError", "library_path", "load_library", "gqmm_quantize", "gqmm_workspace_size",
     "new_workspace", "gqmm_route_sort", "gqmm_gather_qmm", "gqmm_gather_qmm_simt",
+    "gqmm_moe_mlp_workspace_size", "new_mlp_workspace", "gqmm_moe_mlp",
     "gqmm_device_status", "gqmm_status_string", "launch_count", "kernel_timer",
     "kernel_timer_read", "dispatch_count", "STATUS_BAD_INDEX", "STATUS_NOT_SORTED",
     "STATUS_TIMEOUT", "VARIANTS", "MAX_EXPERTS",
@@ -67,6 +68,8 @@ def load_library():
             "gqmm_route_sort": ([P, I64, I, P, P, P, SZ, P], I),
             "gqmm_gather_qmm": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P, SZ, P], I),
             "gqmm_gather_qmm_simt": ([P, P, P, P, P, I64, I, I, I, I, I, I, P, P], I),
+            "gqmm_moe_mlp_workspace_size": ([I64, I, I, I], SZ),
+            "gqmm_moe_mlp": ([P, P, P, P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P, SZ, P], I),
             "gqmm_device_status": ([P, P], I),
             "gqmm_status_string": ([I], ctypes.c_char_p),
             "gqmm_last_error": ([], ctypes.c_char_p),
@@ -214,6 +217,52 @@ def gqmm_gather_qmm_simt(x, wq, scales, biases, idx, group_size: int = 64, bits:
     lib = load_library()
     _check(lib.gqmm_gather_qmm_simt(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(idx), T, A, H, F, E,
                                     group_size, bits, _ptr(y), _stream(stream, x.device)), "gqmm_gather_qmm_simt")
+    return y
+
+
+def gqmm_moe_mlp_workspace_size(n: int, H: int, I: int, E: int) -> int:
+    return int(load_library().gqmm_moe_mlp_workspace_size(n, H, I, E))
+
+
+def new_mlp_workspace(n: int, H: int, I: int, E: int, device="cuda") -> torch.Tensor:
+    """A zero-filled workspace of the size gqmm_moe_mlp_workspace_size asks for."""
+    size = gqmm_moe_mlp_workspace_size(int(n), H, I, E)
+    if size == 0:
+        raise ValueError(f"no MLP workspace size for n={n}, H={H}, I={I}, E={E}")
+    return torch.zeros(size, dtype=torch.uint8, device=device)
+
+
+def gqmm_moe_mlp(x: torch.Tensor, q_gu, q_dn, idx: Optional[torch.Tensor], group_size: int = 64, bits: int = 4,
+                 sorted_indices: bool = False, y: Optional[torch.Tensor] = None,
+                 ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The MoE expert MLP: y[t, a] = W_dn[e] (SiLU(W_g[e] x[t, a]) * (W_u[e] x[t, a])), e = idx[t, a].
+
+    x bf16 [T, A, H] (or [n, H]); q_gu = (wq, scales, biases) of W_gu = [W_gate; W_up]
+    [E, 2I, H]; q_dn the same for W_dn [E, H, I]; idx as for gqmm_gather_qmm.  Returns y
+    bf16 with x's shape.
+    """
+    wq_gu, sc_gu, bs_gu = q_gu
+    wq_dn, sc_dn, bs_dn = q_dn
+    _need(x, "x", torch.bfloat16)
+    for t, name, dt in ((wq_gu, "wq_gu", torch.uint8), (sc_gu, "sc_gu", torch.bfloat16), (bs_gu, "bs_gu", torch.bfloat16),
+                        (wq_dn, "wq_dn", torch.uint8), (sc_dn, "sc_dn", torch.bfloat16), (bs_dn, "bs_dn", torch.bfloat16)):
+        _need(t, name, dt)
+    if idx is not None and (not idx.is_cuda or not idx.is_contiguous() or idx.element_size() != 4):
+        raise ValueError("idx must be a contiguous 32-bit CUDA tensor")
+    T, A, H, I2, E = _gather_shapes(x, idx, wq_gu)
+    I = I2 // 2
+    if tuple(wq_dn.shape[:2]) != (E, H) or wq_dn.shape[2] * 2 != I:
+        raise ValueError(f"wq_dn must be [E, H, I/2] = [{E}, {H}, {I // 2}], got {tuple(wq_dn.shape)}")
+    if y is None:
+        y = torch.empty(tuple(x.shape), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(y, "y", torch.bfloat16)
+    if ws is None:
+        ws = new_mlp_workspace(T * A, H, I, E, x.device)
+    lib = load_library()
+    _check(lib.gqmm_moe_mlp(_ptr(x), _ptr(wq_gu), _ptr(sc_gu), _ptr(bs_gu), _ptr(wq_dn), _ptr(sc_dn), _ptr(bs_dn),
+                            _ptr(idx), T, A, H, I, E, group_size, bits, 1 if sorted_indices else 0, _ptr(y), _ptr(ws),
+                            ws.numel(), _stream(stream, x.device)), "gqmm_moe_mlp")
     return y
 
 

@@ -117,6 +117,44 @@ int gqmm::report_error(int code, const char* fmt, ...) {
   return code;
 }
 
+namespace gqmm {
+namespace {
+
+// Launches one projection (the streaming kernel or the tensor-core GEMM, as `shape` says) with
+// the kernel timer around it, and counts and optionally logs the variant.
+int launch_projection(const GemmArgs& ga, const UnitShape& shape, int sms, cudaStream_t s, const char* what,
+                      int route_variant) {
+  size_t slot = 0;
+  const bool timed = timer_begin(s, &slot);
+  int gemm_launched = 0;
+  cudaError_t e;
+  if (shape.stream) {
+    e = launch_gemv(ga, shape.chunk_rows, sms, s);
+    gemm_launched = 1;
+  } else {
+    e = launch_gemm_tc(ga, s, &gemm_launched);
+  }
+  if (timed) timer_end(s, slot);
+  g_launches.fetch_add(gemm_launched);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "grouped GEMM launch: %s", cudaGetErrorString(e));
+  const bool stream_mma = shape.stream && gemv_uses_mma(shape.chunk_rows, ga.H, ga.E);
+  count_variant(shape.stream ? (stream_mma ? GQMM_VARIANT_GEMV_MMA : GQMM_VARIANT_GEMV)
+                : shape.chunk_rows <= kChunkRowsNarrow ? GQMM_VARIANT_GEMM_NARROW : GQMM_VARIANT_GEMM_TC);
+  if (ga.ks_cap > 1) count_variant(GQMM_VARIANT_SPLIT_K);
+  if (log_dispatch())
+    std::fprintf(stderr, "[gqmm] %s n=%lld H=%d F=%d E=%d route=%s gemm=%s ks_cap=%d\n", what, (long long)ga.n, ga.H,
+                 ga.F, ga.E,
+                 route_variant == GQMM_VARIANT_ROUTE_DENSE ? "dense"
+                 : route_variant == GQMM_VARIANT_ROUTE_SORTED ? "sorted" : "unsorted",
+                 shape.stream ? (stream_mma ? "stream-mma" : "stream")
+                 : shape.chunk_rows <= kChunkRowsNarrow ? "narrow" : "wide",
+                 ga.ks_cap);
+  return GQMM_OK;
+}
+
+}  // namespace
+}  // namespace gqmm
+
 int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, const void* biases,
                           const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size, int bits,
                           int sorted, void* y, void* ws, size_t ws_bytes, cudaStream_t s, bool allow_split) {
@@ -183,33 +221,108 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   ga.dense_plan = idx == nullptr ? 1 : 0;
   ga.acc = L.has_acc ? reinterpret_cast<float*>(w + L.acc) : nullptr;
   ga.offsets = ra.offsets;
-  size_t slot = 0;
-  const bool timed = timer_begin(s, &slot);
-  int gemm_launched = 0;
-  if (shape.stream) {
-    e = launch_gemv(ga, shape.chunk_rows, sms, s);
-    gemm_launched = 1;
-  } else {
-    e = launch_gemm_tc(ga, s, &gemm_launched);
-  }
-  if (timed) timer_end(s, slot);
-  g_launches.fetch_add(gemm_launched);
-  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "grouped GEMM launch: %s", cudaGetErrorString(e));
-  const bool stream_mma = shape.stream && gemv_uses_mma(shape.chunk_rows, H, E);
-  count_variant(shape.stream ? (stream_mma ? GQMM_VARIANT_GEMV_MMA : GQMM_VARIANT_GEMV)
-                : shape.chunk_rows <= kChunkRowsNarrow ? GQMM_VARIANT_GEMM_NARROW : GQMM_VARIANT_GEMM_TC);
-  if (ga.ks_cap > 1) count_variant(GQMM_VARIANT_SPLIT_K);
-  if (log_dispatch())
-    std::fprintf(stderr, "[gqmm] gather_qmm n=%lld H=%d F=%d E=%d route=%s gemm=%s ks_cap=%d\n", (long long)n, H,
-                 F, E,
-                 route_variant == GQMM_VARIANT_ROUTE_DENSE ? "dense"
-                 : route_variant == GQMM_VARIANT_ROUTE_SORTED ? "sorted" : "unsorted",
-                 shape.stream ? (stream_mma ? "stream-mma" : "stream")
-                 : shape.chunk_rows <= kChunkRowsNarrow ? "narrow" : "wide",
-                 ga.ks_cap);
+  rc = launch_projection(ga, shape, sms, s, "gather_qmm", route_variant);
+  if (rc) return rc;
   return ok();
 }
 
+
+int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, const void* bs_gu, const void* wq_dn,
+                       const void* sc_dn, const void* bs_dn, const uint32_t* idx, int64_t T, int A, int H, int I, int E,
+                       int group_size, int bits, int sorted, void* y, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (I <= 0 || I > (1 << 29)) return fail(GQMM_ERR_SHAPE, "I must be in [1, 2^29] (got %d)", I);
+  // gate/up projection: K = H, 2I output columns; down projection: K = I, H output columns
+  int rc = validate_gather(x, wq_gu, sc_gu, bs_gu, idx, T, A, H, 2 * I, E, group_size, bits, y);
+  if (rc) return rc;
+  rc = validate_gather(x, wq_dn, sc_dn, bs_dn, idx, T, A, I, H, E, group_size, bits, y);
+  if (rc) return rc;
+  if (sorted != 0 && sorted != 1) return fail(GQMM_ERR_SHAPE, "sorted must be 0 or 1");
+  if (!ws) return fail(GQMM_ERR_NULL, "ws must be non-NULL");
+  const int64_t n = T * (int64_t)A;
+  const MlpLayout M = mlp_ws_layout(n, H, I, E);
+  const WsLayout& L = M.route;
+  if (!aligned(ws, 256) || ws_bytes < M.total)
+    return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", M.total, ws_bytes);
+  rc = check_device(nullptr);
+  if (rc) return rc;
+  UnitShape shape1 = unit_shape(n, H, 2 * I, E);
+  UnitShape shape2 = unit_shape(n, I, H, E);
+  shape1.ksplit = shape2.ksplit = 1;  // one work list serves both: no K split, no partial-sum planes
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  WsHeader* header = reinterpret_cast<WsHeader*>(w);
+  __nv_bfloat16* h1 = reinterpret_cast<__nv_bfloat16*>(w + M.h1);
+  __nv_bfloat16* hg = reinterpret_cast<__nv_bfloat16*>(w + M.h);
+  int sms = 0;
+  cudaError_t e = device_sm_count(&sms);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+
+  RouteArgs ra;
+  ra.idx = idx;
+  ra.n = n;
+  ra.E = E;
+  ra.sorted = sorted;
+  ra.perm = reinterpret_cast<int32_t*>(w + L.perm);
+  ra.offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+  ra.tile_hist = reinterpret_cast<uint32_t*>(w + L.tile_hist);
+  ra.chunks = reinterpret_cast<Chunk*>(w + L.chunks);
+  ra.header = header;
+  ra.y = static_cast<__nv_bfloat16*>(y);  // rows with an invalid index are zeroed in the final y
+  ra.F = H;
+  ra.n_tiles = L.n_tiles;
+  ra.chunk_rows = shape1.chunk_rows;
+  ra.n_fpairs = (2 * I + kUnitRows - 1) / kUnitRows;
+  ra.ks_cap = 1;
+  ra.sms = sms;
+  const bool permuted = idx != nullptr && !sorted;
+  int launched = 0;
+  e = launch_route(ra, s, &launched);
+  g_launches.fetch_add(launched);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
+  const int route_variant = idx == nullptr ? GQMM_VARIANT_ROUTE_DENSE
+                                           : (sorted ? GQMM_VARIANT_ROUTE_SORTED : GQMM_VARIANT_ROUTE_UNSORTED);
+  count_variant(route_variant);
+
+  GemmArgs g1;  // gate/up: x gathered by the route's permutation, output in sorted order
+  g1.x = static_cast<const __nv_bfloat16*>(x);
+  g1.n = n;
+  g1.wq = static_cast<const uint8_t*>(wq_gu);
+  g1.scales = static_cast<const __nv_bfloat16*>(sc_gu);
+  g1.biases = static_cast<const __nv_bfloat16*>(bs_gu);
+  g1.y = h1;
+  g1.perm = permuted ? ra.perm : nullptr;
+  g1.y_perm = nullptr;
+  g1.chunks = ra.chunks;
+  g1.header = header;
+  g1.acc = nullptr;
+  g1.offsets = ra.offsets;
+  g1.H = H;
+  g1.F = 2 * I;
+  g1.E = E;
+  g1.chunk_rows = shape1.chunk_rows;
+  g1.ks_cap = 1;
+  g1.dense_plan = idx == nullptr ? 1 : 0;
+  rc = launch_projection(g1, shape1, sms, s, "moe_mlp gate/up", route_variant);
+  if (rc) return rc;
+
+  e = launch_swiglu(h1, hg, n, I, header, sms, s);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "gating launch: %s", cudaGetErrorString(e));
+  g_launches.fetch_add(1);
+
+  GemmArgs g2 = g1;  // down: the sorted intermediate in, y scattered to the routed rows
+  g2.x = hg;
+  g2.wq = static_cast<const uint8_t*>(wq_dn);
+  g2.scales = static_cast<const __nv_bfloat16*>(sc_dn);
+  g2.biases = static_cast<const __nv_bfloat16*>(bs_dn);
+  g2.y = static_cast<__nv_bfloat16*>(y);
+  g2.perm = nullptr;
+  g2.y_perm = permuted ? ra.perm : nullptr;
+  g2.H = I;
+  g2.F = H;
+  g2.chunk_rows = shape2.chunk_rows;
+  rc = launch_projection(g2, shape2, sms, s, "moe_mlp down", route_variant);
+  if (rc) return rc;
+  return ok();
+}
 
 extern "C" {
 
@@ -278,6 +391,18 @@ int gqmm_gather_qmm(const void* x, const void* wq, const void* scales, const voi
                     void* ws, size_t ws_bytes, gqmm_stream_t stream) {
   return gqmm::gather_qmm_impl(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, sorted, y, ws, ws_bytes,
                                reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+size_t gqmm_moe_mlp_workspace_size(int64_t n, int H, int I, int E) {
+  if (n < 0 || n > 2147483647LL || H < 0 || I < 1 || I > (1 << 29) || E < 1 || E > GQMM_MAX_EXPERTS) return 0;
+  return mlp_ws_layout(n, H, I, E).total;
+}
+
+int gqmm_moe_mlp(const void* x, const void* wq_gu, const void* sc_gu, const void* bs_gu, const void* wq_dn,
+                 const void* sc_dn, const void* bs_dn, const uint32_t* idx, int64_t T, int A, int H, int I, int E,
+                 int group_size, int bits, int sorted, void* y, void* ws, size_t ws_bytes, gqmm_stream_t stream) {
+  return gqmm::moe_mlp_impl(x, wq_gu, sc_gu, bs_gu, wq_dn, sc_dn, bs_dn, idx, T, A, H, I, E, group_size, bits, sorted,
+                            y, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* scales, const void* biases,

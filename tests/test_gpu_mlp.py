@@ -1,0 +1,82 @@
+"""gqmm_moe_mlp on the GPU against the oracle's MoE expert MLP (float64): the two quantized
+projections chained through one route sort, SiLU gating between them.
+
+Inputs: x ~ N(0, 1); W_gu ~ N(0, 1/H) and W_dn ~ N(0, 1/I) so that the gate pre-activations are
+about N(0, 1) and SiLU works in its curved range, not as a plain ReLU.  The GPU keeps the gate/up
+outputs and the gated hidden rows in bfloat16 between the kernels (two more roundings of relative
+2^-9 than one projection); the expected relative Frobenius error grows to about 2^-9 * sqrt(4/3)
+~ 2.3e-3, inside the same 5e-3 bound the single projection uses."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from helpers import assert_parity, to_dev_idx
+
+pytestmark = pytest.mark.gpu
+
+
+def _q(shape, seed):
+    wq, sc, bs = oracle.quantize(wl.normal_bf16(shape, seed, std=shape[-1] ** -0.5, chunk_rows=1))
+    host = (wq, sc, bs)
+    dev = (torch.from_numpy(wq).cuda(), torch.from_numpy(sc.view(np.int16)).cuda().view(torch.bfloat16),
+           torch.from_numpy(bs.view(np.int16)).cuda().view(torch.bfloat16))
+    return host, dev
+
+
+def _run(T, A, H, I, E, idx, sorted_indices=False, seed=0):
+    import quantized_moe_expert_device_gb300 as g
+
+    hgu, dgu = _q((E, 2 * I, H), 40 + seed)
+    hdn, ddn = _q((E, H, I), 50 + seed)
+    x = wl.normal_bf16((T, A, H) if idx is not None else (T, H), 60 + seed)
+    ws = g.new_mlp_workspace(T * A, H, I, E)
+    d_idx = None if idx is None else to_dev_idx(idx)
+    y = g.gqmm_moe_mlp(x.cuda(), dgu, ddn, d_idx, sorted_indices=sorted_indices, ws=ws)
+    status = g.gqmm_device_status(ws)
+    ref = oracle.moe_mlp(x, hgu, hdn, idx, E)
+    torch.cuda.synchronize()
+    return y, ref, status
+
+
+@pytest.mark.parametrize("T,A,H,I,E", [(16, 2, 256, 128, 8), (4, 8, 2048, 768, 64), (2, 8, 1024, 512, 128),
+                                       (256, 8, 1024, 512, 16), (130, 2, 512, 256, 4)])
+def test_moe_mlp_matches_oracle(T, A, H, I, E):
+    idx = np.random.default_rng(T * 31 + E).integers(0, E, size=(T, A)).astype(np.uint32)
+    y, ref, status = _run(T, A, H, I, E, idx)
+    assert status == 0
+    assert_parity(y, ref, f"moe_mlp T={T} A={A} H={H} I={I} E={E}")
+
+
+@pytest.mark.parametrize("T,H,I", [(1, 1024, 512), (3, 2048, 768), (64, 512, 256)])
+def test_moe_mlp_dense_matches_oracle(T, H, I):
+    y, ref, status = _run(T, 1, H, I, 1, None)
+    assert status == 0
+    assert_parity(y, ref, f"dense mlp T={T} H={H} I={I}")
+
+
+def test_moe_mlp_sorted_equals_unsorted_bitwise():
+    import quantized_moe_expert_device_gb300 as g
+
+    T, A, H, I, E = 64, 4, 512, 256, 8
+    hgu, dgu = _q((E, 2 * I, H), 70)
+    hdn, ddn = _q((E, H, I), 71)
+    idx = np.sort(np.random.default_rng(7).integers(0, E, size=T * A).astype(np.uint32)).reshape(T, A)
+    x = wl.normal_bf16((T, A, H), 72).cuda()
+    y0 = g.gqmm_moe_mlp(x, dgu, ddn, to_dev_idx(idx), sorted_indices=False)
+    y1 = g.gqmm_moe_mlp(x, dgu, ddn, to_dev_idx(idx), sorted_indices=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y0, y1)
+
+
+def test_moe_mlp_invalid_indices_are_zero_and_flagged():
+    import quantized_moe_expert_device_gb300 as g
+
+    T, A, H, I, E = 20, 3, 512, 256, 6
+    idx = np.random.default_rng(9).integers(0, E, size=(T, A)).astype(np.uint32)
+    idx[::4, 1] = E + 3
+    y, ref, status = _run(T, A, H, I, E, idx, seed=1)
+    assert status & g.STATUS_BAD_INDEX
+    assert not y.reshape(T, A, H)[::4, 1].float().abs().sum().item()
+    assert_parity(y, ref, "moe_mlp invalid indices")
