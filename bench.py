@@ -21,6 +21,7 @@ import json
 import os
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -30,6 +31,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 import workloads as wl  # noqa: E402
+
+# gate activation of the expert-MLP workloads (the activation's cost is a few microseconds of
+# elementwise work next to the projections; every activation is parity-tested)
+MLP_ACTIVATION = "silu"
+# GEMM launches (projections) per step, each timed by the library's kernel timer
+GEMM_LAUNCHES_PER_STEP = {"gather": 1, "mlp": 2}
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -44,11 +51,16 @@ def load_peaks():
 
 
 def algorithmic_bytes(w: wl.Workload, idx: np.ndarray | None) -> int:
-    """Packed codes + scales/biases of the experts actually hit, x, y and idx, each once."""
+    """Packed codes + scales/biases of the experts actually hit, x, y and idx, each once.  For
+    the expert MLP: both projections' weights, x and y (the gate/up output and the gated
+    hidden rows are intermediates, not counted: a kernel that kept them on chip moves none)."""
     hit = w.E if idx is None else len(np.unique(idx))
-    G = w.H // 64
-    weights = hit * w.F * (w.H // 2 + 4 * G)
-    return int(weights + w.n * w.H * 2 + w.n * w.F * 2 + (0 if idx is None else w.n * 4))
+
+    def qbytes(rows, K):  # one expert's packed codes + bf16 scale and bias per 64-wide group
+        return rows * (K // 2 + 4 * (K // 64))
+
+    weights = hit * (qbytes(2 * w.F, w.H) + qbytes(w.H, w.F) if w.kind == "mlp" else qbytes(w.F, w.H))
+    return int(weights + w.n * w.H * 2 + w.n * w.out_cols * 2 + (0 if idx is None else w.n * 4))
 
 
 class ClockSampler:
@@ -61,7 +73,7 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"gqmm_clocks_bench_{os.getpid()}.csv")
 
     def start(self):
         try:
@@ -140,57 +152,90 @@ def max_over_ranks(v: float, world: int) -> float:
 # CPU oracle legs (the only places this script runs the oracle)
 # ----------------------------------------------------------------------------------------------
 
-def oracle_rate(w: wl.Workload, x_cpu, qw, idx, target_s: float, max_rows: int | None = None):
-    """Times the oracle on a bounded sample of rows; returns (TFLOP/s, rows, seconds, threads)."""
+def oracle_inputs(w: wl.Workload, inp):
+    """The oracle's quantized weights for the workload: (wq, scales, biases), or for the
+    expert MLP ((gate/up), (down))."""
     import oracle
 
+    if w.kind == "mlp":
+        return oracle.quantize(inp["w_gu"]), oracle.quantize(inp["w_dn"])
+    return oracle.quantize(inp["w"])
+
+
+def oracle_rows(w: wl.Workload, x_cpu, qw, idx, rows):
+    """The oracle on the listed flat rows; returns its thread count."""
+    import oracle
+
+    if w.kind == "mlp":
+        oracle.moe_mlp(x_cpu, qw[0], qw[1], idx, w.E, rows=rows)
+    else:
+        oracle.gather_qmm(x_cpu, *qw, idx, w.E, rows=rows)
+    return oracle.gather_qmm.last_threads
+
+
+def oracle_rate(w: wl.Workload, x_cpu, qw, idx, target_s: float, max_rows: int | None = None):
+    """Times the oracle on a bounded sample of rows; returns (TFLOP/s, rows, seconds, threads)."""
     rng = np.random.default_rng(0)
     probe = np.sort(rng.choice(w.n, size=min(w.n, 32), replace=False))
     t0 = time.perf_counter()
-    oracle.gather_qmm(x_cpu, *qw, idx, w.E, rows=probe)
+    oracle_rows(w, x_cpu, qw, idx, probe)
     dt = time.perf_counter() - t0
     rows = int(max(1, min(w.n, len(probe) * target_s / max(dt, 1e-6))))
     if max_rows:
         rows = min(rows, max_rows)
     sample = np.sort(rng.choice(w.n, size=rows, replace=False))
     t0 = time.perf_counter()
-    oracle.gather_qmm(x_cpu, *qw, idx, w.E, rows=sample)
+    threads = oracle_rows(w, x_cpu, qw, idx, sample)
     dt = time.perf_counter() - t0
-    flops = 2.0 * rows * w.H * w.F
-    return flops / dt / 1e12, rows, dt, oracle.gather_qmm.last_threads
+    flops = w.flops / w.n * rows
+    return flops / dt / 1e12, rows, dt, threads
+
+
+def metric_name(w: wl.Workload) -> str:
+    if w.kind == "mlp":
+        return "moe_mlp TFLOPs (6*T*A*H*I/time)"
+    return "gather_qmm TFLOPs (2*T*A*H*F/time)"
+
+
+def workload_config(w: wl.Workload) -> dict:
+    c = {"workload": w.name, "T": w.T, "A": w.A, "H": w.H}
+    c.update({"I": w.F} if w.kind == "mlp" else {"F": w.F})
+    c.update({"E": w.E, "group_size": 64, "bits": 4, "routing": w.routing})
+    if w.kind == "mlp":
+        c["op"] = "gqmm_moe_mlp: gate/up projection, act(gate) * up, down projection"
+        c["activation"] = MLP_ACTIVATION
+    return c
 
 
 def run_reference(args, w: wl.Workload, world: int, rank: int):
     """The oracle, as it stands, on the host cores: each step computes a bounded sample of rows."""
     if rank != 0:
         return
-    import oracle
-
     inp = wl.make_inputs(w)
-    qw = oracle.quantize(inp["w"])
+    qw = oracle_inputs(w, inp)
     idx = inp["idx"]
     budget_s = 90.0
     rng = np.random.default_rng(1)
     probe = np.sort(rng.choice(w.n, size=min(w.n, 16), replace=False))
     t0 = time.perf_counter()
-    oracle.gather_qmm(inp["x"], *qw, idx, w.E, rows=probe)
+    oracle_rows(w, inp["x"], qw, idx, probe)
     per_row = (time.perf_counter() - t0) / len(probe)
     rows_per_step = int(max(1, min(w.n, budget_s / (args.steps + args.warmup) / max(per_row, 1e-9))))
     for _ in range(args.warmup):
-        oracle.gather_qmm(inp["x"], *qw, idx, w.E, rows=rng.choice(w.n, rows_per_step, replace=False))
+        oracle_rows(w, inp["x"], qw, idx, np.sort(rng.choice(w.n, rows_per_step, replace=False)))
     t0 = time.perf_counter()
+    threads = 1
     for _ in range(args.steps):
-        oracle.gather_qmm(inp["x"], *qw, idx, w.E, rows=rng.choice(w.n, rows_per_step, replace=False))
+        threads = oracle_rows(w, inp["x"], qw, idx, np.sort(rng.choice(w.n, rows_per_step, replace=False)))
     dt = time.perf_counter() - t0
-    flops = 2.0 * rows_per_step * w.H * w.F * args.steps
+    flops = w.flops / w.n * rows_per_step * args.steps
     value = flops / dt / 1e12
     line = {
-        "impl": "reference", "metric": "gather_qmm TFLOPs (2*T*A*H*F/time)", "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": metric_name(w), "value": value, "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "A": w.A, "H": w.H, "F": w.F, "E": w.E, "group_size": 64,
-                   "bits": 4, "routing": w.routing},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": oracle.gather_qmm.last_threads,
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads,
                          "kind": "oracle",
                          "sample": f"{rows_per_step} random rows of the workload per step (of {w.n})"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -215,41 +260,51 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     # Rotate enough distinct copies of every input that the working set exceeds 3x L2.
     per_copy = algorithmic_bytes(w, idx_np)
     copies = int(max(2, min(16, np.ceil(3 * l2 / max(per_copy, 1)))))
-    w_dev = inp["w"].to(dev)
-    wq0, sc0, bs0 = g.gqmm_quantize(w_dev)
-    del w_dev
+    if w.kind == "mlp":
+        weights0 = []
+        for key in ("w_gu", "w_dn"):
+            w_dev = inp[key].to(dev)
+            weights0 += list(g.gqmm_quantize(w_dev))
+            del w_dev
+        fn, ws_new = lib.gqmm_moe_mlp, (lambda: g.new_mlp_workspace(w.n, w.H, w.F, w.E, dev))
+        sizes = (w.T, w.A, w.H, w.F, w.E, 64, 4, g.ACTIVATIONS[MLP_ACTIVATION])
+    else:
+        w_dev = inp["w"].to(dev)
+        weights0 = list(g.gqmm_quantize(w_dev))
+        del w_dev
+        fn, ws_new = lib.gqmm_gather_qmm, (lambda: g.new_workspace(w.n, w.F, w.E, dev))
+        sizes = (w.T, w.A, w.H, w.F, w.E, 64, 4)
     x0 = inp["x"].to(dev)
     idx0 = None if idx_np is None else torch.from_numpy(np.ascontiguousarray(idx_np).view(np.int32)).to(dev)
     sets = []
     for c in range(copies):
-        s = dict(x=x0.clone(), wq=wq0.clone(), sc=sc0.clone(), bs=bs0.clone(),
-                 idx=None if idx0 is None else idx0.clone(),
-                 y=torch.empty(w.T, w.A, w.F, dtype=torch.bfloat16, device=dev),
-                 ws=g.new_workspace(w.n, w.F, w.E, dev))
+        s = dict(x=x0.clone(), w=[t.clone() for t in weights0], idx=None if idx0 is None else idx0.clone(),
+                 y=torch.empty(w.T, w.A, w.out_cols, dtype=torch.bfloat16, device=dev), ws=ws_new())
         sets.append(s)
-    del x0, wq0, sc0, bs0, idx0
+    del x0, weights0, idx0
     torch.cuda.synchronize(dev)
 
-    fn = lib.gqmm_gather_qmm
     sptr = ctypes.c_void_p(stream.cuda_stream)
+    fn_name = fn.__name__
 
     def argv(s, sorted_flag=0):
         P = ctypes.c_void_p
-        return (P(s["x"].data_ptr()), P(s["wq"].data_ptr()), P(s["sc"].data_ptr()), P(s["bs"].data_ptr()),
-                None if s["idx"] is None else P(s["idx"].data_ptr()), w.T, w.A, w.H, w.F, w.E, 64, 4,
-                sorted_flag, P(s["y"].data_ptr()), P(s["ws"].data_ptr()), s["ws"].numel(), sptr)
+        return ((P(s["x"].data_ptr()),) + tuple(P(t.data_ptr()) for t in s["w"])
+                + (None if s["idx"] is None else P(s["idx"].data_ptr()),) + sizes
+                + (sorted_flag, P(s["y"].data_ptr()), P(s["ws"].data_ptr()), s["ws"].numel(), sptr))
 
     calls = [argv(s) for s in sets]
 
     def step(i):
         rc = fn(*calls[i % copies])
         if rc != 0:
-            raise RuntimeError(f"gqmm_gather_qmm failed: {rc} {lib.gqmm_last_error().decode()}")
+            raise RuntimeError(f"{fn_name} failed: {rc} {lib.gqmm_last_error().decode()}")
 
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
-    g.kernel_timer(args.steps)  # events are created here, before the timed region
+    timer_slots = args.steps * GEMM_LAUNCHES_PER_STEP[w.kind]
+    g.kernel_timer(timer_slots)  # events are created here, before the timed region
     g.kernel_timer(0)
 
     sampler = ClockSampler(local)
@@ -291,7 +346,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     hot_ms = max_over_ranks(h0.elapsed_time(h1), world) / hot_steps
     # Timed pass 2, the roofline: the same K steps with CUDA events around every GEMM launch
     # on the call's stream (the library's kernel timer).
-    g.kernel_timer(args.steps)
+    g.kernel_timer(timer_slots)
     barrier(world)
     torch.cuda.synchronize(dev)
     for i in range(args.steps):
@@ -301,6 +356,8 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     clocks = sampler.stop()
     n_timed, gemm_ms_total = g.kernel_timer_read()
     g.kernel_timer(0)
+    if n_timed != timer_slots:
+        raise RuntimeError(f"kernel timer recorded {n_timed} GEMM launches, expected {timer_slots}")
     status = 0
     for s in sets:
         status |= g.gqmm_device_status(s["ws"])
@@ -314,7 +371,10 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
 
     peaks, peaks_src = load_peaks()
     alg_bytes = algorithmic_bytes(w, idx_np)
-    gemm_ms = gemm_ms_total / max(n_timed, 1)
+    # GEMM launches per step: 1 for gather_qmm, 2 for the expert MLP (its gate/up and down
+    # projections); the roofline takes the step's FLOPs (bytes) over their summed durations.
+    gemm_launches_per_step = n_timed / max(args.steps, 1)
+    gemm_ms = gemm_ms_total / max(args.steps, 1)
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if flops / alg_bytes >= ridge else "hbm"
     if bound == "tensor":
@@ -337,7 +397,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     e2e_steps = max(3, min(args.steps, 200))
     x_h = inp["x"].pin_memory()
     idx_h = None if idx_np is None else torch.from_numpy(np.ascontiguousarray(idx_np).view(np.int32)).pin_memory()
-    y_h = [torch.empty(w.T, w.A, w.F, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    y_h = [torch.empty(w.T, w.A, w.out_cols, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     h2d = x_h.numel() * 2 + (0 if idx_h is None else idx_h.numel() * 4)
     d2h = y_h[0].numel() * 2
     h2d_s = torch.cuda.Stream(dev)
@@ -356,7 +416,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
                 s["idx"].copy_(idx_h, non_blocking=True)
             rc = fn(*calls[b])
             if rc != 0:
-                raise RuntimeError(f"gqmm_gather_qmm failed: {rc} {lib.gqmm_last_error().decode()}")
+                raise RuntimeError(f"{fn_name} failed: {rc} {lib.gqmm_last_error().decode()}")
             y_h[b].copy_(s["y"], non_blocking=True)
             return
         with torch.cuda.stream(h2d_s):
@@ -371,7 +431,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
             stream.wait_event(ev_out[b])  # step i - 2's result has left this set's y
         rc = fn(*calls[b])
         if rc != 0:
-            raise RuntimeError(f"gqmm_gather_qmm failed: {rc} {lib.gqmm_last_error().decode()}")
+            raise RuntimeError(f"{fn_name} failed: {rc} {lib.gqmm_last_error().decode()}")
         ev_done[b].record(stream)
         with torch.cuda.stream(d2h_s):
             d2h_s.wait_event(ev_done[b])
@@ -400,15 +460,15 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
 
-        qw = oracle.quantize(inp["w"])
+        qw = oracle_inputs(w, inp)
         rate, rows, secs, threads = oracle_rate(w, inp["x"], qw, idx_np, target_s=12.0)
         cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{rows} random rows of the workload ({rows * 2 * w.H * w.F / 1e9:.2f} GFLOP, {secs:.1f} s)"}
+               "sample": f"{rows} random rows of the workload ({w.flops / w.n * rows / 1e9:.2f} GFLOP, {secs:.1f} s)"}
 
     if rank != 0:
         return
     line = {
-        "metric": "gather_qmm TFLOPs (2*T*A*H*F/time)",
+        "metric": metric_name(w),
         "value": value,
         "unit": "TFLOP/s",
         "n_gpus": world,
@@ -420,9 +480,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "T": w.T, "A": w.A, "H": w.H, "F": w.F, "E": w.E, "group_size": 64,
-                   "bits": 4, "routing": w.routing, "sorted_indices": False,
-                   "rows_per_expert": w.n / w.E,
+        "config": {**workload_config(w), "sorted_indices": False, "rows_per_expert": w.n / w.E,
                    "l2": f"inputs rotate over {copies} copies ({copies * per_copy / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)",
                    "gpu": torch.cuda.get_device_name(dev), "seeds": {"x": wl.SEED_X, "w": wl.SEED_W, "idx": wl.SEED_IDX},
                    "parallelism": f"replicas x{world}",
@@ -430,7 +488,9 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
                            "note": "one input set repeated (L2-warm where it fits); context, not the metric"}},
         "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
                      "traffic": measured_traffic(kernel, w.name), "kernel": kernel, "kernel_ms": gemm_ms,
-                     "kernel_timing": "second timed pass of the same steps, CUDA events around each GEMM launch",
+                     "kernel_launches_per_step": gemm_launches_per_step,
+                     "kernel_timing": "second timed pass of the same steps, CUDA events around each GEMM launch;"
+                                      " kernel_ms = their summed duration per step",
                      "peak_source": f"{peaks_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"},
         "op_roofline": {"t_min_us": t_roof_s * 1e6, "frac": t_roof_s / (ms_per_step * 1e-3),
                         "algorithmic_bytes": alg_bytes, "flops": flops},
@@ -468,8 +528,10 @@ def kernel_source_sha(kernel):
 
 
 def measured_traffic(kernel, workload):
-    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu capture of this
-    workload, or None when there is none or the kernel's sources changed since it was taken."""
+    """DRAM bytes (read + write) of `kernel` from the committed ncu capture of this workload, per
+    launch, or per step where a step launches it more than once (the expert MLP's two
+    projections), matching the roofline's `achieved`; None when there is none or the kernel's
+    sources changed since it was taken."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
     if kernel not in KERNEL_SOURCES or not os.path.exists(path):
         return None
@@ -477,7 +539,7 @@ def measured_traffic(kernel, workload):
         prof = json.load(f)
     if prof.get("source_sha256") != kernel_source_sha(kernel):
         return None
-    return prof.get("dram_bytes_per_launch")
+    return prof.get("dram_bytes_per_step", prof.get("dram_bytes_per_launch"))
 
 
 def main():

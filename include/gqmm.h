@@ -76,6 +76,11 @@ typedef struct CUstream_st* gqmm_stream_t; /* identical to cudaStream_t */
 
 #define GQMM_MAX_EXPERTS 1024
 
+/* Gate activations of gqmm_moe_mlp. */
+#define GQMM_ACT_SILU 0
+#define GQMM_ACT_GELU 1
+#define GQMM_ACT_GELU_TANH 2
+
 /*
  * gqmm_quantize -- affine 4-bit group quantization (mx.quantize(w, group_size=64, bits=4)
  * in mlx #4339 "Kernel microbenchmark"), format as stated at the top of this header.
@@ -166,8 +171,13 @@ GQMM_API size_t gqmm_moe_mlp_workspace_size(int64_t n, int H, int I, int E);
  * chained up and down projection pairs; mlxcel #629 References: a fused switch MLP over
  * gather_qmm):
  *     g = x[t, a, :] . deq(W_gu[e])[0 : I]^T,   u = x[t, a, :] . deq(W_gu[e])[I : 2I]^T,
- *     y[t, a, :] = (SiLU(g) * u) . deq(W_dn[e])^T,   e = idx[t, a],   SiLU(v) = v / (1 + e^-v).
- * g and u are rounded to bfloat16 as the first projection writes them, SiLU(g) * u is
+ *     y[t, a, :] = (act(g) * u) . deq(W_dn[e])^T,   e = idx[t, a],
+ * with the gate activation act chosen by `activation` (the switch-GeGLU of mlxcel #629
+ * References and the SwiGLU of most MoE models):
+ *     GQMM_ACT_SILU       act(v) = v / (1 + e^-v)                                  (SwiGLU)
+ *     GQMM_ACT_GELU       act(v) = v/2 (1 + erf(v / sqrt 2))                       (GeGLU)
+ *     GQMM_ACT_GELU_TANH  act(v) = v/2 (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3)))   (GeGLU, tanh form)
+ * g and u are rounded to bfloat16 as the first projection writes them, act(g) * u is
  * computed in float32 and rounded to bfloat16, and each projection accumulates in float32.
  *
  *  x        bfloat16 [T, A, H], 16-byte aligned
@@ -176,6 +186,7 @@ GQMM_API size_t gqmm_moe_mlp_workspace_size(int64_t n, int H, int I, int E);
  *  wq_dn, sc_dn, bs_dn   W_dn quantized, [E, H, ...] with K = I
  *  idx, T, A, E, group_size, bits, sorted   as for gqmm_gather_qmm
  *  H        > 0, multiple of 64;   I > 0, multiple of 64 (it is the down projection's K)
+ *  activation  GQMM_ACT_SILU, GQMM_ACT_GELU or GQMM_ACT_GELU_TANH (else GQMM_ERR_UNSUPPORTED)
  *  y        out: bfloat16 [T, A, H] in (t, a) order, 16-byte aligned
  *  ws       workspace of at least gqmm_moe_mlp_workspace_size(T*A, H, I, E) bytes
  * Rows whose idx is >= E are written as zeros and set GQMM_STATUS_BAD_INDEX.
@@ -183,8 +194,8 @@ GQMM_API size_t gqmm_moe_mlp_workspace_size(int64_t n, int H, int I, int E);
  */
 GQMM_API int gqmm_moe_mlp(const void* x, const void* wq_gu, const void* sc_gu, const void* bs_gu,
                           const void* wq_dn, const void* sc_dn, const void* bs_dn, const uint32_t* idx,
-                          int64_t T, int A, int H, int I, int E, int group_size, int bits, int sorted,
-                          void* y, void* ws, size_t ws_bytes, gqmm_stream_t stream);
+                          int64_t T, int A, int H, int I, int E, int group_size, int bits, int activation,
+                          int sorted, void* y, void* ws, size_t ws_bytes, gqmm_stream_t stream);
 
 /*
  * gqmm_gather_qmm_simt -- the same operation computed on CUDA cores, one thread per output

@@ -168,10 +168,31 @@ def silu(v: np.ndarray) -> np.ndarray:
     return v / (1.0 + np.exp(-v))
 
 
-def moe_mlp(x, q_gu, q_dn, idx, E: int, group_size: int = 64, bits: int = 4, nthreads: int = 0, rows=None):
+def gelu(v: np.ndarray) -> np.ndarray:
+    """GELU in float64 by its definition v * Phi(v) = v/2 * (1 + erf(v / sqrt 2)) (Hendrycks and
+    Gimpel, "Gaussian Error Linear Units"), the gate of GeGLU (Shazeer, "GLU Variants Improve
+    Transformer")."""
+    from scipy.special import erf
+
+    return 0.5 * v * (1.0 + erf(v / np.sqrt(2.0)))
+
+
+def gelu_tanh(v: np.ndarray) -> np.ndarray:
+    """The tanh form of GELU from the same paper, in float64:
+    v/2 * (1 + tanh(sqrt(2/pi) * (v + 0.044715 v^3)))."""
+    return 0.5 * v * (1.0 + np.tanh(np.sqrt(2.0 / np.pi) * (v + 0.044715 * v ** 3)))
+
+
+# gate activations of the expert MLP, by the name the binding uses
+ACTIVATIONS = {"silu": silu, "gelu": gelu, "gelu_tanh": gelu_tanh}
+
+
+def moe_mlp(x, q_gu, q_dn, idx, E: int, group_size: int = 64, bits: int = 4, nthreads: int = 0, rows=None,
+            activation: str = "silu"):
     """The MoE expert MLP on the routed rows, in float64:
-    y[i] = W_dn[e] (SiLU(W_g[e] x[i]) * (W_u[e] x[i])), e = idx[i], with W_gu[e] = [W_g[e]; W_u[e]]
-    (gate rows 0 .. I-1, up rows I .. 2I-1) and every weight dequantized from its 4-bit codes.
+    y[i] = W_dn[e] (act(W_g[e] x[i]) * (W_u[e] x[i])), e = idx[i], with W_gu[e] = [W_g[e]; W_u[e]]
+    (gate rows 0 .. I-1, up rows I .. 2I-1) and every weight dequantized from its 4-bit codes;
+    act is SiLU (SwiGLU), GELU (GeGLU) or GELU's tanh form, by ``activation``.
     q_gu = (wq, scales, biases) for W_gu [E, 2I, H]; q_dn the same for W_dn [E, H, I].
     Rows whose index is >= E are zero.  Returns float64 [n, H] (or [len(rows), H])."""
     wq_gu, sc_gu, bs_gu = q_gu
@@ -179,7 +200,7 @@ def moe_mlp(x, q_gu, q_dn, idx, E: int, group_size: int = 64, bits: int = 4, nth
     I2 = np.asarray(wq_gu).shape[-2]
     I = I2 // 2
     gu = gather_qmm(x, wq_gu, sc_gu, bs_gu, idx, E, group_size, bits, nthreads, rows)  # [m, 2I]
-    h = silu(gu[:, :I]) * gu[:, I:]
+    h = ACTIVATIONS[activation](gu[:, :I]) * gu[:, I:]
     x16 = _u16(x)
     n = x16.reshape(-1, x16.shape[-1]).shape[0]
     r = np.arange(n) if rows is None else np.asarray(rows, np.int64)

@@ -22,7 +22,7 @@ __all__ = [
     "gqmm_moe_mlp_workspace_size", "new_mlp_workspace", "gqmm_moe_mlp",
     "gqmm_device_status", "gqmm_status_string", "launch_count", "kernel_timer",
     "kernel_timer_read", "dispatch_count", "STATUS_BAD_INDEX", "STATUS_NOT_SORTED",
-    "STATUS_TIMEOUT", "VARIANTS", "MAX_EXPERTS",
+    "STATUS_TIMEOUT", "VARIANTS", "MAX_EXPERTS", "ACTIVATIONS",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -36,6 +36,7 @@ STATUS_BAD_INDEX = 0x100
 STATUS_NOT_SORTED = 0x200
 STATUS_TIMEOUT = 0x400
 MAX_EXPERTS = 1024
+ACTIVATIONS = {"silu": 0, "gelu": 1, "gelu_tanh": 2}  # GQMM_ACT_* of gqmm_moe_mlp
 VARIANTS = {"route_unsorted": 0, "route_sorted": 1, "route_dense": 2, "gemm_tc": 3, "gemm_narrow": 4,
             "split_k": 5, "gemv": 6, "gemv_mma": 7}
 
@@ -69,7 +70,7 @@ def load_library():
             "gqmm_gather_qmm": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P, SZ, P], I),
             "gqmm_gather_qmm_simt": ([P, P, P, P, P, I64, I, I, I, I, I, I, P, P], I),
             "gqmm_moe_mlp_workspace_size": ([I64, I, I, I], SZ),
-            "gqmm_moe_mlp": ([P, P, P, P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P, SZ, P], I),
+            "gqmm_moe_mlp": ([P, P, P, P, P, P, P, P, I64, I, I, I, I, I, I, I, I, P, P, SZ, P], I),
             "gqmm_device_status": ([P, P], I),
             "gqmm_status_string": ([I], ctypes.c_char_p),
             "gqmm_last_error": ([], ctypes.c_char_p),
@@ -234,13 +235,16 @@ def new_mlp_workspace(n: int, H: int, I: int, E: int, device="cuda") -> torch.Te
 
 def gqmm_moe_mlp(x: torch.Tensor, q_gu, q_dn, idx: Optional[torch.Tensor], group_size: int = 64, bits: int = 4,
                  sorted_indices: bool = False, y: Optional[torch.Tensor] = None,
-                 ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """The MoE expert MLP: y[t, a] = W_dn[e] (SiLU(W_g[e] x[t, a]) * (W_u[e] x[t, a])), e = idx[t, a].
+                 ws: Optional[torch.Tensor] = None, stream=None, activation: str = "silu") -> torch.Tensor:
+    """The MoE expert MLP: y[t, a] = W_dn[e] (act(W_g[e] x[t, a]) * (W_u[e] x[t, a])), e = idx[t, a],
+    act one of ACTIVATIONS: "silu" (SwiGLU), "gelu" (GeGLU) or "gelu_tanh" (GeGLU, tanh form).
 
     x bf16 [T, A, H] (or [n, H]); q_gu = (wq, scales, biases) of W_gu = [W_gate; W_up]
     [E, 2I, H]; q_dn the same for W_dn [E, H, I]; idx as for gqmm_gather_qmm.  Returns y
     bf16 with x's shape.
     """
+    if activation not in ACTIVATIONS:
+        raise ValueError(f"activation must be one of {sorted(ACTIVATIONS)}, got {activation!r}")
     wq_gu, sc_gu, bs_gu = q_gu
     wq_dn, sc_dn, bs_dn = q_dn
     _need(x, "x", torch.bfloat16)
@@ -261,7 +265,8 @@ def gqmm_moe_mlp(x: torch.Tensor, q_gu, q_dn, idx: Optional[torch.Tensor], group
         ws = new_mlp_workspace(T * A, H, I, E, x.device)
     lib = load_library()
     _check(lib.gqmm_moe_mlp(_ptr(x), _ptr(wq_gu), _ptr(sc_gu), _ptr(bs_gu), _ptr(wq_dn), _ptr(sc_dn), _ptr(bs_dn),
-                            _ptr(idx), T, A, H, I, E, group_size, bits, 1 if sorted_indices else 0, _ptr(y), _ptr(ws),
+                            _ptr(idx), T, A, H, I, E, group_size, bits, ACTIVATIONS[activation],
+                            1 if sorted_indices else 0, _ptr(y), _ptr(ws),
                             ws.numel(), _stream(stream, x.device)), "gqmm_moe_mlp")
     return y
 

@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "gqmm_internal.cuh"
+#include "mlp.cuh"
 
 using namespace gqmm;
 
@@ -229,8 +230,11 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
 
 int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, const void* bs_gu, const void* wq_dn,
                        const void* sc_dn, const void* bs_dn, const uint32_t* idx, int64_t T, int A, int H, int I, int E,
-                       int group_size, int bits, int sorted, void* y, void* ws, size_t ws_bytes, cudaStream_t s) {
+                       int group_size, int bits, int activation, int sorted, void* y, void* ws, size_t ws_bytes,
+                       cudaStream_t s) {
   if (I <= 0 || I > (1 << 29)) return fail(GQMM_ERR_SHAPE, "I must be in [1, 2^29] (got %d)", I);
+  if (activation != GQMM_ACT_SILU && activation != GQMM_ACT_GELU && activation != GQMM_ACT_GELU_TANH)
+    return fail(GQMM_ERR_UNSUPPORTED, "unknown activation %d", activation);
   // gate/up projection: K = H, 2I output columns; down projection: K = I, H output columns
   int rc = validate_gather(x, wq_gu, sc_gu, bs_gu, idx, T, A, H, 2 * I, E, group_size, bits, y);
   if (rc) return rc;
@@ -304,7 +308,7 @@ int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, cons
   rc = launch_projection(g1, shape1, sms, s, "moe_mlp gate/up", route_variant);
   if (rc) return rc;
 
-  e = launch_swiglu(h1, hg, n, I, header, sms, s);
+  e = launch_glu(h1, hg, n, I, activation, header, sms, s);
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "gating launch: %s", cudaGetErrorString(e));
   g_launches.fetch_add(1);
 
@@ -400,9 +404,10 @@ size_t gqmm_moe_mlp_workspace_size(int64_t n, int H, int I, int E) {
 
 int gqmm_moe_mlp(const void* x, const void* wq_gu, const void* sc_gu, const void* bs_gu, const void* wq_dn,
                  const void* sc_dn, const void* bs_dn, const uint32_t* idx, int64_t T, int A, int H, int I, int E,
-                 int group_size, int bits, int sorted, void* y, void* ws, size_t ws_bytes, gqmm_stream_t stream) {
-  return gqmm::moe_mlp_impl(x, wq_gu, sc_gu, bs_gu, wq_dn, sc_dn, bs_dn, idx, T, A, H, I, E, group_size, bits, sorted,
-                            y, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+                 int group_size, int bits, int activation, int sorted, void* y, void* ws, size_t ws_bytes,
+                 gqmm_stream_t stream) {
+  return gqmm::moe_mlp_impl(x, wq_gu, sc_gu, bs_gu, wq_dn, sc_dn, bs_dn, idx, T, A, H, I, E, group_size, bits,
+                            activation, sorted, y, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* scales, const void* biases,

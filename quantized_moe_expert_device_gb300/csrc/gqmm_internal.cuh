@@ -148,27 +148,6 @@ int gather_qmm_impl(const void* x, const void* wq, const void* scales, const voi
                     int64_t T, int A, int H, int F, int E, int group_size, int bits, int sorted, void* y, void* ws,
                     size_t ws_bytes, cudaStream_t s, bool allow_split);
 
-// Workspace of the MoE expert MLP: the route/plan region of a gate/up gather (no K split),
-// then the gate/up output [n, 2I] and the gated intermediate [n, I], bf16, in sorted row order.
-struct MlpLayout {
-  WsLayout route;
-  size_t h1, h, total;
-};
-inline MlpLayout mlp_ws_layout(int64_t n, int H, int I, int E) {
-  (void)H;
-  MlpLayout M;
-  M.route = ws_layout(n, 2 * I, E, false);
-  size_t off = align256(M.route.total);
-  M.h1 = off;
-  off = align256(off + (size_t)(n > 0 ? n : 1) * 2 * (size_t)I * 2);
-  M.h = off;
-  off = align256(off + (size_t)(n > 0 ? n : 1) * (size_t)I * 2);
-  M.total = off;
-  return M;
-}
-int moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, const void* bs_gu, const void* wq_dn,
-                 const void* sc_dn, const void* bs_dn, const uint32_t* idx, int64_t T, int A, int H, int I, int E,
-                 int group_size, int bits, int sorted, void* y, void* ws, size_t ws_bytes, cudaStream_t s);
 
 // ------------------------------------------------------------------------------------------
 // Kernel launchers (defined in the .cu files).  All return cudaError_t of the launch.
@@ -229,9 +208,6 @@ cudaError_t launch_gemv_fma(const GemmArgs& a, int rows, int sms, cudaStream_t s
 bool gemv_mma_supported(int rows, int H);
 cudaError_t launch_gemv_mma(const GemmArgs& a, int rows, int sms, cudaStream_t s);
 cudaError_t launch_gemv(const GemmArgs& a, int rows, int sms, cudaStream_t s);
-// SiLU gating of the MLP's gate/up output (sorted rows); also resets header->next_unit.
-cudaError_t launch_swiglu(const __nv_bfloat16* h1, __nv_bfloat16* h, int64_t n, int I, WsHeader* header, int sms,
-                          cudaStream_t s);
 bool gemv_uses_mma(int rows, int H, int E);  // which of the two launch_gemv runs
 
 cudaError_t launch_gemm_simt(const __nv_bfloat16* x, const uint8_t* wq,

@@ -1,9 +1,13 @@
-"""Pins for the oracle's MoE expert MLP (y = W_dn (SiLU(W_g x) * (W_u x)) per routed row),
-against a brute-force loop with its own nibble decode, a closed form on exactly representable
-weights, and invariants.  None of these calls the oracle's own dequantization."""
+"""Pins for the oracle's MoE expert MLP (y = W_dn (act(W_g x) * (W_u x)) per routed row, act =
+SiLU, GELU or GELU's tanh form), against a brute-force loop with its own nibble decode, a closed
+form on exactly representable weights, and invariants; and pins for the three activations
+against printed values, identities and PyTorch's float64 implementations.  None of these calls
+the oracle's own dequantization."""
 import math
 
 import numpy as np
+import pytest
+import torch
 
 import oracle
 import workloads as wl
@@ -19,13 +23,43 @@ def _decode(wq, sc, bs, e, f, h):
     return _bits_to_f64(sc[e, f, h // 64]) * code + _bits_to_f64(bs[e, f, h // 64])
 
 
-def test_mlp_brute_force_tiny():
+_ACT = {"silu": lambda v: v / (1.0 + math.exp(-v)),
+        "gelu": lambda v: 0.5 * v * (1.0 + math.erf(v / math.sqrt(2.0))),
+        "gelu_tanh": lambda v: 0.5 * v * (1.0 + math.tanh(math.sqrt(2.0 / math.pi) * (v + 0.044715 * v ** 3)))}
+
+
+def test_activation_values_and_identities():
+    # Phi(1) = 0.8413447460685429 (standard normal table), so GELU(1) = Phi(1) and GELU(-1) = Phi(1) - 1
+    np.testing.assert_allclose(oracle.gelu(np.array([1.0, -1.0, 0.0])), [0.8413447460685429, -0.1586552539314571, 0.0],
+                               rtol=0, atol=1e-15)
+    # SiLU(1) = 1 / (1 + e^-1); SiLU(-v) = SiLU(v) - v
+    assert oracle.silu(np.array([1.0]))[0] == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), abs=1e-16)
+    v = np.random.default_rng(5).normal(0, 3, 1000)
+    for f in (oracle.silu, oracle.gelu, oracle.gelu_tanh):
+        np.testing.assert_allclose(f(v) - f(-v), v, rtol=0, atol=1e-12)  # act(v) = v * (odd-symmetric CDF)
+    # the tanh form stays within 5e-4 of the exact GELU on [-6, 6] (its published accuracy)
+    grid = np.linspace(-6, 6, 4001)
+    assert np.abs(oracle.gelu_tanh(grid) - oracle.gelu(grid)).max() < 5e-4
+
+
+def test_activations_match_torch_float64():
+    v = np.random.default_rng(6).normal(0, 4, 4096)
+    t = torch.from_numpy(v)
+    np.testing.assert_allclose(oracle.silu(v), torch.nn.functional.silu(t).numpy(), rtol=1e-14, atol=1e-15)
+    np.testing.assert_allclose(oracle.gelu(v), torch.nn.functional.gelu(t).numpy(), rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(oracle.gelu_tanh(v), torch.nn.functional.gelu(t, approximate="tanh").numpy(),
+                               rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("activation", ["silu", "gelu", "gelu_tanh"])
+def test_mlp_brute_force_tiny(activation):
     E, I, H, n = 3, 64, 64, 5  # one quantization group per row in both projections
     q_gu = oracle.quantize(wl.normal_bf16((E, 2 * I, H), 11))
     q_dn = oracle.quantize(wl.normal_bf16((E, H, I), 12))
     x = wl.normal_bf16((n, H), 13)
     idx = np.array([2, 0, 1, 5, 2], np.uint32)  # 5 >= E: a zero row
-    y = oracle.moe_mlp(x, q_gu, q_dn, idx, E)
+    y = oracle.moe_mlp(x, q_gu, q_dn, idx, E, activation=activation)
+    act = _ACT[activation]
     xf = _bits_to_f64(wl.bf16_bits(x))
     ref = np.zeros((n, H))
     for i in range(n):
@@ -34,7 +68,7 @@ def test_mlp_brute_force_tiny():
             continue
         g = [sum(xf[i, h] * _decode(*q_gu, e, f, h) for h in range(H)) for f in range(I)]
         u = [sum(xf[i, h] * _decode(*q_gu, e, I + f, h) for h in range(H)) for f in range(I)]
-        hh = [g[k] / (1.0 + math.exp(-g[k])) * u[k] for k in range(I)]
+        hh = [act(g[k]) * u[k] for k in range(I)]
         for o in range(H):
             ref[i, o] = sum(hh[k] * _decode(*q_dn, e, o, k) for k in range(I))
     np.testing.assert_allclose(y, ref, rtol=1e-11, atol=1e-11)

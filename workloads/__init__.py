@@ -127,6 +127,8 @@ class Workload:
     w_std: float = 1.0
     r: int = 0              # rows per expert for "balanced"
     note: str = ""
+    kind: str = "gather"    # "gather": one projection, F output columns;
+                            # "mlp": the expert MLP, F = intermediate width I (gate/up 2F rows, down H rows)
 
     @property
     def n(self) -> int:
@@ -134,7 +136,12 @@ class Workload:
 
     @property
     def flops(self) -> int:
-        return 2 * self.T * self.A * self.H * self.F
+        per = 6 if self.kind == "mlp" else 2  # mlp: 2*n*H*2I (gate/up) + 2*n*I*H (down)
+        return per * self.T * self.A * self.H * self.F
+
+    @property
+    def out_cols(self) -> int:
+        return self.H if self.kind == "mlp" else self.F
 
 
 def workloads() -> Dict[str, Workload]:
@@ -151,6 +158,12 @@ def workloads() -> Dict[str, Workload]:
                                     note=f"rows-per-expert sweep, exactly {r} rows per expert")
     w["mixtral"] = Workload("mixtral", T=2048, A=2, H=4096, F=14336, E=8, routing="zipf", w_std=0.02,
                             note="Mixtral-like expert shape, Zipf(1.1)-skewed top-2 routing")
+    w["mlp_tiny"] = Workload("mlp_tiny", T=16, A=2, H=256, F=128, E=8, routing="uniform", kind="mlp",
+                             note="expert MLP correctness case")
+    w["mlp_e64"] = Workload("mlp_e64", T=2048, A=8, H=2048, F=768, E=64, routing="uniform", kind="mlp",
+                            note="expert MLP (gate/up + SiLU + down) on the MoE prefill microbenchmark shape")
+    w["mlp_decode_m8"] = Workload("mlp_decode_m8", T=8, A=8, H=2048, F=768, E=128, routing="topk_distinct",
+                                  kind="mlp", note="expert MLP, MoE decode, 8 tokens, top-8")
     for m in (1, 2, 4, 8):
         w[f"decode_dense_m{m}"] = Workload(f"decode_dense_m{m}", T=m, A=1, H=4096, F=14336, E=1,
                                            routing="dense", note="dense decode, M rows")
@@ -174,8 +187,14 @@ def make_idx(wl: Workload, seed: int = SEED_IDX) -> Optional[np.ndarray]:
 
 
 def make_inputs(wl: Workload, seed_x: int = SEED_X, seed_w: int = SEED_W, seed_idx: int = SEED_IDX):
-    """Returns dict(x=bf16 [T, A, H], w=bf16 [E, F, H], idx=uint32 [T, A] or None)."""
+    """Returns dict(x=bf16 [T, A, H], w=bf16 [E, F, H], idx=uint32 [T, A] or None); for an
+    "mlp" workload w_gu=bf16 [E, 2F, H] ~ N(0, 1/H) and w_dn=bf16 [E, H, F] ~ N(0, 1/F) in place
+    of w, scaled so the gate pre-activations are about N(0, 1)."""
     x = normal_bf16((wl.T, wl.A, wl.H), seed_x)
+    if wl.kind == "mlp":
+        w_gu = normal_bf16((wl.E, 2 * wl.F, wl.H), seed_w, std=wl.H ** -0.5, chunk_rows=1)
+        w_dn = normal_bf16((wl.E, wl.H, wl.F), seed_w + 1, std=wl.F ** -0.5, chunk_rows=1)
+        return dict(x=x, w_gu=w_gu, w_dn=w_dn, idx=make_idx(wl, seed_idx))
     w = normal_bf16((wl.E, wl.F, wl.H), seed_w, std=wl.w_std, chunk_rows=1)
     return dict(x=x, w=w, idx=make_idx(wl, seed_idx))
 
