@@ -56,8 +56,8 @@ def algorithmic_bytes(w: wl.Workload, idx: np.ndarray | None) -> int:
     hidden rows are intermediates, not counted: a kernel that kept them on chip moves none)."""
     hit = w.E if idx is None else len(np.unique(idx))
 
-    def qbytes(rows, K):  # one expert's packed codes + bf16 scale and bias per 64-wide group
-        return rows * (K // 2 + 4 * (K // 64))
+    def qbytes(rows, K):  # one expert's packed codes + bf16 scale and bias per group
+        return rows * (K // 2 + 4 * (K // w.group_size))
 
     weights = hit * (qbytes(2 * w.F, w.H) + qbytes(w.H, w.F) if w.kind == "mlp" else qbytes(w.F, w.H))
     return int(weights + w.n * w.H * 2 + w.n * w.out_cols * 2 + (0 if idx is None else w.n * 4))
@@ -158,8 +158,9 @@ def oracle_inputs(w: wl.Workload, inp):
     import oracle
 
     if w.kind == "mlp":
-        return oracle.quantize(inp["w_gu"]), oracle.quantize(inp["w_dn"])
-    return oracle.quantize(inp["w"])
+        return (oracle.quantize(inp["w_gu"], group_size=w.group_size),
+                oracle.quantize(inp["w_dn"], group_size=w.group_size))
+    return oracle.quantize(inp["w"], group_size=w.group_size)
 
 
 def oracle_rows(w: wl.Workload, x_cpu, qw, idx, rows):
@@ -167,9 +168,9 @@ def oracle_rows(w: wl.Workload, x_cpu, qw, idx, rows):
     import oracle
 
     if w.kind == "mlp":
-        oracle.moe_mlp(x_cpu, qw[0], qw[1], idx, w.E, rows=rows)
+        oracle.moe_mlp(x_cpu, qw[0], qw[1], idx, w.E, group_size=w.group_size, rows=rows)
     else:
-        oracle.gather_qmm(x_cpu, *qw, idx, w.E, rows=rows)
+        oracle.gather_qmm(x_cpu, *qw, idx, w.E, group_size=w.group_size, rows=rows)
     return oracle.gather_qmm.last_threads
 
 
@@ -200,7 +201,7 @@ def metric_name(w: wl.Workload) -> str:
 def workload_config(w: wl.Workload) -> dict:
     c = {"workload": w.name, "T": w.T, "A": w.A, "H": w.H}
     c.update({"I": w.F} if w.kind == "mlp" else {"F": w.F})
-    c.update({"E": w.E, "group_size": 64, "bits": 4, "routing": w.routing})
+    c.update({"E": w.E, "group_size": w.group_size, "bits": 4, "routing": w.routing})
     if w.kind == "mlp":
         c["op"] = "gqmm_moe_mlp: gate/up projection, act(gate) * up, down projection"
         c["activation"] = MLP_ACTIVATION
@@ -264,16 +265,16 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
         weights0 = []
         for key in ("w_gu", "w_dn"):
             w_dev = inp[key].to(dev)
-            weights0 += list(g.gqmm_quantize(w_dev))
+            weights0 += list(g.gqmm_quantize(w_dev, group_size=w.group_size))
             del w_dev
         fn, ws_new = lib.gqmm_moe_mlp, (lambda: g.new_mlp_workspace(w.n, w.H, w.F, w.E, dev))
-        sizes = (w.T, w.A, w.H, w.F, w.E, 64, 4, g.ACTIVATIONS[MLP_ACTIVATION])
+        sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4, g.ACTIVATIONS[MLP_ACTIVATION])
     else:
         w_dev = inp["w"].to(dev)
-        weights0 = list(g.gqmm_quantize(w_dev))
+        weights0 = list(g.gqmm_quantize(w_dev, group_size=w.group_size))
         del w_dev
         fn, ws_new = lib.gqmm_gather_qmm, (lambda: g.new_workspace(w.n, w.F, w.E, dev))
-        sizes = (w.T, w.A, w.H, w.F, w.E, 64, 4)
+        sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4)
     x0 = inp["x"].to(dev)
     idx0 = None if idx_np is None else torch.from_numpy(np.ascontiguousarray(idx_np).view(np.int32)).to(dev)
     sets = []

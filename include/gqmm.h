@@ -29,8 +29,8 @@
  *    most recent non-OK return.
  *
  * Quantized weight format (the reading this library takes of mx.quantize(..., 64, 4); the
- * pages name the call but do not print its formula): for each group of 64 consecutive
- * weights along H,
+ * pages name the call but do not print its formula): for each group of group_size (64; also
+ * 32 or 128) consecutive weights along H,
  *     scale = bf16((max - min) / 15)  (IEEE float32 division, round to nearest even)
  *     bias  = min                     (exact)
  *     q     = clamp(round_half_even((w - bias) / scale), 0, 15)  using the stored scale
@@ -38,8 +38,8 @@
  *     byte j of a row = q[2j] | (q[2j + 1] << 4)
  * and deq(q) = scale * q + bias.  Shapes for E experts of F x H weights:
  *     wq      uint8     [E, F, H/2]
- *     scales  bfloat16  [E, F, H/64]
- *     biases  bfloat16  [E, F, H/64]
+ *     scales  bfloat16  [E, F, H/group_size]
+ *     biases  bfloat16  [E, F, H/group_size]
  */
 #ifndef GQMM_H
 #define GQMM_H
@@ -63,7 +63,7 @@ typedef struct CUstream_st* gqmm_stream_t; /* identical to cudaStream_t */
 #define GQMM_OK 0
 #define GQMM_ERR_NULL 1         /* a required pointer is NULL */
 #define GQMM_ERR_SHAPE 2        /* a size is out of range (see each entry point) */
-#define GQMM_ERR_UNSUPPORTED 3  /* group_size != 64, bits != 4, or E above GQMM_MAX_EXPERTS */
+#define GQMM_ERR_UNSUPPORTED 3  /* group_size not 32/64/128, bits != 4, or E above GQMM_MAX_EXPERTS */
 #define GQMM_ERR_ALIGN 4        /* a pointer is not aligned as required */
 #define GQMM_ERR_WORKSPACE 5    /* workspace too small or misaligned */
 #define GQMM_ERR_CUDA 6         /* a CUDA runtime/driver call or a kernel launch failed */
@@ -86,10 +86,11 @@ typedef struct CUstream_st* gqmm_stream_t; /* identical to cudaStream_t */
  * in mlx #4339 "Kernel microbenchmark"), format as stated at the top of this header.
  *
  *  w       bfloat16 [rows, H] (for E experts of F x H weights, rows = E*F), 16-byte aligned
- *  rows    >= 0;  H > 0 and H % 64 == 0
- *  group_size must be 64, bits must be 4
+ *  rows    >= 0;  H > 0, H % 64 == 0 and H % group_size == 0
+ *  group_size 32, 64 or 128 (64 is the pages' setting; 32 and 128 are the other group sizes
+ *          of the same affine format), bits must be 4
  *  wq      out: uint8 [rows, H/2], 16-byte aligned
- *  scales  out: bfloat16 [rows, H/64];  biases  out: bfloat16 [rows, H/64]
+ *  scales  out: bfloat16 [rows, H/group_size];  biases  out: bfloat16 [rows, H/group_size]
  * Results are bit-identical to the float32 reference formula above (no fast math).
  * Errors: GQMM_ERR_NULL, GQMM_ERR_SHAPE, GQMM_ERR_UNSUPPORTED, GQMM_ERR_ALIGN, GQMM_ERR_CUDA.
  */
@@ -140,8 +141,9 @@ GQMM_API int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* per
  *  idx      uint32 [T, A] expert per row, or NULL for the dense quantized matmul
  *           (mx.quantized_matmul, same issue), which requires E == 1
  *  T, A     T >= 1, A >= 1, T*A <= 2^31 - 1
- *  H        > 0, multiple of 64;   F > 0, multiple of 16;   E in [1, GQMM_MAX_EXPERTS]
- *  group_size 64, bits 4
+ *  H        > 0, multiple of 64 and of group_size;   F > 0, multiple of 16;   E in [1, GQMM_MAX_EXPERTS]
+ *  group_size 32, 64 or 128 (the weight-streaming kernels of decode-sized calls take 64; other
+ *           group sizes run those calls on the tensor-core GEMM), bits 4
  *  sorted   0: idx in any order (the library sorts rows by expert on device);
  *           1: the caller promises idx is nondecreasing in flat order (the issue's
  *              sorted_indices=True).  The result is identical either way; a broken

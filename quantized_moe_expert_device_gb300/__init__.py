@@ -164,6 +164,12 @@ def gqmm_route_sort(idx: torch.Tensor, E: int, ws: Optional[torch.Tensor] = None
     return perm, offsets
 
 
+def _check_groups(scales: torch.Tensor, K: int, group_size: int, name: str):
+    if group_size <= 0 or scales.shape[-1] * group_size != K:
+        raise ValueError(f"{name} has {scales.shape[-1]} groups per row; K={K} with group_size={group_size} "
+                         f"needs {K // max(group_size, 1)}")
+
+
 def _gather_shapes(x: torch.Tensor, idx: Optional[torch.Tensor], wq: torch.Tensor):
     H = x.shape[-1]
     if idx is None:
@@ -185,7 +191,7 @@ def gqmm_gather_qmm(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, bia
     """y[t, a, :] = x[t, a, :] . deq(W[idx[t, a]])^T.
 
     x bf16 [T, A, H] (or [T, A, 1, H], or [n, H]); wq uint8 [E, F, H/2]; scales/biases bf16
-    [E, F, H/64]; idx uint32/int32 [T, A] or None (dense, E == 1).  Returns y bf16 with
+    [E, F, H/group_size] (group_size 32, 64 or 128); idx uint32/int32 [T, A] or None (dense, E == 1).  Returns y bf16 with
     x's leading shape and last dimension F.
     """
     _need(x, "x", torch.bfloat16)
@@ -195,6 +201,7 @@ def gqmm_gather_qmm(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, bia
     if idx is not None and (not idx.is_cuda or not idx.is_contiguous() or idx.element_size() != 4):
         raise ValueError("idx must be a contiguous 32-bit CUDA tensor")
     T, A, H, F, E = _gather_shapes(x, idx, wq)
+    _check_groups(scales, H, group_size, "scales")
     if y is None:
         y = torch.empty(tuple(x.shape[:-1]) + (F,), dtype=torch.bfloat16, device=x.device)
     else:
@@ -213,6 +220,7 @@ def gqmm_gather_qmm_simt(x, wq, scales, biases, idx, group_size: int = 64, bits:
     """CUDA-core cross-check of gqmm_gather_qmm (same arguments, no workspace)."""
     _need(x, "x", torch.bfloat16)
     T, A, H, F, E = _gather_shapes(x, idx, wq)
+    _check_groups(scales, H, group_size, "scales")
     if y is None:
         y = torch.empty(tuple(x.shape[:-1]) + (F,), dtype=torch.bfloat16, device=x.device)
     lib = load_library()
@@ -257,6 +265,8 @@ def gqmm_moe_mlp(x: torch.Tensor, q_gu, q_dn, idx: Optional[torch.Tensor], group
     I = I2 // 2
     if tuple(wq_dn.shape[:2]) != (E, H) or wq_dn.shape[2] * 2 != I:
         raise ValueError(f"wq_dn must be [E, H, I/2] = [{E}, {H}, {I // 2}], got {tuple(wq_dn.shape)}")
+    _check_groups(sc_gu, H, group_size, "sc_gu")
+    _check_groups(sc_dn, I, group_size, "sc_dn")
     if y is None:
         y = torch.empty(tuple(x.shape), dtype=torch.bfloat16, device=x.device)
     else:

@@ -90,11 +90,12 @@ int validate_gather(const void* x, const void* wq, const void* scales, const voi
                     const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size,
                     int bits, const void* y) {
   if (!x || !wq || !scales || !biases || !y) return fail(GQMM_ERR_NULL, "x, wq, scales, biases and y must be non-NULL");
-  if (group_size != 64 || bits != 4)
-    return fail(GQMM_ERR_UNSUPPORTED, "only group_size=64, bits=4 are supported (got %d, %d)", group_size, bits);
+  if ((group_size != 32 && group_size != 64 && group_size != 128) || bits != 4)
+    return fail(GQMM_ERR_UNSUPPORTED, "need group_size 32, 64 or 128 and bits=4 (got %d, %d)", group_size, bits);
   if (T < 1 || A < 1 || T * (int64_t)A > 2147483647LL)
     return fail(GQMM_ERR_SHAPE, "need T >= 1, A >= 1, T*A < 2^31 (got T=%lld A=%d)", (long long)T, A);
-  if (H <= 0 || H % 64) return fail(GQMM_ERR_SHAPE, "H must be a positive multiple of 64 (got %d)", H);
+  if (H <= 0 || H % 64 || H % group_size)
+    return fail(GQMM_ERR_SHAPE, "H must be a positive multiple of 64 and of group_size (got %d, %d)", H, group_size);
   if (F <= 0 || F % 16) return fail(GQMM_ERR_SHAPE, "F must be a positive multiple of 16 (got %d)", F);
   if (E < 1) return fail(GQMM_ERR_SHAPE, "E must be >= 1 (got %d)", E);
   if (E > GQMM_MAX_EXPERTS) return fail(GQMM_ERR_UNSUPPORTED, "E=%d exceeds %d", E, GQMM_MAX_EXPERTS);
@@ -167,6 +168,7 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   const WsLayout L = ws_layout(n, F, E, allow_split);
   UnitShape shape = unit_shape(n, H, F, E);
   if (!allow_split) shape.ksplit = 1;
+  if (group_size != 64) shape.stream = false;  // the weight-streaming kernels take 64-wide groups
   if (!aligned(ws, 256) || ws_bytes < L.total)
     return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
   rc = check_device(nullptr);
@@ -222,6 +224,7 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   ga.dense_plan = idx == nullptr ? 1 : 0;
   ga.acc = L.has_acc ? reinterpret_cast<float*>(w + L.acc) : nullptr;
   ga.offsets = ra.offsets;
+  ga.group_size = group_size;
   rc = launch_projection(ga, shape, sms, s, "gather_qmm", route_variant);
   if (rc) return rc;
   return ok();
@@ -252,6 +255,7 @@ int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, cons
   UnitShape shape1 = unit_shape(n, H, 2 * I, E);
   UnitShape shape2 = unit_shape(n, I, H, E);
   shape1.ksplit = shape2.ksplit = 1;  // one work list serves both: no K split, no partial-sum planes
+  if (group_size != 64) shape1.stream = shape2.stream = false;  // streaming kernels: 64-wide groups
   uint8_t* w = static_cast<uint8_t*>(ws);
   WsHeader* header = reinterpret_cast<WsHeader*>(w);
   __nv_bfloat16* h1 = reinterpret_cast<__nv_bfloat16*>(w + M.h1);
@@ -305,6 +309,7 @@ int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, cons
   g1.chunk_rows = shape1.chunk_rows;
   g1.ks_cap = 1;
   g1.dense_plan = idx == nullptr ? 1 : 0;
+  g1.group_size = group_size;
   rc = launch_projection(g1, shape1, sms, s, "moe_mlp gate/up", route_variant);
   if (rc) return rc;
 
@@ -333,18 +338,19 @@ extern "C" {
 int gqmm_quantize(const void* w, int64_t rows, int64_t H, int group_size, int bits, void* wq,
                   void* scales, void* biases, gqmm_stream_t stream) {
   if (!w || !wq || !scales || !biases) return fail(GQMM_ERR_NULL, "w, wq, scales, biases must be non-NULL");
-  if (group_size != 64 || bits != 4)
-    return fail(GQMM_ERR_UNSUPPORTED, "only group_size=64, bits=4 are supported (got %d, %d)", group_size, bits);
-  if (rows < 0 || H <= 0 || H % 64) return fail(GQMM_ERR_SHAPE, "need rows >= 0 and H a positive multiple of 64");
+  if ((group_size != 32 && group_size != 64 && group_size != 128) || bits != 4)
+    return fail(GQMM_ERR_UNSUPPORTED, "need group_size 32, 64 or 128 and bits=4 (got %d, %d)", group_size, bits);
+  if (rows < 0 || H <= 0 || H % 64 || H % group_size)
+    return fail(GQMM_ERR_SHAPE, "need rows >= 0 and H a positive multiple of 64 and of group_size");
   if (!aligned(w, 16) || !aligned(wq, 16)) return fail(GQMM_ERR_ALIGN, "w and wq must be 16-byte aligned");
   if (!aligned(scales, 2) || !aligned(biases, 2)) return fail(GQMM_ERR_ALIGN, "scales and biases must be 2-byte aligned");
   int rc = check_device(nullptr);
   if (rc) return rc;
-  cudaError_t e = launch_quantize(static_cast<const __nv_bfloat16*>(w), rows, H, static_cast<uint8_t*>(wq),
+  cudaError_t e = launch_quantize(static_cast<const __nv_bfloat16*>(w), rows, H, group_size, static_cast<uint8_t*>(wq),
                                   static_cast<__nv_bfloat16*>(scales), static_cast<__nv_bfloat16*>(biases),
                                   reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(e));
-  if (rows * (H / 64) > 0) g_launches.fetch_add(1);
+  if (rows * (H / group_size) > 0) g_launches.fetch_add(1);
   return ok();
 }
 
@@ -419,7 +425,7 @@ int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* scales, cons
   if (rc) return rc;
   cudaError_t e = launch_gemm_simt(static_cast<const __nv_bfloat16*>(x), static_cast<const uint8_t*>(wq),
                                    static_cast<const __nv_bfloat16*>(scales), static_cast<const __nv_bfloat16*>(biases),
-                                   idx, T * (int64_t)A, H, F, E, static_cast<__nv_bfloat16*>(y),
+                                   idx, T * (int64_t)A, H, F, E, group_size, static_cast<__nv_bfloat16*>(y),
                                    reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "simt launch: %s", cudaGetErrorString(e));
   g_launches.fetch_add(1);

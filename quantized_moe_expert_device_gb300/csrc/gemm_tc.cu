@@ -189,7 +189,7 @@ __device__ __forceinline__ uint4 deq8(uint32_t w, uint32_t s2, uint32_t b2) {
   return o;
 }
 
-template <class C>
+template <class C, int GS>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_wq, const __grid_constant__ CUtensorMap tmap_x,
                    const GemmArgs p) {
@@ -239,8 +239,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dependents_launch();  // the split-K finalize may be scheduled; it waits for this grid
 
   const int H = p.H, F = p.F;
-  const int G = H / BK;
-  const int num_kb = G;
+  static_assert(GS == 32 || GS == 64 || GS == 128, "group sizes");
+  const int num_kb = H / BK;
+  const int G = H / GS;  // scale groups per weight row
 
   // Unit queue: the scheduler (TMA thread) pushes decoded units; every consumer warp pops
   // each entry in order and releases it once its lanes hold a copy.
@@ -532,9 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(p.scales);
     const uint16_t* bs16 = reinterpret_cast<const uint16_t*>(p.biases);
     // Flat walk over (unit, k-block) steps in queue order; this group processes every
-    // DEQ_GROUPS-th step.  Scales and biases come one step ahead: when H/64 is a multiple of 8, as one
-    // 16-byte load each covering eight groups of the thread's row (reloaded when the step
-    // leaves the block of eight); else one 2-byte load each per step.
+    // DEQ_GROUPS-th step.  Scales and biases come one step ahead: when the row's group count
+    // H/GS is a multiple of 8, as one 16-byte load each covering eight groups of the thread's
+    // row (reloaded when the step leaves the block of eight); else 2-byte loads per step (two
+    // each for 32-wide groups).
     const bool sb_vec = (G & 7) == 0;
     uint32_t qi = 0;
     bool ok = true;
@@ -557,24 +559,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // scale / bias block of the thread's row in unit U: eight bf16 (sb_vec) or one (low half
     // of .x); zero for rows past F (their outputs are dropped)
     uint4 sblk = make_uint4(0, 0, 0, 0), bblk = make_uint4(0, 0, 0, 0);
+    // The scale group of k-block kb's codes: kb for 64-wide groups, kb / 2 for 128-wide ones;
+    // for 32-wide groups the block's first 32 codes are group 2 kb and the other 32 group 2 kb + 1.
+    auto grp_of = [](int kb) -> int { return GS == 64 ? kb : GS == 128 ? (kb >> 1) : (kb << 1); };
     auto load_sb = [&](const UnitEntry& U, int kb) {
       if (!U.valid || U.f0 + r >= F) {
         sblk = bblk = make_uint4(0, 0, 0, 0);
         return;
       }
       const int64_t row = (int64_t)(U.expert * F + U.f0) + r;  // E * F fits in int
+      const int g = grp_of(kb);
       if (sb_vec) {
-        sblk = __ldg(reinterpret_cast<const uint4*>(sc16 + row * G) + (kb >> 3));
-        bblk = __ldg(reinterpret_cast<const uint4*>(bs16 + row * G) + (kb >> 3));
+        sblk = __ldg(reinterpret_cast<const uint4*>(sc16 + row * G) + (g >> 3));
+        bblk = __ldg(reinterpret_cast<const uint4*>(bs16 + row * G) + (g >> 3));
       } else {
-        sblk.x = __ldg(sc16 + row * G + kb);
-        bblk.x = __ldg(bs16 + row * G + kb);
+        sblk.x = __ldg(sc16 + row * G + g);
+        bblk.x = __ldg(bs16 + row * G + g);
+        if (GS == 32) {
+          sblk.y = __ldg(sc16 + row * G + g + 1);
+          bblk.y = __ldg(bs16 + row * G + g + 1);
+        }
       }
     };
-    // (v, v) as bf16x2 for the block's element of k-block kb
-    auto pick = [&](const uint4& blk, int kb) -> uint32_t {
-      if (!sb_vec) return splat16(blk.x);
-      const int j = kb & 7;
+    // (v, v) as bf16x2 for the block's element of group g (second: the block's second group,
+    // g + 1, of a 32-wide k-block)
+    auto pick = [&](const uint4& blk, int g, bool second) -> uint32_t {
+      if (!sb_vec) return splat16(second ? blk.y : blk.x);
+      const int j = g & 7;
       const uint32_t w = (j & 4) ? ((j & 2) ? blk.w : blk.z) : ((j & 2) ? blk.y : blk.x);
       return __byte_perm(w, 0, (j & 1) ? 0x3232 : 0x1010);
     };
@@ -586,7 +597,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // stage indices and phase parities of the current step (global step index grp, grp+2, ...)
     uint32_t sn = grp, phn = 0, sa = grp, pha = 0;
     while (ok && U.valid) {
-      const uint32_t s2 = pick(sblk, kb), b2 = pick(bblk, kb);
+      const int g = grp_of(kb);
+      const uint32_t s2 = pick(sblk, g, false), b2 = pick(bblk, g, false);
+      // 32-wide groups: the row's second 32 codes (n1 below) have their own scale and bias
+      const uint32_t s2b = GS == 32 ? pick(sblk, g + 1, true) : s2;
+      const uint32_t b2b = GS == 32 ? pick(bblk, g + 1, true) : b2;
       // the next step of this group: same unit, or carried into the following ones
       int kbn = kb + C::DEQ_GROUPS;
       UnitEntry Un;
@@ -595,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         Un = U;
         normalize(Un, kbn);
         load_sb(Un, kbn);
-      } else if (!sb_vec || (kbn >> 3) != (kb >> 3)) {
+      } else if (!sb_vec || (grp_of(kbn) >> 3) != (g >> 3)) {
         load_sb(U, kbn);
       }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(C::nib_full(sn)), phn, abort_flag, status))) break;
@@ -617,10 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       o[1] = deq8(n0.y, s2, b2);
       o[2] = deq8(n0.z, s2, b2);
       o[3] = deq8(n0.w, s2, b2);
-      o[4] = deq8(n1.x, s2, b2);
-      o[5] = deq8(n1.y, s2, b2);
-      o[6] = deq8(n1.z, s2, b2);
-      o[7] = deq8(n1.w, s2, b2);
+      o[4] = deq8(n1.x, s2b, b2b);
+      o[5] = deq8(n1.y, s2b, b2b);
+      o[6] = deq8(n1.z, s2b, b2b);
+      o[7] = deq8(n1.w, s2b, b2b);
       if (!__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
       if (C::A_TMEM) {
         // the row's 64 bf16 into the warp's TMEM lane quarter, 32 columns of the A stage
@@ -715,7 +730,18 @@ DeviceInfo g_dev[64];
 
 template <class C>
 cudaError_t configure() {
-  return cudaFuncSetAttribute(gemm_tc_kernel<C>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DYN);
+  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<C, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DYN);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tc_kernel<C, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DYN);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(gemm_tc_kernel<C, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DYN);
+  return e;
+}
+
+// The instance of the grouped GEMM for a variant and a group size.
+template <class C>
+decltype(&gemm_tc_kernel<C, 64>) gemm_tc_instance(int group_size) {
+  return group_size == 32 ? gemm_tc_kernel<C, 32> : group_size == 128 ? gemm_tc_kernel<C, 128> : gemm_tc_kernel<C, 64>;
 }
 
 }  // namespace
@@ -793,10 +819,10 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   cfg.numAttrs = 1;
   if (a.chunk_rows <= kChunkRowsNarrow) {
     cfg.dynamicSmemBytes = CfgNarrow::SMEM_DYN;
-    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CfgNarrow>, map_wq, map_x, a);
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_instance<CfgNarrow>(a.group_size), map_wq, map_x, a);
   } else {
     cfg.dynamicSmemBytes = CfgWide::SMEM_DYN;
-    e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<CfgWide>, map_wq, map_x, a);
+    e = cudaLaunchKernelEx(&cfg, gemm_tc_instance<CfgWide>(a.group_size), map_wq, map_x, a);
   }
   if (e != cudaSuccess) return e;
   *launched = 1;

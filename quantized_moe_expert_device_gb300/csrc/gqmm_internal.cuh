@@ -152,7 +152,7 @@ int gather_qmm_impl(const void* x, const void* wq, const void* scales, const voi
 // ------------------------------------------------------------------------------------------
 // Kernel launchers (defined in the .cu files).  All return cudaError_t of the launch.
 // ------------------------------------------------------------------------------------------
-cudaError_t launch_quantize(const __nv_bfloat16* w, int64_t rows, int64_t H, uint8_t* wq,
+cudaError_t launch_quantize(const __nv_bfloat16* w, int64_t rows, int64_t H, int group_size, uint8_t* wq,
                             __nv_bfloat16* scales, __nv_bfloat16* biases, cudaStream_t s);
 
 struct RouteArgs {
@@ -193,6 +193,7 @@ struct GemmArgs {
   int chunk_rows;       // rows per chunk: <= kChunkRowsNarrow selects the narrow variant
   int ks_cap;           // > 1: the plan step may split K (header->ksplit) and the finalize runs
   int dense_plan;       // 1: idx is NULL, so the plan is the single chunk (expert 0, start 0, n rows)
+  int group_size = 64;  // quantization group along H: 32, 64 or 128 (the streaming kernels: 64)
 };
 // Launches the grouped GEMM (and, when ks_cap > 1, the kernel that turns the partial sums into
 // y).  *launched gets the number of kernels enqueued.
@@ -212,7 +213,7 @@ bool gemv_uses_mma(int rows, int H, int E);  // which of the two launch_gemv run
 
 cudaError_t launch_gemm_simt(const __nv_bfloat16* x, const uint8_t* wq,
                              const __nv_bfloat16* scales, const __nv_bfloat16* biases,
-                             const uint32_t* idx, int64_t n, int H, int F, int E,
+                             const uint32_t* idx, int64_t n, int H, int F, int E, int group_size,
                              __nv_bfloat16* y, cudaStream_t s);
 
 // ------------------------------------------------------------------------------------------

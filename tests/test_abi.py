@@ -79,7 +79,10 @@ def test_validation_rejects_bad_arguments_without_a_gpu(lib):
                  a["bits"], a["sorted"], a["y"], a["ws"], a["wsb"], a["s"])
 
     assert call(x=None) == 1                  # ERR_NULL
-    assert call(gs=32) == 3                   # ERR_UNSUPPORTED
+    assert call(gs=96) == 3                   # ERR_UNSUPPORTED: group sizes are 32, 64 and 128
+    assert call(gs=16) == 3
+    assert call(gs=256) == 3
+    assert call(gs=128, H=192) == 2           # ERR_SHAPE: H must be a multiple of the group size
     assert call(bits=8) == 3
     assert call(H=100) == 2                   # ERR_SHAPE
     assert call(F=120) == 2
@@ -118,7 +121,8 @@ def test_mlp_validation_rejects_bad_arguments_without_a_gpu(lib):
     assert call(I=96) == 2                    # ERR_SHAPE: I is the down projection's K (multiple of 64)
     assert call(I=0) == 2
     assert call(H=100) == 2
-    assert call(gs=128) == 3                  # ERR_UNSUPPORTED
+    assert call(gs=96) == 3                   # ERR_UNSUPPORTED
+    assert call(gs=128, I=192) == 2           # ERR_SHAPE: I (the down projection's K) % group_size
     assert call(act=3) == 3                   # no such activation
     assert call(act=-1) == 3
     assert call(idx=None) == 1                # dense needs E == 1

@@ -56,5 +56,9 @@ def test_quantize_rejects_unsupported():
     w = torch.zeros(4, 96, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(g.GqmmError):
         g.gqmm_quantize(w)
+    with pytest.raises(g.GqmmError):  # group sizes are 32, 64 and 128
+        g.gqmm_quantize(torch.zeros(4, 128, dtype=torch.bfloat16, device="cuda"), group_size=96)
+    with pytest.raises(g.GqmmError):  # H must be a multiple of the group size
+        g.gqmm_quantize(torch.zeros(4, 192, dtype=torch.bfloat16, device="cuda"), group_size=128)
     with pytest.raises(g.GqmmError):
-        g.gqmm_quantize(torch.zeros(4, 128, dtype=torch.bfloat16, device="cuda"), group_size=32)
+        g.gqmm_quantize(torch.zeros(4, 128, dtype=torch.bfloat16, device="cuda"), bits=8)

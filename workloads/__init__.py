@@ -127,6 +127,7 @@ class Workload:
     w_std: float = 1.0
     r: int = 0              # rows per expert for "balanced"
     note: str = ""
+    group_size: int = 64    # quantization group along the reduction dimension (32, 64 or 128)
     kind: str = "gather"    # "gather": one projection, F output columns;
                             # "mlp": the expert MLP, F = intermediate width I (gate/up 2F rows, down H rows)
 
@@ -150,6 +151,9 @@ def workloads() -> Dict[str, Workload]:
                          note="correctness case, sorted and unsorted")
     w["prefill_e64"] = Workload("prefill_e64", T=2048, A=8, H=2048, F=768, E=64, routing="uniform",
                                 note="MoE prefill microbenchmark shape (rows/expert avg 256)")
+    for gs in (32, 128):
+        w[f"prefill_e64_g{gs}"] = Workload(f"prefill_e64_g{gs}", T=2048, A=8, H=2048, F=768, E=64, routing="uniform",
+                                           group_size=gs, note=f"MoE prefill microbenchmark shape, {gs}-wide groups")
     w["prefill_dense"] = Workload("prefill_dense", T=16384, A=1, H=2048, F=768, E=1, routing="dense",
                                   note="equal-FLOPs dense control x[16384,2048] x W[768,2048]^T")
     for r in (4, 8, 16, 32, 64, 128):
