@@ -292,7 +292,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
         P = ctypes.c_void_p
         return ((P(s["x"].data_ptr()),) + tuple(P(t.data_ptr()) for t in s["w"])
                 + (None if s["idx"] is None else P(s["idx"].data_ptr()),) + sizes
-                + (sorted_flag, P(s["y"].data_ptr()), P(s["ws"].data_ptr()), s["ws"].numel(), sptr))
+                + (sorted_flag, 0, P(s["y"].data_ptr()), P(s["ws"].data_ptr()), s["ws"].numel(), sptr))
 
     calls = [argv(s) for s in sets]
 

@@ -144,6 +144,9 @@ GQMM_API int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* per
  *  H        > 0, multiple of 64 and of group_size;   F > 0, multiple of 16;   E in [1, GQMM_MAX_EXPERTS]
  *  group_size 32, 64 or 128 (the weight-streaming kernels of decode-sized calls take 64; other
  *           group sizes run those calls on the tensor-core GEMM), bits 4
+ *  x_shared 0: x is [T, A, H], one row per (t, a);  1: x is [T, H], the A routed rows of
+ *           token t all read x[t] (the x of an MoE layer, broadcast over its A experts;
+ *           needs idx != NULL)
  *  sorted   0: idx in any order (the library sorts rows by expert on device);
  *           1: the caller promises idx is nondecreasing in flat order (the issue's
  *              sorted_indices=True).  The result is identical either way; a broken
@@ -156,7 +159,7 @@ GQMM_API int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* per
  */
 GQMM_API int gqmm_gather_qmm(const void* x, const void* wq, const void* scales, const void* biases,
                     const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size,
-                    int bits, int sorted, void* y, void* ws, size_t ws_bytes,
+                    int bits, int sorted, int x_shared, void* y, void* ws, size_t ws_bytes,
                     gqmm_stream_t stream);
 
 /*
@@ -189,6 +192,7 @@ GQMM_API size_t gqmm_moe_mlp_workspace_size(int64_t n, int H, int I, int E);
  *  idx, T, A, E, group_size, bits, sorted   as for gqmm_gather_qmm
  *  H        > 0, multiple of 64;   I > 0, multiple of 64 (it is the down projection's K)
  *  activation  GQMM_ACT_SILU, GQMM_ACT_GELU or GQMM_ACT_GELU_TANH (else GQMM_ERR_UNSUPPORTED)
+ *  x_shared as for gqmm_gather_qmm (x [T, H] shared by a token's A experts)
  *  y        out: bfloat16 [T, A, H] in (t, a) order, 16-byte aligned
  *  ws       workspace of at least gqmm_moe_mlp_workspace_size(T*A, H, I, E) bytes
  * Rows whose idx is >= E are written as zeros and set GQMM_STATUS_BAD_INDEX.
@@ -197,7 +201,7 @@ GQMM_API size_t gqmm_moe_mlp_workspace_size(int64_t n, int H, int I, int E);
 GQMM_API int gqmm_moe_mlp(const void* x, const void* wq_gu, const void* sc_gu, const void* bs_gu,
                           const void* wq_dn, const void* sc_dn, const void* bs_dn, const uint32_t* idx,
                           int64_t T, int A, int H, int I, int E, int group_size, int bits, int activation,
-                          int sorted, void* y, void* ws, size_t ws_bytes, gqmm_stream_t stream);
+                          int sorted, int x_shared, void* y, void* ws, size_t ws_bytes, gqmm_stream_t stream);
 
 /*
  * gqmm_gather_qmm_simt -- the same operation computed on CUDA cores, one thread per output
@@ -207,12 +211,13 @@ GQMM_API int gqmm_moe_mlp(const void* x, const void* wq_gu, const void* sc_gu, c
  */
 GQMM_API int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* scales, const void* biases,
                          const uint32_t* idx, int64_t T, int A, int H, int F, int E,
-                         int group_size, int bits, void* y, gqmm_stream_t stream);
+                         int group_size, int bits, int x_shared, void* y, gqmm_stream_t stream);
 
 /*
  * gqmm_gather_qmm_noalloc -- the pages have no counterpart to this entry point; it is a
- * convenience of this library.  Same operation, arguments and results as gqmm_gather_qmm,
- * but without a workspace argument: the scratch it needs is a fixed array of
+ * convenience of this library.  Same operation, arguments and results as gqmm_gather_qmm
+ * with x_shared = 0 (x [T, A, H]), but without a workspace argument: the scratch it needs is a
+ * fixed array of
  * GQMM_NOALLOC_SCRATCH_BYTES inside the library's device code, and the call allocates
  * nothing (no cudaMalloc, no cudaFree, no allocating library routine).  It is meant for
  * callers that cannot allocate device memory or keep a workspace: a plugin whose host

@@ -67,10 +67,10 @@ def load_library():
             "gqmm_quantize": ([P, I64, I64, I, I, P, P, P, P], I),
             "gqmm_workspace_size": ([I64, I, I], SZ),
             "gqmm_route_sort": ([P, I64, I, P, P, P, SZ, P], I),
-            "gqmm_gather_qmm": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P, SZ, P], I),
-            "gqmm_gather_qmm_simt": ([P, P, P, P, P, I64, I, I, I, I, I, I, P, P], I),
+            "gqmm_gather_qmm": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, I, P, P, SZ, P], I),
+            "gqmm_gather_qmm_simt": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P], I),
             "gqmm_moe_mlp_workspace_size": ([I64, I, I, I], SZ),
-            "gqmm_moe_mlp": ([P, P, P, P, P, P, P, P, I64, I, I, I, I, I, I, I, I, P, P, SZ, P], I),
+            "gqmm_moe_mlp": ([P, P, P, P, P, P, P, P, I64, I, I, I, I, I, I, I, I, I, P, P, SZ, P], I),
             "gqmm_device_status": ([P, P], I),
             "gqmm_status_string": ([I], ctypes.c_char_p),
             "gqmm_last_error": ([], ctypes.c_char_p),
@@ -178,10 +178,19 @@ def _gather_shapes(x: torch.Tensor, idx: Optional[torch.Tensor], wq: torch.Tenso
         T, A = idx.shape[0], idx.numel() // idx.shape[0]
     else:
         T, A = idx.numel(), 1
-    if T * A * H != x.numel():
-        raise ValueError(f"x has {x.numel()} elements, expected T*A*H = {T}*{A}*{H}")
+    if T * A * H != x.numel() and not (idx is not None and T * H == x.numel()):
+        raise ValueError(f"x has {x.numel()} elements, expected T*A*H = {T}*{A}*{H} (or T*H, shared by the A rows)")
     E, F = wq.shape[0], wq.shape[1]
     return T, A, H, F, E
+
+
+def _x_shared(x: torch.Tensor, T: int, A: int, H: int) -> int:
+    """1 when x holds one row per token for its A routed rows ([T, H] or [T, 1, H])."""
+    return 1 if A > 1 and x.numel() == T * H else 0
+
+
+def _out_shape(x: torch.Tensor, T: int, A: int, cols: int):
+    return (T, A, cols) if _x_shared(x, T, A, x.shape[-1]) else tuple(x.shape[:-1]) + (cols,)
 
 
 def gqmm_gather_qmm(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
@@ -203,14 +212,15 @@ def gqmm_gather_qmm(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, bia
     T, A, H, F, E = _gather_shapes(x, idx, wq)
     _check_groups(scales, H, group_size, "scales")
     if y is None:
-        y = torch.empty(tuple(x.shape[:-1]) + (F,), dtype=torch.bfloat16, device=x.device)
+        y = torch.empty(_out_shape(x, T, A, F), dtype=torch.bfloat16, device=x.device)
     else:
         _need(y, "y", torch.bfloat16)
     if ws is None:
         ws = new_workspace(T * A, F, E, x.device)
     lib = load_library()
     _check(lib.gqmm_gather_qmm(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(idx), T, A, H, F, E,
-                               group_size, bits, 1 if sorted_indices else 0, _ptr(y), _ptr(ws), ws.numel(),
+                               group_size, bits, 1 if sorted_indices else 0, _x_shared(x, T, A, H), _ptr(y), _ptr(ws),
+                               ws.numel(),
                                _stream(stream, x.device)), "gqmm_gather_qmm")
     return y
 
@@ -222,10 +232,11 @@ def gqmm_gather_qmm_simt(x, wq, scales, biases, idx, group_size: int = 64, bits:
     T, A, H, F, E = _gather_shapes(x, idx, wq)
     _check_groups(scales, H, group_size, "scales")
     if y is None:
-        y = torch.empty(tuple(x.shape[:-1]) + (F,), dtype=torch.bfloat16, device=x.device)
+        y = torch.empty(_out_shape(x, T, A, F), dtype=torch.bfloat16, device=x.device)
     lib = load_library()
     _check(lib.gqmm_gather_qmm_simt(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(idx), T, A, H, F, E,
-                                    group_size, bits, _ptr(y), _stream(stream, x.device)), "gqmm_gather_qmm_simt")
+                                    group_size, bits, _x_shared(x, T, A, H), _ptr(y), _stream(stream, x.device)),
+           "gqmm_gather_qmm_simt")
     return y
 
 
@@ -268,7 +279,7 @@ def gqmm_moe_mlp(x: torch.Tensor, q_gu, q_dn, idx: Optional[torch.Tensor], group
     _check_groups(sc_gu, H, group_size, "sc_gu")
     _check_groups(sc_dn, I, group_size, "sc_dn")
     if y is None:
-        y = torch.empty(tuple(x.shape), dtype=torch.bfloat16, device=x.device)
+        y = torch.empty(_out_shape(x, T, A, H), dtype=torch.bfloat16, device=x.device)
     else:
         _need(y, "y", torch.bfloat16)
     if ws is None:
@@ -276,7 +287,7 @@ def gqmm_moe_mlp(x: torch.Tensor, q_gu, q_dn, idx: Optional[torch.Tensor], group
     lib = load_library()
     _check(lib.gqmm_moe_mlp(_ptr(x), _ptr(wq_gu), _ptr(sc_gu), _ptr(bs_gu), _ptr(wq_dn), _ptr(sc_dn), _ptr(bs_dn),
                             _ptr(idx), T, A, H, I, E, group_size, bits, ACTIVATIONS[activation],
-                            1 if sorted_indices else 0, _ptr(y), _ptr(ws),
+                            1 if sorted_indices else 0, _x_shared(x, T, A, H), _ptr(y), _ptr(ws),
                             ws.numel(), _stream(stream, x.device)), "gqmm_moe_mlp")
     return y
 

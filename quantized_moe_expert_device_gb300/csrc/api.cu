@@ -107,6 +107,12 @@ int validate_gather(const void* x, const void* wq, const void* scales, const voi
   return GQMM_OK;
 }
 
+int validate_shared(int x_shared, const uint32_t* idx) {
+  if (x_shared != 0 && x_shared != 1) return fail(GQMM_ERR_SHAPE, "x_shared must be 0 or 1");
+  if (x_shared && !idx) return fail(GQMM_ERR_NULL, "x_shared needs idx (a token's rows are its A routed rows)");
+  return GQMM_OK;
+}
+
 }  // namespace
 
 int gqmm::report_error(int code, const char* fmt, ...) {
@@ -159,8 +165,11 @@ int launch_projection(const GemmArgs& ga, const UnitShape& shape, int sms, cudaS
 
 int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, const void* biases,
                           const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size, int bits,
-                          int sorted, void* y, void* ws, size_t ws_bytes, cudaStream_t s, bool allow_split) {
+                          int sorted, int x_shared, void* y, void* ws, size_t ws_bytes, cudaStream_t s,
+                          bool allow_split) {
   int rc = validate_gather(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y);
+  if (rc) return rc;
+  rc = validate_shared(x_shared, idx);
   if (rc) return rc;
   if (sorted != 0 && sorted != 1) return fail(GQMM_ERR_SHAPE, "sorted must be 0 or 1");
   if (!ws) return fail(GQMM_ERR_NULL, "ws must be non-NULL");
@@ -225,6 +234,7 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   ga.acc = L.has_acc ? reinterpret_cast<float*>(w + L.acc) : nullptr;
   ga.offsets = ra.offsets;
   ga.group_size = group_size;
+  ga.x_div = x_shared ? A : 1;
   rc = launch_projection(ga, shape, sms, s, "gather_qmm", route_variant);
   if (rc) return rc;
   return ok();
@@ -233,8 +243,8 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
 
 int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, const void* bs_gu, const void* wq_dn,
                        const void* sc_dn, const void* bs_dn, const uint32_t* idx, int64_t T, int A, int H, int I, int E,
-                       int group_size, int bits, int activation, int sorted, void* y, void* ws, size_t ws_bytes,
-                       cudaStream_t s) {
+                       int group_size, int bits, int activation, int sorted, int x_shared, void* y, void* ws,
+                       size_t ws_bytes, cudaStream_t s) {
   if (I <= 0 || I > (1 << 29)) return fail(GQMM_ERR_SHAPE, "I must be in [1, 2^29] (got %d)", I);
   if (activation != GQMM_ACT_SILU && activation != GQMM_ACT_GELU && activation != GQMM_ACT_GELU_TANH)
     return fail(GQMM_ERR_UNSUPPORTED, "unknown activation %d", activation);
@@ -244,6 +254,8 @@ int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, cons
   rc = validate_gather(x, wq_dn, sc_dn, bs_dn, idx, T, A, I, H, E, group_size, bits, y);
   if (rc) return rc;
   if (sorted != 0 && sorted != 1) return fail(GQMM_ERR_SHAPE, "sorted must be 0 or 1");
+  rc = validate_shared(x_shared, idx);
+  if (rc) return rc;
   if (!ws) return fail(GQMM_ERR_NULL, "ws must be non-NULL");
   const int64_t n = T * (int64_t)A;
   const MlpLayout M = mlp_ws_layout(n, H, I, E);
@@ -310,6 +322,7 @@ int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, cons
   g1.ks_cap = 1;
   g1.dense_plan = idx == nullptr ? 1 : 0;
   g1.group_size = group_size;
+  g1.x_div = x_shared ? A : 1;  // the down projection reads the sorted intermediate (x_div 1)
   rc = launch_projection(g1, shape1, sms, s, "moe_mlp gate/up", route_variant);
   if (rc) return rc;
 
@@ -324,6 +337,7 @@ int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, cons
   g2.biases = static_cast<const __nv_bfloat16*>(bs_dn);
   g2.y = static_cast<__nv_bfloat16*>(y);
   g2.perm = nullptr;
+  g2.x_div = 1;
   g2.y_perm = permuted ? ra.perm : nullptr;
   g2.H = I;
   g2.F = H;
@@ -397,10 +411,10 @@ int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* perm, int32_
 }
 
 int gqmm_gather_qmm(const void* x, const void* wq, const void* scales, const void* biases, const uint32_t* idx,
-                    int64_t T, int A, int H, int F, int E, int group_size, int bits, int sorted, void* y,
-                    void* ws, size_t ws_bytes, gqmm_stream_t stream) {
-  return gqmm::gather_qmm_impl(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, sorted, y, ws, ws_bytes,
-                               reinterpret_cast<cudaStream_t>(stream), true);
+                    int64_t T, int A, int H, int F, int E, int group_size, int bits, int sorted, int x_shared,
+                    void* y, void* ws, size_t ws_bytes, gqmm_stream_t stream) {
+  return gqmm::gather_qmm_impl(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, sorted, x_shared, y, ws,
+                               ws_bytes, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 size_t gqmm_moe_mlp_workspace_size(int64_t n, int H, int I, int E) {
@@ -410,22 +424,25 @@ size_t gqmm_moe_mlp_workspace_size(int64_t n, int H, int I, int E) {
 
 int gqmm_moe_mlp(const void* x, const void* wq_gu, const void* sc_gu, const void* bs_gu, const void* wq_dn,
                  const void* sc_dn, const void* bs_dn, const uint32_t* idx, int64_t T, int A, int H, int I, int E,
-                 int group_size, int bits, int activation, int sorted, void* y, void* ws, size_t ws_bytes,
-                 gqmm_stream_t stream) {
+                 int group_size, int bits, int activation, int sorted, int x_shared, void* y, void* ws,
+                 size_t ws_bytes, gqmm_stream_t stream) {
   return gqmm::moe_mlp_impl(x, wq_gu, sc_gu, bs_gu, wq_dn, sc_dn, bs_dn, idx, T, A, H, I, E, group_size, bits,
-                            activation, sorted, y, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+                            activation, sorted, x_shared, y, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* scales, const void* biases,
                          const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size, int bits,
-                         void* y, gqmm_stream_t stream) {
+                         int x_shared, void* y, gqmm_stream_t stream) {
   int rc = validate_gather(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y);
+  if (rc) return rc;
+  rc = validate_shared(x_shared, idx);
   if (rc) return rc;
   rc = check_device(nullptr);
   if (rc) return rc;
   cudaError_t e = launch_gemm_simt(static_cast<const __nv_bfloat16*>(x), static_cast<const uint8_t*>(wq),
                                    static_cast<const __nv_bfloat16*>(scales), static_cast<const __nv_bfloat16*>(biases),
-                                   idx, T * (int64_t)A, H, F, E, group_size, static_cast<__nv_bfloat16*>(y),
+                                   idx, T * (int64_t)A, H, F, E, group_size, x_shared ? A : 1,
+                                   static_cast<__nv_bfloat16*>(y),
                                    reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "simt launch: %s", cudaGetErrorString(e));
   g_launches.fetch_add(1);

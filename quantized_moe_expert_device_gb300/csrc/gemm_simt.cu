@@ -12,7 +12,7 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(const __nv_bfloat16* __r
                                                         const __nv_bfloat16* __restrict__ scales,
                                                         const __nv_bfloat16* __restrict__ biases,
                                                         const uint32_t* __restrict__ idx, int H, int F,
-                                                        int E, int gs, __nv_bfloat16* __restrict__ y) {
+                                                        int E, int gs, int x_div, __nv_bfloat16* __restrict__ y) {
   const int64_t i = blockIdx.x;
   const int f = blockIdx.y * blockDim.x + threadIdx.x;
   if (f >= F) return;
@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(const __nv_bfloat16* __r
   const int G = H / gs;
   const int64_t wr = (int64_t)e * F + f;
   const uint8_t* wrow = wq + wr * (H / 2);
-  const __nv_bfloat16* xr = x + i * H;
+  const __nv_bfloat16* xr = x + (i / x_div) * H;
   float acc = 0.0f;
   for (int g = 0; g < G; ++g) {
     const float s = __bfloat162float(scales[wr * G + g]);
@@ -44,10 +44,10 @@ __global__ void __launch_bounds__(128) gemm_simt_kernel(const __nv_bfloat16* __r
 
 cudaError_t launch_gemm_simt(const __nv_bfloat16* x, const uint8_t* wq, const __nv_bfloat16* scales,
                              const __nv_bfloat16* biases, const uint32_t* idx, int64_t n, int H, int F,
-                             int E, int group_size, __nv_bfloat16* y, cudaStream_t s) {
+                             int E, int group_size, int x_div, __nv_bfloat16* y, cudaStream_t s) {
   if (n == 0) return cudaSuccess;
   dim3 grid((unsigned)n, (unsigned)((F + 127) / 128));
-  gemm_simt_kernel<<<grid, 128, 0, s>>>(x, wq, scales, biases, idx, H, F, E, group_size, y);
+  gemm_simt_kernel<<<grid, 128, 0, s>>>(x, wq, scales, biases, idx, H, F, E, group_size, x_div, y);
   return cudaGetLastError();
 }
 

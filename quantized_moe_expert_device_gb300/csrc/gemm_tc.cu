@@ -415,6 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < 4; ++j) {
         const int pos = 4 * g + j < U.rows ? 4 * g + j : 0;
         rr[j] = mine ? (p.perm ? __ldg(p.perm + U.start + pos) : U.start + pos) : 0;
+        if (p.x_div != 1) rr[j] /= p.x_div;  // a token's A rows share one x row
       }
       const int wops = nops > gw ? min(32, (nops - gw + C::GATHER_WARPS - 1) / C::GATHER_WARPS) : 0;
       for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
@@ -798,7 +799,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   // x as a [n, H] bf16 matrix; one box = 64 columns (one k-block, 128 bytes) of one row, for
   // tile::gather4 into the 128-byte-swizzled B tile.
   CUtensorMap map_x;
-  const cuuint64_t xdims[2] = {(cuuint64_t)a.H, (cuuint64_t)a.n};
+  const cuuint64_t xdims[2] = {(cuuint64_t)a.H, (cuuint64_t)(a.n / a.x_div)};
   const cuuint64_t xstrides[1] = {(cuuint64_t)a.H * 2};
   const cuuint32_t xbox[2] = {BK, 1};
   cr = encode(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(a.x), xdims, xstrides, xbox,

@@ -224,7 +224,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
           for (int t = 0; t < 2; ++t) {
             const bool live = t < M && t < rec.z;
             trow[t] = live ? (p.y_perm ? __ldg(p.y_perm + rec.y + t) : rec.y + t) : 0;
-            xrow[t] = live ? (p.perm ? __ldg(p.perm + rec.y + t) : rec.y + t) : 0;
+            xrow[t] = live ? (p.perm ? __ldg(p.perm + rec.y + t) : rec.y + t) / p.x_div : 0;
           }
           prev_c = c;
         }

@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemmArgs
           if (!__all_sync(0xffffffffu, ok)) break;
         }
         trow_lane = lane < xr ? (p.y_perm ? __ldg(p.y_perm + rec.y + lane) : rec.y + lane) : 0;
-        xrow_lane = lane < xr ? (p.perm ? __ldg(p.perm + rec.y + lane) : rec.y + lane) : 0;
+        xrow_lane = lane < xr ? (p.perm ? __ldg(p.perm + rec.y + lane) : rec.y + lane) / p.x_div : 0;
         if (lane == 0) mbar_arrive_expect_tx(smem_u32(&xfull_bar), (uint32_t)xr * H * 2);
         __syncwarp();
         if (lane < xr)

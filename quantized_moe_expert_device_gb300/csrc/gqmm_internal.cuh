@@ -145,8 +145,8 @@ int report_error(int code, const char* fmt, ...);
 // gqmm_gather_qmm with a switch: allow_split = false never splits K, so its workspace needs no
 // split-K sum buffer (ws_layout(n, F, E, false)).
 int gather_qmm_impl(const void* x, const void* wq, const void* scales, const void* biases, const uint32_t* idx,
-                    int64_t T, int A, int H, int F, int E, int group_size, int bits, int sorted, void* y, void* ws,
-                    size_t ws_bytes, cudaStream_t s, bool allow_split);
+                    int64_t T, int A, int H, int F, int E, int group_size, int bits, int sorted, int x_shared,
+                    void* y, void* ws, size_t ws_bytes, cudaStream_t s, bool allow_split);
 
 
 // ------------------------------------------------------------------------------------------
@@ -194,6 +194,8 @@ struct GemmArgs {
   int ks_cap;           // > 1: the plan step may split K (header->ksplit) and the finalize runs
   int dense_plan;       // 1: idx is NULL, so the plan is the single chunk (expert 0, start 0, n rows)
   int group_size = 64;  // quantization group along H: 32, 64 or 128 (the streaming kernels: 64)
+  int x_div = 1;        // x row of routed row r: r / x_div (A when the A rows of a token share
+                        // one x row, else 1); x has n / x_div rows
 };
 // Launches the grouped GEMM (and, when ks_cap > 1, the kernel that turns the partial sums into
 // y).  *launched gets the number of kernels enqueued.
@@ -213,7 +215,7 @@ bool gemv_uses_mma(int rows, int H, int E);  // which of the two launch_gemv run
 
 cudaError_t launch_gemm_simt(const __nv_bfloat16* x, const uint8_t* wq,
                              const __nv_bfloat16* scales, const __nv_bfloat16* biases,
-                             const uint32_t* idx, int64_t n, int H, int F, int E, int group_size,
+                             const uint32_t* idx, int64_t n, int H, int F, int E, int group_size, int x_div,
                              __nv_bfloat16* y, cudaStream_t s);
 
 // ------------------------------------------------------------------------------------------

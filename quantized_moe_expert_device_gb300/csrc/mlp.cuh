@@ -26,8 +26,8 @@ inline MlpLayout mlp_ws_layout(int64_t n, int H, int I, int E) {
 
 int moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, const void* bs_gu, const void* wq_dn,
                  const void* sc_dn, const void* bs_dn, const uint32_t* idx, int64_t T, int A, int H, int I, int E,
-                 int group_size, int bits, int activation, int sorted, void* y, void* ws, size_t ws_bytes,
-                 cudaStream_t s);
+                 int group_size, int bits, int activation, int sorted, int x_shared, void* y, void* ws,
+                 size_t ws_bytes, cudaStream_t s);
 
 // Gating of the MLP's gate/up output (n sorted rows of [g | u]) by a GQMM_ACT_* activation into
 // h [n, I]; also resets header->next_unit to `sms` for the down projection's tensor-core GEMM

@@ -76,6 +76,6 @@ extern "C" int gqmm_gather_qmm_noalloc(const void* x, const void* wq, const void
   // back through this entry point, and it must not carry bits from earlier calls.
   cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(gqmm::WsHeader), s);
   if (e != cudaSuccess) return gqmm::report_error(GQMM_ERR_CUDA, "gqmm_gather_qmm_noalloc: clearing scratch failed");
-  return gqmm::gather_qmm_impl(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, sorted, y, ws,
+  return gqmm::gather_qmm_impl(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, sorted, 0, y, ws,
                                kScratchBytes, s, allow_split);
 }

@@ -66,19 +66,21 @@ def test_validation_rejects_bad_arguments_without_a_gpu(lib):
     P = ctypes.c_void_p
     f = lib.gqmm_gather_qmm
     f.argtypes = [P, P, P, P, P, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                  ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_size_t, P]
+                  ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, P, P, ctypes.c_size_t, P]
     f.restype = ctypes.c_int
     fake = P(0x10000)  # never dereferenced: every call below fails validation first
     args = dict(x=fake, wq=fake, sc=fake, bs=fake, idx=fake, T=16, A=2, H=256, F=128, E=8, gs=64, bits=4,
-                sorted=0, y=fake, ws=fake, wsb=1 << 20, s=None)
+                sorted=0, shared=0, y=fake, ws=fake, wsb=1 << 20, s=None)
 
     def call(**kw):
         a = dict(args)
         a.update(kw)
         return f(a["x"], a["wq"], a["sc"], a["bs"], a["idx"], a["T"], a["A"], a["H"], a["F"], a["E"], a["gs"],
-                 a["bits"], a["sorted"], a["y"], a["ws"], a["wsb"], a["s"])
+                 a["bits"], a["sorted"], a["shared"], a["y"], a["ws"], a["wsb"], a["s"])
 
     assert call(x=None) == 1                  # ERR_NULL
+    assert call(shared=2) == 2                # x_shared is 0 or 1
+    assert call(shared=1, idx=None, E=1) == 1  # a shared x needs the routed rows of idx
     assert call(gs=96) == 3                   # ERR_UNSUPPORTED: group sizes are 32, 64 and 128
     assert call(gs=16) == 3
     assert call(gs=256) == 3
@@ -102,19 +104,20 @@ def test_validation_rejects_bad_arguments_without_a_gpu(lib):
 def test_mlp_validation_rejects_bad_arguments_without_a_gpu(lib):
     P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
     f = lib.gqmm_moe_mlp
-    f.argtypes = [P, P, P, P, P, P, P, P, I64, I, I, I, I, I, I, I, I, P, P, ctypes.c_size_t, P]
+    f.argtypes = [P, P, P, P, P, P, P, P, I64, I, I, I, I, I, I, I, I, I, P, P, ctypes.c_size_t, P]
     f.restype = I
     lib.gqmm_moe_mlp_workspace_size.argtypes = [I64, I, I, I]
     lib.gqmm_moe_mlp_workspace_size.restype = ctypes.c_size_t
     fake = P(0x10000)  # never dereferenced: every call below fails validation first
     args = dict(x=fake, wgu=fake, sgu=fake, bgu=fake, wdn=fake, sdn=fake, bdn=fake, idx=fake, T=16, A=2, H=256,
-                I=128, E=8, gs=64, bits=4, act=0, sorted=0, y=fake, ws=fake, wsb=1 << 20, s=None)
+                I=128, E=8, gs=64, bits=4, act=0, sorted=0, shared=0, y=fake, ws=fake, wsb=1 << 20, s=None)
 
     def call(**kw):
         a = dict(args)
         a.update(kw)
         return f(a["x"], a["wgu"], a["sgu"], a["bgu"], a["wdn"], a["sdn"], a["bdn"], a["idx"], a["T"], a["A"],
-                 a["H"], a["I"], a["E"], a["gs"], a["bits"], a["act"], a["sorted"], a["y"], a["ws"], a["wsb"], a["s"])
+                 a["H"], a["I"], a["E"], a["gs"], a["bits"], a["act"], a["sorted"], a["shared"], a["y"], a["ws"],
+                 a["wsb"], a["s"])
 
     assert call(wdn=None) == 1                # ERR_NULL (down projection)
     assert call(x=None) == 1
@@ -124,6 +127,7 @@ def test_mlp_validation_rejects_bad_arguments_without_a_gpu(lib):
     assert call(gs=96) == 3                   # ERR_UNSUPPORTED
     assert call(gs=128, I=192) == 2           # ERR_SHAPE: I (the down projection's K) % group_size
     assert call(act=3) == 3                   # no such activation
+    assert call(shared=3) == 2
     assert call(act=-1) == 3
     assert call(idx=None) == 1                # dense needs E == 1
     assert call(sorted=3) == 2
