@@ -163,6 +163,29 @@ def gather_qmm(x, wq, scales, biases, idx, E: int, group_size: int = 64, bits: i
 gather_qmm.last_threads = 0
 
 
+def gather_qmm_nn(x, wq, scales, biases, idx, E: int, group_size: int = 64, rows=None):
+    """gather_qmm with transpose=False, in float64: y[i] = x[i] . deq(W[e]), e = idx[i], where W[e]
+    is [K, N] quantized along N (the layout mx.quantize gives a [E, K, N] weight: wq u8
+    [E, K, N/2], scales/biases [E, K, N/gs]).  x: bf16 [..., K] (n rows); idx None for E == 1.
+    Rows whose index is >= E are zero.  Returns float64 [n, N] (or [len(rows), N])."""
+    x16 = _u16(x)
+    K = x16.shape[-1]
+    xf = (x16.reshape(-1, K).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    n = xf.shape[0]
+    r = np.arange(n) if rows is None else np.asarray(rows, np.int64)
+    e = np.zeros(r.size, np.int64) if idx is None else np.asarray(idx, np.uint32).reshape(-1)[r].astype(np.int64)
+    wq = np.asarray(wq)
+    N = wq.shape[-1] * 2
+    y = np.zeros((r.size, N), np.float64)
+    for ex in np.unique(e):
+        if ex >= E:
+            continue
+        w_hat = dequantize(wq[ex], _u16(scales)[ex], _u16(biases)[ex], group_size)  # [K, N]
+        for i in np.nonzero(e == ex)[0]:  # one vector-matrix product per row
+            y[i] = xf[r[i]] @ w_hat
+    return y
+
+
 def silu(v: np.ndarray) -> np.ndarray:
     """SiLU in float64: v / (1 + exp(-v))."""
     return v / (1.0 + np.exp(-v))
