@@ -36,7 +36,7 @@ import workloads as wl  # noqa: E402
 # elementwise work next to the projections; every activation is parity-tested)
 MLP_ACTIVATION = "silu"
 # GEMM launches (projections) per step, each timed by the library's kernel timer
-GEMM_LAUNCHES_PER_STEP = {"gather": 1, "mlp": 2}
+GEMM_LAUNCHES_PER_STEP = {"gather": 1, "mlp": 2, "nn": 1}
 
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -59,7 +59,12 @@ def algorithmic_bytes(w: wl.Workload, idx: np.ndarray | None) -> int:
     def qbytes(rows, K):  # one expert's packed codes + bf16 scale and bias per group
         return rows * (K // 2 + 4 * (K // w.group_size))
 
-    weights = hit * (qbytes(2 * w.F, w.H) + qbytes(w.H, w.F) if w.kind == "mlp" else qbytes(w.F, w.H))
+    if w.kind == "mlp":
+        weights = hit * (qbytes(2 * w.F, w.H) + qbytes(w.H, w.F))
+    elif w.kind == "nn":  # W[e] is [K = H, N = F], quantized along F
+        weights = hit * qbytes(w.H, w.F)
+    else:
+        weights = hit * qbytes(w.F, w.H)
     return int(weights + w.n * w.H * 2 + w.n * w.out_cols * 2 + (0 if idx is None else w.n * 4))
 
 
@@ -169,6 +174,9 @@ def oracle_rows(w: wl.Workload, x_cpu, qw, idx, rows):
 
     if w.kind == "mlp":
         oracle.moe_mlp(x_cpu, qw[0], qw[1], idx, w.E, group_size=w.group_size, rows=rows)
+    elif w.kind == "nn":
+        oracle.gather_qmm_nn(x_cpu, *qw, idx, w.E, group_size=w.group_size, rows=rows)
+        return 1  # numpy row products, one thread
     else:
         oracle.gather_qmm(x_cpu, *qw, idx, w.E, group_size=w.group_size, rows=rows)
     return oracle.gather_qmm.last_threads
@@ -195,12 +203,14 @@ def oracle_rate(w: wl.Workload, x_cpu, qw, idx, target_s: float, max_rows: int |
 def metric_name(w: wl.Workload) -> str:
     if w.kind == "mlp":
         return "moe_mlp TFLOPs (6*T*A*H*I/time)"
+    if w.kind == "nn":
+        return "gather_qmm_nn TFLOPs (2*T*A*K*N/time)"
     return "gather_qmm TFLOPs (2*T*A*H*F/time)"
 
 
 def workload_config(w: wl.Workload) -> dict:
     c = {"workload": w.name, "T": w.T, "A": w.A, "H": w.H}
-    c.update({"I": w.F} if w.kind == "mlp" else {"F": w.F})
+    c.update({"I": w.F} if w.kind == "mlp" else {"K": w.H, "N": w.F} if w.kind == "nn" else {"F": w.F})
     c.update({"E": w.E, "group_size": w.group_size, "bits": 4, "routing": w.routing})
     if w.kind == "mlp":
         c["op"] = "gqmm_moe_mlp: gate/up projection, act(gate) * up, down projection"
@@ -273,8 +283,12 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
         w_dev = inp["w"].to(dev)
         weights0 = list(g.gqmm_quantize(w_dev, group_size=w.group_size))
         del w_dev
-        fn, ws_new = lib.gqmm_gather_qmm, (lambda: g.new_workspace(w.n, w.F, w.E, dev))
-        sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4)
+        if w.kind == "nn":  # no workspace: rows are independent, no route sort
+            fn, ws_new = lib.gqmm_gather_qmm_nn, (lambda: None)
+            sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4, 0)
+        else:
+            fn, ws_new = lib.gqmm_gather_qmm, (lambda: g.new_workspace(w.n, w.F, w.E, dev))
+            sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4)
     x0 = inp["x"].to(dev)
     idx0 = None if idx_np is None else torch.from_numpy(np.ascontiguousarray(idx_np).view(np.int32)).to(dev)
     sets = []
@@ -290,6 +304,9 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
 
     def argv(s, sorted_flag=0):
         P = ctypes.c_void_p
+        if w.kind == "nn":
+            return ((P(s["x"].data_ptr()),) + tuple(P(t.data_ptr()) for t in s["w"])
+                    + (None if s["idx"] is None else P(s["idx"].data_ptr()),) + sizes + (P(s["y"].data_ptr()), sptr))
         return ((P(s["x"].data_ptr()),) + tuple(P(t.data_ptr()) for t in s["w"])
                 + (None if s["idx"] is None else P(s["idx"].data_ptr()),) + sizes
                 + (sorted_flag, 0, P(s["y"].data_ptr()), P(s["ws"].data_ptr()), s["ws"].numel(), sptr))
@@ -361,7 +378,8 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
         raise RuntimeError(f"kernel timer recorded {n_timed} GEMM launches, expected {timer_slots}")
     status = 0
     for s in sets:
-        status |= g.gqmm_device_status(s["ws"])
+        if s["ws"] is not None:
+            status |= g.gqmm_device_status(s["ws"])
     if status:
         raise RuntimeError(f"device status after timed region: {status:#x}")
 
@@ -378,7 +396,19 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     gemm_ms = gemm_ms_total / max(args.steps, 1)
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if flops / alg_bytes >= ridge else "hbm"
-    if bound == "tensor":
+    peak_source = f"{peaks_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"
+    if w.kind == "nn":
+        # CUDA-core kernel: the float32 FMA pipes (128 lanes per SM, 2 FLOP per FMA) at the
+        # maximum SM clock; it issues two FMAs (dequantize, accumulate) per multiply-add of the
+        # metric, so half of this peak is its ceiling
+        bound = "alu"
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        sm_max = (clocks or {}).get("sm_max_mhz") or 2070
+        peak = sms * 128 * 2 * sm_max * 1e6 / 1e12
+        achieved = flops / (gemm_ms * 1e-3) / 1e12
+        unit = "TFLOP/s"
+        peak_source = f"derived: {sms} SMs x 128 FP32 lanes x 2 FLOP x {sm_max} MHz"
+    elif bound == "tensor":
         achieved = flops / (gemm_ms * 1e-3) / 1e12
         peak = peaks["bf16_tflops"]
         unit = "TFLOP/s"
@@ -492,7 +522,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
                      "kernel_launches_per_step": gemm_launches_per_step,
                      "kernel_timing": "second timed pass of the same steps, CUDA events around each GEMM launch;"
                                       " kernel_ms = their summed duration per step",
-                     "peak_source": f"{peaks_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"},
+                     "peak_source": peak_source},
         "op_roofline": {"t_min_us": t_roof_s * 1e6, "frac": t_roof_s / (ms_per_step * 1e-3),
                         "algorithmic_bytes": alg_bytes, "flops": flops},
         "cpu_baseline": cpu,
@@ -512,10 +542,11 @@ KERNEL_SOURCES = {
     "gemm_tc_kernel": (_CSRC + "gemm_tc.cu", _CSRC + "gqmm_internal.cuh"),
     "gemv_fma_kernel": (_CSRC + "gemv.cu", _CSRC + "gqmm_internal.cuh"),
     "gemv_mma_kernel": (_CSRC + "gemv_mma.cu", _CSRC + "gqmm_internal.cuh"),
+    "gemm_nn_kernel": (_CSRC + "gemm_nn.cu", _CSRC + "gqmm_internal.cuh"),
 }
 # dispatch-count variant -> the kernel it launches for the GEMM step
 _VARIANT_KERNEL = {"gemv": "gemv_fma_kernel", "gemv_mma": "gemv_mma_kernel", "gemm_narrow": "gemm_tc_kernel",
-                   "gemm_tc": "gemm_tc_kernel"}
+                   "gemm_tc": "gemm_tc_kernel", "nn": "gemm_nn_kernel"}
 
 
 def kernel_source_sha(kernel):

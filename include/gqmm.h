@@ -86,7 +86,8 @@ typedef struct CUstream_st* gqmm_stream_t; /* identical to cudaStream_t */
  * in mlx #4339 "Kernel microbenchmark"), format as stated at the top of this header.
  *
  *  w       bfloat16 [rows, H] (for E experts of F x H weights, rows = E*F), 16-byte aligned
- *  rows    >= 0;  H > 0, H % 64 == 0 and H % group_size == 0
+ *  rows    >= 0;  H > 0 and H % group_size == 0 (the quantized axis; gqmm_gather_qmm also needs
+ *          its K a multiple of 64)
  *  group_size 32, 64 or 128 (64 is the pages' setting; 32 and 128 are the other group sizes
  *          of the same affine format), bits must be 4
  *  wq      out: uint8 [rows, H/2], 16-byte aligned
@@ -204,6 +205,28 @@ GQMM_API int gqmm_moe_mlp(const void* x, const void* wq_gu, const void* sc_gu, c
                           int sorted, int x_shared, void* y, void* ws, size_t ws_bytes, gqmm_stream_t stream);
 
 /*
+ * gqmm_gather_qmm_nn -- gather_qmm with transpose=False (mlx PR #4023 "Pick BM from rows per
+ * expert in gather_qmm_rhs_nax", the author's follow-up: the shape of the backward pass and of
+ * fine-tuning):
+ *     y[t, a, :] = x[t, a, :] . deq(W[idx[t, a]]),   W[e] of shape [K, N], quantized along N
+ * (mx.quantize applied to an [E, K, N] weight, the format at the top of this header with H := N).
+ * A first version on CUDA cores: every routed row streams its expert's [K, N] codes (from L2
+ * after the first row of an expert); float32 dequantization and accumulation, bf16 output.
+ *
+ *  x        bfloat16 [T, A, K] (or [T, K] with x_shared = 1), 2-byte aligned
+ *  wq       uint8 [E, K, N/2], 16-byte aligned;  scales, biases  bfloat16 [E, K, N/group_size]
+ *  idx, T, A, E, group_size, bits, x_shared   as for gqmm_gather_qmm (no sorted flag: rows
+ *           are independent and need no route sort)
+ *  K        in [1, 2^24];   N  positive multiple of group_size, at most 2^24
+ *  y        out: bfloat16 [T, A, N], 16-byte aligned
+ * Rows whose idx is >= E are written as zeros (no status word: this call takes no workspace).
+ * Errors: GQMM_ERR_NULL, GQMM_ERR_SHAPE, GQMM_ERR_UNSUPPORTED, GQMM_ERR_ALIGN, GQMM_ERR_CUDA.
+ */
+GQMM_API int gqmm_gather_qmm_nn(const void* x, const void* wq, const void* scales, const void* biases,
+                               const uint32_t* idx, int64_t T, int A, int K, int N, int E, int group_size,
+                               int bits, int x_shared, void* y, gqmm_stream_t stream);
+
+/*
  * gqmm_gather_qmm_simt -- the same operation computed on CUDA cores, one thread per output
  * element with float32 accumulation; needs no workspace.  A slow, independent GPU
  * cross-check of gqmm_gather_qmm's data handling, never used by it.  Same argument rules
@@ -279,7 +302,8 @@ GQMM_API int gqmm_kernel_timer_read(int64_t* launches, double* total_ms);
 #define GQMM_VARIANT_SPLIT_K 5        /* K split into slices, fp32 partial sums + finalize */
 #define GQMM_VARIANT_GEMV 6           /* weight-streaming CUDA-core kernel: routed chunks of 1-2 rows, dense 1 row */
 #define GQMM_VARIANT_GEMV_MMA 7       /* weight-streaming MMA kernel, dense calls of 2 to 8 rows */
-#define GQMM_VARIANT_COUNT 8
+#define GQMM_VARIANT_NN 8             /* gqmm_gather_qmm_nn (transpose=False), CUDA cores */
+#define GQMM_VARIANT_COUNT 9
 GQMM_API int64_t gqmm_dispatch_count(int variant);
 
 #ifdef __cplusplus

@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "GqmmError", "library_path", "load_library", "gqmm_quantize", "gqmm_workspace_size",
     "new_workspace", "gqmm_route_sort", "gqmm_gather_qmm", "gqmm_gather_qmm_simt",
-    "gqmm_moe_mlp_workspace_size", "new_mlp_workspace", "gqmm_moe_mlp",
+    "gqmm_moe_mlp_workspace_size", "new_mlp_workspace", "gqmm_moe_mlp", "gqmm_gather_qmm_nn",
     "gqmm_device_status", "gqmm_status_string", "launch_count", "kernel_timer",
     "kernel_timer_read", "dispatch_count", "STATUS_BAD_INDEX", "STATUS_NOT_SORTED",
     "STATUS_TIMEOUT", "VARIANTS", "MAX_EXPERTS", "ACTIVATIONS",
@@ -38,7 +38,7 @@ STATUS_TIMEOUT = 0x400
 MAX_EXPERTS = 1024
 ACTIVATIONS = {"silu": 0, "gelu": 1, "gelu_tanh": 2}  # GQMM_ACT_* of gqmm_moe_mlp
 VARIANTS = {"route_unsorted": 0, "route_sorted": 1, "route_dense": 2, "gemm_tc": 3, "gemm_narrow": 4,
-            "split_k": 5, "gemv": 6, "gemv_mma": 7}
+            "split_k": 5, "gemv": 6, "gemv_mma": 7, "nn": 8}
 
 
 class GqmmError(RuntimeError):
@@ -69,6 +69,7 @@ def load_library():
             "gqmm_route_sort": ([P, I64, I, P, P, P, SZ, P], I),
             "gqmm_gather_qmm": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, I, P, P, SZ, P], I),
             "gqmm_gather_qmm_simt": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P], I),
+            "gqmm_gather_qmm_nn": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P], I),
             "gqmm_moe_mlp_workspace_size": ([I64, I, I, I], SZ),
             "gqmm_moe_mlp": ([P, P, P, P, P, P, P, P, I64, I, I, I, I, I, I, I, I, I, P, P, SZ, P], I),
             "gqmm_device_status": ([P, P], I),
@@ -237,6 +238,33 @@ def gqmm_gather_qmm_simt(x, wq, scales, biases, idx, group_size: int = 64, bits:
     _check(lib.gqmm_gather_qmm_simt(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(idx), T, A, H, F, E,
                                     group_size, bits, _x_shared(x, T, A, H), _ptr(y), _stream(stream, x.device)),
            "gqmm_gather_qmm_simt")
+    return y
+
+
+def gqmm_gather_qmm_nn(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
+                       idx: Optional[torch.Tensor], group_size: int = 64, bits: int = 4,
+                       y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """gather_qmm with transpose=False: y[t, a, :] = x[t, a, :] . deq(W[idx[t, a]]), W[e] [K, N]
+    quantized along N.  x bf16 [T, A, K] (or [T, K], shared by the A rows, or [n, K]); wq uint8
+    [E, K, N/2] and scales/biases [E, K, N/group_size], as gqmm_quantize writes for an [E, K, N]
+    weight; idx as for gqmm_gather_qmm.  Returns y bf16 [..., N]."""
+    _need(x, "x", torch.bfloat16)
+    if idx is not None and (not idx.is_cuda or not idx.is_contiguous() or idx.element_size() != 4):
+        raise ValueError("idx must be a contiguous 32-bit CUDA tensor")
+    K = x.shape[-1]
+    if wq.dim() != 3 or wq.shape[1] != K:
+        raise ValueError(f"wq must be [E, K, N/2] with K = {K}, got {tuple(wq.shape)}")
+    E, N = wq.shape[0], wq.shape[2] * 2
+    _check_groups(scales, N, group_size, "scales")
+    T, A, _, _, _ = _gather_shapes(x, idx, wq)
+    if y is None:
+        y = torch.empty(_out_shape(x, T, A, N), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(y, "y", torch.bfloat16)
+    lib = load_library()
+    _check(lib.gqmm_gather_qmm_nn(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(idx), T, A, K, N, E,
+                                  group_size, bits, _x_shared(x, T, A, K), _ptr(y), _stream(stream, x.device)),
+           "gqmm_gather_qmm_nn")
     return y
 
 

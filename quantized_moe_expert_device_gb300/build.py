@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libgqmm.so")
-SOURCES = ["api.cu", "quantize.cu", "route.cu", "gemm_tc.cu", "gemm_simt.cu", "noalloc.cu", "gemv.cu", "gemv_mma.cu", "mlp.cu"]
+SOURCES = ["api.cu", "quantize.cu", "route.cu", "gemm_tc.cu", "gemm_simt.cu", "noalloc.cu", "gemv.cu", "gemv_mma.cu", "mlp.cu", "gemm_nn.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "gqmm_internal.cuh"
+#include "gemm_nn.cuh"
 #include "mlp.cuh"
 
 using namespace gqmm;
@@ -354,8 +355,8 @@ int gqmm_quantize(const void* w, int64_t rows, int64_t H, int group_size, int bi
   if (!w || !wq || !scales || !biases) return fail(GQMM_ERR_NULL, "w, wq, scales, biases must be non-NULL");
   if ((group_size != 32 && group_size != 64 && group_size != 128) || bits != 4)
     return fail(GQMM_ERR_UNSUPPORTED, "need group_size 32, 64 or 128 and bits=4 (got %d, %d)", group_size, bits);
-  if (rows < 0 || H <= 0 || H % 64 || H % group_size)
-    return fail(GQMM_ERR_SHAPE, "need rows >= 0 and H a positive multiple of 64 and of group_size");
+  if (rows < 0 || H <= 0 || H % group_size)
+    return fail(GQMM_ERR_SHAPE, "need rows >= 0 and H a positive multiple of group_size");
   if (!aligned(w, 16) || !aligned(wq, 16)) return fail(GQMM_ERR_ALIGN, "w and wq must be 16-byte aligned");
   if (!aligned(scales, 2) || !aligned(biases, 2)) return fail(GQMM_ERR_ALIGN, "scales and biases must be 2-byte aligned");
   int rc = check_device(nullptr);
@@ -428,6 +429,42 @@ int gqmm_moe_mlp(const void* x, const void* wq_gu, const void* sc_gu, const void
                  size_t ws_bytes, gqmm_stream_t stream) {
   return gqmm::moe_mlp_impl(x, wq_gu, sc_gu, bs_gu, wq_dn, sc_dn, bs_dn, idx, T, A, H, I, E, group_size, bits,
                             activation, sorted, x_shared, y, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int gqmm_gather_qmm_nn(const void* x, const void* wq, const void* scales, const void* biases, const uint32_t* idx,
+                       int64_t T, int A, int K, int N, int E, int group_size, int bits, int x_shared, void* y,
+                       gqmm_stream_t stream) {
+  if (!x || !wq || !scales || !biases || !y) return fail(GQMM_ERR_NULL, "x, wq, scales, biases and y must be non-NULL");
+  if ((group_size != 32 && group_size != 64 && group_size != 128) || bits != 4)
+    return fail(GQMM_ERR_UNSUPPORTED, "need group_size 32, 64 or 128 and bits=4 (got %d, %d)", group_size, bits);
+  if (T < 1 || A < 1 || T * (int64_t)A > 2147483647LL)
+    return fail(GQMM_ERR_SHAPE, "need T >= 1, A >= 1, T*A < 2^31 (got T=%lld A=%d)", (long long)T, A);
+  if (K < 1 || K > (1 << 24)) return fail(GQMM_ERR_SHAPE, "K must be in [1, 2^24] (got %d)", K);
+  if (N <= 0 || N % group_size || N > (1 << 24))
+    return fail(GQMM_ERR_SHAPE, "N must be a positive multiple of group_size, at most 2^24 (got %d)", N);
+  if (E < 1) return fail(GQMM_ERR_SHAPE, "E must be >= 1 (got %d)", E);
+  if (E > GQMM_MAX_EXPERTS) return fail(GQMM_ERR_UNSUPPORTED, "E=%d exceeds %d", E, GQMM_MAX_EXPERTS);
+  if ((int64_t)E * K * N / 2 > (int64_t)1 << 40) return fail(GQMM_ERR_SHAPE, "E*K*N too large");
+  if (!idx && E != 1) return fail(GQMM_ERR_NULL, "idx may be NULL only for the dense case E == 1");
+  int rc = validate_shared(x_shared, idx);
+  if (rc) return rc;
+  if (!aligned(x, 2) || !aligned(wq, 16) || !aligned(scales, 2) || !aligned(biases, 2) || !aligned(y, 16))
+    return fail(GQMM_ERR_ALIGN, "wq and y must be 16-byte aligned, x, scales and biases 2-byte aligned");
+  if (idx && !aligned(idx, 4)) return fail(GQMM_ERR_ALIGN, "idx must be 4-byte aligned");
+  rc = check_device(nullptr);
+  if (rc) return rc;
+  size_t slot = 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool timed = timer_begin(s, &slot);
+  cudaError_t e = launch_gemm_nn(static_cast<const __nv_bfloat16*>(x), static_cast<const uint8_t*>(wq),
+                                 static_cast<const __nv_bfloat16*>(scales), static_cast<const __nv_bfloat16*>(biases),
+                                 idx, T * (int64_t)A, K, N, E, group_size, x_shared ? A : 1,
+                                 static_cast<__nv_bfloat16*>(y), s);
+  if (timed) timer_end(s, slot);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "transpose=False launch: %s", cudaGetErrorString(e));
+  g_launches.fetch_add(1);
+  count_variant(GQMM_VARIANT_NN);
+  return ok();
 }
 
 int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* scales, const void* biases,

@@ -41,7 +41,8 @@ def test_binding_covers_the_boundary():
 
     lib = g.load_library()
     for name in ("gqmm_quantize", "gqmm_route_sort", "gqmm_gather_qmm", "gqmm_workspace_size",
-                 "gqmm_device_status", "gqmm_gather_qmm_simt", "gqmm_moe_mlp", "gqmm_moe_mlp_workspace_size"):
+                 "gqmm_device_status", "gqmm_gather_qmm_simt", "gqmm_moe_mlp", "gqmm_moe_mlp_workspace_size",
+                 "gqmm_gather_qmm_nn"):
         assert hasattr(g, name)
         assert getattr(lib, name).argtypes is not None
 

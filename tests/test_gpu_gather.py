@@ -224,6 +224,14 @@ def test_dispatch_coverage_every_variant_runs_and_matches():
         x = wl.normal_bf16((rows, H), wl.SEED_X)
         yd, yd_ref, _ = _run(x, None, 1, host1, dev1)
         assert_parity(yd, yd_ref, f"coverage dense {rows} rows")
+    # transpose=False: W [E, K = H, N = 256] quantized along N
+    w_nn = wl.normal_bf16((E, H, 256), 91, chunk_rows=1)
+    q_nn_host, q_nn_dev = oracle.quantize(w_nn), g.gqmm_quantize(w_nn.cuda())
+    idx_nn = wl.idx_uniform(8, 2, E)
+    x_nn = wl.normal_bf16((8, 2, H), 92)
+    y_nn = g.gqmm_gather_qmm_nn(x_nn.cuda(), *q_nn_dev, to_dev_idx(idx_nn))
+    torch.cuda.synchronize()
+    assert_parity(y_nn, oracle.gather_qmm_nn(x_nn, *q_nn_host, idx_nn, E), "coverage transpose=False")
     after = {k: g.dispatch_count(k) for k in g.VARIANTS}
     for k in g.VARIANTS:
         assert after[k] > before[k], f"variant {k} never dispatched"

@@ -128,7 +128,8 @@ class Workload:
     r: int = 0              # rows per expert for "balanced"
     note: str = ""
     group_size: int = 64    # quantization group along the reduction dimension (32, 64 or 128)
-    kind: str = "gather"    # "gather": one projection, F output columns;
+    kind: str = "gather"    # "gather": one projection, F output columns; "nn": transpose=False, W [E, H, F]
+                            # quantized along F (K = H, N = F);
                             # "mlp": the expert MLP, F = intermediate width I (gate/up 2F rows, down H rows)
 
     @property
@@ -154,6 +155,8 @@ def workloads() -> Dict[str, Workload]:
     for gs in (32, 128):
         w[f"prefill_e64_g{gs}"] = Workload(f"prefill_e64_g{gs}", T=2048, A=8, H=2048, F=768, E=64, routing="uniform",
                                            group_size=gs, note=f"MoE prefill microbenchmark shape, {gs}-wide groups")
+    w["nn_e4"] = Workload("nn_e4", T=1024, A=1, H=512, F=512, E=4, routing="uniform", kind="nn",
+                          note="transpose=False gather_qmm, E=4, K=N=512, 1024 rows (the mlx PR #4023 follow-up timing)")
     w["prefill_dense"] = Workload("prefill_dense", T=16384, A=1, H=2048, F=768, E=1, routing="dense",
                                   note="equal-FLOPs dense control x[16384,2048] x W[768,2048]^T")
     for r in (4, 8, 16, 32, 64, 128):
@@ -195,6 +198,9 @@ def make_inputs(wl: Workload, seed_x: int = SEED_X, seed_w: int = SEED_W, seed_i
     "mlp" workload w_gu=bf16 [E, 2F, H] ~ N(0, 1/H) and w_dn=bf16 [E, H, F] ~ N(0, 1/F) in place
     of w, scaled so the gate pre-activations are about N(0, 1)."""
     x = normal_bf16((wl.T, wl.A, wl.H), seed_x)
+    if wl.kind == "nn":
+        w = normal_bf16((wl.E, wl.H, wl.F), seed_w, std=wl.w_std, chunk_rows=1)
+        return dict(x=x, w=w, idx=make_idx(wl, seed_idx))
     if wl.kind == "mlp":
         w_gu = normal_bf16((wl.E, 2 * wl.F, wl.H), seed_w, std=wl.H ** -0.5, chunk_rows=1)
         w_dn = normal_bf16((wl.E, wl.H, wl.F), seed_w + 1, std=wl.F ** -0.5, chunk_rows=1)
