@@ -7,7 +7,10 @@
 // 32-bit code word per k, so a warp reads 128 contiguous bytes of a weight row), a block 1024
 // columns.  The row's x is staged in shared memory 1024 values at a time; each k costs a
 // thread one code word, one scale and one bias (its eight columns share a group, since groups
-// are at least 32 wide), and eight dequantize-and-accumulate FMA pairs in float32.
+// are at least 32 wide).  With s q + b = 16 s (1 + q/16) - 16 s + b, where 1 + q/16 is exact in
+// float32 with the code in the mantissa (0x3F800000 | q << 19), a column costs a shift, a
+// masked OR and one FMA, and the k's bias term joins one accumulator shared by the eight:
+//     y[c] = sum_k (16 x_k s_k) v_kc + sum_k x_k (b_k - 16 s_k).
 #include "gqmm_internal.cuh"
 
 namespace gqmm {
@@ -41,6 +44,7 @@ __global__ void __launch_bounds__(kNnThreads) gemm_nn_kernel(const __nv_bfloat16
   float acc[kNnColsPerThread];
 #pragma unroll
   for (int m = 0; m < kNnColsPerThread; ++m) acc[m] = 0.f;
+  float corr = 0.f;  // sum_k x_k (b_k - 16 s_k), shared by the thread's columns
   for (int k0 = 0; k0 < K; k0 += kNnChunk) {
     const int kn = K - k0 < kNnChunk ? K - k0 : kNnChunk;
     __syncthreads();  // the previous chunk is consumed
@@ -53,9 +57,14 @@ __global__ void __launch_bounds__(kNnThreads) gemm_nn_kernel(const __nv_bfloat16
         const float s = __bfloat162float(srow[k * G]);
         const float b = __bfloat162float(brow[k * G]);
         const float xk = xs[kk];
+        const float a16 = (xk * s) * 16.f;  // exact scaling by 16
+        corr = fmaf(xk, b, corr) - a16;
 #pragma unroll
-        for (int m = 0; m < kNnColsPerThread; ++m)
-          acc[m] = fmaf(xk, fmaf(s, (float)((word >> (4 * m)) & 15u), b), acc[m]);
+        for (int m = 0; m < kNnColsPerThread; ++m) {
+          // nibble m to mantissa bits 19..22: 1 + q/16
+          const uint32_t bits = 4 * m <= 19 ? (word << (19 - 4 * m)) : (word >> (4 * m - 19));
+          acc[m] = fmaf(a16, __uint_as_float((bits & 0x00780000u) | 0x3F800000u), acc[m]);
+        }
       }
     }
   }
@@ -63,8 +72,8 @@ __global__ void __launch_bounds__(kNnThreads) gemm_nn_kernel(const __nv_bfloat16
     uint32_t o[4];
 #pragma unroll
     for (int m = 0; m < 4; ++m)
-      o[m] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * m])) |
-             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * m + 1])) << 16);
+      o[m] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * m] + corr)) |
+             ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(acc[2 * m + 1] + corr)) << 16);
     *reinterpret_cast<uint4*>(y + i * N + (int64_t)w * kNnColsPerThread) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
