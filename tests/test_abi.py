@@ -136,3 +136,33 @@ def test_mlp_validation_rejects_bad_arguments_without_a_gpu(lib):
     assert lib.gqmm_moe_mlp_workspace_size(32, 256, 128, 8) > lib.gqmm_moe_mlp_workspace_size(32, 256, 64, 8) > 0
     assert lib.gqmm_moe_mlp_workspace_size(32, 256, 0, 8) == 0
     assert lib.gqmm_moe_mlp_workspace_size(32, 256, 128, 0) == 0
+
+
+def test_nn_validation_rejects_bad_arguments_without_a_gpu(lib):
+    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    f = lib.gqmm_gather_qmm_nn
+    f.argtypes = [P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P]
+    f.restype = I
+    fake = P(0x10000)  # never dereferenced: every call below fails validation first
+    args = dict(x=fake, wq=fake, sc=fake, bs=fake, idx=fake, T=16, A=2, K=256, N=128, E=8, gs=64, bits=4, shared=0,
+                y=fake, s=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return f(a["x"], a["wq"], a["sc"], a["bs"], a["idx"], a["T"], a["A"], a["K"], a["N"], a["E"], a["gs"],
+                 a["bits"], a["shared"], a["y"], a["s"])
+
+    assert call(wq=None) == 1                 # ERR_NULL
+    assert call(gs=96) == 3                   # ERR_UNSUPPORTED
+    assert call(bits=2) == 3
+    assert call(N=96) == 2                    # ERR_SHAPE: N must be a multiple of the group size
+    assert call(K=0) == 2
+    assert call(T=0) == 2
+    assert call(E=0) == 2
+    assert call(E=2048) == 3
+    assert call(idx=None) == 1                # dense needs E == 1
+    assert call(shared=2) == 2
+    assert call(shared=1, idx=None, E=1) == 1
+    assert call(y=P(0x10008)) == 4            # ERR_ALIGN: y is stored 16 bytes at a time
+    assert call(wq=P(0x10004)) == 4
