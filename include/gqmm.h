@@ -12,6 +12,11 @@
  *
  * i.e. for every routed row (t, a):  y[t, a, :] = x[t, a, :] . deq(W[idx[t, a]])^T.
  *
+ * Entry points: gqmm_quantize (the weight format below), gqmm_route_sort, gqmm_gather_qmm
+ * (the operation; gqmm_gather_qmm_noalloc without a workspace), gqmm_moe_mlp (the expert MLP
+ * built on it: gate/up, SiLU or GELU gating, down), gqmm_gather_qmm_nn (transpose=False),
+ * gqmm_gather_qmm_simt (a CUDA-core cross-check), and status / instrumentation calls.
+ *
  * Conventions shared by every entry point
  *  - All tensor arguments are DEVICE pointers on the current CUDA device, except where a
  *    comment says otherwise.  The caller allocates and owns every buffer (outputs and the
