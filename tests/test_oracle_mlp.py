@@ -109,3 +109,27 @@ def test_mlp_permutation_invariance_and_rows_subset():
     np.testing.assert_array_equal(yp, y[p])
     rows = [11, 0, 5]
     np.testing.assert_array_equal(oracle.moe_mlp(x, q_gu, q_dn, idx, E, rows=rows), y[rows])
+
+
+@pytest.mark.parametrize("gs", [32, 128])
+def test_mlp_brute_force_other_group_sizes(gs):
+    E, I, H, n = 2, 128, 128, 3
+    q_gu = oracle.quantize(wl.normal_bf16((E, 2 * I, H), 31), group_size=gs)
+    q_dn = oracle.quantize(wl.normal_bf16((E, H, I), 32), group_size=gs)
+    x = wl.normal_bf16((n, H), 33)
+    idx = np.array([1, 0, 1], np.uint32)
+    y = oracle.moe_mlp(x, q_gu, q_dn, idx, E, group_size=gs)
+    xf = _bits_to_f64(wl.bf16_bits(x))
+
+    def deq(q, e, f, h):
+        wq, sc, bs = q
+        code = (int(wq[e, f, h // 2]) >> (4 * (h % 2))) & 15
+        return _bits_to_f64(sc[e, f, h // gs]) * code + _bits_to_f64(bs[e, f, h // gs])
+
+    for i in range(n):
+        e = int(idx[i])
+        g = [sum(xf[i, h] * deq(q_gu, e, f, h) for h in range(H)) for f in range(I)]
+        u = [sum(xf[i, h] * deq(q_gu, e, I + f, h) for h in range(H)) for f in range(I)]
+        hh = [_ACT["silu"](g[k]) * u[k] for k in range(I)]
+        ref = [sum(hh[k] * deq(q_dn, e, o, k) for k in range(I)) for o in range(H)]
+        np.testing.assert_allclose(y[i], ref, rtol=1e-11, atol=1e-11)
