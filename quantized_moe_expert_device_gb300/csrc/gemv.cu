@@ -193,8 +193,22 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
   }
   __syncthreads();
 
-  // The dense plan is known without the route step's output: the wait comes later.
-  if (!p.dense_plan) grid_dependency_wait();
+  // The kernel may start while the previous kernel on the stream is still running
+  // (programmatic dependent launch), and that kernel may be writing this call's x, weights or
+  // y.  A dense call knows its items without the route step, so before the wait its producer
+  // only asks L2 to pull in the block's share of the weights (a prefetch is a hint served by
+  // L2, the point of coherence, so it cannot hand back stale bytes); every copy into shared
+  // memory and every store to y comes after the wait.
+  if (p.dense_plan && warp == NW && lane == 0) {
+    const int per0 = (n_batches + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int f0 = min(F, (int)blockIdx.x * per0 * RB), f1 = min(F, f0 + per0 * RB);
+    if (f1 > f0) {
+      prefetch_l2_bulk(p.wq + (int64_t)f0 * (H / 2), (uint32_t)(f1 - f0) * (H / 2));
+      prefetch_l2_bulk(p.scales + (int64_t)f0 * G, (uint32_t)(f1 - f0) * G * 2);
+      prefetch_l2_bulk(p.biases + (int64_t)f0 * G, (uint32_t)(f1 - f0) * G * 2);
+    }
+  }
+  grid_dependency_wait();
   const int n_chunks = p.dense_plan ? 1 : p.header->n_chunks;
   const int n_items = n_chunks * n_batches;
   const int per = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
@@ -250,9 +264,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
           for (int t = 0; t < xr; ++t)
             bulk_load(base + RB * (H / 2 + 4 * G) + t * H * 2, p.x + (int64_t)xrow[t] * H, H * 2, bar);
         ++issued;
-        if (p.dense_plan && k == NS - 1) grid_dependency_wait();
       }
-      if (p.dense_plan && issued < NS) grid_dependency_wait();
       if (!ok || abort_flag) {
         // unwinding: wait (bounded) for the copies still in flight into this block's memory
         for (int k = max(0, issued - NS); k < issued; ++k)

@@ -27,18 +27,18 @@ def _weights(shape, gs, seed, std=1.0):
     return host, dev
 
 
-@pytest.mark.parametrize("gs", [32, 128])
-@pytest.mark.parametrize("T,A,H,F,E", [(256, 8, 1024, 512, 8),    # wide, H/gs a multiple of 8
-                                       (32, 2, 1024, 256, 8),     # narrow
-                                       (4, 2, 2048, 768, 16),     # decode-sized: narrow with split K
-                                       (64, 2, 384, 128, 4),      # H/128 = 3 scale groups per row
-                                       (40, 1, 192, 128, 1),      # dense; H/32 = 6
-                                       (3, 1, 1024, 256, 1)])     # dense decode-sized
+_GROUP_SHAPES = [(256, 8, 1024, 512, 8),    # wide, H/gs a multiple of 8
+                 (32, 2, 1024, 256, 8),     # narrow
+                 (4, 2, 2048, 768, 16),     # decode-sized: narrow with split K
+                 (64, 2, 384, 128, 4),      # H/128 = 3 scale groups per row
+                 (40, 1, 192, 128, 1),      # dense; H/32 = 6 (192 is no multiple of 128: 32 only)
+                 (3, 1, 1024, 256, 1)]      # dense decode-sized
+
+
+@pytest.mark.parametrize("gs,T,A,H,F,E", [(gs,) + s for gs in (32, 128) for s in _GROUP_SHAPES if s[2] % gs == 0])
 def test_gather_group_sizes_match_oracle(gs, T, A, H, F, E):
     import quantized_moe_expert_device_gb300 as g
 
-    if H % gs:
-        pytest.skip("H must be a multiple of the group size")
     host, dev = _weights((E, F, H), gs, seed=41 + gs)
     x = wl.normal_bf16((T, A, H) if E > 1 else (T, H), 43)
     idx = None if E == 1 else np.random.default_rng(T + gs).integers(0, E, size=(T, A)).astype(np.uint32)
