@@ -156,7 +156,7 @@ GQMM_API int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* per
  *  sorted   0: idx in any order (the library sorts rows by expert on device);
  *           1: the caller promises idx is nondecreasing in flat order (the issue's
  *              sorted_indices=True).  The result is identical either way; a broken
- *              promise sets GQMM_STATUS_NOT_SORTED.
+ *              promise sets GQMM_STATUS_NOT_SORTED, computes nothing and writes y as zeros.
  *  y        out: bfloat16 [T, A, F] in (t, a) order, 16-byte aligned
  *  ws       workspace of at least gqmm_workspace_size(T*A, F, E) bytes (see above)
  * Rows whose idx is >= E are written as zeros and set GQMM_STATUS_BAD_INDEX.
@@ -262,9 +262,14 @@ GQMM_API int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* sca
  *  - Every call on a device shares the one array: calls whose GPU work overlaps (different
  *    streams, no ordering between them) race and give undefined results.  Calls on one
  *    stream are ordered and safe.
- *  - Each call clears the scratch's status word; device-detected conditions are not
- *    reported (rows with an index >= E are still zeroed).  Use gqmm_gather_qmm with
- *    gqmm_device_status when the status is needed.
+ *  - Each call clears the scratch's status word (after validating its arguments: a refused
+ *    call enqueues nothing), and nothing reads it back, so device-detected conditions are
+ *    NOT reported and the call still returns GQMM_OK: rows with an index >= E come out as
+ *    zeros, a false sorted = 1 promise gives a y of all zeros, and a bounded wait that ran
+ *    out leaves y undefined.  Use gqmm_gather_qmm with gqmm_device_status when these
+ *    conditions must be seen.
+ *  - The device address of the array is cached per device ordinal for the life of the
+ *    process; after cudaDeviceReset on a device, do not call this entry point on it again.
  */
 #define GQMM_NOALLOC_SCRATCH_BYTES (1u << 20)
 GQMM_API int gqmm_gather_qmm_noalloc(const void* x, const void* wq, const void* scales, const void* biases,

@@ -167,7 +167,7 @@ int launch_projection(const GemmArgs& ga, const UnitShape& shape, int sms, cudaS
 int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, const void* biases,
                           const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size, int bits,
                           int sorted, int x_shared, void* y, void* ws, size_t ws_bytes, cudaStream_t s,
-                          bool allow_split) {
+                          bool allow_split, bool clear_header) {
   int rc = validate_gather(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y);
   if (rc) return rc;
   rc = validate_shared(x_shared, idx);
@@ -185,6 +185,10 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   if (rc) return rc;
   uint8_t* w = static_cast<uint8_t*>(ws);
   WsHeader* header = reinterpret_cast<WsHeader*>(w);
+  if (clear_header) {
+    cudaError_t ce = cudaMemsetAsync(header, 0, sizeof(WsHeader), s);
+    if (ce != cudaSuccess) return fail(GQMM_ERR_CUDA, "clearing the workspace header: %s", cudaGetErrorString(ce));
+  }
 
   RouteArgs ra;
   ra.idx = idx;

@@ -142,11 +142,13 @@ inline WsLayout ws_layout(int64_t n, int F, int E, bool allow_split = true) {
 // Records a printf-style message as the calling thread's gqmm_last_error() and returns code.
 int report_error(int code, const char* fmt, ...);
 
-// gqmm_gather_qmm with a switch: allow_split = false never splits K, so its workspace needs no
-// split-K sum buffer (ws_layout(n, F, E, false)).
+// gqmm_gather_qmm with two switches: allow_split = false never splits K, so its workspace needs
+// no split-K sum buffer (ws_layout(n, F, E, false)); clear_header = true zeroes the workspace's
+// 256-byte header (status word included) on the stream once every argument has been validated,
+// before the first kernel.
 int gather_qmm_impl(const void* x, const void* wq, const void* scales, const void* biases, const uint32_t* idx,
                     int64_t T, int A, int H, int F, int E, int group_size, int bits, int sorted, int x_shared,
-                    void* y, void* ws, size_t ws_bytes, cudaStream_t s, bool allow_split);
+                    void* y, void* ws, size_t ws_bytes, cudaStream_t s, bool allow_split, bool clear_header = false);
 
 
 // ------------------------------------------------------------------------------------------

@@ -72,10 +72,9 @@ extern "C" int gqmm_gather_qmm_noalloc(const void* x, const void* wq, const void
   int rc = scratch_for_current_device(&ws);
   if (rc != GQMM_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The status word at the start of the scratch is cleared on every call: nothing reads it
-  // back through this entry point, and it must not carry bits from earlier calls.
-  cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(gqmm::WsHeader), s);
-  if (e != cudaSuccess) return gqmm::report_error(GQMM_ERR_CUDA, "gqmm_gather_qmm_noalloc: clearing scratch failed");
+  // The header at the start of the scratch (status word included) is cleared on every call,
+  // after the arguments have been validated (a refused call enqueues nothing): nothing reads
+  // the status back through this entry point, and it must not carry bits from earlier calls.
   return gqmm::gather_qmm_impl(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, sorted, 0, y, ws,
-                               kScratchBytes, s, allow_split);
+                               kScratchBytes, s, allow_split, /*clear_header=*/true);
 }

@@ -452,7 +452,14 @@ __global__ void __launch_bounds__(kPlanThreads) route_plan_sorted(RouteArgs a) {
     uint32_t bits = (bad ? GQMM_STATUS_BAD_INDEX : 0u) | (unsorted ? GQMM_STATUS_NOT_SORTED : 0u);
     if (bits) atomicOr(&a.header->status, bits);
   }
-  if (unsorted) {  // the promise is broken: no segments can be trusted, compute nothing
+  if (unsorted) {
+    // The promise is broken: no segment can be trusted, so nothing is computed and y is
+    // defined as all zeros (F is a multiple of 16 and y 16-byte aligned: whole 16-byte stores).
+    if (a.y != nullptr) {
+      uint4* y4 = reinterpret_cast<uint4*>(a.y);
+      const int64_t n16 = n * (int64_t)a.F / 8;
+      for (int64_t i = threadIdx.x; i < n16; i += kPlanThreads) y4[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
     for (int e = threadIdx.x; e <= E; e += kPlanThreads) a.offsets[e] = 0;
     if (threadIdx.x == 0) {
       a.header->n_chunks = 0;
