@@ -69,26 +69,43 @@ def algorithmic_bytes(w: wl.Workload, idx: np.ndarray | None) -> int:
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling while the timed region runs."""
+    """nvidia-smi clock / throttle sampling while the timed region runs.  With timestamps, each
+    sample carries nvidia-smi's own time, so summary(t0, t1) can take the samples of one window
+    of host time (time.time())."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, device_index: int):
+    def __init__(self, device_index: int, timestamps: bool = False):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(tempfile.gettempdir(), f"gqmm_clocks_bench_{os.getpid()}.csv")
+        self.timestamps = timestamps
+        self.samples = []  # (time or None, sm MHz, max sm MHz, set of active reasons)
+        self.path = os.path.join(tempfile.gettempdir(), f"gqmm_clocks_bench_{os.getpid()}_{id(self)}.csv")
 
     def start(self):
+        query = ("timestamp," if self.timestamps else "") + self.QUERY
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={query}", "--format=csv,noheader,nounits",
                  "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+
+    @staticmethod
+    def _stamp(text):
+        import datetime
+
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y/%m/%d %H:%M:%S"):
+            try:
+                return datetime.datetime.strptime(text, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
 
     def stop(self):
         if self.proc is None:
@@ -99,25 +116,38 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as fh:
             for line in fh:
                 parts = [p.strip() for p in line.split(",")]
+                ts = None
+                if self.timestamps:
+                    if not parts:
+                        continue
+                    ts = self._stamp(parts[0])
+                    parts = parts[1:]
                 if len(parts) < 9:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
+                    sm, smax = float(parts[1]), float(parts[2])
                 except ValueError:
                     continue
-                for nm, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(nm)
-        if not sm:
+                active = {nm for nm, v in zip(self.REASONS, parts[5:9]) if v.lower() == "active"}
+                self.samples.append((ts, sm, smax, active))
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
+        return self.summary()
+
+    def summary(self, t0=None, t1=None):
+        sel = [s_ for s_ in self.samples if t0 is None or (s_[0] is not None and t0 <= s_[0] <= t1)]
+        if not sel:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        reasons = set()
+        for s_ in sel:
+            reasons |= s_[3]
+        return {"sm_mhz": float(np.median([s_[1] for s_ in sel])), "sm_max_mhz": max(s_[2] for s_ in sel),
+                "reasons": sorted(reasons), "samples": len(sel)}
 
 
 def dist_setup():
@@ -258,128 +288,258 @@ def run_reference(args, w: wl.Workload, world: int, rank: int):
 # GPU arm
 # ----------------------------------------------------------------------------------------------
 
+# Workloads timed after the headline, each on its own rotated inputs, into the line's per_config
+# block: the equal-FLOPs dense control, the rows-per-expert sweep, the Mixtral-like expert shape,
+# dense and MoE decode at 1-8 rows, the other group sizes, the expert MLP and transpose=False.
+PER_CONFIG = ["prefill_dense", "prefill_e64_g32", "prefill_e64_g128",
+              "sweep_r4", "sweep_r8", "sweep_r16", "sweep_r32", "sweep_r64", "sweep_r128", "mixtral",
+              "decode_dense_m1", "decode_dense_m2", "decode_dense_m4", "decode_dense_m8",
+              "decode_moe_m1", "decode_moe_m2", "decode_moe_m4", "decode_moe_m8",
+              "mlp_e64", "mlp_decode_m8", "nn_e4"]
+ROTATE_L2_MULTIPLE = 4        # distinct input copies cover at least this many times the L2 size
+MAX_COPIES = 96               # ... within this many copies
+MAX_CLONE_BYTES = 24 << 30    # ... and this many bytes of copies
+STRIPS = 5                    # the timed steps are split into this many strips (median reported)
+
+
+def _weights_on_device(g, w: wl.Workload, inp, dev):
+    """The workload's weights quantized on the GPU: [wq, scales, biases] (both projections for the
+    expert MLP)."""
+    out = []
+    for key in (("w_gu", "w_dn") if w.kind == "mlp" else ("w",)):
+        w_dev = inp[key].to(dev)
+        out += list(g.gqmm_quantize(w_dev, group_size=w.group_size))
+        del w_dev
+    return out
+
+
+class Prepared:
+    """Device-resident inputs of one workload, rotated over enough copies that one pass over them
+    reads at least ROTATE_L2_MULTIPLE x L2 of distinct bytes, and the C-ABI call of each copy."""
+
+    def __init__(self, g, lib, w: wl.Workload, dev, stream, cache):
+        self.w, self.g, self.lib = w, g, lib
+        self.inp = wl.make_inputs(w, cache=cache)
+        idx_np = self.inp["idx"]
+        self.idx_np = idx_np
+        self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.per_copy = algorithmic_bytes(w, idx_np)
+        weights0 = _weights_on_device(g, w, self.inp, dev)
+        clone_bytes = sum(t.numel() * t.element_size() for t in weights0) + w.n * (w.H + w.out_cols) * 2 + w.n * 4
+        want = int(np.ceil(ROTATE_L2_MULTIPLE * self.l2 / max(self.per_copy, 1)))
+        self.copies = int(max(2, min(want, MAX_COPIES, MAX_CLONE_BYTES // max(clone_bytes, 1))))
+        if w.kind == "mlp":
+            fn, ws_new = lib.gqmm_moe_mlp, (lambda: g.new_mlp_workspace(w.n, w.H, w.F, w.E, dev))
+            sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4, g.ACTIVATIONS[MLP_ACTIVATION])
+        elif w.kind == "nn":  # no workspace: rows are independent, no route sort
+            fn, ws_new = lib.gqmm_gather_qmm_nn, (lambda: None)
+            sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4, 0)
+        else:
+            fn, ws_new = lib.gqmm_gather_qmm, (lambda: g.new_workspace(w.n, w.F, w.E, dev))
+            sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4)
+        x0 = self.inp["x"].to(dev)
+        idx0 = None if idx_np is None else torch.from_numpy(np.ascontiguousarray(idx_np).view(np.int32)).to(dev)
+        self.sets = []
+        for c in range(self.copies):
+            last = c == self.copies - 1  # the last copy takes the originals instead of cloning them
+            self.sets.append(dict(
+                x=x0 if last else x0.clone(), w=weights0 if last else [t.clone() for t in weights0],
+                idx=None if idx0 is None else (idx0 if last else idx0.clone()),
+                y=torch.empty(w.T, w.A, w.out_cols, dtype=torch.bfloat16, device=dev), ws=ws_new()))
+        torch.cuda.synchronize(dev)
+        self.fn, self.fn_name = fn, fn.__name__
+        sptr = ctypes.c_void_p(stream.cuda_stream)
+        P = ctypes.c_void_p
+
+        def argv(st):
+            head = (P(st["x"].data_ptr()),) + tuple(P(t.data_ptr()) for t in st["w"]) + (
+                None if st["idx"] is None else P(st["idx"].data_ptr()),) + sizes
+            if w.kind == "nn":
+                return head + (P(st["y"].data_ptr()), sptr)
+            return head + (0, 0, P(st["y"].data_ptr()), P(st["ws"].data_ptr()), st["ws"].numel(), sptr)
+
+        self.calls = [argv(st) for st in self.sets]
+
+    def step(self, i):
+        rc = self.fn(*self.calls[i % self.copies])
+        if rc != 0:
+            raise RuntimeError(f"{self.fn_name} failed: {rc} {self.lib.gqmm_last_error().decode()}")
+
+    def status(self):
+        st = 0
+        for s_ in self.sets:
+            if s_["ws"] is not None:
+                st |= self.g.gqmm_device_status(s_["ws"])
+        return st
+
+    def l2_note(self):
+        return (f"inputs rotate over {self.copies} copies ({self.copies * self.per_copy / 1e6:.0f} MB of algorithmic "
+                f"bytes; L2 {self.l2 / 1e6:.0f} MB)")
+
+
+def timed_strips(prep: Prepared, steps: int, stream, world: int):
+    """The metric's timed region: `steps` calls with nothing between the library's kernels, split
+    into STRIPS strips with CUDA events on the call's stream at the strip boundaries.  Returns
+    (total ms, [ms per step of each strip])."""
+    bounds = [round(k * steps / STRIPS) for k in range(STRIPS + 1)]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(STRIPS + 1)]
+    barrier(world)
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for k in range(STRIPS):
+        for i in range(bounds[k], bounds[k + 1]):
+            prep.step(i)
+        evs[k + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    strips = [evs[k].elapsed_time(evs[k + 1]) / max(bounds[k + 1] - bounds[k], 1) for k in range(STRIPS)]
+    return evs[0].elapsed_time(evs[STRIPS]), strips
+
+
+def kernel_pass(prep: Prepared, steps: int, world: int):
+    """The same steps again with CUDA events around every GEMM launch on the call's stream (the
+    library's kernel timer; those events would stop the GEMM's prologue from overlapping the route
+    step, hence a separate pass).  Returns (GEMM ms per step, GEMM launches per step)."""
+    g = prep.g
+    slots = steps * GEMM_LAUNCHES_PER_STEP[prep.w.kind]
+    g.kernel_timer(slots)
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        prep.step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    n_timed, ms_total = g.kernel_timer_read()
+    g.kernel_timer(0)
+    if n_timed != slots:
+        raise RuntimeError(f"kernel timer recorded {n_timed} GEMM launches, expected {slots}")
+    return ms_total / max(steps, 1), n_timed / max(steps, 1)
+
+
+def roofline_entry(w: wl.Workload, alg_bytes: int, gemm_ms: float, peaks, peaks_src, sm_max, sms, kernel):
+    flops = float(w.flops)
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if flops / alg_bytes >= ridge else "hbm"
+    peak_source = f"{peaks_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"
+    if w.kind == "nn":
+        # CUDA-core kernel: the float32 FMA pipes (128 lanes per SM, 2 FLOP per FMA) at the
+        # maximum SM clock
+        bound = "alu"
+        peak = sms * 128 * 2 * sm_max * 1e6 / 1e12
+        achieved, unit = flops / (gemm_ms * 1e-3) / 1e12, "TFLOP/s"
+        peak_source = f"derived: {sms} SMs x 128 FP32 lanes x 2 FLOP x {sm_max} MHz"
+    elif bound == "tensor":
+        achieved, peak, unit = flops / (gemm_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = alg_bytes / (gemm_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "traffic": measured_traffic(kernel, w.name), "kernel": kernel, "kernel_ms": gemm_ms,
+            "peak_source": peak_source}
+
+
+def op_roofline_entry(w: wl.Workload, alg_bytes: int, ms_per_step: float, peaks):
+    flops = float(w.flops)
+    t_roof_s = max(flops / (peaks["bf16_tflops"] * 1e12), alg_bytes / (peaks["hbm_gbs"] * 1e9))
+    return {"t_min_us": t_roof_s * 1e6, "frac": t_roof_s / (ms_per_step * 1e-3), "algorithmic_bytes": alg_bytes,
+            "flops": flops}
+
+
+def _kernel_of(g, variants0):
+    ran = [v for v in _VARIANT_KERNEL if g.dispatch_count(v) > variants0[v]]
+    return _VARIANT_KERNEL[ran[0]] if ran else "gemm_tc_kernel"
+
+
+def measure_config(g, lib, w: wl.Workload, dev, stream, world, cache, peaks, peaks_src, sms, target_s: float,
+                   max_steps: int):
+    """One per_config entry: the headline's method (rotated inputs, strips, kernel-timer pass) on
+    another workload, with the step count chosen so its timed region lasts about target_s."""
+    prep = Prepared(g, lib, w, dev, stream, cache)
+    for i in range(max(3, min(prep.copies, 20))):
+        prep.step(i)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(10):
+        prep.step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    est_ms = e0.elapsed_time(e1) / 10
+    steps = int(min(max_steps, max(4 * STRIPS, target_s * 1e3 / max(est_ms, 1e-4))))
+    launches0 = g.launch_count()
+    variants0 = {v: g.dispatch_count(v) for v in _VARIANT_KERNEL}
+    t0 = time.time()
+    ms_total, strips = timed_strips(prep, steps, stream, world)
+    t1 = time.time()
+    launches = (g.launch_count() - launches0) / steps
+    kernel = _kernel_of(g, variants0)
+    gemm_ms, gemm_launches = kernel_pass(prep, steps, world)
+    status = prep.status()
+    if status:
+        raise RuntimeError(f"{w.name}: device status after the timed region: {status:#x}")
+    ms_max = max_over_ranks(ms_total, world)
+    ms_per_step = ms_max / steps
+    alg = algorithmic_bytes(w, prep.idx_np)
+    entry = {
+        "workload": w.name, "metric": metric_name(w), "config": workload_config(w),
+        "value": float(w.flops) * world / (ms_per_step * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "ms_per_step": ms_per_step, "steps": steps,
+        "strips": {"n": STRIPS, "median_ms_per_step": float(np.median(strips)), "ms_per_step": strips},
+        "hbm_gbs": alg / (ms_per_step * 1e-3) / 1e9,
+        "roofline": dict(roofline_entry(w, alg, gemm_ms, peaks, peaks_src, 2070, sms, kernel),
+                         kernel_launches_per_step=gemm_launches),
+        "op_roofline": op_roofline_entry(w, alg, ms_per_step, peaks),
+        "gpu_launches_per_step": launches, "l2": prep.l2_note(), "window": (t0, t1),
+    }
+    del prep
+    torch.cuda.empty_cache()
+    return entry
+
+
 def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     import quantized_moe_expert_device_gb300 as g
 
     lib = g.load_library()
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
-    inp = wl.make_inputs(w)
-    idx_np = inp["idx"]
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-
-    # Rotate enough distinct copies of every input that the working set exceeds 3x L2.
-    per_copy = algorithmic_bytes(w, idx_np)
-    copies = int(max(2, min(16, np.ceil(3 * l2 / max(per_copy, 1)))))
-    if w.kind == "mlp":
-        weights0 = []
-        for key in ("w_gu", "w_dn"):
-            w_dev = inp[key].to(dev)
-            weights0 += list(g.gqmm_quantize(w_dev, group_size=w.group_size))
-            del w_dev
-        fn, ws_new = lib.gqmm_moe_mlp, (lambda: g.new_mlp_workspace(w.n, w.H, w.F, w.E, dev))
-        sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4, g.ACTIVATIONS[MLP_ACTIVATION])
-    else:
-        w_dev = inp["w"].to(dev)
-        weights0 = list(g.gqmm_quantize(w_dev, group_size=w.group_size))
-        del w_dev
-        if w.kind == "nn":  # no workspace: rows are independent, no route sort
-            fn, ws_new = lib.gqmm_gather_qmm_nn, (lambda: None)
-            sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4, 0)
-        else:
-            fn, ws_new = lib.gqmm_gather_qmm, (lambda: g.new_workspace(w.n, w.F, w.E, dev))
-            sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4)
-    x0 = inp["x"].to(dev)
-    idx0 = None if idx_np is None else torch.from_numpy(np.ascontiguousarray(idx_np).view(np.int32)).to(dev)
-    sets = []
-    for c in range(copies):
-        s = dict(x=x0.clone(), w=[t.clone() for t in weights0], idx=None if idx0 is None else idx0.clone(),
-                 y=torch.empty(w.T, w.A, w.out_cols, dtype=torch.bfloat16, device=dev), ws=ws_new())
-        sets.append(s)
-    del x0, weights0, idx0
-    torch.cuda.synchronize(dev)
-
-    sptr = ctypes.c_void_p(stream.cuda_stream)
-    fn_name = fn.__name__
-
-    def argv(s, sorted_flag=0):
-        P = ctypes.c_void_p
-        if w.kind == "nn":
-            return ((P(s["x"].data_ptr()),) + tuple(P(t.data_ptr()) for t in s["w"])
-                    + (None if s["idx"] is None else P(s["idx"].data_ptr()),) + sizes + (P(s["y"].data_ptr()), sptr))
-        return ((P(s["x"].data_ptr()),) + tuple(P(t.data_ptr()) for t in s["w"])
-                + (None if s["idx"] is None else P(s["idx"].data_ptr()),) + sizes
-                + (sorted_flag, 0, P(s["y"].data_ptr()), P(s["ws"].data_ptr()), s["ws"].numel(), sptr))
-
-    calls = [argv(s) for s in sets]
-
-    def step(i):
-        rc = fn(*calls[i % copies])
-        if rc != 0:
-            raise RuntimeError(f"{fn_name} failed: {rc} {lib.gqmm_last_error().decode()}")
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cache = {}
+    prep = Prepared(g, lib, w, dev, stream, cache)
+    inp, idx_np = prep.inp, prep.idx_np
 
     for i in range(args.warmup):
-        step(i)
+        prep.step(i)
     torch.cuda.synchronize(dev)
-    timer_slots = args.steps * GEMM_LAUNCHES_PER_STEP[w.kind]
-    g.kernel_timer(timer_slots)  # events are created here, before the timed region
+    g.kernel_timer(args.steps * GEMM_LAUNCHES_PER_STEP[w.kind])  # events are created here, before the timed region
     g.kernel_timer(0)
 
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    # Timed pass 1, the metric: K steps with nothing between the library's kernels (its own
-    # kernel timer would put events between the route step and the GEMM, which stops the
-    # GEMM's prologue from overlapping the route step).
-    barrier(world)
-    torch.cuda.synchronize(dev)
+    # Timed pass 1, the metric: K steps with nothing between the library's kernels, in strips.
     launches0 = g.launch_count()
     variants0 = {v: g.dispatch_count(v) for v in _VARIANT_KERNEL}
     t_host0 = time.perf_counter()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    ev1.record(stream)
+    ms_total, strips = timed_strips(prep, args.steps, stream, world)
     t_host_enqueue = time.perf_counter() - t_host0
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    ms_total = ev0.elapsed_time(ev1)
     launches = g.launch_count() - launches0
-    ran = [v for v in _VARIANT_KERNEL if g.dispatch_count(v) > variants0[v]]
-    kernel = _VARIANT_KERNEL[ran[0]] if ran else "gemm_tc_kernel"
+    kernel = _kernel_of(g, variants0)
     # Hot pass (context only, not the metric): the same call repeated on one input set, so
     # inputs that fit in L2 stay there between steps.
     hot_steps = min(args.steps, 200)
     h0 = torch.cuda.Event(enable_timing=True)
     h1 = torch.cuda.Event(enable_timing=True)
     for _ in range(3):
-        fn(*calls[0])
+        prep.fn(*prep.calls[0])
     h0.record(stream)
     for _ in range(hot_steps):
-        fn(*calls[0])
+        prep.fn(*prep.calls[0])
     h1.record(stream)
     torch.cuda.synchronize(dev)
     hot_ms = max_over_ranks(h0.elapsed_time(h1), world) / hot_steps
-    # Timed pass 2, the roofline: the same K steps with CUDA events around every GEMM launch
-    # on the call's stream (the library's kernel timer).
-    g.kernel_timer(timer_slots)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    for i in range(args.steps):
-        step(i)
-    torch.cuda.synchronize(dev)
-    barrier(world)
+    # Timed pass 2, the roofline: the same K steps with CUDA events around every GEMM launch.
+    gemm_ms, gemm_launches_per_step = kernel_pass(prep, args.steps, world)
     clocks = sampler.stop()
-    n_timed, gemm_ms_total = g.kernel_timer_read()
-    g.kernel_timer(0)
-    if n_timed != timer_slots:
-        raise RuntimeError(f"kernel timer recorded {n_timed} GEMM launches, expected {timer_slots}")
-    status = 0
-    for s in sets:
-        if s["ws"] is not None:
-            status |= g.gqmm_device_status(s["ws"])
+    status = prep.status()
     if status:
         raise RuntimeError(f"device status after timed region: {status:#x}")
 
@@ -387,36 +547,13 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     ms_per_step = ms_max / args.steps
     flops = float(w.flops)
     value = flops * world * args.steps / (ms_max * 1e-3) / 1e12
-
     peaks, peaks_src = load_peaks()
     alg_bytes = algorithmic_bytes(w, idx_np)
-    # GEMM launches per step: 1 for gather_qmm, 2 for the expert MLP (its gate/up and down
-    # projections); the roofline takes the step's FLOPs (bytes) over their summed durations.
-    gemm_launches_per_step = n_timed / max(args.steps, 1)
-    gemm_ms = gemm_ms_total / max(args.steps, 1)
-    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    bound = "tensor" if flops / alg_bytes >= ridge else "hbm"
-    peak_source = f"{peaks_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"
-    if w.kind == "nn":
-        # CUDA-core kernel: the float32 FMA pipes (128 lanes per SM, 2 FLOP per FMA) at the
-        # maximum SM clock; it issues two FMAs (dequantize, accumulate) per multiply-add of the
-        # metric, so half of this peak is its ceiling
-        bound = "alu"
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        sm_max = (clocks or {}).get("sm_max_mhz") or 2070
-        peak = sms * 128 * 2 * sm_max * 1e6 / 1e12
-        achieved = flops / (gemm_ms * 1e-3) / 1e12
-        unit = "TFLOP/s"
-        peak_source = f"derived: {sms} SMs x 128 FP32 lanes x 2 FLOP x {sm_max} MHz"
-    elif bound == "tensor":
-        achieved = flops / (gemm_ms * 1e-3) / 1e12
-        peak = peaks["bf16_tflops"]
-        unit = "TFLOP/s"
-    else:
-        achieved = alg_bytes / (gemm_ms * 1e-3) / 1e9
-        peak = peaks["hbm_gbs"]
-        unit = "GB/s"
-    t_roof_s = max(flops / (peaks["bf16_tflops"] * 1e12), alg_bytes / (peaks["hbm_gbs"] * 1e9))
+    sm_max = (clocks or {}).get("sm_max_mhz") or 2070
+    roof = dict(roofline_entry(w, alg_bytes, gemm_ms, peaks, peaks_src, sm_max, sms, kernel),
+                kernel_launches_per_step=gemm_launches_per_step,
+                kernel_timing="second timed pass of the same steps, CUDA events around each GEMM launch;"
+                              " kernel_ms = their summed duration per step")
 
     # ---- end to end: host-resident inputs, pinned, copied in and out every step ----
     # Every step copies its own inputs in from pinned host memory and its own result back.
@@ -425,6 +562,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     # result is copied out; a set is refilled only once the step that used it has finished with
     # its inputs and its result has left the device.  Smaller steps run everything on the call's
     # stream, where cross-stream events would cost more than the overlap saves.
+    sets, calls, fn = prep.sets, prep.calls, prep.fn
     e2e_steps = max(3, min(args.steps, 200))
     x_h = inp["x"].pin_memory()
     idx_h = None if idx_np is None else torch.from_numpy(np.ascontiguousarray(idx_np).view(np.int32)).pin_memory()
@@ -438,6 +576,11 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     ev_out = [torch.cuda.Event() for _ in range(2)]
     pipelined = h2d + d2h >= (1 << 20)
 
+    def call(b):
+        rc = fn(*calls[b])
+        if rc != 0:
+            raise RuntimeError(f"{prep.fn_name} failed: {rc} {lib.gqmm_last_error().decode()}")
+
     def e2e_step(i):
         b = i & 1
         s = sets[b]
@@ -445,9 +588,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
             s["x"].copy_(x_h, non_blocking=True)
             if idx_h is not None:
                 s["idx"].copy_(idx_h, non_blocking=True)
-            rc = fn(*calls[b])
-            if rc != 0:
-                raise RuntimeError(f"{fn_name} failed: {rc} {lib.gqmm_last_error().decode()}")
+            call(b)
             y_h[b].copy_(s["y"], non_blocking=True)
             return
         with torch.cuda.stream(h2d_s):
@@ -460,9 +601,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
         stream.wait_event(ev_in[b])
         if i >= 2:
             stream.wait_event(ev_out[b])  # step i - 2's result has left this set's y
-        rc = fn(*calls[b])
-        if rc != 0:
-            raise RuntimeError(f"{fn_name} failed: {rc} {lib.gqmm_last_error().decode()}")
+        call(b)
         ev_done[b].record(stream)
         with torch.cuda.stream(d2h_s):
             d2h_s.wait_event(ev_done[b])
@@ -486,15 +625,27 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     torch.cuda.synchronize(dev)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / e2e_steps
     e2e_value = flops * world / (e2e_ms * 1e-3) / 1e12
+    l2_note = prep.l2_note()
+    del prep, sets, calls
+    torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        import oracle
+        cpu = cpu_baseline(w, inp, idx_np)
 
-        qw = oracle_inputs(w, inp)
-        rate, rows, secs, threads = oracle_rate(w, inp["x"], qw, idx_np, target_s=12.0)
-        cpu = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-               "sample": f"{rows} random rows of the workload ({w.flops / w.n * rows / 1e9:.2f} GFLOP, {secs:.1f} s)"}
+    per_config = None
+    if not args.no_per_config:
+        names = [n for n in (args.per_config.split(",") if args.per_config else PER_CONFIG) if n and n != w.name]
+        sampler = ClockSampler(local, timestamps=True)
+        sampler.start()
+        time.sleep(0.3)
+        per_config = []
+        for name in names:
+            per_config.append(measure_config(g, lib, wl.workloads()[name], dev, stream, world, cache, peaks, peaks_src,
+                                             sms, target_s=args.config_seconds, max_steps=max(args.steps, 20000)))
+        sampler.stop()
+        for e in per_config:
+            e["clocks"] = sampler.summary(*e.pop("window"))
 
     if rank != 0:
         return
@@ -512,19 +663,16 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
         "dtype": "bf16",
         "data": "synthetic",
         "config": {**workload_config(w), "sorted_indices": False, "rows_per_expert": w.n / w.E,
-                   "l2": f"inputs rotate over {copies} copies ({copies * per_copy / 1e6:.0f} MB > L2 {l2 / 1e6:.0f} MB)",
-                   "gpu": torch.cuda.get_device_name(dev), "seeds": {"x": wl.SEED_X, "w": wl.SEED_W, "idx": wl.SEED_IDX},
+                   "l2": l2_note, "gpu": torch.cuda.get_device_name(dev),
+                   "seeds": {"x": wl.SEED_X, "w": wl.SEED_W, "idx": wl.SEED_IDX},
                    "parallelism": f"replicas x{world}",
+                   "strips": {"n": STRIPS, "median_ms_per_step": float(np.median(strips)), "ms_per_step": strips,
+                              "note": "the timed steps in 5 strips of plain stream launches, CUDA events at the"
+                                      " boundaries; value and ms_per_step cover all of them"},
                    "hot": {"ms_per_step": hot_ms, "value": flops * world / (hot_ms * 1e-3) / 1e12,
                            "note": "one input set repeated (L2-warm where it fits); context, not the metric"}},
-        "roofline": {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
-                     "traffic": measured_traffic(kernel, w.name), "kernel": kernel, "kernel_ms": gemm_ms,
-                     "kernel_launches_per_step": gemm_launches_per_step,
-                     "kernel_timing": "second timed pass of the same steps, CUDA events around each GEMM launch;"
-                                      " kernel_ms = their summed duration per step",
-                     "peak_source": peak_source},
-        "op_roofline": {"t_min_us": t_roof_s * 1e6, "frac": t_roof_s / (ms_per_step * 1e-3),
-                        "algorithmic_bytes": alg_bytes, "flops": flops},
+        "roofline": roof,
+        "op_roofline": op_roofline_entry(w, alg_bytes, ms_per_step, peaks),
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_ms, "steps": e2e_steps,
@@ -532,8 +680,60 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
         "gpu_launches": launches,
         "clocks": clocks,
         "host_enqueue_ms_per_step": t_host_enqueue / args.steps * 1e3,
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
+
+
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+
+    return platform.processor() or platform.machine()
+
+
+def cpu_baseline(w: wl.Workload, inp, idx_np):
+    """The oracle, as it stands, on the host cores: the headline workload on a bounded row sample
+    (all cores), its dequantize and gather steps timed apart, and single-threaded rates on the
+    tiny correctness case and on one-row dense and MoE decode."""
+    import oracle
+
+    qw = oracle_inputs(w, inp)
+    rate, rows, secs, threads = oracle_rate(w, inp["x"], qw, idx_np, target_s=12.0)
+    out = {"value": rate, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+           "sample": f"{rows} random rows of the workload ({w.flops / w.n * rows / 1e9:.2f} GFLOP, {secs:.1f} s)",
+           "cpu_model": cpu_model()}
+    if w.kind == "gather":
+        # the two steps of the oracle apart: dequantizing every hit expert's weights (float64),
+        # and the dot products of the sampled rows against them (numpy matmul, float64)
+        hit = np.unique(idx_np) if idx_np is not None else np.arange(w.E)
+        t0 = time.perf_counter()
+        deq = [oracle.dequantize(qw[0][e], qw[1][e], qw[2][e], w.group_size) for e in hit[:8]]
+        t_deq = (time.perf_counter() - t0) / len(deq) * len(hit)
+        out["dequant_s_per_step"] = t_deq
+        out["dequant_note"] = f"dequantize of the {len(hit)} hit experts, timed on {len(deq)} and scaled"
+        del deq
+    single = {}
+    for name in ("tiny", "decode_dense_m1", "decode_moe_m1"):
+        sw = wl.workloads()[name]
+        sin = wl.make_inputs(sw)
+        sq = oracle.quantize(sin["w"])
+        t0 = time.perf_counter()
+        oracle.gather_qmm(sin["x"], *sq, sin["idx"], sw.E, nthreads=1)
+        dt = time.perf_counter() - t0
+        single[name] = {"value": sw.flops / dt / 1e12, "unit": "TFLOP/s", "s_per_call": dt, "threads": 1}
+    out["single_thread"] = single
+    return out
 
 
 _CSRC = "quantized_moe_expert_device_gb300/csrc/"
@@ -582,6 +782,9 @@ def main():
     ap.add_argument("--workload", default="prefill_e64", choices=sorted(wl.workloads()))
     ap.add_argument("--impl", default="gqmm", choices=["gqmm", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="time the headline workload only")
+    ap.add_argument("--per-config", default="", help="comma-separated workloads for the per_config block")
+    ap.add_argument("--config-seconds", type=float, default=0.25, help="timed seconds per per_config workload")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

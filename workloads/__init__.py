@@ -193,19 +193,30 @@ def make_idx(wl: Workload, seed: int = SEED_IDX) -> Optional[np.ndarray]:
     raise ValueError(wl.routing)
 
 
-def make_inputs(wl: Workload, seed_x: int = SEED_X, seed_w: int = SEED_W, seed_idx: int = SEED_IDX):
+def make_inputs(wl: Workload, seed_x: int = SEED_X, seed_w: int = SEED_W, seed_idx: int = SEED_IDX,
+                cache: Optional[dict] = None):
     """Returns dict(x=bf16 [T, A, H], w=bf16 [E, F, H], idx=uint32 [T, A] or None); for an
     "mlp" workload w_gu=bf16 [E, 2F, H] ~ N(0, 1/H) and w_dn=bf16 [E, H, F] ~ N(0, 1/F) in place
-    of w, scaled so the gate pre-activations are about N(0, 1)."""
+    of w, scaled so the gate pre-activations are about N(0, 1).  ``cache`` (a dict the caller
+    keeps) reuses weight draws of the same shape, seed and scale across workloads."""
+    def weights(shape, seed, std):
+        key = (tuple(shape), seed, std)
+        if cache is not None and key in cache:
+            return cache[key]
+        t = normal_bf16(shape, seed, std=std, chunk_rows=1)
+        if cache is not None:
+            cache[key] = t
+        return t
+
     x = normal_bf16((wl.T, wl.A, wl.H), seed_x)
     if wl.kind == "nn":
-        w = normal_bf16((wl.E, wl.H, wl.F), seed_w, std=wl.w_std, chunk_rows=1)
+        w = weights((wl.E, wl.H, wl.F), seed_w, wl.w_std)
         return dict(x=x, w=w, idx=make_idx(wl, seed_idx))
     if wl.kind == "mlp":
-        w_gu = normal_bf16((wl.E, 2 * wl.F, wl.H), seed_w, std=wl.H ** -0.5, chunk_rows=1)
-        w_dn = normal_bf16((wl.E, wl.H, wl.F), seed_w + 1, std=wl.F ** -0.5, chunk_rows=1)
+        w_gu = weights((wl.E, 2 * wl.F, wl.H), seed_w, wl.H ** -0.5)
+        w_dn = weights((wl.E, wl.H, wl.F), seed_w + 1, wl.F ** -0.5)
         return dict(x=x, w_gu=w_gu, w_dn=w_dn, idx=make_idx(wl, seed_idx))
-    w = normal_bf16((wl.E, wl.F, wl.H), seed_w, std=wl.w_std, chunk_rows=1)
+    w = weights((wl.E, wl.F, wl.H), seed_w, wl.w_std)
     return dict(x=x, w=w, idx=make_idx(wl, seed_idx))
 
 
