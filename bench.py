@@ -348,17 +348,22 @@ class Prepared:
                 y=torch.empty(w.T, w.A, w.out_cols, dtype=torch.bfloat16, device=dev), ws=ws_new()))
         torch.cuda.synchronize(dev)
         self.fn, self.fn_name = fn, fn.__name__
-        sptr = ctypes.c_void_p(stream.cuda_stream)
         P = ctypes.c_void_p
 
-        def argv(st):
+        def argv(st, sptr):
             head = (P(st["x"].data_ptr()),) + tuple(P(t.data_ptr()) for t in st["w"]) + (
                 None if st["idx"] is None else P(st["idx"].data_ptr()),) + sizes
             if w.kind == "nn":
                 return head + (P(st["y"].data_ptr()), sptr)
             return head + (0, 0, P(st["y"].data_ptr()), P(st["ws"].data_ptr()), st["ws"].numel(), sptr)
 
-        self.calls = [argv(st) for st in self.sets]
+        self._argv = argv
+        self.calls = self.calls_on(stream)
+
+    def calls_on(self, stream):
+        """The C-ABI arguments of every input copy, for a call on `stream`."""
+        sptr = ctypes.c_void_p(stream.cuda_stream)
+        return [self._argv(st, sptr) for st in self.sets]
 
     def step(self, i):
         rc = self.fn(*self.calls[i % self.copies])
@@ -396,6 +401,48 @@ def timed_strips(prep: Prepared, steps: int, stream, world: int):
     return evs[0].elapsed_time(evs[STRIPS]), strips
 
 
+MIN_GRAPH_CALLS = 20  # calls per captured strip
+
+
+def graph_strips(prep: Prepared, steps: int, world: int, stream):
+    """The metric's timed region: `steps` calls captured as CUDA graphs of at least
+    MIN_GRAPH_CALLS back-to-back calls (up to STRIPS strips, each its own graph over the next
+    input copies), replayed once untimed and then once each between CUDA events on the stream.
+    Graph replay takes the host's per-call launch cost out of the device timeline, as a serving
+    loop that replays captured decode steps does.  Returns (total ms, [ms per step of each
+    strip], library launches per step)."""
+    g = prep.g
+    n_strips = max(1, min(STRIPS, steps // MIN_GRAPH_CALLS))
+    bounds = [round(k * steps / n_strips) for k in range(n_strips + 1)]
+    graphs = []
+    launches0 = g.launch_count()
+    for k in range(n_strips):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="relaxed"):
+            calls = prep.calls_on(torch.cuda.current_stream())
+            for i in range(bounds[k], bounds[k + 1]):
+                rc = prep.fn(*calls[i % prep.copies])
+                if rc != 0:
+                    raise RuntimeError(f"{prep.fn_name} failed in capture: {rc} {prep.lib.gqmm_last_error().decode()}")
+        graphs.append(graph)
+    launches = (g.launch_count() - launches0) / max(steps, 1)
+    for graph in graphs:
+        graph.replay()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_strips + 1)]
+    barrier(world)
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for k in range(n_strips):
+        graphs[k].replay()
+        evs[k + 1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    strips = [evs[k].elapsed_time(evs[k + 1]) / max(bounds[k + 1] - bounds[k], 1) for k in range(n_strips)]
+    del graphs
+    return evs[0].elapsed_time(evs[n_strips]), strips, launches
+
+
 def kernel_pass(prep: Prepared, steps: int, world: int):
     """The same steps again with CUDA events around every GEMM launch on the call's stream (the
     library's kernel timer; those events would stop the GEMM's prologue from overlapping the route
@@ -414,6 +461,19 @@ def kernel_pass(prep: Prepared, steps: int, world: int):
     if n_timed != slots:
         raise RuntimeError(f"kernel timer recorded {n_timed} GEMM launches, expected {slots}")
     return ms_total / max(steps, 1), n_timed / max(steps, 1)
+
+
+def kernel_time(prep: Prepared, steps: int, world: int, step_ms: float, launches_per_step: float):
+    """(ms per step of the GEMM kernel(s), their launches per step, how it was timed).  When the
+    step is those launches alone (dense or in-kernel-planned decode), the graph-replayed step time
+    is their time; otherwise a separate pass of plain launches puts CUDA events around each GEMM
+    launch (the library's kernel timer)."""
+    per_step = GEMM_LAUNCHES_PER_STEP[prep.w.kind]
+    if launches_per_step <= per_step:
+        return step_ms, float(per_step), "the step is the kernel alone: graph replay, events at strip boundaries"
+    gemm_ms, n = kernel_pass(prep, steps, world)
+    return gemm_ms, n, ("a separate pass of plain launches, CUDA events around each GEMM launch;"
+                        " kernel_ms = their summed duration per step")
 
 
 def roofline_entry(w: wl.Workload, alg_bytes: int, gemm_ms: float, peaks, peaks_src, sm_max, sms, kernel):
@@ -465,14 +525,12 @@ def measure_config(g, lib, w: wl.Workload, dev, stream, world, cache, peaks, pea
     torch.cuda.synchronize(dev)
     est_ms = e0.elapsed_time(e1) / 10
     steps = int(min(max_steps, max(4 * STRIPS, target_s * 1e3 / max(est_ms, 1e-4))))
-    launches0 = g.launch_count()
     variants0 = {v: g.dispatch_count(v) for v in _VARIANT_KERNEL}
     t0 = time.time()
-    ms_total, strips = timed_strips(prep, steps, stream, world)
+    ms_total, strips, launches = graph_strips(prep, steps, world, stream)
     t1 = time.time()
-    launches = (g.launch_count() - launches0) / steps
     kernel = _kernel_of(g, variants0)
-    gemm_ms, gemm_launches = kernel_pass(prep, steps, world)
+    gemm_ms, gemm_launches, timing = kernel_time(prep, steps, world, ms_total / steps, launches)
     status = prep.status()
     if status:
         raise RuntimeError(f"{w.name}: device status after the timed region: {status:#x}")
@@ -483,10 +541,10 @@ def measure_config(g, lib, w: wl.Workload, dev, stream, world, cache, peaks, pea
         "workload": w.name, "metric": metric_name(w), "config": workload_config(w),
         "value": float(w.flops) * world / (ms_per_step * 1e-3) / 1e12, "unit": "TFLOP/s",
         "ms_per_step": ms_per_step, "steps": steps,
-        "strips": {"n": STRIPS, "median_ms_per_step": float(np.median(strips)), "ms_per_step": strips},
+        "strips": {"n": len(strips), "median_ms_per_step": float(np.median(strips)), "ms_per_step": strips},
         "hbm_gbs": alg / (ms_per_step * 1e-3) / 1e9,
         "roofline": dict(roofline_entry(w, alg, gemm_ms, peaks, peaks_src, 2070, sms, kernel),
-                         kernel_launches_per_step=gemm_launches),
+                         kernel_launches_per_step=gemm_launches, kernel_timing=timing),
         "op_roofline": op_roofline_entry(w, alg, ms_per_step, peaks),
         "gpu_launches_per_step": launches, "l2": prep.l2_note(), "window": (t0, t1),
     }
@@ -515,14 +573,15 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)
-    # Timed pass 1, the metric: K steps with nothing between the library's kernels, in strips.
-    launches0 = g.launch_count()
+    # Timed pass 1, the metric: K steps captured as CUDA graphs, replayed in strips.
     variants0 = {v: g.dispatch_count(v) for v in _VARIANT_KERNEL}
-    t_host0 = time.perf_counter()
-    ms_total, strips = timed_strips(prep, args.steps, stream, world)
-    t_host_enqueue = time.perf_counter() - t_host0
-    launches = g.launch_count() - launches0
+    ms_total, strips, launches_per_step = graph_strips(prep, args.steps, world, stream)
+    launches = int(round(launches_per_step * args.steps))
     kernel = _kernel_of(g, variants0)
+    # Context: the same K steps as plain stream launches from the host (per-call host cost included).
+    t_host0 = time.perf_counter()
+    plain_ms, _ = timed_strips(prep, args.steps, stream, world)
+    t_host_enqueue = time.perf_counter() - t_host0
     # Hot pass (context only, not the metric): the same call repeated on one input set, so
     # inputs that fit in L2 stay there between steps.
     hot_steps = min(args.steps, 200)
@@ -536,8 +595,9 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     h1.record(stream)
     torch.cuda.synchronize(dev)
     hot_ms = max_over_ranks(h0.elapsed_time(h1), world) / hot_steps
-    # Timed pass 2, the roofline: the same K steps with CUDA events around every GEMM launch.
-    gemm_ms, gemm_launches_per_step = kernel_pass(prep, args.steps, world)
+    # The roofline: the GEMM kernel's own time per step.
+    gemm_ms, gemm_launches_per_step, kernel_timing = kernel_time(prep, args.steps, world, ms_total / args.steps,
+                                                                 launches_per_step)
     clocks = sampler.stop()
     status = prep.status()
     if status:
@@ -551,9 +611,7 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
     alg_bytes = algorithmic_bytes(w, idx_np)
     sm_max = (clocks or {}).get("sm_max_mhz") or 2070
     roof = dict(roofline_entry(w, alg_bytes, gemm_ms, peaks, peaks_src, sm_max, sms, kernel),
-                kernel_launches_per_step=gemm_launches_per_step,
-                kernel_timing="second timed pass of the same steps, CUDA events around each GEMM launch;"
-                              " kernel_ms = their summed duration per step")
+                kernel_launches_per_step=gemm_launches_per_step, kernel_timing=kernel_timing)
 
     # ---- end to end: host-resident inputs, pinned, copied in and out every step ----
     # Every step copies its own inputs in from pinned host memory and its own result back.
@@ -666,9 +724,12 @@ def run_gpu(args, w: wl.Workload, world: int, rank: int, local: int):
                    "l2": l2_note, "gpu": torch.cuda.get_device_name(dev),
                    "seeds": {"x": wl.SEED_X, "w": wl.SEED_W, "idx": wl.SEED_IDX},
                    "parallelism": f"replicas x{world}",
-                   "strips": {"n": STRIPS, "median_ms_per_step": float(np.median(strips)), "ms_per_step": strips,
-                              "note": "the timed steps in 5 strips of plain stream launches, CUDA events at the"
-                                      " boundaries; value and ms_per_step cover all of them"},
+                   "strips": {"n": len(strips), "median_ms_per_step": float(np.median(strips)), "ms_per_step": strips,
+                              "note": "the timed steps as CUDA graphs of >= 20 back-to-back calls, replayed with"
+                                      " CUDA events at the strip boundaries; value and ms_per_step cover all of them"},
+                   "stream_launches": {"ms_per_step": plain_ms / args.steps,
+                                       "value": flops * world / (plain_ms / args.steps * 1e-3) / 1e12,
+                                       "note": "the same steps as plain calls from the host, one at a time"},
                    "hot": {"ms_per_step": hot_ms, "value": flops * world / (hot_ms * 1e-3) / 1e12,
                            "note": "one input set repeated (L2-warm where it fits); context, not the metric"}},
         "roofline": roof,

@@ -313,7 +313,8 @@ GQMM_API int gqmm_kernel_timer_read(int64_t* launches, double* total_ms);
 #define GQMM_VARIANT_GEMV 6           /* weight-streaming CUDA-core kernel: routed chunks of 1-2 rows, dense 1 row */
 #define GQMM_VARIANT_GEMV_MMA 7       /* weight-streaming MMA kernel, dense calls of 2 to 8 rows */
 #define GQMM_VARIANT_NN 8             /* gqmm_gather_qmm_nn (transpose=False), CUDA cores */
-#define GQMM_VARIANT_COUNT 9
+#define GQMM_VARIANT_ROUTE_FUSED 9    /* unsorted routed decode (<= 64 rows) planned inside the streaming kernel */
+#define GQMM_VARIANT_COUNT 10
 GQMM_API int64_t gqmm_dispatch_count(int variant);
 
 #ifdef __cplusplus

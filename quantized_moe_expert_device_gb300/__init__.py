@@ -38,7 +38,7 @@ STATUS_TIMEOUT = 0x400
 MAX_EXPERTS = 1024
 ACTIVATIONS = {"silu": 0, "gelu": 1, "gelu_tanh": 2}  # GQMM_ACT_* of gqmm_moe_mlp
 VARIANTS = {"route_unsorted": 0, "route_sorted": 1, "route_dense": 2, "gemm_tc": 3, "gemm_narrow": 4,
-            "split_k": 5, "gemv": 6, "gemv_mma": 7, "nn": 8}
+            "split_k": 5, "gemv": 6, "gemv_mma": 7, "nn": 8, "route_fused": 9}
 
 
 class GqmmError(RuntimeError):

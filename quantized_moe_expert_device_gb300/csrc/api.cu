@@ -154,7 +154,8 @@ int launch_projection(const GemmArgs& ga, const UnitShape& shape, int sms, cudaS
     std::fprintf(stderr, "[gqmm] %s n=%lld H=%d F=%d E=%d route=%s gemm=%s ks_cap=%d\n", what, (long long)ga.n, ga.H,
                  ga.F, ga.E,
                  route_variant == GQMM_VARIANT_ROUTE_DENSE ? "dense"
-                 : route_variant == GQMM_VARIANT_ROUTE_SORTED ? "sorted" : "unsorted",
+                 : route_variant == GQMM_VARIANT_ROUTE_SORTED ? "sorted"
+                 : route_variant == GQMM_VARIANT_ROUTE_FUSED ? "in-kernel" : "unsorted",
                  shape.stream ? (stream_mma ? "stream-mma" : "stream")
                  : shape.chunk_rows <= kChunkRowsNarrow ? "narrow" : "wide",
                  ga.ks_cap);
@@ -210,13 +211,24 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   cudaError_t e = device_sm_count(&sms);
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
   ra.sms = sms;
-  const bool permuted = idx != nullptr && !sorted;
-  int launched = 0;
-  e = launch_route(ra, s, &launched);
-  g_launches.fetch_add(launched);
-  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
+  // Decode-sized calls on the weight-streaming path need no route kernel: a dense call's plan is
+  // the single chunk, and an unsorted routed call of at most kFusedPlanMaxRows rows on the CUDA-core
+  // streaming kernel is planned inside that kernel.  Such a call is one programmatic-dependent
+  // launch, which the previous call's streaming kernel lets start as its blocks retire.
+  const bool fused = shape.stream && idx != nullptr && !sorted && n <= kFusedPlanMaxRows &&
+                     !gemv_uses_mma(shape.chunk_rows, H, E);
+  const bool route_kernel = !(shape.stream && (idx == nullptr || fused));
+  const bool permuted = idx != nullptr && !sorted && !fused;
+  if (route_kernel) {
+    int launched = 0;
+    e = launch_route(ra, s, &launched);
+    g_launches.fetch_add(launched);
+    if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "route launch: %s", cudaGetErrorString(e));
+  }
   const int route_variant = idx == nullptr ? GQMM_VARIANT_ROUTE_DENSE
-                                           : (sorted ? GQMM_VARIANT_ROUTE_SORTED : GQMM_VARIANT_ROUTE_UNSORTED);
+                            : fused        ? GQMM_VARIANT_ROUTE_FUSED
+                            : sorted       ? GQMM_VARIANT_ROUTE_SORTED
+                                           : GQMM_VARIANT_ROUTE_UNSORTED;
   count_variant(route_variant);
 
   GemmArgs ga;
@@ -240,6 +252,8 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   ga.offsets = ra.offsets;
   ga.group_size = group_size;
   ga.x_div = x_shared ? A : 1;
+  ga.idx = idx;
+  ga.fused_plan = fused ? 1 : 0;
   rc = launch_projection(ga, shape, sms, s, "gather_qmm", route_variant);
   if (rc) return rc;
   return ok();

@@ -48,6 +48,78 @@ __host__ __device__ constexpr int stream_stages(int H, int M) {
   return kStreamStages * stream_stage_bytes(H, M) <= kStreamSmemBudget ? kStreamStages : kStreamStages - 1;
 }
 
+// Routed calls of at most this many rows (decode: M tokens x A experts) are planned inside the
+// kernel: every block sorts the call's routing entries into chunks itself, so no route kernel runs
+// in front of it.
+constexpr int kFusedPlanRows = 64;
+static_assert(kFusedPlanRows == kFusedPlanMaxRows, "one bound for the host and the kernel");
+
+// The chunk list of a routed call of n <= 64 rows, computed by one warp: the rows of each expert
+// in flat-row order, in chunks of at most two rows (the first and second, third and fourth, ...
+// occurrences of the expert), numbered in the flat order of their first rows.  Each lane holds
+// entries lane and 32 + lane; one pass over all entries (shuffles) gives an entry's occurrence
+// rank, its expert's total and its next occurrence.  plan[c] = (expert, first row, second row
+// (= first row for a one-row chunk), rows).  Rows whose index is >= E are in no chunk; block 0
+// writes them as zeros and records GQMM_STATUS_BAD_INDEX.  Returns the number of chunks (lane 0).
+__device__ __forceinline__ int fused_plan(const GemmArgs& p, int4* plan, uint32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int n = (int)p.n;
+  uint32_t key[2];
+  int rank[2] = {0, 0}, tot[2] = {0, 0}, next[2] = {-1, -1};
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int i = 32 * r + lane;
+    key[r] = i < n ? __ldg(p.idx + i) : 0xFFFFFFFFu;
+  }
+#pragma unroll
+  for (int rj = 0; rj < 2; ++rj) {
+    for (int jl = 0; jl < 32; ++jl) {
+      const int j = 32 * rj + jl;
+      const uint32_t kj = __shfl_sync(0xffffffffu, key[rj], jl);
+#pragma unroll
+      for (int r = 0; r < 2; ++r) {
+        const int i = 32 * r + lane;
+        if (kj == key[r]) {
+          ++tot[r];
+          if (j < i) ++rank[r];
+          if (j > i && next[r] < 0) next[r] = j;
+        }
+      }
+    }
+  }
+  bool lead[2], bad[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int i = 32 * r + lane;
+    bad[r] = i < n && key[r] >= (uint32_t)p.E;
+    lead[r] = i < n && !bad[r] && (rank[r] & 1) == 0;
+  }
+  const uint32_t b0 = __ballot_sync(0xffffffffu, lead[0]), b1 = __ballot_sync(0xffffffffu, lead[1]);
+  const uint32_t lt = (1u << lane) - 1u;
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    if (lead[r]) {
+      const int i = 32 * r + lane;
+      const int id = r == 0 ? __popc(b0 & lt) : __popc(b0) + __popc(b1 & lt);
+      const int rows = tot[r] - rank[r] >= 2 ? 2 : 1;
+      plan[id] = make_int4((int)key[r], i, rows == 2 ? next[r] : i, rows);
+    }
+  }
+  if (blockIdx.x == 0) {
+    bool any = false;
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      if (bad[r]) {
+        uint4* row = reinterpret_cast<uint4*>(p.y + (int64_t)(32 * r + lane) * p.F);
+        for (int c = 0; c < p.F / 8; ++c) row[c] = make_uint4(0u, 0u, 0u, 0u);
+        any = true;
+      }
+    }
+    if (__any_sync(0xffffffffu, any) && lane == 0) atomicOr(status, GQMM_STATUS_BAD_INDEX);
+  }
+  return __popc(b0) + __popc(b1);
+}
+
 // Per-stage item description written by the producer before it arms the stage's barrier.
 struct StageMeta {
   int rows;     // rows of the chunk (1..M)
@@ -174,6 +246,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
   __shared__ StageMeta meta[kStreamStages];
   __shared__ float red[2][NW][V];
   __shared__ int abort_flag;
+  __shared__ int4 plan[kFusedPlanRows];  // the in-kernel chunk list of a fused-plan call
+  __shared__ int plan_n;
 
   const int H = p.H, F = p.F, G = H / 64;
   const int RB = stream_rows_per_item(H);
@@ -192,6 +266,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
     fence_barrier_init();
   }
   __syncthreads();
+  // The next call's kernel may be scheduled as this one's blocks retire: it waits for this grid
+  // to finish (griddepcontrol.wait) before it reads or writes anything of the call.
+  grid_dependents_launch();
 
   // The kernel may start while the previous kernel on the stream is still running
   // (programmatic dependent launch), and that kernel may be writing this call's x, weights or
@@ -209,7 +286,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
     }
   }
   grid_dependency_wait();
-  const int n_chunks = p.dense_plan ? 1 : p.header->n_chunks;
+  if (p.fused_plan) {
+    if (warp == 0) {
+      const int nc = fused_plan(p, plan, status);
+      if (lane == 0) plan_n = nc;
+    }
+    __syncthreads();
+  }
+  const int n_chunks = p.dense_plan ? 1 : p.fused_plan ? plan_n : p.header->n_chunks;
   const int n_items = n_chunks * n_batches;
   const int per = (n_items + (int)gridDim.x - 1) / (int)gridDim.x;
   const int it0 = min(n_items, (int)blockIdx.x * per);
@@ -233,12 +317,21 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
         const int c = j / n_batches, b = j - c * n_batches;
         const bool newx = c != prev_c;
         if (newx) {
-          rec = p.dense_plan ? make_int4(0, 0, (int)p.n, 0) : __ldg(reinterpret_cast<const int4*>(p.chunks) + c);
+          if (p.fused_plan) {
+            const int4 pc = plan[c];  // (expert, first row, second row, rows)
+            rec = make_int4(pc.x, 0, pc.w, 0);
+            trow[0] = pc.y;
+            trow[1] = M > 1 && pc.w > 1 ? pc.z : 0;
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            const bool live = t < M && t < rec.z;
-            trow[t] = live ? (p.y_perm ? __ldg(p.y_perm + rec.y + t) : rec.y + t) : 0;
-            xrow[t] = live ? (p.perm ? __ldg(p.perm + rec.y + t) : rec.y + t) / p.x_div : 0;
+            for (int t = 0; t < 2; ++t) xrow[t] = trow[t] / p.x_div;
+          } else {
+            rec = p.dense_plan ? make_int4(0, 0, (int)p.n, 0) : __ldg(reinterpret_cast<const int4*>(p.chunks) + c);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const bool live = t < M && t < rec.z;
+              trow[t] = live ? (p.y_perm ? __ldg(p.y_perm + rec.y + t) : rec.y + t) : 0;
+              xrow[t] = live ? (p.perm ? __ldg(p.perm + rec.y + t) : rec.y + t) / p.x_div : 0;
+            }
           }
           prev_c = c;
         }
@@ -356,14 +449,21 @@ cudaError_t launch_gemv_fma(const GemmArgs& a, int rows, int sms, cudaStream_t s
   cfg.stream = s;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  if (rows == 1) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_fma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, gemv_fma_kernel<1>, a);
-  }
-  cudaError_t e = cudaFuncSetAttribute(gemv_fma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // The shared-memory opt-in is set once per device and instance, to the largest size asked so
+  // far (a host call per launch would cost more than a decode-sized kernel takes).
+  static int smem_set[64][2] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, gemv_fma_kernel<2>, a);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int& set = smem_set[dev][rows == 1 ? 0 : 1];
+  if (smem > set) {
+    e = rows == 1 ? cudaFuncSetAttribute(gemv_fma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+                  : cudaFuncSetAttribute(gemv_fma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    set = smem;
+  }
+  return rows == 1 ? cudaLaunchKernelEx(&cfg, gemv_fma_kernel<1>, a) : cudaLaunchKernelEx(&cfg, gemv_fma_kernel<2>, a);
 }
 
 // The weight-streaming path: dense calls of 2 to 8 rows run on the MMA kernel (gemv_mma.cu),

@@ -129,6 +129,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemmArgs
   }
   __syncthreads();
 
+  // The next call's kernel may be scheduled as this one's blocks retire: it waits for this grid
+  // to finish (griddepcontrol.wait) before it reads or writes anything of the call.
+  grid_dependents_launch();
+
   // The kernel may start while the previous kernel on the stream is still running
   // (programmatic dependent launch), and that kernel may be writing this call's x, weights or
   // y.  The dense plan is known without the route step, so before the wait the producer only
@@ -339,14 +343,26 @@ cudaError_t launch_gemv_mma(const GemmArgs& a, int rows, int sms, cudaStream_t s
   cfg.numAttrs = 1;
   GemmArgs args = a;
   args.chunk_rows = rows;
+  // The shared-memory opt-in is set once per device and instance, to the largest size asked so
+  // far (a host call per launch would cost more than a decode-sized kernel takes).
+  static int smem_set[64][3] = {};
+  int dev = 0;
+  cudaError_t e0 = cudaGetDevice(&dev);
+  if (e0 != cudaSuccess) return e0;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const int inst = a.H / 1024 == 1 ? 0 : a.H / 1024 == 2 ? 1 : 2;
   auto run = [&](auto kern) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
+    int& set = smem_set[dev][inst];
+    if (smem > set) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      set = smem;
+    }
     return cudaLaunchKernelEx(&cfg, kern, args);
   };
-  switch (a.H / 1024) {
-    case 1: return run(gemv_mma_kernel<1>);
-    case 2: return run(gemv_mma_kernel<2>);
+  switch (inst) {
+    case 0: return run(gemv_mma_kernel<1>);
+    case 1: return run(gemv_mma_kernel<2>);
     default: return run(gemv_mma_kernel<4>);
   }
 }

@@ -55,6 +55,8 @@ constexpr int kTargetUnits = 2 * 152;         // split K until about this many u
 constexpr int64_t kSplitMaxRows = 1024;       // split K only for decode-sized calls: the fp32
                                               // partial sums cost n*F*4 bytes per slice
 
+constexpr int kFusedPlanMaxRows = 64;        // routed streaming calls of up to this many rows
+                                              // (unsorted) are planned inside the kernel
 constexpr int kStreamMaxRows = 8;             // weight-streaming path: a dense call of <= 8 rows,
 constexpr int kStreamMoeRows = 2;             // or a routed call in chunks of <= 2 rows
 
@@ -198,6 +200,9 @@ struct GemmArgs {
   int group_size = 64;  // quantization group along H: 32, 64 or 128 (the streaming kernels: 64)
   int x_div = 1;        // x row of routed row r: r / x_div (A when the A rows of a token share
                         // one x row, else 1); x has n / x_div rows
+  const uint32_t* idx = nullptr;  // routing entries [n] (fused_plan calls)
+  int fused_plan = 0;   // 1: a routed decode call (n <= kFusedPlanMaxRows, unsorted) that the
+                        // weight-streaming kernel plans itself; no route kernel runs before it
 };
 // Launches the grouped GEMM (and, when ks_cap > 1, the kernel that turns the partial sums into
 // y).  *launched gets the number of kernels enqueued.

@@ -308,3 +308,49 @@ def test_weight_streaming_invalid_indices_and_unsupported_h():
         assert status & g.STATUS_BAD_INDEX
         assert (g.dispatch_count("gemv") > before) == expect_stream
         assert_parity(y.reshape(-1, F), y_ref, f"stream invalid H={H}")
+
+
+@pytest.mark.parametrize("T,A", [(8, 8), (12, 5), (65, 1), (64, 1)])
+def test_in_kernel_plan_matches_route_kernel_bitwise(T, A):
+    """Unsorted routed decode calls of at most 64 rows are planned inside the streaming kernel
+    (no route kernel); 65 rows go through the route kernel.  Either way the result equals, bit
+    for bit, the same rows run caller-sorted through the sorted-route plan, and meets the oracle.
+    Expert 3 is sent five rows (chunks of 2, 2 and 1) and one row has an invalid index."""
+    import quantized_moe_expert_device_gb300 as g
+
+    E, F, H = 96, 272, 2048
+    host_w, dev_w = _weights(E, F, H)
+    idx = np.random.default_rng(T * 7 + A).permutation(E)[np.arange(T * A) % E].astype(np.uint32).reshape(T, A)
+    idx.reshape(-1)[[1, 4, 6, 9, 12]] = 3
+    idx.reshape(-1)[2] = E + 1
+    x = wl.normal_bf16((T, A, H), wl.SEED_X)
+    before = {k: g.dispatch_count(k) for k in ("route_fused", "route_unsorted", "gemv")}
+    y, y_ref, status = _run(x, idx, E, host_w, dev_w)
+    assert status & g.STATUS_BAD_INDEX
+    fused = T * A <= 64
+    assert (g.dispatch_count("route_fused") > before["route_fused"]) == fused
+    assert (g.dispatch_count("route_unsorted") > before["route_unsorted"]) == (not fused)
+    assert g.dispatch_count("gemv") > before["gemv"]
+    assert_parity(y.reshape(-1, F), y_ref, f"in-kernel plan T={T} A={A}")
+    xs, idx_s, order = wl.sorted_by_expert(x, idx)
+    ys, _, _ = _run(xs, idx_s.reshape(-1, 1), E, host_w, dev_w, sorted_indices=True)
+    y_back = torch.empty_like(ys.reshape(-1, F))
+    y_back[torch.from_numpy(order).cuda()] = ys.reshape(-1, F)
+    assert torch.equal(y.reshape(-1, F), y_back), "in-kernel plan and sorted-route plan differ"
+
+
+def test_in_kernel_plan_with_shared_x():
+    """The in-kernel plan with x shared by a token's A rows ([T, H]) equals the call on x repeated
+    A times, bit for bit."""
+    import quantized_moe_expert_device_gb300 as g
+
+    T, A, E, F, H = 6, 8, 128, 256, 2048
+    host_w, dev_w = _weights(E, F, H)
+    idx = wl.idx_topk_distinct_uniform(T, A, E, seed=17)
+    x_tok = wl.normal_bf16((T, H), 18)
+    before = g.dispatch_count("route_fused")
+    y_shared = g.gqmm_gather_qmm(x_tok.cuda(), *dev_w, to_dev_idx(idx))
+    y_rep = g.gqmm_gather_qmm(x_tok.cuda().unsqueeze(1).expand(T, A, H).contiguous(), *dev_w, to_dev_idx(idx))
+    torch.cuda.synchronize()
+    assert g.dispatch_count("route_fused") - before == 2
+    assert torch.equal(y_shared, y_rep)
