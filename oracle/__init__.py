@@ -49,8 +49,14 @@ def _load():
             lib.oracle_nthreads_default.restype = I
             lib.oracle_quantize.argtypes = [P, I64, I64, I, I, P, P, P, I]
             lib.oracle_quantize.restype = I
-            lib.oracle_dequantize.argtypes = [P, P, P, I64, I64, I, P]
+            lib.oracle_dequantize.argtypes = [P, P, P, I64, I64, I, I, P]
             lib.oracle_dequantize.restype = I
+            lib.oracle_quantize_fp.argtypes = [P, I64, I64, I, I64, P, P, P]
+            lib.oracle_quantize_fp.restype = I
+            lib.oracle_dequantize_fp.argtypes = [P, P, P, I64, I64, I, I64, P]
+            lib.oracle_dequantize_fp.restype = I
+            lib.oracle_gather_qmm_fp.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I, P, I64, P, I]
+            lib.oracle_gather_qmm_fp.restype = I
             lib.oracle_route_sort.argtypes = [P, I64, I, P, P]
             lib.oracle_route_sort.restype = I64
             lib.oracle_gather_qmm.argtypes = [P, P, P, P, P, I64, I64, I64, I64, I, I, P, I]
@@ -80,15 +86,22 @@ def nthreads_default() -> int:
     return int(_load().oracle_nthreads_default())
 
 
+# the block-scaled floating-point modes of oracle_quantize_fp (the affine format is mode 0)
+MODES = {"affine": 0, "mxfp4": 1, "nvfp4": 2, "mxfp8": 3}
+# weights per shared scale, and code bytes per weight, of each floating-point mode
+MODE_BLOCK = {"mxfp4": 32, "nvfp4": 16, "mxfp8": 32}
+MODE_CODE_BYTES = {"mxfp4": 0.5, "nvfp4": 0.5, "mxfp8": 1.0}
+
+
 def quantize(w, group_size: int = 64, bits: int = 4, nthreads: int = 0):
-    """w: bf16 [..., H] -> (wq u8 [..., H/2], scales u16 [..., H/gs], biases u16 [..., H/gs])."""
+    """w: bf16 [..., H] -> (wq u8 [..., H*bits/8], scales u16 [..., H/gs], biases u16 [..., H/gs])."""
     w16 = _u16(w)
     H = w16.shape[-1]
     lead = w16.shape[:-1]
     rows = int(np.prod(lead)) if lead else 1
-    if H % group_size or group_size % 2:
+    if H % group_size or group_size % 8:
         raise ValueError("H must be a multiple of group_size")
-    wq = np.empty(lead + (H // 2,), np.uint8)
+    wq = np.empty(lead + (H * bits // 8,), np.uint8)
     sc = np.empty(lead + (H // group_size,), np.uint16)
     bs = np.empty(lead + (H // group_size,), np.uint16)
     rc = _load().oracle_quantize(_ptr(w16), rows, H, group_size, bits, _ptr(wq), _ptr(sc), _ptr(bs), nthreads)
@@ -97,18 +110,87 @@ def quantize(w, group_size: int = 64, bits: int = 4, nthreads: int = 0):
     return wq, sc, bs
 
 
-def dequantize(wq: np.ndarray, scales: np.ndarray, biases: np.ndarray, group_size: int = 64) -> np.ndarray:
-    """-> float64 [..., H]."""
+def dequantize(wq: np.ndarray, scales: np.ndarray, biases: np.ndarray, group_size: int = 64,
+               bits: int = 4) -> np.ndarray:
+    """-> float64 [..., H] with H = wq.shape[-1] * 8 / bits."""
     wq = np.ascontiguousarray(wq, np.uint8)
     scales = _u16(scales)
     biases = _u16(biases)
-    H = wq.shape[-1] * 2
+    H = wq.shape[-1] * 8 // bits
     rows = int(np.prod(wq.shape[:-1])) if wq.ndim > 1 else 1
     out = np.empty(wq.shape[:-1] + (H,), np.float64)
-    rc = _load().oracle_dequantize(_ptr(wq), _ptr(scales), _ptr(biases), rows, H, group_size, _ptr(out))
+    rc = _load().oracle_dequantize(_ptr(wq), _ptr(scales), _ptr(biases), rows, H, group_size, bits, _ptr(out))
     if rc != 0:
         raise ValueError("oracle_dequantize rejected its arguments")
     return out
+
+
+def quantize_fp(w, mode: str):
+    """Block-scaled floating-point quantization of w: bf16 [..., H] (an [E, F, H] stack: each
+    expert is one nvfp4 tensor; a 2-D [F, H] weight is one tensor).  Returns (wq u8 [..., H/2]
+    (mxfp4, nvfp4) or [..., H] (mxfp8), scales u8 [..., H/32] or [..., H/16] (nvfp4), tensor
+    scales float32 [E] (nvfp4; None otherwise))."""
+    w16 = _u16(w)
+    H = w16.shape[-1]
+    lead = w16.shape[:-1]
+    rows = int(np.prod(lead)) if lead else 1
+    per_tensor = int(lead[-1]) if len(lead) >= 2 else rows
+    nb = MODE_BLOCK[mode]
+    wq = np.empty(lead + (int(H * MODE_CODE_BYTES[mode]),), np.uint8)
+    sc = np.empty(lead + (H // nb,), np.uint8)
+    ts = np.empty(max(rows // max(per_tensor, 1), 1), np.float32) if mode == "nvfp4" else None
+    rc = _load().oracle_quantize_fp(_ptr(w16), rows, H, MODES[mode], per_tensor, _ptr(wq), _ptr(sc),
+                                    None if ts is None else _ptr(ts))
+    if rc != 0:
+        raise ValueError("oracle_quantize_fp rejected its arguments")
+    return wq, sc, ts
+
+
+def dequantize_fp(wq: np.ndarray, scales: np.ndarray, tscale, mode: str) -> np.ndarray:
+    """-> float64 [..., H]; the nvfp4 tensor scales apply per expert (per leading-dimension
+    slice of an [E, F, ...] stack)."""
+    wq = np.ascontiguousarray(wq, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    H = int(wq.shape[-1] / MODE_CODE_BYTES[mode])
+    lead = wq.shape[:-1]
+    rows = int(np.prod(lead)) if lead else 1
+    per_tensor = int(lead[-1]) if len(lead) >= 2 else rows
+    out = np.empty(lead + (H,), np.float64)
+    ts = None if tscale is None else np.ascontiguousarray(tscale, np.float32)
+    rc = _load().oracle_dequantize_fp(_ptr(wq), _ptr(scales), None if ts is None else _ptr(ts), rows, H, MODES[mode],
+                                      per_tensor, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle_dequantize_fp rejected its arguments")
+    return out
+
+
+def gather_qmm_fp(x, wq, scales, tscale, idx, E: int, mode: str, nthreads: int = 0, rows=None):
+    """gather_qmm on weights in a floating-point mode (as quantize_fp writes them for [E, F, H]),
+    float64.  Returns [n, F] (or [len(rows), F])."""
+    x16 = _u16(x)
+    H = x16.shape[-1]
+    x16 = x16.reshape(-1, H)
+    n = x16.shape[0]
+    wq = np.ascontiguousarray(wq, np.uint8)
+    scales = np.ascontiguousarray(scales, np.uint8)
+    F = wq.shape[-2]
+    if int(wq.shape[-1] / MODE_CODE_BYTES[mode]) != H:
+        raise ValueError("wq does not match H")
+    ts = None if tscale is None else np.ascontiguousarray(tscale, np.float32)
+    idx_p = None
+    if idx is not None:
+        flat = np.ascontiguousarray(np.asarray(idx, np.uint32).reshape(-1))
+        if flat.size != n:
+            raise ValueError("idx must have one entry per row of x")
+        idx_p = _ptr(flat)
+    r = None if rows is None else np.ascontiguousarray(np.asarray(rows, np.int64))
+    y = np.empty(((n if r is None else r.size), F), np.float64)
+    used = _load().oracle_gather_qmm_fp(_ptr(x16), _ptr(wq), _ptr(scales), None if ts is None else _ptr(ts), idx_p, n,
+                                        H, F, E, MODES[mode], None if r is None else _ptr(r),
+                                        0 if r is None else r.size, _ptr(y), nthreads)
+    if used < 0:
+        raise ValueError("oracle_gather_qmm_fp rejected its arguments")
+    return y
 
 
 def route_sort(idx: np.ndarray, E: int):
@@ -136,8 +218,8 @@ def gather_qmm(x, wq, scales, biases, idx, E: int, group_size: int = 64, bits: i
     scales = _u16(scales)
     biases = _u16(biases)
     F = wq.shape[-2]
-    if wq.shape[-1] * 2 != H:
-        raise ValueError("wq last dim must be H/2")
+    if wq.shape[-1] * 8 != H * bits:
+        raise ValueError("wq last dim must be H*bits/8")
     idx_p = None
     if idx is not None:
         flat = np.ascontiguousarray(np.asarray(idx, np.uint32).reshape(-1))
