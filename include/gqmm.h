@@ -45,6 +45,25 @@
  *     wq      uint8     [E, F, H/2]
  *     scales  bfloat16  [E, F, H/group_size]
  *     biases  bfloat16  [E, F, H/group_size]
+ * Other bit widths (mlx PR #4023 "Pick BM from rows per expert", the author's follow-up: every
+ * mode, group size and bit width): bits b in {2, 3, 5, 6, 8} with 64-wide groups keep the steps
+ * above with 2^b - 1 levels in place of 15; a row's codes are one little-endian bit stream
+ * (element k in bits [k*b, (k+1)*b), bit j of the stream in bit j%8 of byte j/8; at b = 4 this is
+ * the layout above), so wq is uint8 [E, F, H*b/8].
+ *
+ * Block-scaled floating-point modes (mlx #4339, Activity, nastya236: mxfp8 and nvfp4 are what the
+ * CUDA back end is to support); the pages give no formulas, so these are the published formats:
+ *   GQMM_MODE_MXFP4  OCP MX v1.0: E2M1 codes (two per byte as above), one E8M0 scale per 32
+ *                    weights: X = 2^(floor(log2 amax) - 2), element = nearest E2M1 to w / X
+ *                    (ties to even, saturating at 6).   wq [E, F, H/2], scales uint8 [E, F, H/32]
+ *   GQMM_MODE_MXFP8  the same with E4M3 codes (one per byte), X = 2^(floor(log2 amax) - 8),
+ *                    saturating at 448.                 wq [E, F, H],   scales uint8 [E, F, H/32]
+ *   GQMM_MODE_NVFP4  NVFP4: E2M1 codes, one E4M3 scale per 16 weights and a float32 scale t per
+ *                    expert: t = amax_expert / 2688, S = E4M3((amax_block / 6) / t), element =
+ *                    E2M1(w / (S t)), all float32 operations.
+ *                                                       wq [E, F, H/2], scales uint8 [E, F, H/16],
+ *                                                       tscale float32 [E]
+ *   and deq = element * X (mx) or element * S * t (nvfp4).
  */
 #ifndef GQMM_H
 #define GQMM_H
@@ -68,7 +87,7 @@ typedef struct CUstream_st* gqmm_stream_t; /* identical to cudaStream_t */
 #define GQMM_OK 0
 #define GQMM_ERR_NULL 1         /* a required pointer is NULL */
 #define GQMM_ERR_SHAPE 2        /* a size is out of range (see each entry point) */
-#define GQMM_ERR_UNSUPPORTED 3  /* group_size not 32/64/128, bits != 4, or E above GQMM_MAX_EXPERTS */
+#define GQMM_ERR_UNSUPPORTED 3  /* a format the call does not take, or E above GQMM_MAX_EXPERTS */
 #define GQMM_ERR_ALIGN 4        /* a pointer is not aligned as required */
 #define GQMM_ERR_WORKSPACE 5    /* workspace too small or misaligned */
 #define GQMM_ERR_CUDA 6         /* a CUDA runtime/driver call or a kernel launch failed */
@@ -80,6 +99,11 @@ typedef struct CUstream_st* gqmm_stream_t; /* identical to cudaStream_t */
 #define GQMM_STATUS_TIMEOUT 0x400u    /* a bounded device-side wait gave up: y unspecified */
 
 #define GQMM_MAX_EXPERTS 1024
+
+/* Block-scaled floating-point modes of gqmm_quantize_fp and gqmm_gather_qmm_fp. */
+#define GQMM_MODE_MXFP4 1
+#define GQMM_MODE_NVFP4 2
+#define GQMM_MODE_MXFP8 3
 
 /* Gate activations of gqmm_moe_mlp. */
 #define GQMM_ACT_SILU 0
@@ -93,15 +117,31 @@ typedef struct CUstream_st* gqmm_stream_t; /* identical to cudaStream_t */
  *  w       bfloat16 [rows, H] (for E experts of F x H weights, rows = E*F), 16-byte aligned
  *  rows    >= 0;  H > 0 and H % group_size == 0 (the quantized axis; gqmm_gather_qmm also needs
  *          its K a multiple of 64)
- *  group_size 32, 64 or 128 (64 is the pages' setting; 32 and 128 are the other group sizes
- *          of the same affine format), bits must be 4
- *  wq      out: uint8 [rows, H/2], 16-byte aligned
+ *  group_size, bits   4-bit codes with 32-, 64- or 128-wide groups (64 is the pages' setting), or
+ *          2-, 3-, 5-, 6- or 8-bit codes with 64-wide groups
+ *  wq      out: uint8 [rows, H*bits/8], 16-byte aligned
  *  scales  out: bfloat16 [rows, H/group_size];  biases  out: bfloat16 [rows, H/group_size]
  * Results are bit-identical to the float32 reference formula above (no fast math).
  * Errors: GQMM_ERR_NULL, GQMM_ERR_SHAPE, GQMM_ERR_UNSUPPORTED, GQMM_ERR_ALIGN, GQMM_ERR_CUDA.
  */
 GQMM_API int gqmm_quantize(const void* w, int64_t rows, int64_t H, int group_size, int bits, void* wq,
                   void* scales, void* biases, gqmm_stream_t stream);
+
+/*
+ * gqmm_quantize_fp -- block-scaled floating-point quantization (GQMM_MODE_*, formats at the top
+ * of this header; mlx #4339, Activity).
+ *  w       bfloat16 [rows, H], 16-byte aligned; H a positive multiple of 64
+ *  rows_per_tensor  nvfp4: rows sharing one float32 scale (F for an [E, F, H] expert stack;
+ *          rows a multiple of it, at most 65535 tensors); ignored otherwise
+ *  wq      out: uint8 [rows, H/2] (mxfp4, nvfp4) or [rows, H] (mxfp8), 16-byte aligned
+ *  scales  out: uint8 [rows, H/32] (mx) or [rows, H/16] (nvfp4)
+ *  tscale  out: float32 [rows / rows_per_tensor] (nvfp4; may be NULL otherwise)
+ * Codes and scales are bit-identical to the float32 steps stated above.  nvfp4 runs three kernels
+ * (the tensors' largest magnitudes, their scales, the blocks).
+ * Errors: GQMM_ERR_NULL, GQMM_ERR_SHAPE, GQMM_ERR_UNSUPPORTED, GQMM_ERR_ALIGN, GQMM_ERR_CUDA.
+ */
+GQMM_API int gqmm_quantize_fp(const void* w, int64_t rows, int64_t H, int64_t rows_per_tensor, int mode, void* wq,
+                              void* scales, float* tscale, gqmm_stream_t stream);
 
 /*
  * gqmm_workspace_size -- bytes of device workspace gqmm_gather_qmm and gqmm_route_sort
@@ -148,8 +188,11 @@ GQMM_API int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* per
  *           (mx.quantized_matmul, same issue), which requires E == 1
  *  T, A     T >= 1, A >= 1, T*A <= 2^31 - 1
  *  H        > 0, multiple of 64 and of group_size;   F > 0, multiple of 16;   E in [1, GQMM_MAX_EXPERTS]
- *  group_size 32, 64 or 128 (the weight-streaming kernels of decode-sized calls take 64; other
- *           group sizes run those calls on the tensor-core GEMM), bits 4
+ *  group_size, bits   as for gqmm_quantize; a row's codes (H*bits/8 bytes) must be a multiple
+ *           of 16 bytes (for 3- and 5-bit codes: H a multiple of 128).  The weight-streaming
+ *           kernels of decode-sized calls take 4-bit codes in 64-wide groups; 3-, 5-, 6- and
+ *           8-bit codes run every call on the tensor-core GEMM's narrow variant (chunks of at
+ *           most 32 rows per expert)
  *  x_shared 0: x is [T, A, H], one row per (t, a);  1: x is [T, H], the A routed rows of
  *           token t all read x[t] (the x of an MoE layer, broadcast over its A experts;
  *           needs idx != NULL)
@@ -167,6 +210,23 @@ GQMM_API int gqmm_gather_qmm(const void* x, const void* wq, const void* scales, 
                     const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size,
                     int bits, int sorted, int x_shared, void* y, void* ws, size_t ws_bytes,
                     gqmm_stream_t stream);
+
+/*
+ * gqmm_gather_qmm_fp -- gqmm_gather_qmm on weights in a block-scaled floating-point mode
+ * (mx.gather_qmm with mode "mxfp4", "nvfp4" or "mxfp8"; mlx #4339, Activity):
+ *     y[t, a, :] = x[t, a, :] . deq(W[idx[t, a]])^T,
+ * x bfloat16, each weight decoded exactly and scaled in float32 to one bfloat16 rounding
+ * (like the affine path's dequantized weights), float32 accumulation, bfloat16 y.
+ *  wq, scales, tscale   as gqmm_quantize_fp writes them for rows = E*F, rows_per_tensor = F;
+ *           scales and tscale 4-byte aligned
+ *  mode     GQMM_MODE_MXFP4, GQMM_MODE_NVFP4 (needs tscale) or GQMM_MODE_MXFP8
+ *  the rest as for gqmm_gather_qmm (H a positive multiple of 64; the same workspace size).
+ * mxfp4 and nvfp4 run on both tensor-core variants; mxfp8 on the narrow one.
+ * Errors: as gqmm_gather_qmm.
+ */
+GQMM_API int gqmm_gather_qmm_fp(const void* x, const void* wq, const void* scales, const float* tscale,
+                                const uint32_t* idx, int64_t T, int A, int H, int F, int E, int mode, int sorted,
+                                int x_shared, void* y, void* ws, size_t ws_bytes, gqmm_stream_t stream);
 
 /*
  * gqmm_moe_mlp_workspace_size -- bytes of workspace for gqmm_moe_mlp with n = T*A rows,

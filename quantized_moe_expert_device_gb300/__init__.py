@@ -22,7 +22,7 @@ __all__ = [
     "gqmm_moe_mlp_workspace_size", "new_mlp_workspace", "gqmm_moe_mlp", "gqmm_gather_qmm_nn",
     "gqmm_device_status", "gqmm_status_string", "launch_count", "kernel_timer",
     "kernel_timer_read", "dispatch_count", "STATUS_BAD_INDEX", "STATUS_NOT_SORTED",
-    "STATUS_TIMEOUT", "VARIANTS", "MAX_EXPERTS", "ACTIVATIONS",
+    "STATUS_TIMEOUT", "VARIANTS", "MAX_EXPERTS", "ACTIVATIONS", "MODES", "gqmm_quantize_fp", "gqmm_gather_qmm_fp",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -37,6 +37,8 @@ STATUS_NOT_SORTED = 0x200
 STATUS_TIMEOUT = 0x400
 MAX_EXPERTS = 1024
 ACTIVATIONS = {"silu": 0, "gelu": 1, "gelu_tanh": 2}  # GQMM_ACT_* of gqmm_moe_mlp
+MODES = {"mxfp4": 1, "nvfp4": 2, "mxfp8": 3}  # GQMM_MODE_* of gqmm_quantize_fp / gqmm_gather_qmm_fp
+MODE_BLOCK = {"mxfp4": 32, "nvfp4": 16, "mxfp8": 32}  # weights per scale byte
 VARIANTS = {"route_unsorted": 0, "route_sorted": 1, "route_dense": 2, "gemm_tc": 3, "gemm_narrow": 4,
             "split_k": 5, "gemv": 6, "gemv_mma": 7, "nn": 8, "route_fused": 9}
 
@@ -68,6 +70,8 @@ def load_library():
             "gqmm_workspace_size": ([I64, I, I], SZ),
             "gqmm_route_sort": ([P, I64, I, P, P, P, SZ, P], I),
             "gqmm_gather_qmm": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, I, P, P, SZ, P], I),
+            "gqmm_quantize_fp": ([P, I64, I64, I64, I, P, P, P, P], I),
+            "gqmm_gather_qmm_fp": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P, SZ, P], I),
             "gqmm_gather_qmm_simt": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P], I),
             "gqmm_gather_qmm_nn": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P], I),
             "gqmm_moe_mlp_workspace_size": ([I64, I, I, I], SZ),
@@ -115,20 +119,70 @@ def _need(t: torch.Tensor, name: str, dtype):
 
 def gqmm_quantize(w: torch.Tensor, group_size: int = 64, bits: int = 4, stream=None
                   ) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """w bf16 [..., H] -> (wq uint8 [..., H/2], scales bf16 [..., H/64], biases bf16 [..., H/64])."""
+    """w bf16 [..., H] -> (wq uint8 [..., H*bits/8], scales bf16 [..., H/gs], biases bf16 [..., H/gs])."""
     _need(w, "w", torch.bfloat16)
     H = w.shape[-1]
     lead = tuple(w.shape[:-1])
     rows = 1
     for s in lead:
         rows *= s
-    wq = torch.empty(lead + (H // 2,), dtype=torch.uint8, device=w.device)
+    wq = torch.empty(lead + (H * bits // 8,), dtype=torch.uint8, device=w.device)
     sc = torch.empty(lead + (max(H // max(group_size, 1), 0),), dtype=torch.bfloat16, device=w.device)
     bs = torch.empty_like(sc)
     lib = load_library()
     _check(lib.gqmm_quantize(_ptr(w), rows, H, group_size, bits, _ptr(wq), _ptr(sc), _ptr(bs),
                              _stream(stream, w.device)), "gqmm_quantize")
     return wq, sc, bs
+
+
+def gqmm_quantize_fp(w: torch.Tensor, mode: str, stream=None):
+    """Block-scaled floating-point quantization of w bf16 [E, F, H] (or [F, H]): mode "mxfp4",
+    "nvfp4" or "mxfp8".  Returns (wq uint8 [..., H/2] or [..., H] (mxfp8), scales uint8
+    [..., H/32] or [..., H/16] (nvfp4), tscale float32 [E] for nvfp4 (one per expert) or None)."""
+    _need(w, "w", torch.bfloat16)
+    if mode not in MODES:
+        raise ValueError(f"mode must be one of {sorted(MODES)}, got {mode!r}")
+    H = w.shape[-1]
+    lead = tuple(w.shape[:-1])
+    rows = 1
+    for s_ in lead:
+        rows *= s_
+    per_tensor = lead[-1] if len(lead) >= 2 else rows
+    wq = torch.empty(lead + ((H if mode == "mxfp8" else H // 2),), dtype=torch.uint8, device=w.device)
+    sc = torch.empty(lead + (H // MODE_BLOCK[mode],), dtype=torch.uint8, device=w.device)
+    ts = torch.empty(max(rows // max(per_tensor, 1), 1), dtype=torch.float32, device=w.device) if mode == "nvfp4" else None
+    lib = load_library()
+    _check(lib.gqmm_quantize_fp(_ptr(w), rows, H, per_tensor, MODES[mode], _ptr(wq), _ptr(sc), _ptr(ts),
+                                _stream(stream, w.device)), "gqmm_quantize_fp")
+    return wq, sc, ts
+
+
+def gqmm_gather_qmm_fp(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, tscale: Optional[torch.Tensor],
+                       idx: Optional[torch.Tensor], mode: str, sorted_indices: bool = False,
+                       y: Optional[torch.Tensor] = None, ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """gqmm_gather_qmm on weights quantized by gqmm_quantize_fp (mode "mxfp4", "nvfp4" or "mxfp8");
+    x, idx and the result as for gqmm_gather_qmm."""
+    _need(x, "x", torch.bfloat16)
+    _need(wq, "wq", torch.uint8)
+    _need(scales, "scales", torch.uint8)
+    if mode not in MODES:
+        raise ValueError(f"mode must be one of {sorted(MODES)}, got {mode!r}")
+    if tscale is not None:
+        _need(tscale, "tscale", torch.float32)
+    if idx is not None and (not idx.is_cuda or not idx.is_contiguous() or idx.element_size() != 4):
+        raise ValueError("idx must be a contiguous 32-bit CUDA tensor")
+    T, A, H, F, E = _gather_shapes(x, idx, wq)
+    if y is None:
+        y = torch.empty(_out_shape(x, T, A, F), dtype=torch.bfloat16, device=x.device)
+    else:
+        _need(y, "y", torch.bfloat16)
+    if ws is None:
+        ws = new_workspace(T * A, F, E, x.device)
+    lib = load_library()
+    _check(lib.gqmm_gather_qmm_fp(_ptr(x), _ptr(wq), _ptr(scales), _ptr(tscale), _ptr(idx), T, A, H, F, E, MODES[mode],
+                                  1 if sorted_indices else 0, _x_shared(x, T, A, H), _ptr(y), _ptr(ws), ws.numel(),
+                                  _stream(stream, x.device)), "gqmm_gather_qmm_fp")
+    return y
 
 
 def gqmm_workspace_size(n: int, F: int, E: int) -> int:
@@ -200,9 +254,10 @@ def gqmm_gather_qmm(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, bia
                     ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """y[t, a, :] = x[t, a, :] . deq(W[idx[t, a]])^T.
 
-    x bf16 [T, A, H] (or [T, A, 1, H], or [n, H]); wq uint8 [E, F, H/2]; scales/biases bf16
-    [E, F, H/group_size] (group_size 32, 64 or 128); idx uint32/int32 [T, A] or None (dense, E == 1).  Returns y bf16 with
-    x's leading shape and last dimension F.
+    x bf16 [T, A, H] (or [T, A, 1, H], or [n, H]); wq uint8 [E, F, H*bits/8]; scales/biases bf16
+    [E, F, H/group_size] (4-bit codes with group_size 32, 64 or 128; 2-, 3-, 5-, 6- or 8-bit codes with
+    group_size 64); idx uint32/int32 [T, A] or None (dense, E == 1).  Returns y bf16 with x's leading
+    shape and last dimension F.
     """
     _need(x, "x", torch.bfloat16)
     _need(wq, "wq", torch.uint8)

@@ -87,12 +87,25 @@ void timer_end(cudaStream_t s, size_t slot) {
   cudaEventRecord(g_events[slot].second, s);
 }
 
+// Affine formats the kernels take: 4-bit codes with 32-, 64- or 128-wide groups; 2-, 3-, 5-, 6- and
+// 8-bit codes with 64-wide groups.
+int check_affine_format(int group_size, int bits) {
+  if (bits == 4 && (group_size == 32 || group_size == 64 || group_size == 128)) return GQMM_OK;
+  if ((bits == 2 || bits == 3 || bits == 5 || bits == 6 || bits == 8) && group_size == 64) return GQMM_OK;
+  return fail(GQMM_ERR_UNSUPPORTED,
+              "need bits=4 with group_size 32, 64 or 128, or bits 2, 3, 5, 6 or 8 with group_size 64 (got %d, %d)",
+              group_size, bits);
+}
+
 int validate_gather(const void* x, const void* wq, const void* scales, const void* biases,
                     const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size,
                     int bits, const void* y) {
   if (!x || !wq || !scales || !biases || !y) return fail(GQMM_ERR_NULL, "x, wq, scales, biases and y must be non-NULL");
-  if ((group_size != 32 && group_size != 64 && group_size != 128) || bits != 4)
-    return fail(GQMM_ERR_UNSUPPORTED, "need group_size 32, 64 or 128 and bits=4 (got %d, %d)", group_size, bits);
+  int rc = check_affine_format(group_size, bits);
+  if (rc) return rc;
+  if (H > 0 && ((int64_t)H * bits / 8) % 16)
+    return fail(GQMM_ERR_SHAPE, "a weight row's codes (H*bits/8 = %lld bytes) must be a multiple of 16 bytes",
+                (long long)H * bits / 8);
   if (T < 1 || A < 1 || T * (int64_t)A > 2147483647LL)
     return fail(GQMM_ERR_SHAPE, "need T >= 1, A >= 1, T*A < 2^31 (got T=%lld A=%d)", (long long)T, A);
   if (H <= 0 || H % 64 || H % group_size)
@@ -104,6 +117,28 @@ int validate_gather(const void* x, const void* wq, const void* scales, const voi
   if (!idx && E != 1) return fail(GQMM_ERR_NULL, "idx may be NULL only for the dense case E == 1");
   if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(scales, 16) || !aligned(biases, 16) || !aligned(y, 16))
     return fail(GQMM_ERR_ALIGN, "x, wq, scales, biases and y must be 16-byte aligned");
+  if (idx && !aligned(idx, 4)) return fail(GQMM_ERR_ALIGN, "idx must be 4-byte aligned");
+  return GQMM_OK;
+}
+
+// gqmm_gather_qmm_fp's weights: codes, one scale byte per block, and for nvfp4 a float32 scale
+// per expert.
+int validate_gather_fp(const void* x, const void* wq, const void* scales, const float* tscale, const uint32_t* idx,
+                       int64_t T, int A, int H, int F, int E, int mode, const void* y) {
+  if (mode != GQMM_MODE_MXFP4 && mode != GQMM_MODE_NVFP4 && mode != GQMM_MODE_MXFP8)
+    return fail(GQMM_ERR_UNSUPPORTED, "mode must be GQMM_MODE_MXFP4, GQMM_MODE_NVFP4 or GQMM_MODE_MXFP8 (got %d)", mode);
+  if (!x || !wq || !scales || !y) return fail(GQMM_ERR_NULL, "x, wq, scales and y must be non-NULL");
+  if (mode == GQMM_MODE_NVFP4 && !tscale) return fail(GQMM_ERR_NULL, "nvfp4 needs the per-expert scales");
+  if (T < 1 || A < 1 || T * (int64_t)A > 2147483647LL)
+    return fail(GQMM_ERR_SHAPE, "need T >= 1, A >= 1, T*A < 2^31 (got T=%lld A=%d)", (long long)T, A);
+  if (H <= 0 || H % 64) return fail(GQMM_ERR_SHAPE, "H must be a positive multiple of 64 (got %d)", H);
+  if (F <= 0 || F % 16) return fail(GQMM_ERR_SHAPE, "F must be a positive multiple of 16 (got %d)", F);
+  if (E < 1) return fail(GQMM_ERR_SHAPE, "E must be >= 1 (got %d)", E);
+  if (E > GQMM_MAX_EXPERTS) return fail(GQMM_ERR_UNSUPPORTED, "E=%d exceeds %d", E, GQMM_MAX_EXPERTS);
+  if ((int64_t)E * F > 2147483647LL) return fail(GQMM_ERR_SHAPE, "E*F must be < 2^31");
+  if (!idx && E != 1) return fail(GQMM_ERR_NULL, "idx may be NULL only for the dense case E == 1");
+  if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(y, 16) || !aligned(scales, 4) || (tscale && !aligned(tscale, 4)))
+    return fail(GQMM_ERR_ALIGN, "x, wq and y must be 16-byte aligned, scales and tscale 4-byte aligned");
   if (idx && !aligned(idx, 4)) return fail(GQMM_ERR_ALIGN, "idx must be 4-byte aligned");
   return GQMM_OK;
 }
@@ -168,8 +203,9 @@ int launch_projection(const GemmArgs& ga, const UnitShape& shape, int sms, cudaS
 int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, const void* biases,
                           const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size, int bits,
                           int sorted, int x_shared, void* y, void* ws, size_t ws_bytes, cudaStream_t s,
-                          bool allow_split, bool clear_header) {
-  int rc = validate_gather(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y);
+                          bool allow_split, bool clear_header, int kind, const float* tscale) {
+  int rc = kind == 0 ? validate_gather(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y)
+                     : validate_gather_fp(x, wq, scales, tscale, idx, T, A, H, F, E, kind, y);
   if (rc) return rc;
   rc = validate_shared(x_shared, idx);
   if (rc) return rc;
@@ -179,7 +215,12 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   const WsLayout L = ws_layout(n, F, E, allow_split);
   UnitShape shape = unit_shape(n, H, F, E);
   if (!allow_split) shape.ksplit = 1;
-  if (group_size != 64) shape.stream = false;  // the weight-streaming kernels take 64-wide groups
+  const bool affine4 = kind == 0 && bits == 4;
+  // the weight-streaming kernels take 4-bit affine codes in 64-wide groups
+  if (group_size != 64 || !affine4) shape.stream = false;
+  // formats with code windows wider than 32 bytes have only the narrow tensor-core variant
+  const bool wide_ok = affine4 || (kind == 0 && bits == 2) || kind == GQMM_MODE_MXFP4 || kind == GQMM_MODE_NVFP4;
+  if (!wide_ok && shape.chunk_rows > kChunkRowsNarrow) shape.chunk_rows = kChunkRowsNarrow;
   if (!aligned(ws, 256) || ws_bytes < L.total)
     return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
   rc = check_device(nullptr);
@@ -254,6 +295,9 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   ga.x_div = x_shared ? A : 1;
   ga.idx = idx;
   ga.fused_plan = fused ? 1 : 0;
+  ga.kind = kind;
+  ga.bits = kind == 0 ? bits : 4;
+  ga.tscale = tscale;
   rc = launch_projection(ga, shape, sms, s, "gather_qmm", route_variant);
   if (rc) return rc;
   return ok();
@@ -267,6 +311,7 @@ int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, cons
   if (I <= 0 || I > (1 << 29)) return fail(GQMM_ERR_SHAPE, "I must be in [1, 2^29] (got %d)", I);
   if (activation != GQMM_ACT_SILU && activation != GQMM_ACT_GELU && activation != GQMM_ACT_GELU_TANH)
     return fail(GQMM_ERR_UNSUPPORTED, "unknown activation %d", activation);
+  if (bits != 4) return fail(GQMM_ERR_UNSUPPORTED, "the expert MLP takes 4-bit codes (got bits=%d)", bits);
   // gate/up projection: K = H, 2I output columns; down projection: K = I, H output columns
   int rc = validate_gather(x, wq_gu, sc_gu, bs_gu, idx, T, A, H, 2 * I, E, group_size, bits, y);
   if (rc) return rc;
@@ -371,15 +416,15 @@ extern "C" {
 int gqmm_quantize(const void* w, int64_t rows, int64_t H, int group_size, int bits, void* wq,
                   void* scales, void* biases, gqmm_stream_t stream) {
   if (!w || !wq || !scales || !biases) return fail(GQMM_ERR_NULL, "w, wq, scales, biases must be non-NULL");
-  if ((group_size != 32 && group_size != 64 && group_size != 128) || bits != 4)
-    return fail(GQMM_ERR_UNSUPPORTED, "need group_size 32, 64 or 128 and bits=4 (got %d, %d)", group_size, bits);
+  int rc0 = check_affine_format(group_size, bits);
+  if (rc0) return rc0;
   if (rows < 0 || H <= 0 || H % group_size)
     return fail(GQMM_ERR_SHAPE, "need rows >= 0 and H a positive multiple of group_size");
   if (!aligned(w, 16) || !aligned(wq, 16)) return fail(GQMM_ERR_ALIGN, "w and wq must be 16-byte aligned");
   if (!aligned(scales, 2) || !aligned(biases, 2)) return fail(GQMM_ERR_ALIGN, "scales and biases must be 2-byte aligned");
   int rc = check_device(nullptr);
   if (rc) return rc;
-  cudaError_t e = launch_quantize(static_cast<const __nv_bfloat16*>(w), rows, H, group_size, static_cast<uint8_t*>(wq),
+  cudaError_t e = launch_quantize(static_cast<const __nv_bfloat16*>(w), rows, H, group_size, bits, static_cast<uint8_t*>(wq),
                                   static_cast<__nv_bfloat16*>(scales), static_cast<__nv_bfloat16*>(biases),
                                   reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(e));
@@ -436,6 +481,40 @@ int gqmm_gather_qmm(const void* x, const void* wq, const void* scales, const voi
                                ws_bytes, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
+int gqmm_quantize_fp(const void* w, int64_t rows, int64_t H, int64_t rows_per_tensor, int mode, void* wq, void* scales,
+                     float* tscale, gqmm_stream_t stream) {
+  if (mode != GQMM_MODE_MXFP4 && mode != GQMM_MODE_NVFP4 && mode != GQMM_MODE_MXFP8)
+    return fail(GQMM_ERR_UNSUPPORTED, "mode must be GQMM_MODE_MXFP4, GQMM_MODE_NVFP4 or GQMM_MODE_MXFP8 (got %d)", mode);
+  if (!w || !wq || !scales) return fail(GQMM_ERR_NULL, "w, wq and scales must be non-NULL");
+  if (rows < 0 || H <= 0 || H % 64) return fail(GQMM_ERR_SHAPE, "need rows >= 0 and H a positive multiple of 64");
+  if (mode == GQMM_MODE_NVFP4) {
+    if (!tscale) return fail(GQMM_ERR_NULL, "nvfp4 needs tscale (one float32 per tensor)");
+    if (rows_per_tensor < 1 || rows % rows_per_tensor)
+      return fail(GQMM_ERR_SHAPE, "rows must be a multiple of rows_per_tensor >= 1");
+    if (rows / rows_per_tensor > 65535) return fail(GQMM_ERR_SHAPE, "at most 65535 tensors");
+  }
+  if (!aligned(w, 16) || !aligned(wq, 16) || (tscale && !aligned(tscale, 4)))
+    return fail(GQMM_ERR_ALIGN, "w and wq must be 16-byte aligned, tscale 4-byte aligned");
+  int rc = check_device(nullptr);
+  if (rc) return rc;
+  cudaError_t e = launch_quantize_fp(static_cast<const __nv_bfloat16*>(w), rows, H, rows_per_tensor, mode,
+                                     static_cast<uint8_t*>(wq), static_cast<uint8_t*>(scales), tscale,
+                                     reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "quantize launch: %s", cudaGetErrorString(e));
+  if (rows > 0) g_launches.fetch_add(mode == GQMM_MODE_NVFP4 ? 3 : 1);
+  return ok();
+}
+
+int gqmm_gather_qmm_fp(const void* x, const void* wq, const void* scales, const float* tscale, const uint32_t* idx,
+                       int64_t T, int A, int H, int F, int E, int mode, int sorted, int x_shared, void* y, void* ws,
+                       size_t ws_bytes, gqmm_stream_t stream) {
+  if (mode != GQMM_MODE_MXFP4 && mode != GQMM_MODE_NVFP4 && mode != GQMM_MODE_MXFP8)
+    return fail(GQMM_ERR_UNSUPPORTED, "mode must be GQMM_MODE_MXFP4, GQMM_MODE_NVFP4 or GQMM_MODE_MXFP8 (got %d)", mode);
+  return gqmm::gather_qmm_impl(x, wq, scales, nullptr, idx, T, A, H, F, E, mode == GQMM_MODE_NVFP4 ? 16 : 32, 4,
+                               sorted, x_shared, y, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), true, false,
+                               mode, tscale);
+}
+
 size_t gqmm_moe_mlp_workspace_size(int64_t n, int H, int I, int E) {
   if (n < 0 || n > 2147483647LL || H < 0 || I < 1 || I > (1 << 29) || E < 1 || E > GQMM_MAX_EXPERTS) return 0;
   return mlp_ws_layout(n, H, I, E).total;
@@ -488,6 +567,7 @@ int gqmm_gather_qmm_nn(const void* x, const void* wq, const void* scales, const 
 int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* scales, const void* biases,
                          const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size, int bits,
                          int x_shared, void* y, gqmm_stream_t stream) {
+  if (bits != 4) return fail(GQMM_ERR_UNSUPPORTED, "the CUDA-core cross-check takes 4-bit codes (got bits=%d)", bits);
   int rc = validate_gather(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y);
   if (rc) return rc;
   rc = validate_shared(x_shared, idx);

@@ -49,6 +49,7 @@
 //
 // Every wait is bounded (mbar_wait): on expiry the CTA raises GQMM_STATUS_TIMEOUT, unwinds,
 // waits (bounded) for its own copies and MMAs in flight and frees its TMEM.
+#include "formats.cuh"
 #include "gqmm_internal.cuh"
 
 namespace gqmm {
@@ -61,7 +62,6 @@ static_assert(UM == kUnitRows, "unit height");
 constexpr int BK = 64;                   // K per stage = one quantization group
 constexpr int A_TILE_BYTES = BM * BK * 2;      // 16 KB bf16
 constexpr int A_BYTES = NT * A_TILE_BYTES;     // 32 KB
-constexpr int NIB_BYTES = UM * BK / 2;         // 8 KB packed codes
 constexpr int EPI_WARP_BYTES = 16 * 32 * 2;
 
 constexpr int kThreads = 1024;
@@ -82,10 +82,12 @@ constexpr int kUnitQ = 8;  // queue depth: how far the scheduler may run ahead o
 // Variant: largest chunk (UMMA N), code ring depth, and the warp roles: DEQ_GROUPS groups of 8
 // dequant warps (warps 0 ..), EPI_WARPS epilogue warps, then the scheduler/TMA warp, the MMA
 // warp and the gather warps.
-template <int NMAX_, int NIB_STAGES_, int DEQ_GROUPS_, int EPI_WARPS_, bool A_TMEM_, int AB_STAGES_>
+template <int NMAX_, int NIB_STAGES_, int DEQ_GROUPS_, int EPI_WARPS_, bool A_TMEM_, int AB_STAGES_, int W_ = 32>
 struct Cfg {
   static constexpr int NMAX = NMAX_;              // rows per chunk = largest UMMA N
   static constexpr int NIB_STAGES = NIB_STAGES_;  // code ring depth
+  static constexpr int W = W_;                    // bytes of a weight row's code window per k-block
+  static constexpr int NIB_BYTES = UM * W;        // one code stage: the unit's rows' windows
   // A (dequantized weights) in tensor memory instead of shared memory; AB_STAGES = depth of
   // the A / x ring.  Tensor memory: accumulators of NMAX columns per tile at column
   // tile * ACC_COLS, then (A_TMEM) the A stages, NT * 32 columns each (64 bf16 per row).
@@ -143,6 +145,13 @@ struct Cfg {
 // gives it a 7-deep A / x ring next to a 13-deep code ring.
 using CfgWide = Cfg<kChunkRowsWide, 3, 2, 8, false, 3>;
 using CfgNarrow = Cfg<kChunkRowsNarrow, 13, 3, 4, true, 7>;
+// Other code-window widths (formats.cuh): 16 bytes (2-bit affine) in both variants; 48 and 64
+// bytes (3-, 5-, 6- and 8-bit affine, mxfp8) in the narrow variant only, with as many code stages
+// as fit in the narrow variant's code ring budget (13 x 8 KB).
+using CfgWide16 = Cfg<kChunkRowsWide, 3, 2, 8, false, 3, 16>;
+using CfgNarrow16 = Cfg<kChunkRowsNarrow, 13, 3, 4, true, 7, 16>;
+using CfgNarrow48 = Cfg<kChunkRowsNarrow, 8, 3, 4, true, 7, 48>;
+using CfgNarrow64 = Cfg<kChunkRowsNarrow, 6, 3, 4, true, 7, 64>;
 
 __device__ __forceinline__ UnitEntry decode_unit(const Chunk* chunks, int u, int n_fpairs, int ksplit, int num_kb) {
   const int ks = u % ksplit;
@@ -189,7 +198,7 @@ __device__ __forceinline__ uint4 deq8(uint32_t w, uint32_t s2, uint32_t b2) {
   return o;
 }
 
-template <class C, int GS>
+template <class C, class FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmap_wq, const __grid_constant__ CUtensorMap tmap_x,
                    const GemmArgs p) {
@@ -239,7 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dependents_launch();  // the split-K finalize may be scheduled; it waits for this grid
 
   const int H = p.H, F = p.F;
-  static_assert(GS == 32 || GS == 64 || GS == 128, "group sizes");
+  static_assert(FMT::W == C::W, "the code stages hold this format's windows");
+  constexpr int GS = FMT::GS;
+  static_assert(FMT::KIND != kAffine || GS == 32 || GS == 64 || GS == 128, "group sizes");
   const int num_kb = H / BK;
   const int G = H / GS;  // scale groups per weight row
 
@@ -324,8 +335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(C::nib_full(s)), NIB_BYTES);
-          tma_load_2d(sbase + C::OFF_NIB + s * NIB_BYTES, &tmap_wq, bar(C::nib_full(s)), kb * (BK / 2), row0);
+          mbar_arrive_expect_tx(bar(C::nib_full(s)), C::NIB_BYTES);
+          tma_load_2d(sbase + C::OFF_NIB + s * C::NIB_BYTES, &tmap_wq, bar(C::nib_full(s)), code_window_x<FMT>(kb),
+                      row0);
           ++itn;
         }
         if (!ok) break;
@@ -523,9 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = t % UM;                        // weight row within the unit
     const uint32_t grp = (uint32_t)(t / UM);     // handles the steps with it % DEQ_GROUPS == grp
     const int tile = r >> 7, rr = r & (BM - 1);
-    // code tile rows are 32 bytes, TMA-swizzled in 32-byte mode: 16-byte chunk c of row r
-    // sits at chunk position c ^ ((r >> 2) & 1)
-    const uint32_t nib_row = sbase + C::OFF_NIB + (uint32_t)(r * 32);
+    // code tile rows are W bytes; 32-byte rows are TMA-swizzled in 32-byte mode (16-byte chunk c
+    // of row r at chunk position c ^ ((r >> 2) & 1)), other widths are not swizzled
+    const uint32_t nib_row = sbase + C::OFF_NIB + (uint32_t)(r * C::W);
     const uint32_t nib_c0 = (uint32_t)(((r >> 2) & 1) << 4), nib_c1 = nib_c0 ^ 16u;
     // the row in A stage 0, with its 128-byte-swizzle XOR folded in: chunk c of the row is at
     // a_row ^ (c << 4) (the unswizzled row address has bits 4-6 clear)
@@ -563,12 +575,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The scale group of k-block kb's codes: kb for 64-wide groups, kb / 2 for 128-wide ones;
     // for 32-wide groups the block's first 32 codes are group 2 kb and the other 32 group 2 kb + 1.
     auto grp_of = [](int kb) -> int { return GS == 64 ? kb : GS == 128 ? (kb >> 1) : (kb << 1); };
+    // Floating-point formats keep the k-block's scale bytes in sblk.x (two E8M0 bytes, or four
+    // E4M3 bytes for nvfp4 with the expert's float32 scale in sblk.y).
     auto load_sb = [&](const UnitEntry& U, int kb) {
       if (!U.valid || U.f0 + r >= F) {
         sblk = bblk = make_uint4(0, 0, 0, 0);
         return;
       }
       const int64_t row = (int64_t)(U.expert * F + U.f0) + r;  // E * F fits in int
+      if constexpr (FMT::KIND != kAffine) {
+        const uint8_t* sc8 = reinterpret_cast<const uint8_t*>(p.scales);
+        if constexpr (FMT::KIND == kNvfp4) {
+          sblk.x = __ldg(reinterpret_cast<const uint32_t*>(sc8 + row * (H / 16) + 4 * kb));
+          sblk.y = __float_as_uint(__ldg(p.tscale + U.expert));
+        } else {
+          sblk.x = __ldg(reinterpret_cast<const uint16_t*>(sc8 + row * (H / 32) + 2 * kb));
+        }
+        return;
+      }
       const int g = grp_of(kb);
       if (sb_vec) {
         sblk = __ldg(reinterpret_cast<const uint4*>(sc16 + row * G) + (g >> 3));
@@ -600,6 +624,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && U.valid) {
       const int g = grp_of(kb);
       const uint32_t s2 = pick(sblk, g, false), b2 = pick(bblk, g, false);
+      // floating-point formats: the float32 scale of each 16 weights of the k-block
+      float sc4[4] = {0.f, 0.f, 0.f, 0.f};
+      if constexpr (FMT::KIND == kNvfp4) {
+        const float tsc = __uint_as_float(sblk.y);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) sc4[j] = e4m3_to_f32((sblk.x >> (8 * j)) & 0xFFu) * tsc;
+      } else if constexpr (FMT::KIND != kAffine) {
+        sc4[0] = sc4[1] = e8m0_to_f32(sblk.x & 0xFFu);
+        sc4[2] = sc4[3] = e8m0_to_f32((sblk.x >> 8) & 0xFFu);
+      }
       // 32-wide groups: the row's second 32 codes (n1 below) have their own scale and bias
       const uint32_t s2b = GS == 32 ? pick(sblk, g + 1, true) : s2;
       const uint32_t b2b = GS == 32 ? pick(bblk, g + 1, true) : b2;
@@ -611,32 +645,59 @@ __global__ void __launch_bounds__(kThreads, 1)
         Un = U;
         normalize(Un, kbn);
         load_sb(Un, kbn);
-      } else if (!sb_vec || (grp_of(kbn) >> 3) != (g >> 3)) {
+      } else if (FMT::KIND != kAffine || !sb_vec || (grp_of(kbn) >> 3) != (g >> 3)) {
         load_sb(U, kbn);
       }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(C::nib_full(sn)), phn, abort_flag, status))) break;
-      const uint32_t nib_tile = nib_row + sn * NIB_BYTES;
-      uint4 n0, n1;
-      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(n0.x), "=r"(n0.y), "=r"(n0.z), "=r"(n0.w)
-                   : "r"(nib_tile + nib_c0)
-                   : "memory");
-      asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
-                   : "=r"(n1.x), "=r"(n1.y), "=r"(n1.z), "=r"(n1.w)
-                   : "r"(nib_tile + nib_c1)
-                   : "memory");
+      const uint32_t nib_tile = nib_row + sn * C::NIB_BYTES;
       // The code stage is released only after the proxy fence below: the next TMA into it
       // is an async-proxy write, which is not ordered after these generic-proxy reads by the
       // mbarrier alone.
       uint4 o[8];
-      o[0] = deq8(n0.x, s2, b2);
-      o[1] = deq8(n0.y, s2, b2);
-      o[2] = deq8(n0.z, s2, b2);
-      o[3] = deq8(n0.w, s2, b2);
-      o[4] = deq8(n1.x, s2b, b2b);
-      o[5] = deq8(n1.y, s2b, b2b);
-      o[6] = deq8(n1.z, s2b, b2b);
-      o[7] = deq8(n1.w, s2b, b2b);
+      if constexpr (FMT::KIND == kAffine && FMT::BITS == 4) {
+        uint4 n0, n1;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(n0.x), "=r"(n0.y), "=r"(n0.z), "=r"(n0.w)
+                     : "r"(nib_tile + nib_c0)
+                     : "memory");
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(n1.x), "=r"(n1.y), "=r"(n1.z), "=r"(n1.w)
+                     : "r"(nib_tile + nib_c1)
+                     : "memory");
+        o[0] = deq8(n0.x, s2, b2);
+        o[1] = deq8(n0.y, s2, b2);
+        o[2] = deq8(n0.z, s2, b2);
+        o[3] = deq8(n0.w, s2, b2);
+        o[4] = deq8(n1.x, s2b, b2b);
+        o[5] = deq8(n1.y, s2b, b2b);
+        o[6] = deq8(n1.z, s2b, b2b);
+        o[7] = deq8(n1.w, s2b, b2b);
+      } else {
+        // the row's code window: W / 4 words (for 32-byte windows through the swizzle)
+        uint32_t cw[C::W / 4];
+#pragma unroll
+        for (int c = 0; c < C::W / 16; ++c) {
+          const uint32_t at = C::W == 32 ? (c == 0 ? nib_c0 : nib_c1) : (uint32_t)(16 * c);
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(cw[4 * c]), "=r"(cw[4 * c + 1]), "=r"(cw[4 * c + 2]), "=r"(cw[4 * c + 3])
+                       : "r"(nib_tile + at)
+                       : "memory");
+        }
+        if constexpr (FMT::KIND == kAffine) {
+          if constexpr (C::W == 48 && (FMT::BITS == 3 || FMT::BITS == 5)) {
+            if (code_window_off<FMT>(kb) == 0)
+              dequant_affine<FMT::BITS, 0>(cw, s2, b2, o);
+            else
+              dequant_affine<FMT::BITS, 8>(cw, s2, b2, o);
+          } else {
+            dequant_affine<FMT::BITS, 0>(cw, s2, b2, o);
+          }
+        } else if constexpr (FMT::KIND == kMxfp8) {
+          dequant_e4m3(cw, sc4, o);
+        } else {
+          dequant_e2m1(cw, sc4, o);
+        }
+      }
       if (!__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
       if (C::A_TMEM) {
         // the row's 64 bf16 into the warp's TMEM lane quarter, 32 columns of the A stage
@@ -729,20 +790,88 @@ struct DeviceInfo {
 
 DeviceInfo g_dev[64];
 
-template <class C>
-cudaError_t configure() {
-  cudaError_t e = cudaFuncSetAttribute(gemm_tc_kernel<C, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DYN);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_tc_kernel<C, 32>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DYN);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(gemm_tc_kernel<C, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DYN);
+template <class C, class FMT>
+cudaError_t set_smem() {
+  return cudaFuncSetAttribute(gemm_tc_kernel<C, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_DYN);
+}
+
+cudaError_t configure_all() {
+  cudaError_t e = cudaSuccess;
+  auto need = [&](cudaError_t r) {
+    if (e == cudaSuccess) e = r;
+  };
+  need(set_smem<CfgWide, FmtAffine<32, 4>>());
+  need(set_smem<CfgWide, FmtAffine<64, 4>>());
+  need(set_smem<CfgWide, FmtAffine<128, 4>>());
+  need(set_smem<CfgWide16, FmtAffine<64, 2>>());
+  need(set_smem<CfgWide, FmtMx<false>>());
+  need(set_smem<CfgWide, FmtNv>());
+  need(set_smem<CfgNarrow, FmtAffine<32, 4>>());
+  need(set_smem<CfgNarrow, FmtAffine<64, 4>>());
+  need(set_smem<CfgNarrow, FmtAffine<128, 4>>());
+  need(set_smem<CfgNarrow16, FmtAffine<64, 2>>());
+  need(set_smem<CfgNarrow48, FmtAffine<64, 3>>());
+  need(set_smem<CfgNarrow48, FmtAffine<64, 5>>());
+  need(set_smem<CfgNarrow48, FmtAffine<64, 6>>());
+  need(set_smem<CfgNarrow64, FmtAffine<64, 8>>());
+  need(set_smem<CfgNarrow, FmtMx<false>>());
+  need(set_smem<CfgNarrow, FmtNv>());
+  need(set_smem<CfgNarrow64, FmtMx<true>>());
   return e;
 }
 
-// The instance of the grouped GEMM for a variant and a group size.
-template <class C>
-decltype(&gemm_tc_kernel<C, 64>) gemm_tc_instance(int group_size) {
-  return group_size == 32 ? gemm_tc_kernel<C, 32> : group_size == 128 ? gemm_tc_kernel<C, 128> : gemm_tc_kernel<C, 64>;
+using GemmKernel = decltype(&gemm_tc_kernel<CfgWide, FmtAffine<64, 4>>);
+
+// The kernel instance and its shared-memory size for a format and a variant (nullptr: the
+// format has no instance of that variant; formats with 48- or 64-byte code windows have only
+// the narrow one).
+using FmtA4g32 = FmtAffine<32, 4>;
+using FmtA4g64 = FmtAffine<64, 4>;
+using FmtA4g128 = FmtAffine<128, 4>;
+using FmtA2 = FmtAffine<64, 2>;
+using FmtA3 = FmtAffine<64, 3>;
+using FmtA5 = FmtAffine<64, 5>;
+using FmtA6 = FmtAffine<64, 6>;
+using FmtA8 = FmtAffine<64, 8>;
+using FmtMxfp4 = FmtMx<false>;
+using FmtMxfp8 = FmtMx<true>;
+
+GemmKernel pick_instance(const GemmArgs& a, bool narrow, int* smem) {
+#define GQMM_PICK(CFG, FMT)      \
+  do {                           \
+    *smem = CFG::SMEM_DYN;       \
+    return gemm_tc_kernel<CFG, FMT>; \
+  } while (0)
+  if (a.kind == kAffine && a.bits == 4) {
+    if (narrow) {
+      if (a.group_size == 32) GQMM_PICK(CfgNarrow, FmtA4g32);
+      if (a.group_size == 128) GQMM_PICK(CfgNarrow, FmtA4g128);
+      GQMM_PICK(CfgNarrow, FmtA4g64);
+    }
+    if (a.group_size == 32) GQMM_PICK(CfgWide, FmtA4g32);
+    if (a.group_size == 128) GQMM_PICK(CfgWide, FmtA4g128);
+    GQMM_PICK(CfgWide, FmtA4g64);
+  }
+  if (a.kind == kAffine && a.bits == 2) {
+    if (narrow) GQMM_PICK(CfgNarrow16, FmtA2);
+    GQMM_PICK(CfgWide16, FmtA2);
+  }
+  if (a.kind == kMxfp4) {
+    if (narrow) GQMM_PICK(CfgNarrow, FmtMxfp4);
+    GQMM_PICK(CfgWide, FmtMxfp4);
+  }
+  if (a.kind == kNvfp4) {
+    if (narrow) GQMM_PICK(CfgNarrow, FmtNv);
+    GQMM_PICK(CfgWide, FmtNv);
+  }
+  if (!narrow) return nullptr;
+  if (a.kind == kMxfp8) GQMM_PICK(CfgNarrow64, FmtMxfp8);
+  if (a.kind == kAffine && a.bits == 3) GQMM_PICK(CfgNarrow48, FmtA3);
+  if (a.kind == kAffine && a.bits == 5) GQMM_PICK(CfgNarrow48, FmtA5);
+  if (a.kind == kAffine && a.bits == 6) GQMM_PICK(CfgNarrow48, FmtA6);
+  if (a.kind == kAffine && a.bits == 8) GQMM_PICK(CfgNarrow64, FmtA8);
+#undef GQMM_PICK
+  return nullptr;
 }
 
 }  // namespace
@@ -771,8 +900,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   if (!di.configured) {
     e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    if ((e = configure<CfgWide>()) != cudaSuccess) return e;
-    if ((e = configure<CfgNarrow>()) != cudaSuccess) return e;
+    if ((e = configure_all()) != cudaSuccess) return e;
     di.configured = true;
   }
 
@@ -785,15 +913,23 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
     if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
     encode = reinterpret_cast<decltype(&cuTensorMapEncodeTiled)>(fn);
   }
-  // Packed codes as a [E*F, H/2] byte matrix; one box = the unit's 256 rows x 32 bytes (one
-  // 64-wide group), 32-byte swizzled so the dequant threads read it without bank conflicts.
+  const bool narrow = a.chunk_rows <= kChunkRowsNarrow;
+  int smem = 0;
+  GemmKernel kern = pick_instance(a, narrow, &smem);
+  if (kern == nullptr) return cudaErrorInvalidValue;
+  // Packed codes as an [E*F, row bytes] byte matrix; one box = the unit's 256 rows x one k-block's
+  // code window (W bytes: formats.cuh), 32-byte swizzled when W is 32 so the dequant threads read
+  // it without bank conflicts.  Every window starts on a 16-byte boundary.
+  const int code_bits = a.kind == kMxfp8 ? 8 : a.kind == kAffine ? a.bits : 4;
+  const int W = code_bits == 3 || code_bits == 5 ? 48 : 8 * code_bits;
+  const int64_t row_bytes = (int64_t)a.H * code_bits / 8;
   CUtensorMap map_wq;
-  const cuuint64_t dims[2] = {(cuuint64_t)(a.H / 2), (cuuint64_t)a.E * (cuuint64_t)a.F};
-  const cuuint64_t strides[1] = {(cuuint64_t)(a.H / 2)};
-  const cuuint32_t box[2] = {BK / 2, UM};
+  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)a.E * (cuuint64_t)a.F};
+  const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  const cuuint32_t box[2] = {(cuuint32_t)W, UM};
   const cuuint32_t estr[2] = {1, 1};
   CUresult cr = encode(&map_wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.wq), dims, strides, box,
-                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, W == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
   // x as a [n, H] bf16 matrix; one box = 64 columns (one k-block, 128 bytes) of one row, for
@@ -818,13 +954,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   cfg.stream = s;
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
-  if (a.chunk_rows <= kChunkRowsNarrow) {
-    cfg.dynamicSmemBytes = CfgNarrow::SMEM_DYN;
-    e = cudaLaunchKernelEx(&cfg, gemm_tc_instance<CfgNarrow>(a.group_size), map_wq, map_x, a);
-  } else {
-    cfg.dynamicSmemBytes = CfgWide::SMEM_DYN;
-    e = cudaLaunchKernelEx(&cfg, gemm_tc_instance<CfgWide>(a.group_size), map_wq, map_x, a);
-  }
+  cfg.dynamicSmemBytes = (size_t)smem;
+  e = cudaLaunchKernelEx(&cfg, kern, map_wq, map_x, a);
   if (e != cudaSuccess) return e;
   *launched = 1;
   if (a.ks_cap > 1) {

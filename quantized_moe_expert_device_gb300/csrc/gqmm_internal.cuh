@@ -123,7 +123,9 @@ inline WsLayout ws_layout(int64_t n, int F, int E, bool allow_split = true) {
   WsLayout L;
   L.n_tiles = (n + route_tile(n) - 1) / route_tile(n);
   if (L.n_tiles < 1) L.n_tiles = 1;
-  L.max_chunks = E + n / chunk_rows_for(n, E) + 1;
+  // chunks of at most 32 rows where the format has only the narrow variant (or fewer rows)
+  const int crows = chunk_rows_for(n, E);
+  L.max_chunks = E + n / (crows < kChunkRowsNarrow ? crows : kChunkRowsNarrow) + 1;
   const int ks = allow_split ? ksplit_bound(n, F, E, nullptr) : 1;
   L.has_acc = ks > 1;
   size_t off = sizeof(WsHeader);
@@ -150,14 +152,18 @@ int report_error(int code, const char* fmt, ...);
 // before the first kernel.
 int gather_qmm_impl(const void* x, const void* wq, const void* scales, const void* biases, const uint32_t* idx,
                     int64_t T, int A, int H, int F, int E, int group_size, int bits, int sorted, int x_shared,
-                    void* y, void* ws, size_t ws_bytes, cudaStream_t s, bool allow_split, bool clear_header = false);
+                    void* y, void* ws, size_t ws_bytes, cudaStream_t s, bool allow_split, bool clear_header = false,
+                    int kind = 0, const float* tscale = nullptr);
 
 
 // ------------------------------------------------------------------------------------------
 // Kernel launchers (defined in the .cu files).  All return cudaError_t of the launch.
 // ------------------------------------------------------------------------------------------
-cudaError_t launch_quantize(const __nv_bfloat16* w, int64_t rows, int64_t H, int group_size, uint8_t* wq,
+cudaError_t launch_quantize(const __nv_bfloat16* w, int64_t rows, int64_t H, int group_size, int bits, uint8_t* wq,
                             __nv_bfloat16* scales, __nv_bfloat16* biases, cudaStream_t s);
+// Block-scaled floating-point quantization (kind 1 mxfp4, 2 nvfp4, 3 mxfp8; formats.cuh).
+cudaError_t launch_quantize_fp(const __nv_bfloat16* w, int64_t rows, int64_t H, int64_t rows_per_tensor, int kind,
+                               uint8_t* wq, uint8_t* scales, float* tscale, cudaStream_t s);
 
 struct RouteArgs {
   const uint32_t* idx;  // NULL: dense (E == 1, every row in expert 0)
@@ -198,6 +204,9 @@ struct GemmArgs {
   int ks_cap;           // > 1: the plan step may split K (header->ksplit) and the finalize runs
   int dense_plan;       // 1: idx is NULL, so the plan is the single chunk (expert 0, start 0, n rows)
   int group_size = 64;  // quantization group along H: 32, 64 or 128 (the streaming kernels: 64)
+  int kind = 0;         // weight format: 0 affine, 1 mxfp4, 2 nvfp4, 3 mxfp8 (formats.cuh)
+  int bits = 4;         // affine code width: 2, 3, 4, 5, 6 or 8
+  const float* tscale = nullptr;  // nvfp4: float32 scale per expert [E]
   int x_div = 1;        // x row of routed row r: r / x_div (A when the A rows of a token share
                         // one x row, else 1); x has n / x_div rows
   const uint32_t* idx = nullptr;  // routing entries [n] (fused_plan calls)

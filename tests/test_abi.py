@@ -86,7 +86,9 @@ def test_validation_rejects_bad_arguments_without_a_gpu(lib):
     assert call(gs=16) == 3
     assert call(gs=256) == 3
     assert call(gs=128, H=192) == 2           # ERR_SHAPE: H must be a multiple of the group size
-    assert call(bits=8) == 3
+    assert call(bits=7) == 3                  # code widths are 2, 3, 4, 5, 6 and 8
+    assert call(bits=8, gs=128) == 3          # widths other than 4 take 64-wide groups only
+    assert call(bits=3, H=192) == 2           # a row's 3-bit codes (72 bytes) are no multiple of 16 bytes
     assert call(H=100) == 2                   # ERR_SHAPE
     assert call(F=120) == 2
     assert call(T=0) == 2
@@ -166,3 +168,35 @@ def test_nn_validation_rejects_bad_arguments_without_a_gpu(lib):
     assert call(shared=1, idx=None, E=1) == 1
     assert call(y=P(0x10008)) == 4            # ERR_ALIGN: y is stored 16 bytes at a time
     assert call(wq=P(0x10004)) == 4
+
+
+def test_fp_mode_validation_rejects_bad_arguments_without_a_gpu(lib):
+    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    f = lib.gqmm_gather_qmm_fp
+    f.argtypes = [P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P, ctypes.c_size_t, P]
+    f.restype = I
+    fake = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: validation fails before any launch
+    args = dict(x=fake, wq=fake, sc=fake, ts=fake, idx=fake, T=16, A=2, H=256, F=128, E=8, mode=1, sorted=0, shared=0,
+                y=fake, ws=fake, wsb=1 << 20, s=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return f(a["x"], a["wq"], a["sc"], a["ts"], a["idx"], a["T"], a["A"], a["H"], a["F"], a["E"], a["mode"],
+                 a["sorted"], a["shared"], a["y"], a["ws"], a["wsb"], a["s"])
+
+    assert call(mode=0) == 3 and call(mode=4) == 3  # ERR_UNSUPPORTED: modes 1 (mxfp4), 2 (nvfp4), 3 (mxfp8)
+    assert call(sc=None) == 1                        # ERR_NULL
+    assert call(mode=2, ts=None) == 1                # nvfp4 needs its per-expert scales
+    assert call(H=96) == 2                           # ERR_SHAPE: H a multiple of 64
+    assert call(F=24) == 2
+    assert call(sc=ctypes.c_void_p((1 << 20) + 2)) == 4  # ERR_ALIGN: scales 4-byte aligned
+    assert call(wsb=16) == 5                         # ERR_WORKSPACE
+
+    q = lib.gqmm_quantize_fp
+    q.argtypes = [P, I64, I64, I64, I, P, P, P, P]
+    q.restype = I
+    assert q(fake, 8, 256, 8, 5, fake, fake, fake, None) == 3   # unknown mode
+    assert q(fake, 8, 100, 8, 1, fake, fake, None, None) == 2   # H a multiple of 64
+    assert q(fake, 8, 256, 3, 2, fake, fake, fake, None) == 2   # nvfp4: rows a multiple of rows_per_tensor
+    assert q(fake, 8, 256, 8, 2, fake, fake, None, None) == 1   # nvfp4 needs tscale

@@ -60,5 +60,7 @@ def test_quantize_rejects_unsupported():
         g.gqmm_quantize(torch.zeros(4, 128, dtype=torch.bfloat16, device="cuda"), group_size=96)
     with pytest.raises(g.GqmmError):  # H must be a multiple of the group size
         g.gqmm_quantize(torch.zeros(4, 192, dtype=torch.bfloat16, device="cuda"), group_size=128)
-    with pytest.raises(g.GqmmError):
-        g.gqmm_quantize(torch.zeros(4, 128, dtype=torch.bfloat16, device="cuda"), bits=8)
+    with pytest.raises(g.GqmmError):  # code widths are 2, 3, 4, 5, 6 and 8
+        g.gqmm_quantize(torch.zeros(4, 128, dtype=torch.bfloat16, device="cuda"), bits=7)
+    with pytest.raises(g.GqmmError):  # widths other than 4 take 64-wide groups only
+        g.gqmm_quantize(torch.zeros(4, 128, dtype=torch.bfloat16, device="cuda"), group_size=128, bits=8)
