@@ -56,8 +56,14 @@ def algorithmic_bytes(w: wl.Workload, idx: np.ndarray | None) -> int:
     hidden rows are intermediates, not counted: a kernel that kept them on chip moves none)."""
     hit = w.E if idx is None else len(np.unique(idx))
 
-    def qbytes(rows, K):  # one expert's packed codes + bf16 scale and bias per group
-        return rows * (K // 2 + 4 * (K // w.group_size))
+    def qbytes(rows, K):  # one expert's packed codes + its scales (and biases)
+        if w.mode == "mxfp4":
+            return rows * (K // 2 + K // 32)
+        if w.mode == "nvfp4":
+            return rows * (K // 2 + K // 16) + 4  # + the expert's float32 scale
+        if w.mode == "mxfp8":
+            return rows * (K + K // 32)
+        return rows * (K * w.bits // 8 + 4 * (K // w.group_size))  # bf16 scale and bias per group
 
     if w.kind == "mlp":
         weights = hit * (qbytes(2 * w.F, w.H) + qbytes(w.H, w.F))
@@ -195,7 +201,9 @@ def oracle_inputs(w: wl.Workload, inp):
     if w.kind == "mlp":
         return (oracle.quantize(inp["w_gu"], group_size=w.group_size),
                 oracle.quantize(inp["w_dn"], group_size=w.group_size))
-    return oracle.quantize(inp["w"], group_size=w.group_size)
+    if w.mode != "affine":
+        return oracle.quantize_fp(inp["w"], w.mode)
+    return oracle.quantize(inp["w"], group_size=w.group_size, bits=w.bits)
 
 
 def oracle_rows(w: wl.Workload, x_cpu, qw, idx, rows):
@@ -207,8 +215,11 @@ def oracle_rows(w: wl.Workload, x_cpu, qw, idx, rows):
     elif w.kind == "nn":
         oracle.gather_qmm_nn(x_cpu, *qw, idx, w.E, group_size=w.group_size, rows=rows)
         return 1  # numpy row products, one thread
+    elif w.mode != "affine":
+        oracle.gather_qmm_fp(x_cpu, *qw, idx, w.E, w.mode, rows=rows)
+        return oracle.nthreads_default()
     else:
-        oracle.gather_qmm(x_cpu, *qw, idx, w.E, group_size=w.group_size, rows=rows)
+        oracle.gather_qmm(x_cpu, *qw, idx, w.E, group_size=w.group_size, bits=w.bits, rows=rows)
     return oracle.gather_qmm.last_threads
 
 
@@ -241,7 +252,9 @@ def metric_name(w: wl.Workload) -> str:
 def workload_config(w: wl.Workload) -> dict:
     c = {"workload": w.name, "T": w.T, "A": w.A, "H": w.H}
     c.update({"I": w.F} if w.kind == "mlp" else {"K": w.H, "N": w.F} if w.kind == "nn" else {"F": w.F})
-    c.update({"E": w.E, "group_size": w.group_size, "bits": 4, "routing": w.routing})
+    c.update({"E": w.E, "group_size": w.group_size, "bits": w.bits, "routing": w.routing})
+    if w.mode != "affine":
+        c.update({"mode": w.mode, "bits": 8 if w.mode == "mxfp8" else 4})
     if w.kind == "mlp":
         c["op"] = "gqmm_moe_mlp: gate/up projection, act(gate) * up, down projection"
         c["activation"] = MLP_ACTIVATION
@@ -291,7 +304,8 @@ def run_reference(args, w: wl.Workload, world: int, rank: int):
 # Workloads timed after the headline, each on its own rotated inputs, into the line's per_config
 # block: the equal-FLOPs dense control, the rows-per-expert sweep, the Mixtral-like expert shape,
 # dense and MoE decode at 1-8 rows, the other group sizes, the expert MLP and transpose=False.
-PER_CONFIG = ["prefill_dense", "prefill_e64_g32", "prefill_e64_g128",
+PER_CONFIG = ["prefill_dense", "prefill_e64_g32", "prefill_e64_g128", "prefill_e64_b2", "prefill_e64_b3",
+              "prefill_e64_b8", "prefill_e64_mxfp4", "prefill_e64_nvfp4", "prefill_e64_mxfp8",
               "sweep_r4", "sweep_r8", "sweep_r16", "sweep_r32", "sweep_r64", "sweep_r128", "mixtral",
               "decode_dense_m1", "decode_dense_m2", "decode_dense_m4", "decode_dense_m8",
               "decode_moe_m1", "decode_moe_m2", "decode_moe_m4", "decode_moe_m8",
@@ -304,11 +318,14 @@ STRIPS = 5                    # the timed steps are split into this many strips 
 
 def _weights_on_device(g, w: wl.Workload, inp, dev):
     """The workload's weights quantized on the GPU: [wq, scales, biases] (both projections for the
-    expert MLP)."""
+    expert MLP), or [wq, scales, tensor scales or None] for a floating-point mode."""
     out = []
     for key in (("w_gu", "w_dn") if w.kind == "mlp" else ("w",)):
         w_dev = inp[key].to(dev)
-        out += list(g.gqmm_quantize(w_dev, group_size=w.group_size))
+        if w.mode != "affine":
+            out += list(g.gqmm_quantize_fp(w_dev, w.mode))
+        else:
+            out += list(g.gqmm_quantize(w_dev, group_size=w.group_size, bits=w.bits))
         del w_dev
     return out
 
@@ -325,7 +342,8 @@ class Prepared:
         self.l2 = torch.cuda.get_device_properties(dev).L2_cache_size
         self.per_copy = algorithmic_bytes(w, idx_np)
         weights0 = _weights_on_device(g, w, self.inp, dev)
-        clone_bytes = sum(t.numel() * t.element_size() for t in weights0) + w.n * (w.H + w.out_cols) * 2 + w.n * 4
+        clone_bytes = (sum(t.numel() * t.element_size() for t in weights0 if t is not None)
+                       + w.n * (w.H + w.out_cols) * 2 + w.n * 4)
         want = int(np.ceil(ROTATE_L2_MULTIPLE * self.l2 / max(self.per_copy, 1)))
         self.copies = int(max(2, min(want, MAX_COPIES, MAX_CLONE_BYTES // max(clone_bytes, 1))))
         if w.kind == "mlp":
@@ -335,15 +353,19 @@ class Prepared:
             fn, ws_new = lib.gqmm_gather_qmm_nn, (lambda: None)
             sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4, 0)
         else:
-            fn, ws_new = lib.gqmm_gather_qmm, (lambda: g.new_workspace(w.n, w.F, w.E, dev))
-            sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4)
+            ws_new = lambda: g.new_workspace(w.n, w.F, w.E, dev)  # noqa: E731
+            if w.mode != "affine":
+                fn, sizes = lib.gqmm_gather_qmm_fp, (w.T, w.A, w.H, w.F, w.E, g.MODES[w.mode])
+            else:
+                fn, sizes = lib.gqmm_gather_qmm, (w.T, w.A, w.H, w.F, w.E, w.group_size, w.bits)
         x0 = self.inp["x"].to(dev)
         idx0 = None if idx_np is None else torch.from_numpy(np.ascontiguousarray(idx_np).view(np.int32)).to(dev)
         self.sets = []
         for c in range(self.copies):
             last = c == self.copies - 1  # the last copy takes the originals instead of cloning them
             self.sets.append(dict(
-                x=x0 if last else x0.clone(), w=weights0 if last else [t.clone() for t in weights0],
+                x=x0 if last else x0.clone(),
+                w=weights0 if last else [None if t is None else t.clone() for t in weights0],
                 idx=None if idx0 is None else (idx0 if last else idx0.clone()),
                 y=torch.empty(w.T, w.A, w.out_cols, dtype=torch.bfloat16, device=dev), ws=ws_new()))
         torch.cuda.synchronize(dev)
@@ -351,7 +373,7 @@ class Prepared:
         P = ctypes.c_void_p
 
         def argv(st, sptr):
-            head = (P(st["x"].data_ptr()),) + tuple(P(t.data_ptr()) for t in st["w"]) + (
+            head = (P(st["x"].data_ptr()),) + tuple(None if t is None else P(t.data_ptr()) for t in st["w"]) + (
                 None if st["idx"] is None else P(st["idx"].data_ptr()),) + sizes
             if w.kind == "nn":
                 return head + (P(st["y"].data_ptr()), sptr)

@@ -23,6 +23,11 @@ def test_algorithmic_bytes_by_hand():
     assert bench.algorithmic_bytes(m, wl.make_idx(m)) == 64 * per_expert + 16384 * 2048 * 2 * 2 + 16384 * 4
     nn = W["nn_e4"]  # W[e] = [K = 512, N = 512] quantized along N
     assert bench.algorithmic_bytes(nn, wl.make_idx(nn)) == 4 * 512 * (256 + 4 * 8) + 1024 * 512 * 2 * 2 + 1024 * 4
+    xyi = 16384 * 2048 * 2 + 16384 * 768 * 2 + 16384 * 4
+    assert bench.algorithmic_bytes(W["prefill_e64_b3"], idx) == 64 * 768 * (768 + 4 * 32) + xyi
+    assert bench.algorithmic_bytes(W["prefill_e64_mxfp4"], idx) == 64 * 768 * (1024 + 64) + xyi
+    assert bench.algorithmic_bytes(W["prefill_e64_nvfp4"], idx) == 64 * (768 * (1024 + 128) + 4) + xyi
+    assert bench.algorithmic_bytes(W["prefill_e64_mxfp8"], idx) == 64 * 768 * (2048 + 64) + xyi
     assert W["prefill_dense"].flops == 2 * 16384 * 2048 * 768
     assert m.flops == 6 * 16384 * 2048 * 768 and nn.flops == 2 * 1024 * 512 * 512
 

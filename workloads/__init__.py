@@ -128,6 +128,8 @@ class Workload:
     r: int = 0              # rows per expert for "balanced"
     note: str = ""
     group_size: int = 64    # quantization group along the reduction dimension (32, 64 or 128)
+    bits: int = 4           # affine code width (2, 3, 4, 5, 6 or 8)
+    mode: str = "affine"    # weight format: "affine", or a block-scaled mode "mxfp4", "nvfp4", "mxfp8"
     kind: str = "gather"    # "gather": one projection, F output columns; "nn": transpose=False, W [E, H, F]
                             # quantized along F (K = H, N = F);
                             # "mlp": the expert MLP, F = intermediate width I (gate/up 2F rows, down H rows)
@@ -155,6 +157,13 @@ def workloads() -> Dict[str, Workload]:
     for gs in (32, 128):
         w[f"prefill_e64_g{gs}"] = Workload(f"prefill_e64_g{gs}", T=2048, A=8, H=2048, F=768, E=64, routing="uniform",
                                            group_size=gs, note=f"MoE prefill microbenchmark shape, {gs}-wide groups")
+    for b in (2, 3, 8):
+        w[f"prefill_e64_b{b}"] = Workload(f"prefill_e64_b{b}", T=2048, A=8, H=2048, F=768, E=64, routing="uniform",
+                                          bits=b, note=f"MoE prefill microbenchmark shape, {b}-bit affine codes")
+    for m in ("mxfp4", "nvfp4", "mxfp8"):
+        w[f"prefill_e64_{m}"] = Workload(f"prefill_e64_{m}", T=2048, A=8, H=2048, F=768, E=64, routing="uniform",
+                                         mode=m, group_size=16 if m == "nvfp4" else 32,
+                                         note=f"MoE prefill microbenchmark shape, {m} weights")
     w["nn_e4"] = Workload("nn_e4", T=1024, A=1, H=512, F=512, E=4, routing="uniform", kind="nn",
                           note="transpose=False gather_qmm, E=4, K=N=512, 1024 rows (the mlx PR #4023 follow-up timing)")
     w["prefill_dense"] = Workload("prefill_dense", T=16384, A=1, H=2048, F=768, E=1, routing="dense",
