@@ -364,6 +364,16 @@ GQMM_API int64_t gqmm_launch_count(void);
 GQMM_API void gqmm_kernel_timer(int capacity);
 GQMM_API int gqmm_kernel_timer_read(int64_t* launches, double* total_ms);
 
+/*
+ * gqmm_test_stall_next -- failure-path test hook.  The next n tensor-core GEMM launches leave
+ * their first k-block's codes uncopied, so the dequant warps' bounded wait for them runs out
+ * (after 2 s): the launch sets GQMM_STATUS_TIMEOUT, every role unwinds (waits, each bounded,
+ * for its own copies and MMAs in flight) and the tensor memory is freed, so the context and the
+ * next calls stay usable.  y of a stalled call is undefined.  n = 0 disarms.  No fault, trap or
+ * unbounded wait is involved.
+ */
+GQMM_API void gqmm_test_stall_next(int n);
+
 #define GQMM_VARIANT_ROUTE_UNSORTED 0 /* histogram + scatter route sort */
 #define GQMM_VARIANT_ROUTE_SORTED 1   /* segment boundaries from caller-sorted idx */
 #define GQMM_VARIANT_ROUTE_DENSE 2    /* idx == NULL, E == 1 */

@@ -21,7 +21,7 @@ __all__ = [
     "new_workspace", "gqmm_route_sort", "gqmm_gather_qmm", "gqmm_gather_qmm_simt",
     "gqmm_moe_mlp_workspace_size", "new_mlp_workspace", "gqmm_moe_mlp", "gqmm_gather_qmm_nn",
     "gqmm_device_status", "gqmm_status_string", "launch_count", "kernel_timer",
-    "kernel_timer_read", "dispatch_count", "STATUS_BAD_INDEX", "STATUS_NOT_SORTED",
+    "kernel_timer_read", "dispatch_count", "test_stall_next", "STATUS_BAD_INDEX", "STATUS_NOT_SORTED",
     "STATUS_TIMEOUT", "VARIANTS", "MAX_EXPERTS", "ACTIVATIONS", "MODES", "gqmm_quantize_fp", "gqmm_gather_qmm_fp",
 ]
 
@@ -83,6 +83,7 @@ def load_library():
             "gqmm_kernel_timer": ([I], None),
             "gqmm_kernel_timer_read": ([ctypes.POINTER(I64), ctypes.POINTER(ctypes.c_double)], I),
             "gqmm_dispatch_count": ([I], I64),
+            "gqmm_test_stall_next": ([I], None),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -402,6 +403,12 @@ def kernel_timer_read() -> Tuple[int, float]:
     ms = ctypes.c_double(0.0)
     _check(load_library().gqmm_kernel_timer_read(ctypes.byref(n), ctypes.byref(ms)), "gqmm_kernel_timer_read")
     return int(n.value), float(ms.value)
+
+
+def test_stall_next(n: int) -> None:
+    """Failure-path test hook: the next n tensor-core GEMM launches time out (GQMM_STATUS_TIMEOUT)
+    and unwind instead of computing."""
+    load_library().gqmm_test_stall_next(int(n))
 
 
 def dispatch_count(variant: str) -> int:

@@ -19,6 +19,7 @@ namespace {
 
 thread_local std::string t_last_error;
 std::atomic<int64_t> g_launches{0};
+std::atomic<int> g_test_stall{0};  // gqmm_test_stall_next: GEMM launches left to stall
 std::atomic<int64_t> g_dispatch[GQMM_VARIANT_COUNT];
 
 int fail(int code, const char* fmt, ...) {
@@ -176,7 +177,12 @@ int launch_projection(const GemmArgs& ga, const UnitShape& shape, int sms, cudaS
     e = launch_gemv(ga, shape.chunk_rows, sms, s);
     gemm_launched = 1;
   } else {
-    e = launch_gemm_tc(ga, s, &gemm_launched);
+    GemmArgs a = ga;
+    int left = g_test_stall.load();
+    while (left > 0 && !g_test_stall.compare_exchange_weak(left, left - 1)) {
+    }
+    if (left > 0) a.test_stall = 1;
+    e = launch_gemm_tc(a, s, &gemm_launched);
   }
   if (timed) timer_end(s, slot);
   g_launches.fetch_add(gemm_launched);
@@ -618,6 +624,8 @@ const char* gqmm_status_string(int status) {
 const char* gqmm_last_error(void) { return t_last_error.c_str(); }
 
 int64_t gqmm_launch_count(void) { return g_launches.load(); }
+
+void gqmm_test_stall_next(int n) { g_test_stall.store(n > 0 ? n : 0); }
 
 void gqmm_kernel_timer(int capacity) {
   std::lock_guard<std::mutex> lk(g_timer_mu);

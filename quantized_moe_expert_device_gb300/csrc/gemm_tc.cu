@@ -335,6 +335,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
+          if (p.test_stall && itn == 0) {  // failure-path test: this stage's codes never arrive
+            ++itn;
+            continue;
+          }
           mbar_arrive_expect_tx(bar(C::nib_full(s)), C::NIB_BYTES);
           tma_load_2d(sbase + C::OFF_NIB + s * C::NIB_BYTES, &tmap_wq, bar(C::nib_full(s)), code_window_x<FMT>(kb),
                       row0);

@@ -207,6 +207,7 @@ struct GemmArgs {
   int kind = 0;         // weight format: 0 affine, 1 mxfp4, 2 nvfp4, 3 mxfp8 (formats.cuh)
   int bits = 4;         // affine code width: 2, 3, 4, 5, 6 or 8
   const float* tscale = nullptr;  // nvfp4: float32 scale per expert [E]
+  int test_stall = 0;   // 1: leave the first k-block's codes uncopied (gqmm_test_stall_next)
   int x_div = 1;        // x row of routed row r: r / x_div (A when the A rows of a token share
                         // one x row, else 1); x has n / x_div rows
   const uint32_t* idx = nullptr;  // routing entries [n] (fused_plan calls)
