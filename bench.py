@@ -349,9 +349,9 @@ class Prepared:
         if w.kind == "mlp":
             fn, ws_new = lib.gqmm_moe_mlp, (lambda: g.new_mlp_workspace(w.n, w.H, w.F, w.E, dev))
             sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4, g.ACTIVATIONS[MLP_ACTIVATION])
-        elif w.kind == "nn":  # no workspace: rows are independent, no route sort
-            fn, ws_new = lib.gqmm_gather_qmm_nn, (lambda: None)
-            sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4, 0)
+        elif w.kind == "nn":  # W[e] is [K = H, N = F]; the workspace is sized for N output columns
+            fn, ws_new = lib.gqmm_gather_qmm_nn, (lambda: g.new_workspace(w.n, w.F, w.E, dev))
+            sizes = (w.T, w.A, w.H, w.F, w.E, w.group_size, 4)
         else:
             ws_new = lambda: g.new_workspace(w.n, w.F, w.E, dev)  # noqa: E731
             if w.mode != "affine":
@@ -375,8 +375,6 @@ class Prepared:
         def argv(st, sptr):
             head = (P(st["x"].data_ptr()),) + tuple(None if t is None else P(t.data_ptr()) for t in st["w"]) + (
                 None if st["idx"] is None else P(st["idx"].data_ptr()),) + sizes
-            if w.kind == "nn":
-                return head + (P(st["y"].data_ptr()), sptr)
             return head + (0, 0, P(st["y"].data_ptr()), P(st["ws"].data_ptr()), st["ws"].numel(), sptr)
 
         self._argv = argv
@@ -503,14 +501,7 @@ def roofline_entry(w: wl.Workload, alg_bytes: int, gemm_ms: float, peaks, peaks_
     ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
     bound = "tensor" if flops / alg_bytes >= ridge else "hbm"
     peak_source = f"{peaks_src} ({'bf16_tflops' if bound == 'tensor' else 'hbm_gbs'})"
-    if w.kind == "nn":
-        # CUDA-core kernel: the float32 FMA pipes (128 lanes per SM, 2 FLOP per FMA) at the
-        # maximum SM clock
-        bound = "alu"
-        peak = sms * 128 * 2 * sm_max * 1e6 / 1e12
-        achieved, unit = flops / (gemm_ms * 1e-3) / 1e12, "TFLOP/s"
-        peak_source = f"derived: {sms} SMs x 128 FP32 lanes x 2 FLOP x {sm_max} MHz"
-    elif bound == "tensor":
+    if bound == "tensor":
         achieved, peak, unit = flops / (gemm_ms * 1e-3) / 1e12, peaks["bf16_tflops"], "TFLOP/s"
     else:
         achieved, peak, unit = alg_bytes / (gemm_ms * 1e-3) / 1e9, peaks["hbm_gbs"], "GB/s"
@@ -822,14 +813,13 @@ def cpu_baseline(w: wl.Workload, inp, idx_np):
 _CSRC = "quantized_moe_expert_device_gb300/csrc/"
 # The sources each GEMM-step kernel is built from (a traffic record is stale once they change).
 KERNEL_SOURCES = {
-    "gemm_tc_kernel": (_CSRC + "gemm_tc.cu", _CSRC + "gqmm_internal.cuh"),
+    "gemm_tc_kernel": (_CSRC + "gemm_tc.cu", _CSRC + "formats.cuh", _CSRC + "gqmm_internal.cuh"),
     "gemv_fma_kernel": (_CSRC + "gemv.cu", _CSRC + "gqmm_internal.cuh"),
     "gemv_mma_kernel": (_CSRC + "gemv_mma.cu", _CSRC + "gqmm_internal.cuh"),
-    "gemm_nn_kernel": (_CSRC + "gemm_nn.cu", _CSRC + "gqmm_internal.cuh"),
 }
 # dispatch-count variant -> the kernel it launches for the GEMM step
 _VARIANT_KERNEL = {"gemv": "gemv_fma_kernel", "gemv_mma": "gemv_mma_kernel", "gemm_narrow": "gemm_tc_kernel",
-                   "gemm_tc": "gemm_tc_kernel", "nn": "gemm_nn_kernel"}
+                   "gemm_tc": "gemm_tc_kernel"}
 
 
 def kernel_source_sha(kernel):

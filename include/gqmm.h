@@ -15,7 +15,8 @@
  * Entry points: gqmm_quantize (the weight format below), gqmm_route_sort, gqmm_gather_qmm
  * (the operation; gqmm_gather_qmm_noalloc without a workspace), gqmm_moe_mlp (the expert MLP
  * built on it: gate/up, SiLU or GELU gating, down), gqmm_gather_qmm_nn (transpose=False),
- * gqmm_gather_qmm_simt (a CUDA-core cross-check), and status / instrumentation calls.
+ * gqmm_gather_qmm_simt and gqmm_gather_qmm_nn_simt (CUDA-core cross-checks), and status /
+ * instrumentation calls.
  *
  * Conventions shared by every entry point
  *  - All tensor arguments are DEVICE pointers on the current CUDA device, except where a
@@ -275,21 +276,42 @@ GQMM_API int gqmm_moe_mlp(const void* x, const void* wq_gu, const void* sc_gu, c
  * fine-tuning):
  *     y[t, a, :] = x[t, a, :] . deq(W[idx[t, a]]),   W[e] of shape [K, N], quantized along N
  * (mx.quantize applied to an [E, K, N] weight, the format at the top of this header with H := N).
- * A first version on CUDA cores: every routed row streams its expert's [K, N] codes (from L2
- * after the first row of an expert); float32 dequantization and accumulation, bf16 output.
+ * The same route step and tcgen05 grouped GEMM as gqmm_gather_qmm: a unit is 256 output columns
+ * of one expert; each k-block's codes are 64 k-rows of the unit's columns, dequantized column by
+ * column into the same K-major bf16 operand (one rounding per weight), float32 accumulation,
+ * bf16 output.
  *
- *  x        bfloat16 [T, A, K] (or [T, K] with x_shared = 1), 2-byte aligned
- *  wq       uint8 [E, K, N/2], 16-byte aligned;  scales, biases  bfloat16 [E, K, N/group_size]
- *  idx, T, A, E, group_size, bits, x_shared   as for gqmm_gather_qmm (no sorted flag: rows
- *           are independent and need no route sort)
- *  K        in [1, 2^24];   N  positive multiple of group_size, at most 2^24
+ *  x        bfloat16 [T, A, K] (or [T, K] with x_shared = 1), 16-byte aligned
+ *  wq       uint8 [E, K, N/2] (element n of a k-row in the low nibble when n is even), 16-byte
+ *           aligned;  scales, biases  bfloat16 [E, K, N/group_size], 2-byte aligned
+ *  idx, T, A, E, sorted, x_shared, ws, ws_bytes, stream   as for gqmm_gather_qmm, with the
+ *           workspace sized by gqmm_workspace_size(T*A, N, E)
+ *  K        a positive multiple of 64;  N  a positive multiple of 32 and of group_size
+ *  group_size 32, 64 or 128;  bits 4;  E*K and E*N below 2^31
  *  y        out: bfloat16 [T, A, N], 16-byte aligned
- * Rows whose idx is >= E are written as zeros (no status word: this call takes no workspace).
- * Errors: GQMM_ERR_NULL, GQMM_ERR_SHAPE, GQMM_ERR_UNSUPPORTED, GQMM_ERR_ALIGN, GQMM_ERR_CUDA.
+ * Invalid indices, the status word and the sorted-promise rule: as gqmm_gather_qmm.
+ * Errors: GQMM_ERR_NULL, GQMM_ERR_SHAPE, GQMM_ERR_UNSUPPORTED, GQMM_ERR_ALIGN,
+ * GQMM_ERR_WORKSPACE, GQMM_ERR_DEVICE, GQMM_ERR_CUDA.
  */
 GQMM_API int gqmm_gather_qmm_nn(const void* x, const void* wq, const void* scales, const void* biases,
                                const uint32_t* idx, int64_t T, int A, int K, int N, int E, int group_size,
-                               int bits, int x_shared, void* y, gqmm_stream_t stream);
+                               int bits, int sorted, int x_shared, void* y, void* ws, size_t ws_bytes,
+                               gqmm_stream_t stream);
+
+/*
+ * gqmm_gather_qmm_nn_simt -- the transpose=False operation on CUDA cores: every routed row
+ * streams its expert's [K, N] codes (from L2 after the first row of an expert); float32
+ * dequantization and accumulation, bf16 output.  A slow, independent GPU cross-check of
+ * gqmm_gather_qmm_nn, never used by it; needs no workspace.
+ *  x        bfloat16 [T, A, K] (or [T, K] with x_shared = 1), 2-byte aligned
+ *  K        in [1, 2^24];   N  positive multiple of group_size, at most 2^24
+ *  other arguments as gqmm_gather_qmm_nn (no sorted flag: rows are independent)
+ * Rows whose idx is >= E are written as zeros (no status word: this call takes no workspace).
+ * Errors: GQMM_ERR_NULL, GQMM_ERR_SHAPE, GQMM_ERR_UNSUPPORTED, GQMM_ERR_ALIGN, GQMM_ERR_CUDA.
+ */
+GQMM_API int gqmm_gather_qmm_nn_simt(const void* x, const void* wq, const void* scales, const void* biases,
+                                    const uint32_t* idx, int64_t T, int A, int K, int N, int E,
+                                    int group_size, int bits, int x_shared, void* y, gqmm_stream_t stream);
 
 /*
  * gqmm_gather_qmm_simt -- the same operation computed on CUDA cores, one thread per output
@@ -382,7 +404,7 @@ GQMM_API void gqmm_test_stall_next(int n);
 #define GQMM_VARIANT_SPLIT_K 5        /* K split into slices, fp32 partial sums + finalize */
 #define GQMM_VARIANT_GEMV 6           /* weight-streaming CUDA-core kernel: routed chunks of 1-2 rows, dense 1 row */
 #define GQMM_VARIANT_GEMV_MMA 7       /* weight-streaming MMA kernel, dense calls of 2 to 8 rows */
-#define GQMM_VARIANT_NN 8             /* gqmm_gather_qmm_nn (transpose=False), CUDA cores */
+#define GQMM_VARIANT_NN 8             /* gqmm_gather_qmm_nn (transpose=False) calls, on the tcgen05 GEMM */
 #define GQMM_VARIANT_ROUTE_FUSED 9    /* unsorted routed decode (<= 64 rows) planned inside the streaming kernel */
 #define GQMM_VARIANT_COUNT 10
 GQMM_API int64_t gqmm_dispatch_count(int variant);

@@ -19,7 +19,7 @@ import torch
 __all__ = [
     "GqmmError", "library_path", "load_library", "gqmm_quantize", "gqmm_workspace_size",
     "new_workspace", "gqmm_route_sort", "gqmm_gather_qmm", "gqmm_gather_qmm_simt",
-    "gqmm_moe_mlp_workspace_size", "new_mlp_workspace", "gqmm_moe_mlp", "gqmm_gather_qmm_nn",
+    "gqmm_moe_mlp_workspace_size", "new_mlp_workspace", "gqmm_moe_mlp", "gqmm_gather_qmm_nn", "gqmm_gather_qmm_nn_simt",
     "gqmm_device_status", "gqmm_status_string", "launch_count", "kernel_timer",
     "kernel_timer_read", "dispatch_count", "test_stall_next", "STATUS_BAD_INDEX", "STATUS_NOT_SORTED",
     "STATUS_TIMEOUT", "VARIANTS", "MAX_EXPERTS", "ACTIVATIONS", "MODES", "gqmm_quantize_fp", "gqmm_gather_qmm_fp",
@@ -73,7 +73,8 @@ def load_library():
             "gqmm_quantize_fp": ([P, I64, I64, I64, I, P, P, P, P], I),
             "gqmm_gather_qmm_fp": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P, SZ, P], I),
             "gqmm_gather_qmm_simt": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P], I),
-            "gqmm_gather_qmm_nn": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P], I),
+            "gqmm_gather_qmm_nn": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, I, P, P, SZ, P], I),
+            "gqmm_gather_qmm_nn_simt": ([P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P], I),
             "gqmm_moe_mlp_workspace_size": ([I64, I, I, I], SZ),
             "gqmm_moe_mlp": ([P, P, P, P, P, P, P, P, I64, I, I, I, I, I, I, I, I, I, P, P, SZ, P], I),
             "gqmm_device_status": ([P, P], I),
@@ -297,13 +298,8 @@ def gqmm_gather_qmm_simt(x, wq, scales, biases, idx, group_size: int = 64, bits:
     return y
 
 
-def gqmm_gather_qmm_nn(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
-                       idx: Optional[torch.Tensor], group_size: int = 64, bits: int = 4,
-                       y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
-    """gather_qmm with transpose=False: y[t, a, :] = x[t, a, :] . deq(W[idx[t, a]]), W[e] [K, N]
-    quantized along N.  x bf16 [T, A, K] (or [T, K], shared by the A rows, or [n, K]); wq uint8
-    [E, K, N/2] and scales/biases [E, K, N/group_size], as gqmm_quantize writes for an [E, K, N]
-    weight; idx as for gqmm_gather_qmm.  Returns y bf16 [..., N]."""
+def _nn_shapes(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, idx: Optional[torch.Tensor],
+               group_size: int):
     _need(x, "x", torch.bfloat16)
     if idx is not None and (not idx.is_cuda or not idx.is_contiguous() or idx.element_size() != 4):
         raise ValueError("idx must be a contiguous 32-bit CUDA tensor")
@@ -313,14 +309,46 @@ def gqmm_gather_qmm_nn(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, 
     E, N = wq.shape[0], wq.shape[2] * 2
     _check_groups(scales, N, group_size, "scales")
     T, A, _, _, _ = _gather_shapes(x, idx, wq)
+    return T, A, K, N, E
+
+
+def gqmm_gather_qmm_nn(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
+                       idx: Optional[torch.Tensor], group_size: int = 64, bits: int = 4,
+                       sorted_indices: bool = False, y: Optional[torch.Tensor] = None,
+                       ws: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """gather_qmm with transpose=False: y[t, a, :] = x[t, a, :] . deq(W[idx[t, a]]), W[e] [K, N]
+    quantized along N.  x bf16 [T, A, K] (or [T, K], shared by the A rows, or [n, K]); wq uint8
+    [E, K, N/2] and scales/biases [E, K, N/group_size], as gqmm_quantize writes for an [E, K, N]
+    weight; idx, sorted_indices and ws as for gqmm_gather_qmm (the workspace sized for N output
+    columns).  Returns y bf16 [..., N]."""
+    T, A, K, N, E = _nn_shapes(x, wq, scales, idx, group_size)
+    _need(wq, "wq", torch.uint8)
+    _need(scales, "scales", torch.bfloat16)
+    _need(biases, "biases", torch.bfloat16)
     if y is None:
         y = torch.empty(_out_shape(x, T, A, N), dtype=torch.bfloat16, device=x.device)
     else:
         _need(y, "y", torch.bfloat16)
+    if ws is None:
+        ws = new_workspace(T * A, N, E, x.device)
     lib = load_library()
     _check(lib.gqmm_gather_qmm_nn(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(idx), T, A, K, N, E,
-                                  group_size, bits, _x_shared(x, T, A, K), _ptr(y), _stream(stream, x.device)),
-           "gqmm_gather_qmm_nn")
+                                  group_size, bits, 1 if sorted_indices else 0, _x_shared(x, T, A, K), _ptr(y),
+                                  _ptr(ws), ws.numel(), _stream(stream, x.device)), "gqmm_gather_qmm_nn")
+    return y
+
+
+def gqmm_gather_qmm_nn_simt(x: torch.Tensor, wq: torch.Tensor, scales: torch.Tensor, biases: torch.Tensor,
+                            idx: Optional[torch.Tensor], group_size: int = 64, bits: int = 4,
+                            y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """CUDA-core cross-check of gqmm_gather_qmm_nn (same arguments, no workspace; any K >= 1)."""
+    T, A, K, N, E = _nn_shapes(x, wq, scales, idx, group_size)
+    if y is None:
+        y = torch.empty(_out_shape(x, T, A, N), dtype=torch.bfloat16, device=x.device)
+    lib = load_library()
+    _check(lib.gqmm_gather_qmm_nn_simt(_ptr(x), _ptr(wq), _ptr(scales), _ptr(biases), _ptr(idx), T, A, K, N, E,
+                                       group_size, bits, _x_shared(x, T, A, K), _ptr(y), _stream(stream, x.device)),
+           "gqmm_gather_qmm_nn_simt")
     return y
 
 

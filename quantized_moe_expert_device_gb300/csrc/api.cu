@@ -9,6 +9,7 @@
 #include <string>
 #include <vector>
 
+#include "formats.cuh"
 #include "gqmm_internal.cuh"
 #include "gemm_nn.cuh"
 #include "mlp.cuh"
@@ -144,6 +145,30 @@ int validate_gather_fp(const void* x, const void* wq, const void* scales, const 
   return GQMM_OK;
 }
 
+// gqmm_gather_qmm_nn's weights: W[e] is [K, N] with 4-bit affine codes grouped along N.  The
+// tensor-core path copies one k-block (64 k-rows) of a unit's 256 columns per TMA box, so K is
+// a multiple of 64 and a code row (N/2 bytes) a multiple of 16 bytes.
+int validate_gather_nn(const void* x, const void* wq, const void* scales, const void* biases, const uint32_t* idx,
+                       int64_t T, int A, int K, int N, int E, int group_size, int bits, const void* y) {
+  if (!x || !wq || !scales || !biases || !y) return fail(GQMM_ERR_NULL, "x, wq, scales, biases and y must be non-NULL");
+  if ((group_size != 32 && group_size != 64 && group_size != 128) || bits != 4)
+    return fail(GQMM_ERR_UNSUPPORTED, "need group_size 32, 64 or 128 and bits=4 (got %d, %d)", group_size, bits);
+  if (T < 1 || A < 1 || T * (int64_t)A > 2147483647LL)
+    return fail(GQMM_ERR_SHAPE, "need T >= 1, A >= 1, T*A < 2^31 (got T=%lld A=%d)", (long long)T, A);
+  if (K <= 0 || K % 64) return fail(GQMM_ERR_SHAPE, "K must be a positive multiple of 64 (got %d)", K);
+  if (N <= 0 || N % 32 || N % group_size)
+    return fail(GQMM_ERR_SHAPE, "N must be a positive multiple of 32 and of group_size (got %d, %d)", N, group_size);
+  if (E < 1) return fail(GQMM_ERR_SHAPE, "E must be >= 1 (got %d)", E);
+  if (E > GQMM_MAX_EXPERTS) return fail(GQMM_ERR_UNSUPPORTED, "E=%d exceeds %d", E, GQMM_MAX_EXPERTS);
+  if ((int64_t)E * K > 2147483647LL || (int64_t)E * N > 2147483647LL)
+    return fail(GQMM_ERR_SHAPE, "E*K and E*N must be < 2^31");
+  if (!idx && E != 1) return fail(GQMM_ERR_NULL, "idx may be NULL only for the dense case E == 1");
+  if (!aligned(x, 16) || !aligned(wq, 16) || !aligned(scales, 2) || !aligned(biases, 2) || !aligned(y, 16))
+    return fail(GQMM_ERR_ALIGN, "x, wq and y must be 16-byte aligned, scales and biases 2-byte aligned");
+  if (idx && !aligned(idx, 4)) return fail(GQMM_ERR_ALIGN, "idx must be 4-byte aligned");
+  return GQMM_OK;
+}
+
 int validate_shared(int x_shared, const uint32_t* idx) {
   if (x_shared != 0 && x_shared != 1) return fail(GQMM_ERR_SHAPE, "x_shared must be 0 or 1");
   if (x_shared && !idx) return fail(GQMM_ERR_NULL, "x_shared needs idx (a token's rows are its A routed rows)");
@@ -210,8 +235,9 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
                           const uint32_t* idx, int64_t T, int A, int H, int F, int E, int group_size, int bits,
                           int sorted, int x_shared, void* y, void* ws, size_t ws_bytes, cudaStream_t s,
                           bool allow_split, bool clear_header, int kind, const float* tscale) {
-  int rc = kind == 0 ? validate_gather(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y)
-                     : validate_gather_fp(x, wq, scales, tscale, idx, T, A, H, F, E, kind, y);
+  int rc = kind == kAffine     ? validate_gather(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y)
+           : kind == kAffineNn ? validate_gather_nn(x, wq, scales, biases, idx, T, A, H, F, E, group_size, bits, y)
+                               : validate_gather_fp(x, wq, scales, tscale, idx, T, A, H, F, E, kind, y);
   if (rc) return rc;
   rc = validate_shared(x_shared, idx);
   if (rc) return rc;
@@ -225,7 +251,8 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   // the weight-streaming kernels take 4-bit affine codes in 64-wide groups
   if (group_size != 64 || !affine4) shape.stream = false;
   // formats with code windows wider than 32 bytes have only the narrow tensor-core variant
-  const bool wide_ok = affine4 || (kind == 0 && bits == 2) || kind == GQMM_MODE_MXFP4 || kind == GQMM_MODE_NVFP4;
+  const bool wide_ok = affine4 || (kind == 0 && bits == 2) || kind == GQMM_MODE_MXFP4 || kind == GQMM_MODE_NVFP4 ||
+                       kind == kAffineNn;
   if (!wide_ok && shape.chunk_rows > kChunkRowsNarrow) shape.chunk_rows = kChunkRowsNarrow;
   if (!aligned(ws, 256) || ws_bytes < L.total)
     return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
@@ -302,10 +329,11 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   ga.idx = idx;
   ga.fused_plan = fused ? 1 : 0;
   ga.kind = kind;
-  ga.bits = kind == 0 ? bits : 4;
+  ga.bits = kind == kAffine ? bits : 4;
   ga.tscale = tscale;
-  rc = launch_projection(ga, shape, sms, s, "gather_qmm", route_variant);
+  rc = launch_projection(ga, shape, sms, s, kind == kAffineNn ? "gather_qmm_nn" : "gather_qmm", route_variant);
   if (rc) return rc;
+  if (kind == kAffineNn) count_variant(GQMM_VARIANT_NN);
   return ok();
 }
 
@@ -535,8 +563,15 @@ int gqmm_moe_mlp(const void* x, const void* wq_gu, const void* sc_gu, const void
 }
 
 int gqmm_gather_qmm_nn(const void* x, const void* wq, const void* scales, const void* biases, const uint32_t* idx,
-                       int64_t T, int A, int K, int N, int E, int group_size, int bits, int x_shared, void* y,
-                       gqmm_stream_t stream) {
+                       int64_t T, int A, int K, int N, int E, int group_size, int bits, int sorted, int x_shared,
+                       void* y, void* ws, size_t ws_bytes, gqmm_stream_t stream) {
+  return gqmm::gather_qmm_impl(x, wq, scales, biases, idx, T, A, K, N, E, group_size, bits, sorted, x_shared, y, ws,
+                               ws_bytes, reinterpret_cast<cudaStream_t>(stream), true, false, gqmm::kAffineNn, nullptr);
+}
+
+int gqmm_gather_qmm_nn_simt(const void* x, const void* wq, const void* scales, const void* biases,
+                            const uint32_t* idx, int64_t T, int A, int K, int N, int E, int group_size, int bits,
+                            int x_shared, void* y, gqmm_stream_t stream) {
   if (!x || !wq || !scales || !biases || !y) return fail(GQMM_ERR_NULL, "x, wq, scales, biases and y must be non-NULL");
   if ((group_size != 32 && group_size != 64 && group_size != 128) || bits != 4)
     return fail(GQMM_ERR_UNSUPPORTED, "need group_size 32, 64 or 128 and bits=4 (got %d, %d)", group_size, bits);
@@ -566,7 +601,6 @@ int gqmm_gather_qmm_nn(const void* x, const void* wq, const void* scales, const 
   if (timed) timer_end(s, slot);
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "transpose=False launch: %s", cudaGetErrorString(e));
   g_launches.fetch_add(1);
-  count_variant(GQMM_VARIANT_NN);
   return ok();
 }
 

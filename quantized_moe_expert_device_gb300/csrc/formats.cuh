@@ -26,7 +26,7 @@
 
 namespace gqmm {
 
-enum WeightKind { kAffine = 0, kMxfp4 = 1, kNvfp4 = 2, kMxfp8 = 3 };
+enum WeightKind { kAffine = 0, kMxfp4 = 1, kNvfp4 = 2, kMxfp8 = 3, kAffineNn = 4 };
 
 template <int GS_, int BITS_>
 struct FmtAffine {
@@ -53,6 +53,20 @@ struct FmtNv {
   static constexpr int BITS = 4;
   static constexpr int CB = 32;
   static constexpr int W = CB;
+};
+
+// transpose=False (mlx PR #4023, the author's follow-up): W[e] is [K, N] with 4-bit affine codes
+// in groups of GS along N, so one k-block of a unit is a tile of 64 k-rows x 256 n-codes (128
+// bytes each, 8 KB like the other 4-bit stages), copied unswizzled; a dequant thread builds the
+// K-major row of one output column n from one nibble of each of the 64 k-rows, with the scale and
+// bias of (k, n / GS).  The same MMA, gather and epilogue then compute y[:, n] for the unit's n.
+template <int GS_>
+struct FmtNn {
+  static constexpr int KIND = kAffineNn;
+  static constexpr int GS = GS_;
+  static constexpr int BITS = 4;
+  static constexpr int CB = 32;
+  static constexpr int W = 32;  // code stage bytes = 256 rows x 32 = 64 k-rows x 128 bytes
 };
 
 // TMA x coordinate (bytes) of k-block kb's code window, and the codes' offset in it.

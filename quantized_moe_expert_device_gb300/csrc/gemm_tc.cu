@@ -252,7 +252,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int GS = FMT::GS;
   static_assert(FMT::KIND != kAffine || GS == 32 || GS == 64 || GS == 128, "group sizes");
   const int num_kb = H / BK;
-  const int G = H / GS;  // scale groups per weight row
+  // scale groups per weight row (transpose=False: per k-row, along the N = F output columns)
+  const int G = (FMT::KIND == kAffineNn ? F : H) / GS;
 
   // Unit queue: the scheduler (TMA thread) pushes decoded units; every consumer warp pops
   // each entry in order and releases it once its lanes hold a copy.
@@ -319,15 +320,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(C::uq_full(slot)));  // release: the entry is visible to the waiters
         ++qi;
         if (!U.valid) break;
-        {
-          // The unit's scales and biases (its rows are contiguous, rows x H/64 bf16 each) are
+        if constexpr (FMT::KIND == kAffine) {
+          // The unit's scales and biases (its rows are contiguous, rows x H/GS bf16 each) are
           // pulled into L2 now, so the dequant threads' loads a step ahead hit L2 rather
-          // than HBM when they reach this unit.
+          // than HBM when they reach this unit.  (The other formats' scales are fetched on
+          // demand: their scale arrays are only 4-byte aligned, and bulk prefetches want 16.)
           const int rows = F - U.f0 < UM ? F - U.f0 : UM;  // a multiple of 16 (F is)
           const int64_t off = ((int64_t)U.expert * F + U.f0) * G;
           prefetch_l2_bulk(p.scales + off, (uint32_t)(rows * G * 2));
           prefetch_l2_bulk(p.biases + off, (uint32_t)(rows * G * 2));
         }
+        // codes of k-block kb: rows row0.. of the [E*F, row bytes] code matrix at byte
+        // code_window_x(kb); transpose=False: k-rows U.expert*H + 64 kb.. of the [E*K, N/2]
+        // code matrix at byte U.f0 / 2
         const int row0 = U.expert * F + U.f0;
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
           const uint32_t s = itn % NIB_STAGES, ph = (itn / NIB_STAGES) & 1u;
@@ -340,8 +345,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             continue;
           }
           mbar_arrive_expect_tx(bar(C::nib_full(s)), C::NIB_BYTES);
-          tma_load_2d(sbase + C::OFF_NIB + s * C::NIB_BYTES, &tmap_wq, bar(C::nib_full(s)), code_window_x<FMT>(kb),
-                      row0);
+          if constexpr (FMT::KIND == kAffineNn)
+            tma_load_2d(sbase + C::OFF_NIB + s * C::NIB_BYTES, &tmap_wq, bar(C::nib_full(s)), U.f0 / 2,
+                        U.expert * H + kb * BK);
+          else
+            tma_load_2d(sbase + C::OFF_NIB + s * C::NIB_BYTES, &tmap_wq, bar(C::nib_full(s)), code_window_x<FMT>(kb),
+                        row0);
           ++itn;
         }
         if (!ok) break;
@@ -586,6 +595,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         sblk = bblk = make_uint4(0, 0, 0, 0);
         return;
       }
+      if constexpr (FMT::KIND == kAffineNn) {
+        // The warp's 32 output columns lie in one scale group (GS >= 32; units start on multiples
+        // of 256): lane l holds (s, b) of k = 64 kb + 2l and 2l + 1 as bf16 pairs, shuffled to
+        // the whole warp while dequantizing.
+        const int64_t at = ((int64_t)U.expert * H + (int64_t)kb * BK + 2 * lane) * G + (U.f0 + (r & ~31)) / GS;
+        sblk.x = (uint32_t)__ldg(sc16 + at) | ((uint32_t)__ldg(sc16 + at + G) << 16);
+        bblk.x = (uint32_t)__ldg(bs16 + at) | ((uint32_t)__ldg(bs16 + at + G) << 16);
+        return;
+      }
       const int64_t row = (int64_t)(U.expert * F + U.f0) + r;  // E * F fits in int
       if constexpr (FMT::KIND != kAffine) {
         const uint8_t* sc8 = reinterpret_cast<const uint8_t*>(p.scales);
@@ -628,6 +646,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && U.valid) {
       const int g = grp_of(kb);
       const uint32_t s2 = pick(sblk, g, false), b2 = pick(bblk, g, false);
+      const uint32_t nn_s = sblk.x, nn_b = bblk.x;  // transpose=False: this lane's k pair
       // floating-point formats: the float32 scale of each 16 weights of the k-block
       float sc4[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (FMT::KIND == kNvfp4) {
@@ -658,7 +677,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // is an async-proxy write, which is not ordered after these generic-proxy reads by the
       // mbarrier alone.
       uint4 o[8];
-      if constexpr (FMT::KIND == kAffine && FMT::BITS == 4) {
+      if constexpr (FMT::KIND == kAffineNn) {
+        // output column n = U.f0 + r: nibble r of each of the k-block's 64 code rows (128 bytes
+        // each; even n in the low nibble), two k per bf16x2 FMA with the pair's scales and
+        // biases from lane j (zero past F: the warp's columns are all live or all dead)
+        const uint32_t tile = nib_tile - (uint32_t)(r * C::W) + (uint32_t)(r >> 1);
+        const uint32_t sh = (uint32_t)(r & 1) * 4u;
+        uint32_t* out = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          uint32_t c0, c1;
+          asm volatile("ld.shared.u8 %0, [%1];" : "=r"(c0) : "r"(tile + (uint32_t)(2 * j) * 128u) : "memory");
+          asm volatile("ld.shared.u8 %0, [%1];" : "=r"(c1) : "r"(tile + (uint32_t)(2 * j + 1) * 128u) : "memory");
+          const uint32_t p2 = ((c0 >> sh) & 0xFu) | (((c1 >> sh) & 0xFu) << 16) | 0x43004300u;
+          out[j] = deq_pair(p2, __shfl_sync(0xffffffffu, nn_s, j), __shfl_sync(0xffffffffu, nn_b, j));
+        }
+      } else if constexpr (FMT::KIND == kAffine && FMT::BITS == 4) {
         uint4 n0, n1;
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
                      : "=r"(n0.x), "=r"(n0.y), "=r"(n0.z), "=r"(n0.w)
@@ -821,6 +855,12 @@ cudaError_t configure_all() {
   need(set_smem<CfgNarrow, FmtMx<false>>());
   need(set_smem<CfgNarrow, FmtNv>());
   need(set_smem<CfgNarrow64, FmtMx<true>>());
+  need(set_smem<CfgWide, FmtNn<32>>());
+  need(set_smem<CfgWide, FmtNn<64>>());
+  need(set_smem<CfgWide, FmtNn<128>>());
+  need(set_smem<CfgNarrow, FmtNn<32>>());
+  need(set_smem<CfgNarrow, FmtNn<64>>());
+  need(set_smem<CfgNarrow, FmtNn<128>>());
   return e;
 }
 
@@ -839,6 +879,9 @@ using FmtA6 = FmtAffine<64, 6>;
 using FmtA8 = FmtAffine<64, 8>;
 using FmtMxfp4 = FmtMx<false>;
 using FmtMxfp8 = FmtMx<true>;
+using FmtNn32 = FmtNn<32>;
+using FmtNn64 = FmtNn<64>;
+using FmtNn128 = FmtNn<128>;
 
 GemmKernel pick_instance(const GemmArgs& a, bool narrow, int* smem) {
 #define GQMM_PICK(CFG, FMT)      \
@@ -855,6 +898,16 @@ GemmKernel pick_instance(const GemmArgs& a, bool narrow, int* smem) {
     if (a.group_size == 32) GQMM_PICK(CfgWide, FmtA4g32);
     if (a.group_size == 128) GQMM_PICK(CfgWide, FmtA4g128);
     GQMM_PICK(CfgWide, FmtA4g64);
+  }
+  if (a.kind == kAffineNn) {
+    if (narrow) {
+      if (a.group_size == 32) GQMM_PICK(CfgNarrow, FmtNn32);
+      if (a.group_size == 128) GQMM_PICK(CfgNarrow, FmtNn128);
+      GQMM_PICK(CfgNarrow, FmtNn64);
+    }
+    if (a.group_size == 32) GQMM_PICK(CfgWide, FmtNn32);
+    if (a.group_size == 128) GQMM_PICK(CfgWide, FmtNn128);
+    GQMM_PICK(CfgWide, FmtNn64);
   }
   if (a.kind == kAffine && a.bits == 2) {
     if (narrow) GQMM_PICK(CfgNarrow16, FmtA2);
@@ -924,17 +977,22 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   // Packed codes as an [E*F, row bytes] byte matrix; one box = the unit's 256 rows x one k-block's
   // code window (W bytes: formats.cuh), 32-byte swizzled when W is 32 so the dequant threads read
   // it without bank conflicts.  Every window starts on a 16-byte boundary.
+  // transpose=False: codes as an [E*K, N/2] byte matrix; one box = 64 k-rows (one k-block) x the
+  // unit's 256 columns (128 bytes), unswizzled; columns past N read as zero.
+  const bool nn = a.kind == kAffineNn;
   const int code_bits = a.kind == kMxfp8 ? 8 : a.kind == kAffine ? a.bits : 4;
   const int W = code_bits == 3 || code_bits == 5 ? 48 : 8 * code_bits;
-  const int64_t row_bytes = (int64_t)a.H * code_bits / 8;
+  const int64_t row_bytes = nn ? (int64_t)a.F / 2 : (int64_t)a.H * code_bits / 8;
+  const int64_t code_rows = (int64_t)a.E * (nn ? a.H : a.F);
   CUtensorMap map_wq;
-  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)a.E * (cuuint64_t)a.F};
+  const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)code_rows};
   const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  const cuuint32_t box[2] = {(cuuint32_t)W, UM};
+  const cuuint32_t box[2] = {nn ? (cuuint32_t)(UM / 2) : (cuuint32_t)W, nn ? (cuuint32_t)BK : (cuuint32_t)UM};
   const cuuint32_t estr[2] = {1, 1};
+  const CUtensorMapSwizzle swz = !nn && W == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUresult cr = encode(&map_wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.wq), dims, strides, box,
-                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, W == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                       estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (cr != CUDA_SUCCESS) return cudaErrorInvalidValue;
   // x as a [n, H] bf16 matrix; one box = 64 columns (one k-block, 128 bytes) of one row, for
   // tile::gather4 into the 128-byte-swizzled B tile.

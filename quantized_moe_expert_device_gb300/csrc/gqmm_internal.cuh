@@ -204,7 +204,7 @@ struct GemmArgs {
   int ks_cap;           // > 1: the plan step may split K (header->ksplit) and the finalize runs
   int dense_plan;       // 1: idx is NULL, so the plan is the single chunk (expert 0, start 0, n rows)
   int group_size = 64;  // quantization group along H: 32, 64 or 128 (the streaming kernels: 64)
-  int kind = 0;         // weight format: 0 affine, 1 mxfp4, 2 nvfp4, 3 mxfp8 (formats.cuh)
+  int kind = 0;         // weight format (formats.cuh): 0 affine, 1 mxfp4, 2 nvfp4, 3 mxfp8, 4 affine transpose=False
   int bits = 4;         // affine code width: 2, 3, 4, 5, 6 or 8
   const float* tscale = nullptr;  // nvfp4: float32 scale per expert [E]
   int test_stall = 0;   // 1: leave the first k-block's codes uncopied (gqmm_test_stall_next)

@@ -42,7 +42,7 @@ def test_binding_covers_the_boundary():
     lib = g.load_library()
     for name in ("gqmm_quantize", "gqmm_route_sort", "gqmm_gather_qmm", "gqmm_workspace_size",
                  "gqmm_device_status", "gqmm_gather_qmm_simt", "gqmm_moe_mlp", "gqmm_moe_mlp_workspace_size",
-                 "gqmm_gather_qmm_nn"):
+                 "gqmm_gather_qmm_nn", "gqmm_gather_qmm_nn_simt"):
         assert hasattr(g, name)
         assert getattr(lib, name).argtypes is not None
 
@@ -141,12 +141,48 @@ def test_mlp_validation_rejects_bad_arguments_without_a_gpu(lib):
 
 
 def test_nn_validation_rejects_bad_arguments_without_a_gpu(lib):
-    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
     f = lib.gqmm_gather_qmm_nn
-    f.argtypes = [P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P]
+    f.argtypes = [P, P, P, P, P, I64, I, I, I, I, I, I, I, I, P, P, SZ, P]
     f.restype = I
     fake = P(0x10000)  # never dereferenced: every call below fails validation first
-    args = dict(x=fake, wq=fake, sc=fake, bs=fake, idx=fake, T=16, A=2, K=256, N=128, E=8, gs=64, bits=4, shared=0,
+    args = dict(x=fake, wq=fake, sc=fake, bs=fake, idx=fake, T=16, A=2, K=256, N=128, E=8, gs=64, bits=4, sorted=0,
+                shared=0, y=fake, ws=fake, wsb=1 << 30, s=None)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return f(a["x"], a["wq"], a["sc"], a["bs"], a["idx"], a["T"], a["A"], a["K"], a["N"], a["E"], a["gs"],
+                 a["bits"], a["sorted"], a["shared"], a["y"], a["ws"], a["wsb"], a["s"])
+
+    assert call(wq=None) == 1                 # ERR_NULL
+    assert call(gs=96) == 3                   # ERR_UNSUPPORTED
+    assert call(bits=2) == 3
+    assert call(N=96) == 2                    # ERR_SHAPE: N must be a multiple of the group size
+    assert call(N=48, gs=32) == 2             # and of 32 (a code row fills whole 16-byte units)
+    assert call(K=0) == 2
+    assert call(K=300) == 2                   # K a multiple of the 64-wide k-block
+    assert call(T=0) == 2
+    assert call(E=0) == 2
+    assert call(E=2048) == 3
+    assert call(idx=None) == 1                # dense needs E == 1
+    assert call(shared=2) == 2
+    assert call(shared=1, idx=None, E=1) == 1
+    assert call(sorted=2) == 2
+    assert call(y=P(0x10008)) == 4            # ERR_ALIGN: y is stored 16 bytes at a time
+    assert call(x=P(0x10008)) == 4            # x rows are copied by TMA
+    assert call(wq=P(0x10004)) == 4
+    assert call(ws=None) == 1
+    assert call(wsb=16) == 5                  # ERR_WORKSPACE
+
+
+def test_nn_simt_validation_rejects_bad_arguments_without_a_gpu(lib):
+    P, I, I64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+    f = lib.gqmm_gather_qmm_nn_simt
+    f.argtypes = [P, P, P, P, P, I64, I, I, I, I, I, I, I, P, P]
+    f.restype = I
+    fake = P(0x10000)
+    args = dict(x=fake, wq=fake, sc=fake, bs=fake, idx=fake, T=16, A=2, K=300, N=128, E=8, gs=64, bits=4, shared=0,
                 y=fake, s=None)
 
     def call(**kw):
@@ -155,19 +191,12 @@ def test_nn_validation_rejects_bad_arguments_without_a_gpu(lib):
         return f(a["x"], a["wq"], a["sc"], a["bs"], a["idx"], a["T"], a["A"], a["K"], a["N"], a["E"], a["gs"],
                  a["bits"], a["shared"], a["y"], a["s"])
 
-    assert call(wq=None) == 1                 # ERR_NULL
-    assert call(gs=96) == 3                   # ERR_UNSUPPORTED
-    assert call(bits=2) == 3
-    assert call(N=96) == 2                    # ERR_SHAPE: N must be a multiple of the group size
+    assert call(wq=None) == 1
+    assert call(gs=96) == 3
+    assert call(N=96) == 2
     assert call(K=0) == 2
-    assert call(T=0) == 2
-    assert call(E=0) == 2
-    assert call(E=2048) == 3
-    assert call(idx=None) == 1                # dense needs E == 1
-    assert call(shared=2) == 2
-    assert call(shared=1, idx=None, E=1) == 1
-    assert call(y=P(0x10008)) == 4            # ERR_ALIGN: y is stored 16 bytes at a time
-    assert call(wq=P(0x10004)) == 4
+    assert call(idx=None) == 1
+    assert call(y=P(0x10008)) == 4
 
 
 def test_fp_mode_validation_rejects_bad_arguments_without_a_gpu(lib):

@@ -1,8 +1,13 @@
 """gqmm_gather_qmm_nn (transpose=False: W[e] = [K, N] quantized along N) on the GPU against the
-oracle's float64 gather_qmm_nn, on the GPU's own quantized weights (bit-equal to the oracle's):
-the shape of the pages' transpose=False timing (E=4, K=N=512, 1024 rows), every group size, K
-over several 1024-wide x chunks with a ragged tail, N not a multiple of the 1024-column block,
-dense E=1, invalid indices and a shared x."""
+oracle's float64 gather_qmm_nn, on the GPU's own quantized weights (bit-equal to the oracle's).
+
+The tensor-core path: the shape of the pages' transpose=False timing (E=4, K=N=512, 1024 rows),
+every group size, both GEMM variants (wide chunks of up to 256 rows, narrow ones of up to 32), N
+not a multiple of the 256-column unit, a decode-sized call that splits K, dense E=1, invalid
+indices, a shared x, and caller-sorted indices equal to the unsorted call bit for bit.  The
+CUDA-core cross-check gqmm_gather_qmm_nn_simt takes any K; it is checked on K that are not
+multiples of 64 as well.  Tolerances are the gather's (relative Frobenius error <= 5e-3, every
+element within 2e-2 * max|y_ref|): weights are decoded exactly and rounded once to bfloat16."""
 import numpy as np
 import pytest
 import torch
@@ -25,24 +30,30 @@ def _weights(E, K, N, gs, seed):
     return host, dev
 
 
-@pytest.mark.parametrize("T,A,K,N,E,gs", [(1024, 1, 512, 512, 4, 64),    # the pages' transpose=False shape
-                                          (16, 2, 256, 256, 8, 32),
-                                          (7, 3, 3000, 1152, 5, 128),    # K: three x chunks, ragged; N: 1.1 blocks
-                                          (4, 8, 2048, 768, 64, 64),
-                                          (5, 1, 300, 96, 1, 32)])       # dense (idx None)
+NN_CASES = [(1024, 1, 512, 512, 4, 64),     # the pages' transpose=False shape (wide chunks)
+            (16, 2, 256, 256, 8, 32),       # narrow chunks
+            (7, 3, 3072, 1152, 5, 128),     # N = 4.5 units of 256 columns
+            (4, 8, 2048, 768, 64, 64),
+            (2, 4, 4096, 512, 4, 64),       # decode-sized: K split into slices
+            (5, 1, 320, 96, 1, 32),         # dense (idx None), N below one unit
+            (300, 2, 192, 32, 3, 32)]       # the smallest N, ragged chunk tails
+
+
+@pytest.mark.parametrize("T,A,K,N,E,gs", NN_CASES)
 def test_nn_matches_oracle(T, A, K, N, E, gs):
     import quantized_moe_expert_device_gb300 as g
 
     host, dev = _weights(E, K, N, gs, seed=81)
     x = wl.normal_bf16((T, A, K) if E > 1 else (T, K), 82)
     idx = None if E == 1 else np.random.default_rng(T + K).integers(0, E, size=(T, A)).astype(np.uint32)
-    y = g.gqmm_gather_qmm_nn(x.cuda(), *dev, None if idx is None else to_dev_idx(idx), group_size=gs)
-    torch.cuda.synchronize()
+    ws = g.new_workspace(T * A, N, E)
+    y = g.gqmm_gather_qmm_nn(x.cuda(), *dev, None if idx is None else to_dev_idx(idx), group_size=gs, ws=ws)
+    assert g.gqmm_device_status(ws) == 0
     assert y.shape[-1] == N
     assert_parity(y, oracle.gather_qmm_nn(x, *host, idx, E, group_size=gs), f"nn T={T} A={A} K={K} N={N} E={E}")
 
 
-def test_nn_invalid_indices_and_shared_x():
+def test_nn_invalid_indices_shared_x_and_sorted():
     import quantized_moe_expert_device_gb300 as g
 
     T, A, K, N, E = 12, 4, 512, 256, 6
@@ -50,10 +61,44 @@ def test_nn_invalid_indices_and_shared_x():
     x = wl.normal_bf16((T, K), 84)
     idx = np.random.default_rng(8).integers(0, E, size=(T, A)).astype(np.uint32)
     idx[::3, 2] = E + 1
-    y = g.gqmm_gather_qmm_nn(x.cuda(), *dev, to_dev_idx(idx))           # x [T, K] shared by the A rows
+    ws = g.new_workspace(T * A, N, E)
+    y = g.gqmm_gather_qmm_nn(x.cuda(), *dev, to_dev_idx(idx), ws=ws)          # x [T, K] shared by the A rows
+    assert g.gqmm_device_status(ws) & g.STATUS_BAD_INDEX
     x_rep = x.repeat_interleave(A, dim=0).reshape(T, A, K)
     y_rep = g.gqmm_gather_qmm_nn(x_rep.cuda(), *dev, to_dev_idx(idx))
     torch.cuda.synchronize()
     assert y.shape == (T, A, N) and torch.equal(y, y_rep)
     assert not y[::3, 2].float().abs().sum().item()
     assert_parity(y, oracle.gather_qmm_nn(x_rep, *host, idx, E), "nn invalid + shared")
+    # caller-sorted indices through the sorted-route plan equal the unsorted call bit for bit
+    idx_s = np.sort(np.random.default_rng(9).integers(0, E, size=T * A)).astype(np.uint32).reshape(-1, 1)
+    xs = wl.normal_bf16((T * A, 1, K), 85).cuda()
+    y_s = g.gqmm_gather_qmm_nn(xs, *dev, to_dev_idx(idx_s), sorted_indices=True)
+    y_u = g.gqmm_gather_qmm_nn(xs, *dev, to_dev_idx(idx_s), sorted_indices=False)
+    torch.cuda.synchronize()
+    assert torch.equal(y_s, y_u)
+
+
+@pytest.mark.parametrize("T,A,K,N,E,gs", [(16, 2, 256, 256, 8, 32),
+                                          (7, 3, 3000, 1152, 5, 128),   # K not a multiple of 64
+                                          (5, 1, 300, 96, 1, 32)])
+def test_nn_simt_cross_check_matches_oracle(T, A, K, N, E, gs):
+    import quantized_moe_expert_device_gb300 as g
+
+    host, dev = _weights(E, K, N, gs, seed=86)
+    x = wl.normal_bf16((T, A, K) if E > 1 else (T, K), 87)
+    idx = None if E == 1 else np.random.default_rng(T + K).integers(0, E, size=(T, A)).astype(np.uint32)
+    y = g.gqmm_gather_qmm_nn_simt(x.cuda(), *dev, None if idx is None else to_dev_idx(idx), group_size=gs)
+    torch.cuda.synchronize()
+    assert_parity(y, oracle.gather_qmm_nn(x, *host, idx, E, group_size=gs), f"nn simt T={T} A={A} K={K} N={N}")
+
+
+def test_nn_rejects_k_not_a_multiple_of_64():
+    import quantized_moe_expert_device_gb300 as g
+
+    _, dev = _weights(2, 320 - 32, 128, 64, seed=88)
+    x = wl.normal_bf16((4, 288), 89).cuda()
+    idx = to_dev_idx(np.zeros((4, 1), np.uint32))
+    with pytest.raises(g.GqmmError) as ei:
+        g.gqmm_gather_qmm_nn(x, *dev, idx)
+    assert ei.value.code == 2
