@@ -183,18 +183,18 @@ __device__ __forceinline__ uint32_t deq_pair(uint32_t p, uint32_t s2, uint32_t b
   return r;
 }
 
-// 8 codes (one 32-bit word, element k in bits 4k..4k+3) -> 8 bf16 in element order.
+// 8 codes (one 32-bit word, element k in bits 4k..4k+3) -> 8 bf16 in element order.  Output
+// pair j takes byte j of w (elements 2j, 2j+1 in its nibbles) into byte 0 and byte j of w >> 4
+// (element 2j+1 in its low nibble) into byte 2; the mask keeps the two low nibbles and the
+// magic makes them bf16 128 + q.
 __device__ __forceinline__ uint4 deq8(uint32_t w, uint32_t s2, uint32_t b2) {
   constexpr uint32_t kMask = 0x000F000Fu, kMagic = 0x43004300u;  // bf16 128.0 in each half
-  const uint32_t t0 = (w & kMask) | kMagic;          // elements 0, 4
-  const uint32_t t1 = ((w >> 4) & kMask) | kMagic;   // elements 1, 5
-  const uint32_t t2 = ((w >> 8) & kMask) | kMagic;   // elements 2, 6
-  const uint32_t t3 = ((w >> 12) & kMask) | kMagic;  // elements 3, 7
+  const uint32_t ws = w >> 4;
   uint4 o;
-  o.x = deq_pair(__byte_perm(t0, t1, 0x5410), s2, b2);  // (0, 1)
-  o.y = deq_pair(__byte_perm(t2, t3, 0x5410), s2, b2);  // (2, 3)
-  o.z = deq_pair(__byte_perm(t0, t1, 0x7632), s2, b2);  // (4, 5)
-  o.w = deq_pair(__byte_perm(t2, t3, 0x7632), s2, b2);  // (6, 7)
+  o.x = deq_pair((__byte_perm(w, ws, 0x0400) & kMask) | kMagic, s2, b2);  // (0, 1)
+  o.y = deq_pair((__byte_perm(w, ws, 0x0501) & kMask) | kMagic, s2, b2);  // (2, 3)
+  o.z = deq_pair((__byte_perm(w, ws, 0x0602) & kMask) | kMagic, s2, b2);  // (4, 5)
+  o.w = deq_pair((__byte_perm(w, ws, 0x0703) & kMask) | kMagic, s2, b2);  // (6, 7)
   return o;
 }
 
@@ -500,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c0 = 0; c0 < N; c0 += 16) {
             uint32_t v[16];
             tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
-            tc_wait_ld();
+            tc_wait_ld_regs(v);
             if (f < F) {
 #pragma unroll
               for (int j = 0; j < 16; ++j)
@@ -515,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c0 >= N) break;
             uint32_t v[16];
             tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
-            tc_wait_ld();
+            tc_wait_ld_regs(v);
 #pragma unroll
             for (int j = 0; j < 16; ++j)
               epi[j * 32 + lane] = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(v[j])));
