@@ -250,10 +250,6 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   const bool affine4 = kind == 0 && bits == 4;
   // the weight-streaming kernels take 4-bit affine codes in 64-wide groups
   if (group_size != 64 || !affine4) shape.stream = false;
-  // formats with code windows wider than 32 bytes have only the narrow tensor-core variant
-  const bool wide_ok = affine4 || (kind == 0 && bits == 2) || kind == GQMM_MODE_MXFP4 || kind == GQMM_MODE_NVFP4 ||
-                       kind == kAffineNn;
-  if (!wide_ok && shape.chunk_rows > kChunkRowsNarrow) shape.chunk_rows = kChunkRowsNarrow;
   if (!aligned(ws, 256) || ws_bytes < L.total)
     return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
   rc = check_device(nullptr);

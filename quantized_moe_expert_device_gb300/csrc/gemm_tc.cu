@@ -145,13 +145,17 @@ struct Cfg {
 // gives it a 7-deep A / x ring next to a 13-deep code ring.
 using CfgWide = Cfg<kChunkRowsWide, 3, 2, 8, false, 3>;
 using CfgNarrow = Cfg<kChunkRowsNarrow, 13, 3, 4, true, 7>;
-// Other code-window widths (formats.cuh): 16 bytes (2-bit affine) in both variants; 48 and 64
-// bytes (3-, 5-, 6- and 8-bit affine, mxfp8) in the narrow variant only, with as many code stages
-// as fit in the narrow variant's code ring budget (13 x 8 KB).
+// Other code-window widths (formats.cuh): 16 bytes (2-bit affine); 48 and 64 bytes (3-, 5-, 6-
+// and 8-bit affine, mxfp8), the narrow variant with as many code stages as fit in its code ring
+// budget (13 x 8 KB).
 using CfgWide16 = Cfg<kChunkRowsWide, 3, 2, 8, false, 3, 16>;
 using CfgNarrow16 = Cfg<kChunkRowsNarrow, 13, 3, 4, true, 7, 16>;
 using CfgNarrow48 = Cfg<kChunkRowsNarrow, 8, 3, 4, true, 7, 48>;
 using CfgNarrow64 = Cfg<kChunkRowsNarrow, 6, 3, 4, true, 7, 64>;
+// wide variants for 48- and 64-byte windows: a two-stage A / x ring leaves room for the larger
+// code stages (4 x 12 KB, 3 x 16 KB)
+using CfgWide48 = Cfg<kChunkRowsWide, 4, 2, 8, false, 2, 48>;
+using CfgWide64 = Cfg<kChunkRowsWide, 3, 2, 8, false, 2, 64>;
 
 __device__ __forceinline__ UnitEntry decode_unit(const Chunk* chunks, int u, int n_fpairs, int ksplit, int num_kb) {
   const int ks = u % ksplit;
@@ -855,6 +859,11 @@ cudaError_t configure_all() {
   need(set_smem<CfgNarrow, FmtMx<false>>());
   need(set_smem<CfgNarrow, FmtNv>());
   need(set_smem<CfgNarrow64, FmtMx<true>>());
+  need(set_smem<CfgWide48, FmtAffine<64, 3>>());
+  need(set_smem<CfgWide48, FmtAffine<64, 5>>());
+  need(set_smem<CfgWide48, FmtAffine<64, 6>>());
+  need(set_smem<CfgWide64, FmtAffine<64, 8>>());
+  need(set_smem<CfgWide64, FmtMx<true>>());
   need(set_smem<CfgWide, FmtNn<32>>());
   need(set_smem<CfgWide, FmtNn<64>>());
   need(set_smem<CfgWide, FmtNn<128>>());
@@ -866,9 +875,8 @@ cudaError_t configure_all() {
 
 using GemmKernel = decltype(&gemm_tc_kernel<CfgWide, FmtAffine<64, 4>>);
 
-// The kernel instance and its shared-memory size for a format and a variant (nullptr: the
-// format has no instance of that variant; formats with 48- or 64-byte code windows have only
-// the narrow one).
+// The kernel instance and its shared-memory size for a format and a variant (nullptr: no
+// instance for the format).
 using FmtA4g32 = FmtAffine<32, 4>;
 using FmtA4g64 = FmtAffine<64, 4>;
 using FmtA4g128 = FmtAffine<128, 4>;
@@ -921,12 +929,26 @@ GemmKernel pick_instance(const GemmArgs& a, bool narrow, int* smem) {
     if (narrow) GQMM_PICK(CfgNarrow, FmtNv);
     GQMM_PICK(CfgWide, FmtNv);
   }
-  if (!narrow) return nullptr;
-  if (a.kind == kMxfp8) GQMM_PICK(CfgNarrow64, FmtMxfp8);
-  if (a.kind == kAffine && a.bits == 3) GQMM_PICK(CfgNarrow48, FmtA3);
-  if (a.kind == kAffine && a.bits == 5) GQMM_PICK(CfgNarrow48, FmtA5);
-  if (a.kind == kAffine && a.bits == 6) GQMM_PICK(CfgNarrow48, FmtA6);
-  if (a.kind == kAffine && a.bits == 8) GQMM_PICK(CfgNarrow64, FmtA8);
+  if (a.kind == kMxfp8) {
+    if (narrow) GQMM_PICK(CfgNarrow64, FmtMxfp8);
+    GQMM_PICK(CfgWide64, FmtMxfp8);
+  }
+  if (a.kind == kAffine && a.bits == 8) {
+    if (narrow) GQMM_PICK(CfgNarrow64, FmtA8);
+    GQMM_PICK(CfgWide64, FmtA8);
+  }
+  if (a.kind == kAffine && a.bits == 3) {
+    if (narrow) GQMM_PICK(CfgNarrow48, FmtA3);
+    GQMM_PICK(CfgWide48, FmtA3);
+  }
+  if (a.kind == kAffine && a.bits == 5) {
+    if (narrow) GQMM_PICK(CfgNarrow48, FmtA5);
+    GQMM_PICK(CfgWide48, FmtA5);
+  }
+  if (a.kind == kAffine && a.bits == 6) {
+    if (narrow) GQMM_PICK(CfgNarrow48, FmtA6);
+    GQMM_PICK(CfgWide48, FmtA6);
+  }
 #undef GQMM_PICK
   return nullptr;
 }
