@@ -14,10 +14,13 @@
 // 94% wasted) the same kernel reads each weight tile once per call for all of its M <= 8 rows.
 //
 // Two variants (template Cfg), chosen on the host from the rows per expert:
-//   wide    chunks of <= 256 rows; 3 stages of (A 2 x 16 KB, x 32 KB, codes 8 KB)
-//   narrow  chunks of <= 32 rows; 3 stages of (A 2 x 16 KB, x 4 KB) and 13 stages of codes:
-//           with few rows the weight-code stream from HBM is the bottleneck, so the smem the
-//           x tiles do not need goes to a deeper code ring.
+//   wide    chunks of <= 256 rows; 3 stages of (A 2 x 16 KB, x 32 KB) and 3 of codes (8 KB)
+//   narrow  chunks of <= 32 rows; A in tensor memory, 7 stages of x (4 KB) and 13 stages of
+//           codes: with few rows the weight-code stream from HBM is the bottleneck, so the smem
+//           the x tiles do not need goes to a deeper code ring.
+// The kernel is also templated on the weight format (formats.cuh: affine codes of 2-8 bits,
+// mxfp4 / nvfp4 / mxfp8, and transpose=False affine weights), which sets the code tile of a
+// k-block and the dequant arithmetic; the rest is shared.
 // Calls with too few units for the GPU (dense decode: F/256 units) split K into slices; each
 // slice stores its fp32 partial sums in its own plane of a workspace buffer, and a second
 // kernel adds the planes in slice order (so results are deterministic) into bf16 y.
@@ -26,8 +29,9 @@
 // warp numbers are the wide variant's; the narrow one has 3 dequant groups, warps 0-23, 4
 // epilogue warps that drain both tiles, and 2 gather warps):
 //   warps 0-15  dequant:  two groups of 256 threads take alternate k-blocks; a thread owns one
-//                         of the unit's 256 weight rows: reads its 32 bytes of codes, computes
-//                         w = scale*q + bias in bf16x2 and writes the 64 bf16 in the
+//                         of the unit's 256 weight rows: reads its 32 bytes of codes, turns each
+//                         nibble pair into bf16 128 + q (one byte permute and one mask per pair),
+//                         computes w = scale*q + bias in bf16x2 and writes the 64 bf16 in the
 //                         128-byte-swizzle K-major A layout
 //   warps 16-23 epilogue: warp 16+e drains TMEM lanes 32(e%4).. of tile e/4: TMEM -> registers
 //                         -> bf16 -> shared transpose -> 16-byte stores to y rows perm[j]
@@ -687,14 +691,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         // biases from lane j (zero past F: the warp's columns are all live or all dead)
         const uint32_t tile = nib_tile - (uint32_t)(r * C::W) + (uint32_t)(r >> 1);
         const uint32_t sh = (uint32_t)(r & 1) * 4u;
-        uint32_t* out = reinterpret_cast<uint32_t*>(o);
+        auto piece = [&](int c) -> uint4 {  // k = 8c .. 8c + 7
+          uint32_t v[4];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          uint32_t c0, c1;
-          asm volatile("ld.shared.u8 %0, [%1];" : "=r"(c0) : "r"(tile + (uint32_t)(2 * j) * 128u) : "memory");
-          asm volatile("ld.shared.u8 %0, [%1];" : "=r"(c1) : "r"(tile + (uint32_t)(2 * j + 1) * 128u) : "memory");
-          const uint32_t p2 = ((c0 >> sh) & 0xFu) | (((c1 >> sh) & 0xFu) << 16) | 0x43004300u;
-          out[j] = deq_pair(p2, __shfl_sync(0xffffffffu, nn_s, j), __shfl_sync(0xffffffffu, nn_b, j));
+          for (int i = 0; i < 4; ++i) {
+            const int j = 4 * c + i;
+            uint32_t c0, c1;
+            asm volatile("ld.shared.u8 %0, [%1];" : "=r"(c0) : "r"(tile + (uint32_t)(2 * j) * 128u) : "memory");
+            asm volatile("ld.shared.u8 %0, [%1];" : "=r"(c1) : "r"(tile + (uint32_t)(2 * j + 1) * 128u) : "memory");
+            const uint32_t p2 = ((c0 >> sh) & 0xFu) | (((c1 >> sh) & 0xFu) << 16) | 0x43004300u;
+            v[i] = deq_pair(p2, __shfl_sync(0xffffffffu, nn_s, j), __shfl_sync(0xffffffffu, nn_b, j));
+          }
+          return make_uint4(v[0], v[1], v[2], v[3]);
+        };
+        if constexpr (!C::A_TMEM) {
+          // as the 4-bit affine rows: wait for the A stage, store each piece as it is computed
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
+          const uint32_t a_row = a_row0 + sa * A_BYTES;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = piece(c);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row ^ (uint32_t)(c << 4)), "r"(v.x),
+                         "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) o[c] = piece(c);
         }
       } else if constexpr (FMT::KIND == kAffine && FMT::BITS == 4) {
         uint4 n0, n1;
@@ -706,14 +729,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "=r"(n1.x), "=r"(n1.y), "=r"(n1.z), "=r"(n1.w)
                      : "r"(nib_tile + nib_c1)
                      : "memory");
-        o[0] = deq8(n0.x, s2, b2);
-        o[1] = deq8(n0.y, s2, b2);
-        o[2] = deq8(n0.z, s2, b2);
-        o[3] = deq8(n0.w, s2, b2);
-        o[4] = deq8(n1.x, s2b, b2b);
-        o[5] = deq8(n1.y, s2b, b2b);
-        o[6] = deq8(n1.z, s2b, b2b);
-        o[7] = deq8(n1.w, s2b, b2b);
+        const uint32_t cw[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+        if constexpr (!C::A_TMEM) {
+          // wide variant: wait for the A stage first and store each 8-weight piece as soon as it
+          // is computed, so the row's 64 bf16 are never all live in registers at once
+          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
+          const uint32_t a_row = a_row0 + sa * A_BYTES;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 v = deq8(cw[c], c < 4 ? s2 : s2b, c < 4 ? b2 : b2b);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row ^ (uint32_t)(c << 4)), "r"(v.x),
+                         "r"(v.y), "r"(v.z), "r"(v.w)
+                         : "memory");
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 8; ++c) o[c] = deq8(cw[c], c < 4 ? s2 : s2b, c < 4 ? b2 : b2b);
+        }
       } else {
         // the row's code window: W / 4 words (for 32-byte windows through the swizzle)
         uint32_t cw[C::W / 4];
@@ -740,8 +772,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           dequant_e2m1(cw, sc4, o);
         }
       }
-      if (!__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
-      if (C::A_TMEM) {
+      // (the 4-bit affine and transpose=False rows of the wide variant are already stored)
+      constexpr bool kStored = ((FMT::KIND == kAffine && FMT::BITS == 4) || FMT::KIND == kAffineNn) && !C::A_TMEM;
+      if (!kStored && !__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
+      if (kStored) {
+      } else if (C::A_TMEM) {
         // the row's 64 bf16 into the warp's TMEM lane quarter, 32 columns of the A stage
         tc_fence_after();  // after the MMA that last read this stage (ab_empty)
         const uint32_t taddr = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) +
