@@ -257,6 +257,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int H = p.H, F = p.F;
   static_assert(FMT::W == C::W, "the code stages hold this format's windows");
+  // transpose=False on the wide variant: A (the dequantized weights) is MN-major, each k-row of a
+  // 128-row tile two 64-wide atoms (8 KB apart) of 8 k-rows each (1 KB apart)
+  constexpr bool kAmn = FMT::KIND == kAffineNn && !C::A_TMEM;
+  constexpr uint32_t kAmnAtomPitch = 8192u;
   constexpr int GS = FMT::GS;
   static_assert(FMT::KIND != kAffine || GS == 32 || GS == 64 || GS == 128, "group sizes");
   const int num_kb = H / BK;
@@ -381,7 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++qi;
         if (!U.valid) break;
         const int N = (U.rows + 15) & ~15;
-        const uint32_t idesc = umma_idesc_bf16(BM, N);
+        const uint32_t idesc = umma_idesc_bf16(BM, N) | (kAmn ? kIdescTransposeA : 0u);
         if (!mbar_wait(bar(C::tmem_empty()), (lu & 1u) ^ 1u, abort_flag, status)) break;
         tc_fence_after();
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
@@ -401,10 +405,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int k = 0; k < BK / 16; ++k)  // 16 elements = 8 columns of A, 32 bytes of B
                 tc_mma_bf16_ta(d_tmem, a_tmem + 8u * k, bdesc + 2u * k, idesc, (kb > U.kb0 || k > 0) ? 1u : 0u);
             } else {
-              const uint64_t adesc = umma_desc_sw128(sbase + C::OFF_A + s * A_BYTES + t * A_TILE_BYTES);
+              const uint32_t a_addr = sbase + C::OFF_A + s * A_BYTES + t * A_TILE_BYTES;
+              // K-major: 16 elements = 32 bytes along a row; MN-major: two 8-row atoms (2048 bytes)
+              const uint64_t adesc = kAmn ? umma_desc_sw128_mn(a_addr, kAmnAtomPitch, 1024u) : umma_desc_sw128(a_addr);
+              const uint32_t astep = kAmn ? 2048u >> 4 : 2u;
 #pragma unroll
-              for (int k = 0; k < BK / 16; ++k)  // advance 16 elements = 32 bytes along K
-                tc_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kb > U.kb0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < BK / 16; ++k)
+                tc_mma_bf16(d_tmem, adesc + astep * k, bdesc + 2u * k, idesc, (kb > U.kb0 || k > 0) ? 1u : 0u);
             }
           }
           tc_commit(bar(C::ab_empty(s)));
@@ -564,6 +571,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a_row ^ (c << 4) (the unswizzled row address has bits 4-6 clear)
     const uint32_t a_row0 = sbase + C::OFF_A +
                             (uint32_t)(tile * A_TILE_BYTES + (rr >> 3) * 1024 + (rr & 7) * 128 + ((rr & 7) << 4));
+    // transpose=False, wide variant (MN-major A): thread = (k-row kq, 64-column chunk cq) of the
+    // k-block; its 64 bf16 go to one 128-byte k-row of an atom, the swizzle XOR folded in as above
+    const int kq = r >> 2, cq = r & 3;
+    const uint32_t a_nn0 = sbase + C::OFF_A +
+                           (uint32_t)((cq >> 1) * A_TILE_BYTES + (cq & 1) * (int)kAmnAtomPitch + (kq >> 3) * 1024 +
+                                      (kq & 7) * 128 + ((kq & 7) << 4));
     const uint16_t* sc16 = reinterpret_cast<const uint16_t*>(p.scales);
     const uint16_t* bs16 = reinterpret_cast<const uint16_t*>(p.biases);
     // Flat walk over (unit, k-block) steps in queue order; this group processes every
@@ -599,6 +612,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Floating-point formats keep the k-block's scale bytes in sblk.x (two E8M0 bytes, or four
     // E4M3 bytes for nvfp4 with the expert's float32 scale in sblk.y).
     auto load_sb = [&](const UnitEntry& U, int kb) {
+      if constexpr (kAmn) {
+        // the (k-row, chunk) thread's group(s): one scale and bias, or two for 32-wide groups
+        const int n = U.f0 + 64 * cq;
+        if (!U.valid || n >= F) {
+          sblk = bblk = make_uint4(0, 0, 0, 0);
+          return;
+        }
+        const int64_t at = ((int64_t)U.expert * H + (int64_t)kb * BK + kq) * G + n / GS;
+        sblk.x = __ldg(sc16 + at);
+        bblk.x = __ldg(bs16 + at);
+        if (GS == 32) {
+          const bool hi = n + 32 < F;
+          sblk.y = hi ? __ldg(sc16 + at + 1) : 0u;
+          bblk.y = hi ? __ldg(bs16 + at + 1) : 0u;
+        }
+        return;
+      }
       if (!U.valid || U.f0 + r >= F) {
         sblk = bblk = make_uint4(0, 0, 0, 0);
         return;
@@ -654,7 +684,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && U.valid) {
       const int g = grp_of(kb);
       const uint32_t s2 = pick(sblk, g, false), b2 = pick(bblk, g, false);
-      const uint32_t nn_s = sblk.x, nn_b = bblk.x;  // transpose=False: this lane's k pair
+      // transpose=False: this lane's k pair (narrow), or this thread's group(s) (wide)
+      const uint32_t nn_s = sblk.x, nn_b = bblk.x, nn_s2 = sblk.y, nn_b2 = bblk.y;
       // floating-point formats: the float32 scale of each 16 weights of the k-block
       float sc4[4] = {0.f, 0.f, 0.f, 0.f};
       if constexpr (FMT::KIND == kNvfp4) {
@@ -685,39 +716,59 @@ __global__ void __launch_bounds__(kThreads, 1)
       // is an async-proxy write, which is not ordered after these generic-proxy reads by the
       // mbarrier alone.
       uint4 o[8];
-      if constexpr (FMT::KIND == kAffineNn) {
-        // output column n = U.f0 + r: nibble r of each of the k-block's 64 code rows (128 bytes
-        // each; even n in the low nibble), two k per bf16x2 FMA with the pair's scales and
-        // biases from lane j (zero past F: the warp's columns are all live or all dead)
-        const uint32_t tile = nib_tile - (uint32_t)(r * C::W) + (uint32_t)(r >> 1);
+      if constexpr (kAmn) {
+        // k-row kq, columns 64 cq .. 64 cq + 63: 32 bytes of the k-row in the 128-byte-swizzled
+        // code tile (16-byte chunk c of k-row k at chunk c ^ (k % 8)), 8 words of 8 codes in
+        // column order, dequantized like a transpose=True row and stored as they are computed
+        const uint32_t rowa = nib_tile - (uint32_t)(r * C::W) + (uint32_t)(kq * 128);
+        const uint32_t x7 = (uint32_t)(kq & 7);
+        uint4 n0, n1;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(n0.x), "=r"(n0.y), "=r"(n0.z), "=r"(n0.w)
+                     : "r"(rowa + ((((uint32_t)(2 * cq)) ^ x7) << 4))
+                     : "memory");
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(n1.x), "=r"(n1.y), "=r"(n1.z), "=r"(n1.w)
+                     : "r"(rowa + ((((uint32_t)(2 * cq + 1)) ^ x7) << 4))
+                     : "memory");
+        const uint32_t cw[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
+        const uint32_t sa2 = splat16(nn_s), ba2 = splat16(nn_b);
+        const uint32_t sb2 = GS == 32 ? splat16(nn_s2) : sa2, bb2 = GS == 32 ? splat16(nn_b2) : ba2;
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
+        const uint32_t a_row = a_nn0 + sa * A_BYTES;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = deq8(cw[c], c < 4 ? sa2 : sb2, c < 4 ? ba2 : bb2);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row ^ (uint32_t)(c << 4)), "r"(v.x),
+                       "r"(v.y), "r"(v.z), "r"(v.w)
+                       : "memory");
+        }
+      } else if constexpr (FMT::KIND == kAffineNn) {
+        // narrow variant (A in tensor memory, K-major): output column n = U.f0 + r takes nibble r
+        // of each of the k-block's 64 code rows (byte r / 2 of a 128-byte row, 128-byte swizzled;
+        // even n in the low nibble), two k per bf16x2 FMA with the pair's scales and biases from
+        // lane j (zero past F: the warp's columns are all live or all dead)
+        const uint32_t stage = nib_tile - (uint32_t)(r * C::W);
         const uint32_t sh = (uint32_t)(r & 1) * 4u;
-        auto piece = [&](int c) -> uint4 {  // k = 8c .. 8c + 7
+        const uint32_t bchunk = (uint32_t)(r >> 5), boff = (uint32_t)((r >> 1) & 15);
+        auto code_at = [&](int k) -> uint32_t {
+          uint32_t c;
+          asm volatile("ld.shared.u8 %0, [%1];"
+                       : "=r"(c)
+                       : "r"(stage + (uint32_t)(k * 128) + (((bchunk ^ (uint32_t)(k & 7)) << 4) | boff))
+                       : "memory");
+          return (c >> sh) & 0xFu;
+        };
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
           uint32_t v[4];
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int j = 4 * c + i;
-            uint32_t c0, c1;
-            asm volatile("ld.shared.u8 %0, [%1];" : "=r"(c0) : "r"(tile + (uint32_t)(2 * j) * 128u) : "memory");
-            asm volatile("ld.shared.u8 %0, [%1];" : "=r"(c1) : "r"(tile + (uint32_t)(2 * j + 1) * 128u) : "memory");
-            const uint32_t p2 = ((c0 >> sh) & 0xFu) | (((c1 >> sh) & 0xFu) << 16) | 0x43004300u;
+            const uint32_t p2 = code_at(2 * j) | (code_at(2 * j + 1) << 16) | 0x43004300u;
             v[i] = deq_pair(p2, __shfl_sync(0xffffffffu, nn_s, j), __shfl_sync(0xffffffffu, nn_b, j));
           }
-          return make_uint4(v[0], v[1], v[2], v[3]);
-        };
-        if constexpr (!C::A_TMEM) {
-          // as the 4-bit affine rows: wait for the A stage, store each piece as it is computed
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
-          const uint32_t a_row = a_row0 + sa * A_BYTES;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 v = piece(c);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row ^ (uint32_t)(c << 4)), "r"(v.x),
-                         "r"(v.y), "r"(v.z), "r"(v.w)
-                         : "memory");
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 8; ++c) o[c] = piece(c);
+          o[c] = make_uint4(v[0], v[1], v[2], v[3]);
         }
       } else if constexpr (FMT::KIND == kAffine && FMT::BITS == 4) {
         uint4 n0, n1;
@@ -1035,7 +1086,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   // code window (W bytes: formats.cuh), 32-byte swizzled when W is 32 so the dequant threads read
   // it without bank conflicts.  Every window starts on a 16-byte boundary.
   // transpose=False: codes as an [E*K, N/2] byte matrix; one box = 64 k-rows (one k-block) x the
-  // unit's 256 columns (128 bytes), unswizzled; columns past N read as zero.
+  // unit's 256 columns (128 bytes), 128-byte swizzled; columns past N read as zero.
   const bool nn = a.kind == kAffineNn;
   const int code_bits = a.kind == kMxfp8 ? 8 : a.kind == kAffine ? a.bits : 4;
   const int W = code_bits == 3 || code_bits == 5 ? 48 : 8 * code_bits;
@@ -1046,7 +1097,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
   const cuuint32_t box[2] = {nn ? (cuuint32_t)(UM / 2) : (cuuint32_t)W, nn ? (cuuint32_t)BK : (cuuint32_t)UM};
   const cuuint32_t estr[2] = {1, 1};
-  const CUtensorMapSwizzle swz = !nn && W == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
+  const CUtensorMapSwizzle swz = nn ? CU_TENSOR_MAP_SWIZZLE_128B
+                                : W == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
   CUresult cr = encode(&map_wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(a.wq), dims, strides, box,
                        estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -507,6 +507,20 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// The same for an MN-major operand in the 128-byte-swizzle canonical layout: atoms of 8 k-rows
+// x 64 bf16 along M/N (1024 bytes, 16-byte chunk c of k-row r at chunk position c ^ (r % 8)),
+// atoms adjacent along M/N `lbo` bytes apart and atoms adjacent along K (8-row groups) `sbo`
+// bytes apart.
+__device__ __forceinline__ uint64_t umma_desc_sw128_mn(uint32_t smem_addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);       // start address, bits 0-13
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;        // leading byte offset: M/N atom pitch
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;        // stride byte offset: 8-row group pitch
+  d |= (uint64_t)1 << 46;                             // descriptor version (tcgen05)
+  d |= (uint64_t)2 << 61;                             // layout: 128-byte swizzle
+  return d;
+}
+
 // Instruction descriptor for kind::f16 with bf16 A/B, f32 D, both operands K-major.
 __device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N) {
   uint32_t d = 0;
@@ -517,6 +531,7 @@ __device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N) {
   d |= (uint32_t)(M >> 4) << 24;         // M / 16
   return d;
 }
+constexpr uint32_t kIdescTransposeA = 1u << 15;  // A is MN-major
 
 #endif  // __CUDACC__
 
