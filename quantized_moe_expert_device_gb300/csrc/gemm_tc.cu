@@ -31,8 +31,8 @@
 //   warps 0-15  dequant:  two groups of 256 threads take alternate k-blocks; a thread owns one
 //                         of the unit's 256 weight rows: reads its 32 bytes of codes, turns each
 //                         nibble pair into bf16 128 + q (one byte permute and one mask per pair),
-//                         computes w = scale*q + bias in bf16x2 and writes the 64 bf16 in the
-//                         128-byte-swizzle K-major A layout
+//                         computes w = scale*q + bias in bf16x2 and writes the 64 bf16 into the
+//                         K-major A tile (unswizzled core-matrix layout)
 //   warps 16-23 epilogue: warp 16+e drains TMEM lanes 32(e%4).. of tile e/4: TMEM -> registers
 //                         -> bf16 -> shared transpose -> 16-byte stores to y rows perm[j]
 //                         (or fp32 stores into the slice's plane of the split-K sums)
@@ -406,9 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_mma_bf16_ta(d_tmem, a_tmem + 8u * k, bdesc + 2u * k, idesc, (kb > U.kb0 || k > 0) ? 1u : 0u);
             } else {
               const uint32_t a_addr = sbase + C::OFF_A + s * A_BYTES + t * A_TILE_BYTES;
-              // K-major: 16 elements = 32 bytes along a row; MN-major: two 8-row atoms (2048 bytes)
-              const uint64_t adesc = kAmn ? umma_desc_sw128_mn(a_addr, kAmnAtomPitch, 1024u) : umma_desc_sw128(a_addr);
-              const uint32_t astep = kAmn ? 2048u >> 4 : 2u;
+              // K-major (unswizzled): 16 elements = two 16-byte chunks, 256 bytes on; MN-major: two
+              // 8-row atoms (2048 bytes)
+              const uint64_t adesc =
+                  kAmn ? umma_desc_sw128_mn(a_addr, kAmnAtomPitch, 1024u) : umma_desc_kmajor_interleave(a_addr);
+              const uint32_t astep = kAmn ? 2048u >> 4 : 256u >> 4;
 #pragma unroll
               for (int k = 0; k < BK / 16; ++k)
                 tc_mma_bf16(d_tmem, adesc + astep * k, bdesc + 2u * k, idesc, (kb > U.kb0 || k > 0) ? 1u : 0u);
@@ -567,12 +569,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // of row r at chunk position c ^ ((r >> 2) & 1)), other widths are not swizzled
     const uint32_t nib_row = sbase + C::OFF_NIB + (uint32_t)(r * C::W);
     const uint32_t nib_c0 = (uint32_t)(((r >> 2) & 1) << 4), nib_c1 = nib_c0 ^ 16u;
-    // the row in A stage 0, with its 128-byte-swizzle XOR folded in: chunk c of the row is at
-    // a_row ^ (c << 4) (the unswizzled row address has bits 4-6 clear)
-    const uint32_t a_row0 = sbase + C::OFF_A +
-                            (uint32_t)(tile * A_TILE_BYTES + (rr >> 3) * 1024 + (rr & 7) * 128 + ((rr & 7) << 4));
-    // transpose=False, wide variant (MN-major A): thread = (k-row kq, 64-column chunk cq) of the
-    // k-block; its 64 bf16 go to one 128-byte k-row of an atom, the swizzle XOR folded in as above
+    // the row in A stage 0 (shared-memory A is K-major and unswizzled: core matrices of 8 rows x
+    // 16 bytes): chunk c of the row is at a_row + 128 c, so the 8 stores take immediate offsets
+    const uint32_t a_row0 = sbase + C::OFF_A + (uint32_t)(tile * A_TILE_BYTES + (rr >> 3) * 1024 + (rr & 7) * 16);
+    // transpose=False, wide variant (MN-major A, 128-byte swizzled): thread = (k-row kq, 64-column
+    // chunk cq) of the k-block; its 64 bf16 go to one 128-byte k-row of an atom, with the swizzle
+    // XOR folded in: chunk c of the k-row is at a_row ^ (c << 4)
     const int kq = r >> 2, cq = r & 3;
     const uint32_t a_nn0 = sbase + C::OFF_A +
                            (uint32_t)((cq >> 1) * A_TILE_BYTES + (cq & 1) * (int)kAmnAtomPitch + (kq >> 3) * 1024 +
@@ -789,7 +791,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint4 v = deq8(cw[c], c < 4 ? s2 : s2b, c < 4 ? b2 : b2b);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row ^ (uint32_t)(c << 4)), "r"(v.x),
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row + (uint32_t)(c * 128)), "r"(v.x),
                          "r"(v.y), "r"(v.z), "r"(v.w)
                          : "memory");
           }
@@ -839,7 +841,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t a_row = a_row0 + sa * A_BYTES;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
-          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row ^ (uint32_t)(c << 4)), "r"(o[c].x),
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row + (uint32_t)(c * 128)), "r"(o[c].x),
                        "r"(o[c].y), "r"(o[c].z), "r"(o[c].w)
                        : "memory");
       }

@@ -507,6 +507,19 @@ __device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
+// Shared-memory matrix descriptor for a K-major operand without swizzle: core matrices of 8 rows x
+// 16 bytes stored as 128 contiguous bytes; the 16-byte chunks of a row are 128 bytes apart
+// (leading byte offset), 8-row groups 1024 bytes apart (stride byte offset): a 128 x 64 bf16
+// tile, chunk c of row r at (r / 8) * 1024 + c * 128 + (r % 8) * 16.
+__device__ __forceinline__ uint64_t umma_desc_kmajor_interleave(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);       // start address, bits 0-13
+  d |= (uint64_t)(128u >> 4) << 16;                   // leading byte offset: K-adjacent chunks
+  d |= (uint64_t)(1024u >> 4) << 32;                  // stride byte offset: 8-row group pitch
+  d |= (uint64_t)1 << 46;                             // descriptor version (tcgen05); layout 0: no swizzle
+  return d;
+}
+
 // The same for an MN-major operand in the 128-byte-swizzle canonical layout: atoms of 8 k-rows
 // x 64 bf16 along M/N (1024 bytes, 16-byte chunk c of k-row r at chunk position c ^ (r % 8)),
 // atoms adjacent along M/N `lbo` bytes apart and atoms adjacent along K (8-row groups) `sbo`
