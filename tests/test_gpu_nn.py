@@ -2,9 +2,10 @@
 oracle's float64 gather_qmm_nn, on the GPU's own quantized weights (bit-equal to the oracle's).
 
 The tensor-core path: the shape of the pages' transpose=False timing (E=4, K=N=512, 1024 rows),
-every group size, both GEMM variants (wide chunks of up to 256 rows, narrow ones of up to 32), N
-not a multiple of the 256-column unit, a decode-sized call that splits K, dense E=1, invalid
-indices, a shared x, and caller-sorted indices equal to the unsorted call bit for bit.  The
+every group size on both GEMM variants (wide chunks of up to 256 rows, whose A operand is MN-major,
+and narrow ones of up to 32, whose A is K-major in tensor memory), N not a multiple of the
+256-column unit or of 64, a decode-sized call that splits K, dense E=1, invalid indices, a shared x,
+and caller-sorted indices equal to the unsorted call bit for bit on both variants.  The
 CUDA-core cross-check gqmm_gather_qmm_nn_simt takes any K; it is checked on K that are not
 multiples of 64 as well.  Tolerances are the gather's (relative Frobenius error <= 5e-3, every
 element within 2e-2 * max|y_ref|): weights are decoded exactly and rounded once to bfloat16."""
@@ -36,7 +37,9 @@ NN_CASES = [(1024, 1, 512, 512, 4, 64),     # the pages' transpose=False shape (
             (4, 8, 2048, 768, 64, 64),
             (2, 4, 4096, 512, 4, 64),       # decode-sized: K split into slices
             (5, 1, 320, 96, 1, 32),         # dense (idx None), N below one unit
-            (300, 2, 192, 32, 3, 32)]       # the smallest N, ragged chunk tails
+            (300, 2, 192, 32, 3, 32),       # the smallest N, ragged chunk tails (wide)
+            (512, 2, 1024, 640, 4, 128),    # wide, 128-wide groups, N = 2.5 units
+            (600, 1, 512, 800, 1, 32)]      # dense wide, N % 64 == 32 (a 64-column chunk half past N)
 
 
 @pytest.mark.parametrize("T,A,K,N,E,gs", NN_CASES)
@@ -77,6 +80,32 @@ def test_nn_invalid_indices_shared_x_and_sorted():
     y_u = g.gqmm_gather_qmm_nn(xs, *dev, to_dev_idx(idx_s), sorted_indices=False)
     torch.cuda.synchronize()
     assert torch.equal(y_s, y_u)
+
+
+def test_nn_wide_sorted_equals_unsorted_and_invalid_index():
+    """The wide variant (MN-major A): caller-sorted indices equal the unsorted call bit for bit,
+    and an invalid index gives a zero row and the status bit."""
+    import quantized_moe_expert_device_gb300 as g
+
+    T, K, N, E = 1200, 768, 576, 4
+    host, dev = _weights(E, K, N, 64, seed=90)
+    idx_s = np.sort(np.random.default_rng(10).integers(0, E, size=T)).astype(np.uint32).reshape(-1, 1)
+    x = wl.normal_bf16((T, 1, K), 91)
+    xs = x.cuda()
+    y_s = g.gqmm_gather_qmm_nn(xs, *dev, to_dev_idx(idx_s), sorted_indices=True)
+    y_u = g.gqmm_gather_qmm_nn(xs, *dev, to_dev_idx(idx_s), sorted_indices=False)
+    torch.cuda.synchronize()
+    assert torch.equal(y_s, y_u)
+    rows = np.arange(0, T, 5)
+    assert_parity(y_u.reshape(T, N)[torch.from_numpy(rows).cuda()],
+                  oracle.gather_qmm_nn(x, *host, idx_s, E, rows=rows), "nn wide sorted")
+    idx_b = idx_s.copy()
+    idx_b[7, 0] = E + 3
+    ws = g.new_workspace(T, N, E)
+    y_b = g.gqmm_gather_qmm_nn(xs, *dev, to_dev_idx(idx_b), ws=ws)
+    assert g.gqmm_device_status(ws) & g.STATUS_BAD_INDEX
+    assert torch.count_nonzero(y_b.reshape(T, N)[7]).item() == 0
+    assert torch.equal(y_b.reshape(T, N)[8:], y_u.reshape(T, N)[8:])
 
 
 @pytest.mark.parametrize("T,A,K,N,E,gs", [(16, 2, 256, 256, 8, 32),
