@@ -57,35 +57,48 @@ static_assert(kFusedPlanRows == kFusedPlanMaxRows, "one bound for the host and t
 // The chunk list of a routed call of n <= 64 rows, computed by one warp: the rows of each expert
 // in flat-row order, in chunks of at most two rows (the first and second, third and fourth, ...
 // occurrences of the expert), numbered in the flat order of their first rows.  Each lane holds
-// entries lane and 32 + lane; one pass over all entries (shuffles) gives an entry's occurrence
-// rank, its expert's total and its next occurrence.  plan[c] = (expert, first row, second row
+// entries lane and 32 + lane; a match within each half of the entries and, when there is a second
+// half, one unrolled pass of shuffles across the halves give an entry's occurrence rank, its
+// expert's total and its next occurrence.  plan[c] = (expert, first row, second row
 // (= first row for a one-row chunk), rows).  Rows whose index is >= E are in no chunk; block 0
 // writes them as zeros and records GQMM_STATUS_BAD_INDEX.  Returns the number of chunks (lane 0).
 __device__ __forceinline__ int fused_plan(const GemmArgs& p, int4* plan, uint32_t* status) {
   const int lane = threadIdx.x & 31;
   const int n = (int)p.n;
   uint32_t key[2];
-  int rank[2] = {0, 0}, tot[2] = {0, 0}, next[2] = {-1, -1};
+  int rank[2], tot[2], next[2];
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     const int i = 32 * r + lane;
     key[r] = i < n ? __ldg(p.idx + i) : 0xFFFFFFFFu;
   }
+  // Within each half: the lanes holding the same key (padding keys 0xFFFFFFFF match only one
+  // another, never a valid index), their count, the ones below this lane and the next one above.
+  const uint32_t lt = (1u << lane) - 1u, le = lt | (1u << lane);
 #pragma unroll
-  for (int rj = 0; rj < 2; ++rj) {
+  for (int r = 0; r < 2; ++r) {
+    const uint32_t m = __match_any_sync(0xffffffffu, key[r]);
+    tot[r] = __popc(m);
+    rank[r] = __popc(m & lt);
+    const uint32_t above = m & ~le;
+    next[r] = above ? 32 * r + __ffs(above) - 1 : -1;
+  }
+  if (n > 32) {  // uniform: entries 32.. exist; count each half's key in the other half
+    int c0 = 0, c1 = 0, first1 = -1;
+#pragma unroll
     for (int jl = 0; jl < 32; ++jl) {
-      const int j = 32 * rj + jl;
-      const uint32_t kj = __shfl_sync(0xffffffffu, key[rj], jl);
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int i = 32 * r + lane;
-        if (kj == key[r]) {
-          ++tot[r];
-          if (j < i) ++rank[r];
-          if (j > i && next[r] < 0) next[r] = j;
-        }
+      const uint32_t k1 = __shfl_sync(0xffffffffu, key[1], jl);  // entry 32 + jl
+      const uint32_t k0 = __shfl_sync(0xffffffffu, key[0], jl);  // entry jl
+      if (k1 == key[0]) {
+        ++c0;
+        if (first1 < 0) first1 = 32 + jl;
       }
+      if (k0 == key[1]) ++c1;
     }
+    tot[0] += c0;
+    if (next[0] < 0) next[0] = first1;
+    tot[1] += c1;
+    rank[1] += c1;  // every entry of the first half comes before the second half
   }
   bool lead[2], bad[2];
 #pragma unroll
@@ -95,7 +108,6 @@ __device__ __forceinline__ int fused_plan(const GemmArgs& p, int4* plan, uint32_
     lead[r] = i < n && !bad[r] && (rank[r] & 1) == 0;
   }
   const uint32_t b0 = __ballot_sync(0xffffffffu, lead[0]), b1 = __ballot_sync(0xffffffffu, lead[1]);
-  const uint32_t lt = (1u << lane) - 1u;
 #pragma unroll
   for (int r = 0; r < 2; ++r) {
     if (lead[r]) {
