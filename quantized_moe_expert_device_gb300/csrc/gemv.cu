@@ -291,10 +291,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
   if (p.dense_plan && warp == NW && lane == 0) {
     const int per0 = (n_batches + (int)gridDim.x - 1) / (int)gridDim.x;
     const int f0 = min(F, (int)blockIdx.x * per0 * RB), f1 = min(F, f0 + per0 * RB);
-    if (f1 > f0) {
-      prefetch_l2_bulk(p.wq + (int64_t)f0 * (H / 2), (uint32_t)(f1 - f0) * (H / 2));
-      prefetch_l2_bulk(p.scales + (int64_t)f0 * G, (uint32_t)(f1 - f0) * G * 2);
-      prefetch_l2_bulk(p.biases + (int64_t)f0 * G, (uint32_t)(f1 - f0) * G * 2);
+    // the rows beyond the ring's first fill: those are copied (from HBM) as soon as the wait returns,
+    // and a prefetch of them would only sit ahead of those copies in the block's copy engine
+    const int fs = min(f1, f0 + stream_stages(H, M) * RB);
+    if (f1 > fs) {
+      prefetch_l2_bulk(p.wq + (int64_t)fs * (H / 2), (uint32_t)(f1 - fs) * (H / 2));
+      prefetch_l2_bulk(p.scales + (int64_t)fs * G, (uint32_t)(f1 - fs) * G * 2);
+      prefetch_l2_bulk(p.biases + (int64_t)fs * G, (uint32_t)(f1 - fs) * G * 2);
     }
   }
   grid_dependency_wait();

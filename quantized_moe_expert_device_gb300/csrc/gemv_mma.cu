@@ -142,10 +142,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) gemv_mma_kernel(const GemmArgs
   if (p.dense_plan && warp == kMmaWarps && lane == 0) {
     const int per0 = (n_batches + (int)gridDim.x - 1) / (int)gridDim.x;
     const int f0 = min(F, (int)blockIdx.x * per0 * kItemRows), f1 = min(F, f0 + per0 * kItemRows);
-    if (f1 > f0) {
-      prefetch_l2_bulk(p.wq + (int64_t)f0 * (H / 2), (uint32_t)(f1 - f0) * (H / 2));
-      prefetch_l2_bulk(p.scales + (int64_t)f0 * G, (uint32_t)(f1 - f0) * G * 2);
-      prefetch_l2_bulk(p.biases + (int64_t)f0 * G, (uint32_t)(f1 - f0) * G * 2);
+    // the rows beyond the ring's first fill (those are copied as soon as the wait returns, and a
+    // prefetch of them would only sit ahead of those copies in the block's copy engine)
+    const int fs = min(f1, f0 + NS * kItemRows);
+    if (f1 > fs) {
+      prefetch_l2_bulk(p.wq + (int64_t)fs * (H / 2), (uint32_t)(f1 - fs) * (H / 2));
+      prefetch_l2_bulk(p.scales + (int64_t)fs * G, (uint32_t)(f1 - fs) * G * 2);
+      prefetch_l2_bulk(p.biases + (int64_t)fs * G, (uint32_t)(f1 - fs) * G * 2);
     }
   }
   grid_dependency_wait();
