@@ -8,7 +8,8 @@
 //   - work item = (chunk, batch of RB weight rows of the chunk's expert).  The RB rows are
 //     contiguous in wq, scales and biases, so one item is three 1-D bulk copies (plus the
 //     chunk's rows of x when the chunk changes) into a stage of a 3- or 4-deep shared-memory
-//     ring (4 where it fits two blocks per SM);
+//     ring (4 where it fits two blocks per SM); a dense call copies its x rows once into a buffer
+//     of their own, so its stages hold weights only and its ring is 5-6 deep;
 //   - one producer warp issues the copies up to a ring's depth ahead; eight consumer warps
 //     compute;
 //   - consumer thread = (row group, k slice of 32 elements), R = 4 rows per item.  The x slice
@@ -31,6 +32,7 @@ constexpr int kStreamThreads = kStreamConsumers + 32;  // + the producer warp
 constexpr int kStreamKS = 32;                          // k elements per consumer thread
 constexpr int kStreamR = 4;                            // weight rows per consumer thread and item
 constexpr int kStreamStages = 4;                       // ring depth when it fits the budget, else 3
+constexpr int kStreamMaxStages = 6;                    // dense calls: as many weight-only stages as fit
 constexpr int kStreamSmemBudget = 110 * 1024;          // ring bytes per block: two blocks per SM
 constexpr int kStreamMaxXElems = 8192;                 // M * H bound: the x rows of a stage <= 16 KB
 constexpr uint32_t kStreamBarId = 1;                   // named barrier of the consumer warps
@@ -46,6 +48,14 @@ __host__ __device__ constexpr int stream_stage_bytes(int H, int M) {
 
 __host__ __device__ constexpr int stream_stages(int H, int M) {
   return kStreamStages * stream_stage_bytes(H, M) <= kStreamSmemBudget ? kStreamStages : kStreamStages - 1;
+}
+// A dense call has one chunk, so its x rows are copied once, with the first item, into a buffer of
+// their own after the ring; its stages hold weights only, and more of them fit.
+__host__ __device__ constexpr int stream_weight_bytes(int H) { return stream_stage_bytes(H, 0); }
+__host__ __device__ constexpr int stream_stages_dense(int H, int M) {
+  return (kStreamSmemBudget - M * H * 2) / stream_weight_bytes(H) < kStreamMaxStages
+             ? (kStreamSmemBudget - M * H * 2) / stream_weight_bytes(H)
+             : kStreamMaxStages;
 }
 
 // Routed calls of at most this many rows (decode: M tokens x A experts) are planned inside the
@@ -253,9 +263,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
   constexpr int VL = V >= 32 ? V / 32 : 1;
   constexpr int NW = kStreamConsumers / 32;
   extern __shared__ __align__(128) uint8_t stream_smem[];
-  __shared__ __align__(8) uint64_t full_bar[kStreamStages];
-  __shared__ __align__(8) uint64_t empty_bar[kStreamStages];
-  __shared__ StageMeta meta[kStreamStages];
+  __shared__ __align__(8) uint64_t full_bar[kStreamMaxStages];
+  __shared__ __align__(8) uint64_t empty_bar[kStreamMaxStages];
+  __shared__ StageMeta meta[kStreamMaxStages];
   __shared__ float red[2][NW][V];
   __shared__ int abort_flag;
   __shared__ int4 plan[kFusedPlanRows];  // the in-kernel chunk list of a fused-plan call
@@ -263,8 +273,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
 
   const int H = p.H, F = p.F, G = H / 64;
   const int RB = stream_rows_per_item(H);
-  const int stage_bytes = stream_stage_bytes(H, M);
-  const int NS = stream_stages(H, M);
+  const bool dense = p.dense_plan != 0;
+  const int stage_bytes = dense ? stream_weight_bytes(H) : stream_stage_bytes(H, M);
+  const int NS = dense ? stream_stages_dense(H, M) : stream_stages(H, M);
+  // where a stage's x rows are: the stage's own tail, or (dense) the buffer after the ring
+  auto x_at = [&](int s) -> int { return dense ? NS * stage_bytes : s * stage_bytes + RB * (H / 2 + 4 * G); };
   const int n_batches = (F + RB - 1) / RB;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t* status = &p.header->status;
@@ -293,7 +306,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
     const int f0 = min(F, (int)blockIdx.x * per0 * RB), f1 = min(F, f0 + per0 * RB);
     // the rows beyond the ring's first fill: those are copied (from HBM) as soon as the wait returns,
     // and a prefetch of them would only sit ahead of those copies in the block's copy engine
-    const int fs = min(f1, f0 + stream_stages(H, M) * RB);
+    const int fs = min(f1, f0 + NS * RB);
     if (f1 > fs) {
       prefetch_l2_bulk(p.wq + (int64_t)fs * (H / 2), (uint32_t)(f1 - fs) * (H / 2));
       prefetch_l2_bulk(p.scales + (int64_t)fs * G, (uint32_t)(f1 - fs) * G * 2);
@@ -370,7 +383,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
         bulk_load(base + RB * (H / 2) + RB * G * 2, p.biases + row * G, sb_bytes, bar);
         if (newx)
           for (int t = 0; t < xr; ++t)
-            bulk_load(base + RB * (H / 2 + 4 * G) + t * H * 2, p.x + (int64_t)xrow[t] * H, H * 2, bar);
+            bulk_load(smem_u32(stream_smem) + (uint32_t)(x_at(s) + t * H * 2), p.x + (int64_t)xrow[t] * H, H * 2, bar);
         ++issued;
       }
       if (!ok || abort_flag) {
@@ -406,7 +419,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
 #pragma unroll
       for (int t = 0; t < M; ++t) {
         if (t < rows) {
-          X[t] = load_x_pairs(xp[t], reinterpret_cast<const __nv_bfloat16*>(st + RB * (H / 2 + 4 * G) + t * H * 2) +
+          X[t] = load_x_pairs(xp[t], reinterpret_cast<const __nv_bfloat16*>(stream_smem + x_at(s) + t * H * 2) +
                                          lr * kStreamKS);
         } else {
           X[t] = 0.f;
@@ -456,7 +469,8 @@ cudaError_t launch_gemv_fma(const GemmArgs& a, int rows, int sms, cudaStream_t s
   cudaLaunchAttribute pdl[1];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  const int smem = stream_stages(a.H, rows) * stream_stage_bytes(a.H, rows);
+  const int smem = a.dense_plan ? stream_stages_dense(a.H, rows) * stream_weight_bytes(a.H) + rows * a.H * 2
+                                 : stream_stages(a.H, rows) * stream_stage_bytes(a.H, rows);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(2 * sms));  // two blocks per SM
   cfg.blockDim = dim3(kStreamThreads);
