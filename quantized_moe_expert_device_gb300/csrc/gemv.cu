@@ -12,7 +12,9 @@
 //     of their own, so its stages hold weights only and its ring is 5-6 deep;
 //   - one producer warp issues the copies up to a ring's depth ahead; eight consumer warps
 //     compute;
-//   - consumer thread = (row group, k slice of 32 elements), R = 4 rows per item.  The x slice
+//   - consumer thread = (row group, k slice of 32 elements), R = 4 rows per item; a row group
+//     is the next power of two (>= 32) of the row's slice count, the threads past the last slice
+//     adding zeros (H a multiple of 128, at most 8192).  The x slice
 //     stays in registers as bf16 pairs for as long as the block works on the chunk;
 //   - per row the thread reads 16 bytes of codes and the group's scale s and bias b from shared
 //     memory, accumulates acc_t = sum_k x_tk (128 + q_k) with the codes made into exact bf16
@@ -38,8 +40,13 @@ constexpr int kStreamMaxXElems = 8192;                 // M * H bound: the x row
 constexpr uint32_t kStreamBarId = 1;                   // named barrier of the consumer warps
 
 // Rows per item: kStreamConsumers / (H / KS) row groups of kStreamR rows.
+// Consumer threads per weight row: one per 32-element k slice, rounded up to a power of two of at
+// least a warp (threads past the row's last slice add zeros), so a row group is whole warps.
+__host__ __device__ constexpr int stream_lanes(int H) {
+  return H / kStreamKS <= 32 ? 32 : H / kStreamKS <= 64 ? 64 : H / kStreamKS <= 128 ? 128 : 256;
+}
 __host__ __device__ constexpr int stream_rows_per_item(int H) {
-  return kStreamConsumers / (H / kStreamKS) * kStreamR;
+  return kStreamConsumers / stream_lanes(H) * kStreamR;
 }
 // Bytes of one ring stage: codes, scales, biases of the item's rows, then M rows of x.
 __host__ __device__ constexpr int stream_stage_bytes(int H, int M) {
@@ -396,8 +403,9 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
   }
 
   // ---------------- consumers ----------------
-  const int L = H / kStreamKS;  // threads per row
+  const int L = stream_lanes(H);  // threads per row
   const int rg = tid / L, lr = tid - rg * L;
+  const bool active = lr < H / kStreamKS;  // the thread has a k slice of the row
   const int W = L / 32;         // warps per row group
   const int RG = kStreamConsumers / L;
   uint32_t xp[M][16];
@@ -418,7 +426,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
       rows = m.rows;
 #pragma unroll
       for (int t = 0; t < M; ++t) {
-        if (t < rows) {
+        if (t < rows && active) {
           X[t] = load_x_pairs(xp[t], reinterpret_cast<const __nv_bfloat16*>(stream_smem + x_at(s) + t * H * 2) +
                                          lr * kStreamKS);
         } else {
@@ -432,10 +440,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
     const int valid_rows = min(RB, F - m.fb);
     const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + RB * (H / 2));
     const uint16_t* bs = sc + RB * G;
-    if (M == 1 || rows == 1)
+    if (!active) {
+#pragma unroll
+      for (int q = 0; q < V; ++q) part[q] = 0.f;
+    } else if (M == 1 || rows == 1) {
       item_partials<M, 1>(part, st, sc, bs, xp, X, rg * kStreamR, lr, H, valid_rows);
-    else
+    } else {
       item_partials<M, M>(part, st, sc, bs, xp, X, rg * kStreamR, lr, H, valid_rows);
+    }
     warp_reduce_scatter<V>(part);
     const bool writer = V >= 32 || (lane & (32 / V - 1)) == 0;
     float (*rb)[V] = red[k & 1];
@@ -461,8 +473,10 @@ __global__ void __launch_bounds__(kStreamThreads, 2) gemv_fma_kernel(const GemmA
 }  // namespace
 
 bool gemv_fma_supported(int rows, int H) {
-  return (rows == 1 || rows == 2) && H % (32 * kStreamKS) == 0 && H / kStreamKS <= kStreamConsumers &&
-         kStreamConsumers % (H / kStreamKS) == 0 && rows * H <= kStreamMaxXElems;
+  // H a multiple of 128 keeps every bulk copy a multiple of 16 bytes (an item's scale rows are
+  // 4096 H / (32 stream_lanes(H)) bytes)
+  return (rows == 1 || rows == 2) && H > 0 && H % 128 == 0 && H / kStreamKS <= kStreamConsumers &&
+         rows * H <= kStreamMaxXElems;
 }
 
 cudaError_t launch_gemv_fma(const GemmArgs& a, int rows, int sms, cudaStream_t s) {

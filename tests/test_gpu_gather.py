@@ -255,8 +255,27 @@ def test_weight_streaming_dense_matches_oracle(M, H):
     assert_parity(y, y_ref, f"stream dense M={M} H={H}")
 
 
+@pytest.mark.parametrize("M,H", [(1, 768), (2, 768), (3, 768), (1, 640), (2, 1536), (1, 8192)])
+def test_weight_streaming_dense_k_not_a_multiple_of_1024(M, H):
+    """K a multiple of 128 but not of 1024 (the CUDA-core streaming kernel pads a row's threads to a
+    power of two, the extra threads adding zeros): 1 and 2 rows stream on the CUDA-core kernel, the
+    MMA streaming kernel does not take these K, so 3 rows go to the narrow tensor-core kernel."""
+    import quantized_moe_expert_device_gb300 as g
+
+    F = 400
+    host_w, dev_w = _weights(1, F, H)
+    before = g.dispatch_count("gemv"), g.dispatch_count("gemv_mma")
+    x = wl.normal_bf16((M, H), wl.SEED_X + M)
+    y, y_ref, status = _run(x, None, 1, host_w, dev_w)
+    assert status == 0
+    assert (g.dispatch_count("gemv") > before[0]) == (M <= 2)
+    assert g.dispatch_count("gemv_mma") == before[1]
+    assert_parity(y, y_ref, f"stream dense M={M} H={H}")
+
+
 @pytest.mark.parametrize("T,A,E,H,hot", [(1, 8, 128, 2048, 1), (8, 8, 128, 2048, 1), (5, 3, 16, 1024, 1),
-                                         (32, 8, 256, 2048, 1), (32, 8, 256, 2048, 3)])
+                                         (32, 8, 256, 2048, 1), (32, 8, 256, 2048, 3),
+                                         (4, 8, 64, 768, 1), (3, 8, 32, 1536, 1), (2, 8, 16, 640, 1)])
 def test_weight_streaming_moe_matches_oracle(T, A, E, H, hot):
     """MoE decode shapes with at most 1.5 rows per hit expert on average run on the
     weight-streaming kernel in chunks of 2 rows; an expert with more rows gets several chunks
@@ -298,7 +317,7 @@ def test_weight_streaming_invalid_indices_and_unsupported_h():
     import quantized_moe_expert_device_gb300 as g
 
     E, F = 16, 144
-    for H, expect_stream in ((1024, True), (4096, True), (192, False)):
+    for H, expect_stream in ((1024, True), (4096, True), (768, True), (192, False)):
         host_w, dev_w = _weights(E, F, H)
         idx = np.random.default_rng(H).integers(0, E, size=(6, 2), dtype=np.uint32)
         idx[2, 1] = E + 5

@@ -54,6 +54,22 @@ def test_moe_mlp_matches_oracle(T, A, H, I, E):
     assert_parity(y, ref, f"moe_mlp T={T} A={A} H={H} I={I} E={E}")
 
 
+def test_moe_mlp_decode_both_projections_stream():
+    """Decode with I = 768: both projections run on the CUDA-core weight-streaming kernel (the down
+    projection's K = 768 is a multiple of 128), no tensor-core GEMM launch."""
+    import quantized_moe_expert_device_gb300 as g
+
+    T, A, H, I, E = 2, 8, 2048, 768, 128
+    idx = wl.idx_topk_distinct_uniform(T, A, E, seed=21)
+    before = {k: g.dispatch_count(k) for k in ("gemv", "gemm_narrow", "gemm_tc")}
+    y, ref, status = _run(T, A, H, I, E, idx, seed=3)
+    assert status == 0
+    assert g.dispatch_count("gemv") - before["gemv"] == 2
+    assert g.dispatch_count("gemm_narrow") == before["gemm_narrow"]
+    assert g.dispatch_count("gemm_tc") == before["gemm_tc"]
+    assert_parity(y, ref, "moe_mlp decode, both projections streaming")
+
+
 @pytest.mark.parametrize("activation", ["gelu", "gelu_tanh"])
 @pytest.mark.parametrize("T,A,H,I,E", [(16, 2, 256, 128, 8), (2, 8, 1024, 512, 128), (256, 8, 1024, 512, 16)])
 def test_moe_mlp_geglu_matches_oracle(T, A, H, I, E, activation):
