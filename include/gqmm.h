@@ -191,9 +191,9 @@ GQMM_API int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* per
  *  H        > 0, multiple of 64 and of group_size;   F > 0, multiple of 16;   E in [1, GQMM_MAX_EXPERTS]
  *  group_size, bits   as for gqmm_quantize; a row's codes (H*bits/8 bytes) must be a multiple
  *           of 16 bytes (for 3- and 5-bit codes: H a multiple of 128).  The weight-streaming
- *           kernels of decode-sized calls take 4-bit codes in 64-wide groups; 3-, 5-, 6- and
- *           8-bit codes run every call on the tensor-core GEMM's narrow variant (chunks of at
- *           most 32 rows per expert)
+ *           kernels of decode-sized calls take 4-bit codes in 64-wide groups (the CUDA-core one
+ *           H a multiple of 128 up to 8192, the MMA one H of 1024, 2048 or 4096); other formats
+ *           and sizes run decode-sized calls on the tensor-core GEMM's narrow variant
  *  x_shared 0: x is [T, A, H], one row per (t, a);  1: x is [T, H], the A routed rows of
  *           token t all read x[t] (the x of an MoE layer, broadcast over its A experts;
  *           needs idx != NULL)
