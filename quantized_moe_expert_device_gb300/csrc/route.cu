@@ -363,27 +363,57 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter(RouteArgs a) {
 
   const int E = a.E;
   const int tile = blockIdx.x;
-  const int warp = threadIdx.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The tile's keys do not come from route_hist: every kernel before it (a plain launch) has
+  // completed, so they are loaded before the wait and arrive while it lasts.
+  constexpr int kWarpRange = TILE / kWarps;
+  constexpr int kS = kWarpRange / 32;
+  const int64_t w_begin = (int64_t)tile * TILE + (int64_t)warp * kWarpRange;
+  const int64_t w_end = min(a.n, w_begin + kWarpRange);
+  int bad = 0;  // already reported by route_hist
+  const WarpKeys<kS, false> K = load_warp_keys<kS, false>(a.idx, w_begin, w_end, kS, E, &bad);
   grid_dependency_wait();  // route_hist's table is complete and visible
 
-  // 1. key totals over all tiles and this tile's preceding count, one contiguous key run
-  //    per thread, then a block scan over keys gives each key's segment start.
+  // 1. key totals over all tiles and this tile's preceding count: a warp per key, its lanes over
+  //    the tiles (coalesced loads, several keys in flight), summed by warp reductions; then a
+  //    block scan over keys, one contiguous key run per thread, gives each key's segment start.
   const int keys = E + 1;
+  const int64_t n_tiles = a.n_tiles;
+  constexpr int kKeysInFlight = 8;  // keys per warp whose loads are issued together
+  for (int kb = warp; kb < keys; kb += kKeysInFlight * kWarps) {
+    uint32_t tot[kKeysInFlight], before[kKeysInFlight];
+#pragma unroll
+    for (int j = 0; j < kKeysInFlight; ++j) tot[j] = before[j] = 0u;
+    for (int64_t t0 = 0; t0 < n_tiles; t0 += 32) {
+      const int64_t t = t0 + lane;
+      uint32_t c[kKeysInFlight];
+#pragma unroll
+      for (int j = 0; j < kKeysInFlight; ++j) {
+        const int k = kb + j * kWarps;
+        c[j] = (k < keys && t < n_tiles) ? __ldcg(a.tile_hist + (int64_t)k * n_tiles + t) : 0u;
+      }
+#pragma unroll
+      for (int j = 0; j < kKeysInFlight; ++j) {
+        tot[j] += c[j];
+        before[j] += t < tile ? c[j] : 0u;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kKeysInFlight; ++j) {
+      const int k = kb + j * kWarps;
+      const uint32_t s_tot = __reduce_add_sync(0xffffffffu, tot[j]);
+      const uint32_t s_before = __reduce_add_sync(0xffffffffu, before[j]);
+      if (lane == 0 && k < keys) {
+        seg_len[k] = (int32_t)s_tot;
+        base[k] = (int32_t)s_before;
+      }
+    }
+  }
+  __syncthreads();
   const int per = (keys + kRouteThreads - 1) / kRouteThreads;
   const int k0 = threadIdx.x * per, k1 = min(keys, k0 + per);
   int64_t my_total = 0;
-  for (int k = k0; k < k1; ++k) {
-    const uint32_t* row = a.tile_hist + (int64_t)k * a.n_tiles;
-    int64_t tot = 0, before = 0;
-    for (int64_t t = 0; t < a.n_tiles; ++t) {
-      const uint32_t c = row[t];
-      tot += c;
-      if (t < tile) before += c;
-    }
-    seg_len[k] = (int32_t)tot;
-    base[k] = (int32_t)before;
-    my_total += tot;
-  }
+  for (int k = k0; k < k1; ++k) my_total += seg_len[k];
   int64_t total;
   int64_t run = block_exclusive_scan<kRouteThreads>(my_total, warp_tot, &total);
   for (int k = k0; k < k1; ++k) {
@@ -403,13 +433,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_scatter(RouteArgs a) {
     for (int k = threadIdx.x; k <= E + 1; k += kRouteThreads) wc[w][k] = 0;
 
   // 2. stable scatter: warp w ranks the tile's entries [w * kWarpRange, (w + 1) * kWarpRange)
-  //    in order; the per-warp counts of pass 1 give each warp its first position per key.
-  constexpr int kWarpRange = TILE / kWarps;
-  constexpr int kS = kWarpRange / 32;
-  const int64_t w_begin = (int64_t)tile * TILE + (int64_t)warp * kWarpRange;
-  const int64_t w_end = min(a.n, w_begin + kWarpRange);
-  int bad = 0;  // already reported by route_hist
-  const WarpKeys<kS, false> K = load_warp_keys<kS, false>(a.idx, w_begin, w_end, kS, E, &bad);
+  //    in order (keys loaded above); the per-warp counts of pass 1 give each warp its first
+  //    position per key.
   __syncthreads();
   warp_count(K, kS, E, wc[warp]);
   __syncthreads();
