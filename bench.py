@@ -309,7 +309,7 @@ PER_CONFIG = ["prefill_dense", "prefill_e64_g32", "prefill_e64_g128", "prefill_e
               "sweep_r4", "sweep_r8", "sweep_r16", "sweep_r32", "sweep_r64", "sweep_r128", "mixtral",
               "decode_dense_m1", "decode_dense_m2", "decode_dense_m4", "decode_dense_m8",
               "decode_moe_m1", "decode_moe_m2", "decode_moe_m4", "decode_moe_m8",
-              "mlp_e64", "mlp_decode_m8", "nn_e4"]
+              "mlp_e64", "mlp_decode_m8", "nn_e4", "nn_e64"]
 ROTATE_L2_MULTIPLE = 4        # distinct input copies cover at least this many times the L2 size
 MAX_COPIES = 96               # ... within this many copies
 MAX_CLONE_BYTES = 24 << 30    # ... and this many bytes of copies

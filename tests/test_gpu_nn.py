@@ -131,3 +131,25 @@ def test_nn_rejects_k_not_a_multiple_of_64():
     with pytest.raises(g.GqmmError) as ei:
         g.gqmm_gather_qmm_nn(x, *dev, idx)
     assert ei.value.code == 2
+
+
+def test_nn_full_size_prefill_shape_sampled_rows():
+    """The benchmark's transpose=False workload at full size (E=64, K=2048, N=768, 16384 routed
+    rows, unsorted), in the launch configuration the benchmark times: quantized weights bit-equal
+    to the oracle's, and a seeded sample of rows (plus one row of every expert) within the
+    parity criteria."""
+    import quantized_moe_expert_device_gb300 as g
+
+    w = wl.workloads()["nn_e64"]
+    host, dev = _weights(w.E, w.H, w.F, w.group_size, seed=wl.SEED_W)
+    x = wl.normal_bf16((w.T, w.A, w.H), wl.SEED_X)
+    idx = wl.make_idx(w)
+    ws = g.new_workspace(w.n, w.F, w.E)
+    y = g.gqmm_gather_qmm_nn(x.cuda(), *dev, to_dev_idx(idx), ws=ws)
+    assert g.gqmm_device_status(ws) == 0
+    rng = np.random.default_rng(3)
+    _, first = np.unique(idx.reshape(-1), return_index=True)
+    rows = np.array(sorted(set(rng.choice(w.n, size=160, replace=False).tolist()) | set(first.tolist()) | {0, w.n - 1}))
+    ref = oracle.gather_qmm_nn(x, *host, idx, w.E, rows=rows)
+    assert_parity(y.reshape(w.n, w.F)[torch.from_numpy(rows).cuda()], ref, "nn_e64 full size")
+    assert torch.isfinite(y.float()).all()

@@ -164,6 +164,8 @@ def workloads() -> Dict[str, Workload]:
         w[f"prefill_e64_{m}"] = Workload(f"prefill_e64_{m}", T=2048, A=8, H=2048, F=768, E=64, routing="uniform",
                                          mode=m, group_size=16 if m == "nvfp4" else 32,
                                          note=f"MoE prefill microbenchmark shape, {m} weights")
+    w["nn_e64"] = Workload("nn_e64", T=2048, A=8, H=2048, F=768, E=64, routing="uniform", kind="nn",
+                           note="transpose=False gather_qmm on the MoE prefill microbenchmark shape (W[e] is [K=2048, N=768])")
     w["nn_e4"] = Workload("nn_e4", T=1024, A=1, H=512, F=512, E=4, routing="uniform", kind="nn",
                           note="transpose=False gather_qmm, E=4, K=N=512, 1024 rows (the mlx PR #4023 follow-up timing)")
     w["prefill_dense"] = Workload("prefill_dense", T=16384, A=1, H=2048, F=768, E=1, routing="dense",
