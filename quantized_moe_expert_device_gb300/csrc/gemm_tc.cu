@@ -13,11 +13,14 @@
 // "amortizing small-M quantized GEMM": per-row qmv re-reads the weights, a 128-wide tile is
 // 94% wasted) the same kernel reads each weight tile once per call for all of its M <= 8 rows.
 //
-// Two variants (template Cfg), chosen on the host from the rows per expert:
-//   wide    chunks of <= 256 rows; 3 stages of (A 2 x 16 KB, x 32 KB) and 3 of codes (8 KB)
-//   narrow  chunks of <= 32 rows; A in tensor memory, 7 stages of x (4 KB) and 13 stages of
-//           codes: with few rows the weight-code stream from HBM is the bottleneck, so the smem
-//           the x tiles do not need goes to a deeper code ring.
+// Three variants (template Cfg), chosen on the host from the rows per expert:
+//   wide    chunks of <= 256 rows; 3 stages of (A 2 x 16 KB, x 32 KB) and 3 of codes (8 KB); the
+//           MMA is M = 128 weight rows x N = the chunk's rows, two tiles per unit
+//   narrow  chunks of <= 32 rows, and mid chunks of <= 128 rows (4-bit affine codes): the operands
+//           swap places (SWAP: M = 128 token rows, N = the unit's 256 weight rows), so a k-block
+//           is 4 full-size MMAs instead of 8 small ones, and a unit's accumulator (token lanes x
+//           256 columns) takes half of tensor memory: the epilogue of one unit runs under the
+//           MMAs of the next.  4 (mid: 3) stages of (A 32 KB, x 4 KB (mid: 16 KB)), 9 of codes.
 // The kernel is also templated on the weight format (formats.cuh: affine codes of 2-8 bits,
 // mxfp4 / nvfp4 / mxfp8, and transpose=False affine weights), which sets the code tile of a
 // k-block and the dequant arithmetic; the rest is shared.
@@ -26,8 +29,8 @@
 // kernel adds the planes in slice order (so results are deterministic) into bf16 y.
 //
 // Per CTA (one per SM, persistent; units taken from a call-wide counter), warp roles (the
-// warp numbers are the wide variant's; the narrow one has 3 dequant groups, warps 0-23, 4
-// epilogue warps that drain both tiles, and 2 gather warps):
+// warp numbers are the wide variant's; the narrow and mid ones have 3 dequant groups, warps
+// 0-23, 4 epilogue warps (one per TMEM lane quarter: 32 tokens each), and 2 gather warps):
 //   warps 0-15  dequant:  two groups of 256 threads take alternate k-blocks; a thread owns one
 //                         of the unit's 256 weight rows: reads its 32 bytes of codes, turns each
 //                         nibble pair into bf16 128 + q (one byte permute and one mask per pair),
@@ -48,8 +51,8 @@
 //                         copies complete the stage's full barrier.  (Measured on all SMs with
 //                         random 128-byte rows: cp.async from 2 warps moves ~9 B/clk/SM and from
 //                         16 warps ~23; gather4 from one thread ~7, from 8 warps ~26.)
-// The accumulators use all 512 TMEM columns, so the MMA of a unit starts once the epilogue has
-// drained the previous one; the producers keep filling stages meanwhile.
+// The wide variant's accumulators use all 512 TMEM columns, so the MMA of a unit starts once the
+// epilogue has drained the previous one; the producers keep filling stages meanwhile.
 //
 // Every wait is bounded (mbar_wait): on expiry the CTA raises GQMM_STATUS_TIMEOUT, unwinds,
 // waits (bounded) for its own copies and MMAs in flight and frees its TMEM.
@@ -86,21 +89,27 @@ constexpr int kUnitQ = 8;  // queue depth: how far the scheduler may run ahead o
 // Variant: largest chunk (UMMA N), code ring depth, and the warp roles: DEQ_GROUPS groups of 8
 // dequant warps (warps 0 ..), EPI_WARPS epilogue warps, then the scheduler/TMA warp, the MMA
 // warp and the gather warps.
-template <int NMAX_, int NIB_STAGES_, int DEQ_GROUPS_, int EPI_WARPS_, bool A_TMEM_, int AB_STAGES_, int W_ = 32>
+// SWAP: the operands trade places: the chunk's x rows are the MMA's A (M = 128 token rows; rows
+// past the chunk's end are never stored) and the unit's 256 dequantized weight rows its B (N = 256),
+// so a k-block takes 4 MMAs of 128 x 256 x 16 instead of 8 of 128 x NMAX x 16, and each unit's
+// accumulator (token lanes x 256 weight-row columns) takes 256 columns: two fit in tensor memory,
+// so the epilogue of one unit overlaps the MMAs of the next.
+template <int NMAX_, int NIB_STAGES_, int DEQ_GROUPS_, int EPI_WARPS_, int AB_STAGES_, int W_ = 32,
+          bool SWAP_ = false>
 struct Cfg {
-  static constexpr int NMAX = NMAX_;              // rows per chunk = largest UMMA N
+  static constexpr bool SWAP = SWAP_;
+  static constexpr int NMAX = NMAX_;              // rows per chunk = largest UMMA N (SWAP: at most M)
   static constexpr int NIB_STAGES = NIB_STAGES_;  // code ring depth
   static constexpr int W = W_;                    // bytes of a weight row's code window per k-block
   static constexpr int NIB_BYTES = UM * W;        // one code stage: the unit's rows' windows
-  // A (dequantized weights) in tensor memory instead of shared memory; AB_STAGES = depth of
-  // the A / x ring.  Tensor memory: accumulators of NMAX columns per tile at column
-  // tile * ACC_COLS, then (A_TMEM) the A stages, NT * 32 columns each (64 bf16 per row).
-  static constexpr bool A_TMEM = A_TMEM_;
+  // AB_STAGES = depth of the A (dequantized weights) / x ring.  Tensor memory: accumulators of
+  // NMAX columns per tile at column tile * ACC_COLS (SWAP: one accumulator of 256 columns per
+  // unit, in one of two slots).
   static constexpr int AB_STAGES = AB_STAGES_;
-  static constexpr int ACC_COLS = NMAX;
-  static constexpr int A_COL0 = NT * ACC_COLS;
-  static_assert(!A_TMEM || A_COL0 + AB_STAGES * NT * 32 <= (int)kTmemCols, "A stages fit in tensor memory");
-  static_assert(A_TMEM || NT * ACC_COLS <= (int)kTmemCols, "accumulators fit in tensor memory");
+  static constexpr int ACC_COLS = SWAP ? UM : NMAX;
+  static constexpr int SLOTS = SWAP ? 2 : 1;
+  static_assert((SWAP ? SLOTS : NT) * ACC_COLS <= (int)kTmemCols, "accumulators fit in tensor memory");
+  static_assert(!SWAP || NMAX <= BM, "SWAP: chunks of at most M rows");
   static constexpr int DEQ_GROUPS = DEQ_GROUPS_;  // dequant groups of kDeqGroup threads, alternate steps
   static constexpr int EPI_WARPS = EPI_WARPS_;    // 4 * NT (one tile each) or 4 (both tiles each)
   static constexpr int EPI_WARP0 = DEQ_GROUPS * kDeqGroup / 32;
@@ -115,12 +124,16 @@ struct Cfg {
   static_assert(EPI_WARPS % 4 == 0 && (NT * 4) % EPI_WARPS == 0, "epilogue warps cover the TMEM lane quarters");
   static_assert(NIB_STAGES > DEQ_GROUPS && AB_STAGES >= DEQ_GROUPS, "a step advances the rings by DEQ_GROUPS");
   static constexpr int B_BYTES = NMAX * BK * 2;
-  static constexpr int OFF_A = 0;
-  static constexpr int OFF_B = OFF_A + (A_TMEM ? 0 : AB_STAGES * A_BYTES);
-  static constexpr int OFF_NIB = OFF_B + AB_STAGES * B_BYTES;
+  // SWAP: the x stages come first: the MMA reads 128 rows (16 KB) from an x stage's start, past its
+  // NMAX written rows into the following stages (rows whose results are never stored), which keeps
+  // every read inside the block's shared memory
+  static constexpr int OFF_A = SWAP ? AB_STAGES * B_BYTES : 0;
+  static constexpr int OFF_B = SWAP ? 0 : OFF_A + AB_STAGES * A_BYTES;
+  static constexpr int OFF_NIB = SWAP ? OFF_A + AB_STAGES * A_BYTES : OFF_B + AB_STAGES * B_BYTES;
+  static_assert(!SWAP || (AB_STAGES - 1) * B_BYTES + BM * BK * 2 <= OFF_NIB, "SWAP: the A reads stay inside");
   static constexpr int OFF_EPI = OFF_NIB + NIB_STAGES * NIB_BYTES;
   static constexpr int OFF_BAR = OFF_EPI + EPI_WARPS * EPI_WARP_BYTES;
-  static constexpr int NUM_BARS = 2 * NIB_STAGES + 2 * AB_STAGES + 3 + 2 * kUnitQ;
+  static constexpr int NUM_BARS = 2 * NIB_STAGES + 2 * AB_STAGES + 5 + 2 * kUnitQ;
   static constexpr int OFF_MISC = OFF_BAR + ((NUM_BARS * 8 + 127) / 128) * 128;
   static constexpr int OFF_UQ = OFF_MISC + 16;
   static constexpr int SMEM_DYN = OFF_UQ + kUnitQ * 32 + 1024;  // room to align the base to 1024 bytes
@@ -136,30 +149,30 @@ struct Cfg {
   // N=16 is more than half the MMA time of the k-block).
   __device__ static int ab_full(int s) { return 2 * NIB_STAGES + s; }
   __device__ static int ab_empty(int s) { return 2 * NIB_STAGES + AB_STAGES + s; }
-  __device__ static int tmem_full() { return 2 * NIB_STAGES + 2 * AB_STAGES; }
-  __device__ static int tmem_empty() { return 2 * NIB_STAGES + 2 * AB_STAGES + 1; }
-  __device__ static int unwind() { return 2 * NIB_STAGES + 2 * AB_STAGES + 2; }
-  __device__ static int uq_full(int q) { return 2 * NIB_STAGES + 2 * AB_STAGES + 3 + q; }
-  __device__ static int uq_empty(int q) { return 2 * NIB_STAGES + 2 * AB_STAGES + 3 + kUnitQ + q; }
+  __device__ static int tmem_full(int slot) { return 2 * NIB_STAGES + 2 * AB_STAGES + slot; }
+  __device__ static int tmem_empty(int slot) { return 2 * NIB_STAGES + 2 * AB_STAGES + 2 + slot; }
+  __device__ static int unwind() { return 2 * NIB_STAGES + 2 * AB_STAGES + 4; }
+  __device__ static int uq_full(int q) { return 2 * NIB_STAGES + 2 * AB_STAGES + 5 + q; }
+  __device__ static int uq_empty(int q) { return 2 * NIB_STAGES + 2 * AB_STAGES + 5 + kUnitQ + q; }
 };
 // wide: 2 dequant groups, 8 epilogue warps, 6 gather warps (x tiles of up to 256 rows need
-// many TMA issuers).  narrow: the x tile is at most 32 rows and the accumulators 32 columns,
-// so 2 gather warps and 4 epilogue warps suffice and a third dequant group takes the rest.
-// The narrow variant keeps A in tensor memory (its accumulators need only 64 columns), which
-// gives it a 7-deep A / x ring next to a 13-deep code ring.
-using CfgWide = Cfg<kChunkRowsWide, 3, 2, 8, false, 3>;
-using CfgNarrow = Cfg<kChunkRowsNarrow, 13, 3, 4, true, 7>;
+// many TMA issuers).  narrow / mid: the x tile is at most 32 / 128 rows, so 2 gather warps and 4
+// epilogue warps suffice and a third dequant group takes the rest.
+using CfgWide = Cfg<kChunkRowsWide, 3, 2, 8, 3>;
 // Other code-window widths (formats.cuh): 16 bytes (2-bit affine); 48 and 64 bytes (3-, 5-, 6-
-// and 8-bit affine, mxfp8), the narrow variant with as many code stages as fit in its code ring
-// budget (13 x 8 KB).
-using CfgWide16 = Cfg<kChunkRowsWide, 3, 2, 8, false, 3, 16>;
-using CfgNarrow16 = Cfg<kChunkRowsNarrow, 13, 3, 4, true, 7, 16>;
-using CfgNarrow48 = Cfg<kChunkRowsNarrow, 8, 3, 4, true, 7, 48>;
-using CfgNarrow64 = Cfg<kChunkRowsNarrow, 6, 3, 4, true, 7, 64>;
-// wide variants for 48- and 64-byte windows: a two-stage A / x ring leaves room for the larger
-// code stages (4 x 12 KB, 3 x 16 KB)
-using CfgWide48 = Cfg<kChunkRowsWide, 4, 2, 8, false, 2, 48>;
-using CfgWide64 = Cfg<kChunkRowsWide, 3, 2, 8, false, 2, 64>;
+// and 8-bit affine, mxfp8).  The wide variants for 48- and 64-byte windows have a two-stage A / x
+// ring, which leaves room for the larger code stages (4 x 12 KB, 3 x 16 KB).
+using CfgWide16 = Cfg<kChunkRowsWide, 3, 2, 8, 3, 16>;
+using CfgWide48 = Cfg<kChunkRowsWide, 4, 2, 8, 2, 48>;
+using CfgWide64 = Cfg<kChunkRowsWide, 3, 2, 8, 2, 64>;
+// narrow (SWAP): x stages of 4 KB ahead of 32 KB weight stages, a 4-deep ring, and as many code
+// stages as fit
+using CfgSwap = Cfg<kChunkRowsNarrow, 9, 3, 4, 4, 32, true>;
+using CfgSwap16 = Cfg<kChunkRowsNarrow, 12, 3, 4, 4, 16, true>;
+using CfgSwap48 = Cfg<kChunkRowsNarrow, 4, 3, 4, 4, 48, true>;
+using CfgSwap64 = Cfg<kChunkRowsNarrow, 4, 3, 4, 4, 64, true>;
+// mid (SWAP, 4-bit affine codes): the same with 16 KB x stages and a 3-deep ring
+using CfgSwapMid = Cfg<kChunkRowsMid, 9, 3, 4, 3, 32, true>;
 
 __device__ __forceinline__ UnitEntry decode_unit(const Chunk* chunks, int u, int n_fpairs, int ksplit, int num_kb) {
   const int ks = u % ksplit;
@@ -237,8 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::uq_full(q)), 1);
       mbar_init(bar(C::uq_empty(q)), C::UNIT_CONSUMER_WARPS);
     }
-    mbar_init(bar(C::tmem_full()), 1);
-    mbar_init(bar(C::tmem_empty()), C::EPI_WARPS);  // one arrival per epilogue warp
+    for (int slot = 0; slot < 2; ++slot) {
+      mbar_init(bar(C::tmem_full(slot)), 1);
+      mbar_init(bar(C::tmem_empty(slot)), C::EPI_WARPS);  // one arrival per epilogue warp
+    }
     mbar_init(bar(C::unwind()), 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -259,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   static_assert(FMT::W == C::W, "the code stages hold this format's windows");
   // transpose=False on the wide variant: A (the dequantized weights) is MN-major, each k-row of a
   // 128-row tile two 64-wide atoms (8 KB apart) of 8 k-rows each (1 KB apart)
-  constexpr bool kAmn = FMT::KIND == kAffineNn && !C::A_TMEM;
+  constexpr bool kAmn = FMT::KIND == kAffineNn;
   constexpr uint32_t kAmnAtomPitch = 8192u;
   constexpr int GS = FMT::GS;
   static_assert(FMT::KIND != kAffine || GS == 32 || GS == 64 || GS == 128, "group sizes");
@@ -385,8 +400,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++qi;
         if (!U.valid) break;
         const int N = (U.rows + 15) & ~15;
-        const uint32_t idesc = umma_idesc_bf16(BM, N) | (kAmn ? kIdescTransposeA : 0u);
-        if (!mbar_wait(bar(C::tmem_empty()), (lu & 1u) ^ 1u, abort_flag, status)) break;
+        // SWAP: M = 128 token rows x N = 256 weight rows, the weights (B) MN-major for transpose=False
+        const uint32_t idesc = C::SWAP ? umma_idesc_bf16(BM, UM) | (kAmn ? kIdescTransposeB : 0u)
+                                       : umma_idesc_bf16(BM, N) | (kAmn ? kIdescTransposeA : 0u);
+        const uint32_t slot = lu % C::SLOTS, use = lu / C::SLOTS;
+        if (!mbar_wait(bar(C::tmem_empty(slot)), (use & 1u) ^ 1u, abort_flag, status)) break;
         tc_fence_after();
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
           const uint32_t s = it % C::AB_STAGES, ph = (it / C::AB_STAGES) & 1u;
@@ -396,15 +414,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint64_t bdesc = umma_desc_sw128(sbase + C::OFF_B + s * C::B_BYTES);
+          if constexpr (C::SWAP) {
+            // A = the x tile (128-byte-swizzled K-major), B = the 256 weight rows of the stage
+            const uint32_t w_addr = sbase + C::OFF_A + s * A_BYTES;
+            const uint64_t wdesc =
+                kAmn ? umma_desc_sw128_mn(w_addr, kAmnAtomPitch, 1024u) : umma_desc_kmajor_interleave(w_addr);
+            const uint32_t wstep = kAmn ? 2048u >> 4 : 256u >> 4;
+            const uint32_t d_tmem = tmem_base + slot * (uint32_t)C::ACC_COLS;
 #pragma unroll
-          for (int t = 0; t < NT; ++t) {
-            const uint32_t d_tmem = tmem_base + (uint32_t)(t * C::ACC_COLS);
-            if (C::A_TMEM) {
-              const uint32_t a_tmem = tmem_base + (uint32_t)(C::A_COL0 + (int)s * NT * 32 + t * 32);
+            for (int k = 0; k < BK / 16; ++k)
+              tc_mma_bf16(d_tmem, bdesc + 2u * k, wdesc + wstep * k, idesc, (kb > U.kb0 || k > 0) ? 1u : 0u);
+          } else {
 #pragma unroll
-              for (int k = 0; k < BK / 16; ++k)  // 16 elements = 8 columns of A, 32 bytes of B
-                tc_mma_bf16_ta(d_tmem, a_tmem + 8u * k, bdesc + 2u * k, idesc, (kb > U.kb0 || k > 0) ? 1u : 0u);
-            } else {
+            for (int t = 0; t < NT; ++t) {
+              const uint32_t d_tmem = tmem_base + (uint32_t)(t * C::ACC_COLS);
               const uint32_t a_addr = sbase + C::OFF_A + s * A_BYTES + t * A_TILE_BYTES;
               // K-major (unswizzled): 16 elements = two 16-byte chunks, 256 bytes on; MN-major: two
               // 8-row atoms (2048 bytes)
@@ -420,7 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++it;
         }
         if (!ok) break;
-        tc_commit(bar(C::tmem_full()));
+        tc_commit(bar(C::tmem_full(slot)));
       }
       // every MMA issued above completes before this barrier's phase 0 completes
       tc_commit(bar(C::unwind()));
@@ -503,9 +526,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int tok = q * 32 + lane;
         prow[q] = tok < U.rows ? (p.y_perm ? __ldg(p.y_perm + U.start + tok) : U.start + tok) : 0;
       }
-      const bool okl = mbar_wait(bar(C::tmem_full()), lu & 1u, abort_flag, status);
+      const uint32_t slot = lu % C::SLOTS, use = lu / C::SLOTS;
+      const bool okl = mbar_wait(bar(C::tmem_full(slot)), use & 1u, abort_flag, status);
       if (!__all_sync(0xffffffffu, okl)) break;
       tc_fence_after();
+      if constexpr (C::SWAP) {
+        // lane = token 32 quarter + lane of the chunk, columns = the unit's 256 weight rows: each
+        // 16-column load is one token's 16 consecutive outputs (32 bytes of y, or 64 of a split-K
+        // plane), stored straight from registers
+        const int tok = quarter * 32 + lane;
+        if (quarter * 32 < U.rows) {  // warp-uniform: the warp's lanes hold tokens of the chunk
+          const bool live = tok < U.rows;
+          const int64_t yrow = live ? (p.y_perm ? __ldg(p.y_perm + U.start + tok) : U.start + tok) : 0;
+          const uint32_t tcol = tmem_base + ((uint32_t)(quarter * 32) << 16) + slot * (uint32_t)C::ACC_COLS;
+          float* plane = U.ks >= 0 ? p.acc + (int64_t)U.ks * p.n * F + (int64_t)(U.start + tok) * F : nullptr;
+          for (int c0 = 0; c0 < UM && U.f0 + c0 < F; c0 += 16) {
+            uint32_t v[16];
+            tc_ld_32x32b_x16(tcol + (uint32_t)c0, v);
+            tc_wait_ld_regs(v);
+            if (!live) continue;
+            const int f = U.f0 + c0;  // F is a multiple of 16: the 16 columns are all in range
+            if (U.ks >= 0) {
+              uint4* dst = reinterpret_cast<uint4*>(plane + f);
+#pragma unroll
+              for (int q = 0; q < 4; ++q) dst[q] = make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            } else {
+              uint32_t h[8];
+#pragma unroll
+              for (int q = 0; q < 8; ++q) {
+                const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[2 * q]), __uint_as_float(v[2 * q + 1]));
+                h[q] = *reinterpret_cast<const uint32_t*>(&b2);
+              }
+              uint4* dst = reinterpret_cast<uint4*>(p.y + yrow * F + f);
+              dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+              dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+            }
+          }
+        }
+      } else
       for (int tt = 0; tt < C::TILES_PER_EPI_WARP; ++tt) {
         const int tile = (ew >> 2) * C::TILES_PER_EPI_WARP + tt;  // accumulator (weight-row tile)
         const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(tile * C::ACC_COLS);
@@ -557,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::tmem_empty()));
+      if (lane == 0) mbar_arrive(bar(C::tmem_empty(slot)));
     }
   } else {
     // ---------------------------------------------------------------- dequant
@@ -635,15 +693,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         sblk = bblk = make_uint4(0, 0, 0, 0);
         return;
       }
-      if constexpr (FMT::KIND == kAffineNn) {
-        // The warp's 32 output columns lie in one scale group (GS >= 32; units start on multiples
-        // of 256): lane l holds (s, b) of k = 64 kb + 2l and 2l + 1 as bf16 pairs, shuffled to
-        // the whole warp while dequantizing.
-        const int64_t at = ((int64_t)U.expert * H + (int64_t)kb * BK + 2 * lane) * G + (U.f0 + (r & ~31)) / GS;
-        sblk.x = (uint32_t)__ldg(sc16 + at) | ((uint32_t)__ldg(sc16 + at + G) << 16);
-        bblk.x = (uint32_t)__ldg(bs16 + at) | ((uint32_t)__ldg(bs16 + at + G) << 16);
-        return;
-      }
       const int64_t row = (int64_t)(U.expert * F + U.f0) + r;  // E * F fits in int
       if constexpr (FMT::KIND != kAffine) {
         const uint8_t* sc8 = reinterpret_cast<const uint8_t*>(p.scales);
@@ -686,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     while (ok && U.valid) {
       const int g = grp_of(kb);
       const uint32_t s2 = pick(sblk, g, false), b2 = pick(bblk, g, false);
-      // transpose=False: this lane's k pair (narrow), or this thread's group(s) (wide)
+      // transpose=False: this thread's group(s)
       const uint32_t nn_s = sblk.x, nn_b = bblk.x, nn_s2 = sblk.y, nn_b2 = bblk.y;
       // floating-point formats: the float32 scale of each 16 weights of the k-block
       float sc4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -745,33 +794,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                        "r"(v.y), "r"(v.z), "r"(v.w)
                        : "memory");
         }
-      } else if constexpr (FMT::KIND == kAffineNn) {
-        // narrow variant (A in tensor memory, K-major): output column n = U.f0 + r takes nibble r
-        // of each of the k-block's 64 code rows (byte r / 2 of a 128-byte row, 128-byte swizzled;
-        // even n in the low nibble), two k per bf16x2 FMA with the pair's scales and biases from
-        // lane j (zero past F: the warp's columns are all live or all dead)
-        const uint32_t stage = nib_tile - (uint32_t)(r * C::W);
-        const uint32_t sh = (uint32_t)(r & 1) * 4u;
-        const uint32_t bchunk = (uint32_t)(r >> 5), boff = (uint32_t)((r >> 1) & 15);
-        auto code_at = [&](int k) -> uint32_t {
-          uint32_t c;
-          asm volatile("ld.shared.u8 %0, [%1];"
-                       : "=r"(c)
-                       : "r"(stage + (uint32_t)(k * 128) + (((bchunk ^ (uint32_t)(k & 7)) << 4) | boff))
-                       : "memory");
-          return (c >> sh) & 0xFu;
-        };
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint32_t v[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j = 4 * c + i;
-            const uint32_t p2 = code_at(2 * j) | (code_at(2 * j + 1) << 16) | 0x43004300u;
-            v[i] = deq_pair(p2, __shfl_sync(0xffffffffu, nn_s, j), __shfl_sync(0xffffffffu, nn_b, j));
-          }
-          o[c] = make_uint4(v[0], v[1], v[2], v[3]);
-        }
       } else if constexpr (FMT::KIND == kAffine && FMT::BITS == 4) {
         uint4 n0, n1;
         asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -783,21 +805,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                      : "r"(nib_tile + nib_c1)
                      : "memory");
         const uint32_t cw[8] = {n0.x, n0.y, n0.z, n0.w, n1.x, n1.y, n1.z, n1.w};
-        if constexpr (!C::A_TMEM) {
-          // wide variant: wait for the A stage first and store each 8-weight piece as soon as it
-          // is computed, so the row's 64 bf16 are never all live in registers at once
-          if (!__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
-          const uint32_t a_row = a_row0 + sa * A_BYTES;
+        // wait for the A stage first and store each 8-weight piece as soon as it is computed, so
+        // the row's 64 bf16 are never all live in registers at once
+        if (!__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
+        const uint32_t a_row = a_row0 + sa * A_BYTES;
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 v = deq8(cw[c], c < 4 ? s2 : s2b, c < 4 ? b2 : b2b);
-            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row + (uint32_t)(c * 128)), "r"(v.x),
-                         "r"(v.y), "r"(v.z), "r"(v.w)
-                         : "memory");
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 8; ++c) o[c] = deq8(cw[c], c < 4 ? s2 : s2b, c < 4 ? b2 : b2b);
+        for (int c = 0; c < 8; ++c) {
+          const uint4 v = deq8(cw[c], c < 4 ? s2 : s2b, c < 4 ? b2 : b2b);
+          asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row + (uint32_t)(c * 128)), "r"(v.x),
+                       "r"(v.y), "r"(v.z), "r"(v.w)
+                       : "memory");
         }
       } else {
         // the row's code window: W / 4 words (for 32-byte windows through the swizzle)
@@ -825,19 +842,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           dequant_e2m1(cw, sc4, o);
         }
       }
-      // (the 4-bit affine and transpose=False rows of the wide variant are already stored)
-      constexpr bool kStored = ((FMT::KIND == kAffine && FMT::BITS == 4) || FMT::KIND == kAffineNn) && !C::A_TMEM;
+      // (the 4-bit affine and transpose=False rows are already stored)
+      constexpr bool kStored = (FMT::KIND == kAffine && FMT::BITS == 4) || FMT::KIND == kAffineNn;
       if (!kStored && !__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
-      if (kStored) {
-      } else if (C::A_TMEM) {
-        // the row's 64 bf16 into the warp's TMEM lane quarter, 32 columns of the A stage
-        tc_fence_after();  // after the MMA that last read this stage (ab_empty)
-        const uint32_t taddr = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) +
-                               (uint32_t)(C::A_COL0 + (int)sa * NT * 32 + tile * 32);
-        tc_st_32x32b_x32(taddr, o);
-        tc_wait_st();
-        tc_fence_before();
-      } else {
+      if (!kStored) {
         const uint32_t a_row = a_row0 + sa * A_BYTES;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
@@ -936,17 +944,6 @@ cudaError_t configure_all() {
   need(set_smem<CfgWide16, FmtAffine<64, 2>>());
   need(set_smem<CfgWide, FmtMx<false>>());
   need(set_smem<CfgWide, FmtNv>());
-  need(set_smem<CfgNarrow, FmtAffine<32, 4>>());
-  need(set_smem<CfgNarrow, FmtAffine<64, 4>>());
-  need(set_smem<CfgNarrow, FmtAffine<128, 4>>());
-  need(set_smem<CfgNarrow16, FmtAffine<64, 2>>());
-  need(set_smem<CfgNarrow48, FmtAffine<64, 3>>());
-  need(set_smem<CfgNarrow48, FmtAffine<64, 5>>());
-  need(set_smem<CfgNarrow48, FmtAffine<64, 6>>());
-  need(set_smem<CfgNarrow64, FmtAffine<64, 8>>());
-  need(set_smem<CfgNarrow, FmtMx<false>>());
-  need(set_smem<CfgNarrow, FmtNv>());
-  need(set_smem<CfgNarrow64, FmtMx<true>>());
   need(set_smem<CfgWide48, FmtAffine<64, 3>>());
   need(set_smem<CfgWide48, FmtAffine<64, 5>>());
   need(set_smem<CfgWide48, FmtAffine<64, 6>>());
@@ -955,9 +952,23 @@ cudaError_t configure_all() {
   need(set_smem<CfgWide, FmtNn<32>>());
   need(set_smem<CfgWide, FmtNn<64>>());
   need(set_smem<CfgWide, FmtNn<128>>());
-  need(set_smem<CfgNarrow, FmtNn<32>>());
-  need(set_smem<CfgNarrow, FmtNn<64>>());
-  need(set_smem<CfgNarrow, FmtNn<128>>());
+  need(set_smem<CfgSwapMid, FmtAffine<32, 4>>());
+  need(set_smem<CfgSwapMid, FmtAffine<64, 4>>());
+  need(set_smem<CfgSwapMid, FmtAffine<128, 4>>());
+  need(set_smem<CfgSwap, FmtAffine<32, 4>>());
+  need(set_smem<CfgSwap, FmtAffine<64, 4>>());
+  need(set_smem<CfgSwap, FmtAffine<128, 4>>());
+  need(set_smem<CfgSwap16, FmtAffine<64, 2>>());
+  need(set_smem<CfgSwap48, FmtAffine<64, 3>>());
+  need(set_smem<CfgSwap48, FmtAffine<64, 5>>());
+  need(set_smem<CfgSwap48, FmtAffine<64, 6>>());
+  need(set_smem<CfgSwap64, FmtAffine<64, 8>>());
+  need(set_smem<CfgSwap, FmtMx<false>>());
+  need(set_smem<CfgSwap, FmtNv>());
+  need(set_smem<CfgSwap64, FmtMx<true>>());
+  need(set_smem<CfgSwap, FmtNn<32>>());
+  need(set_smem<CfgSwap, FmtNn<64>>());
+  need(set_smem<CfgSwap, FmtNn<128>>());
   return e;
 }
 
@@ -979,7 +990,7 @@ using FmtNn32 = FmtNn<32>;
 using FmtNn64 = FmtNn<64>;
 using FmtNn128 = FmtNn<128>;
 
-GemmKernel pick_instance(const GemmArgs& a, bool narrow, int* smem) {
+GemmKernel pick_instance(const GemmArgs& a, bool narrow, bool mid, int* smem) {
 #define GQMM_PICK(CFG, FMT)      \
   do {                           \
     *smem = CFG::SMEM_DYN;       \
@@ -987,9 +998,14 @@ GemmKernel pick_instance(const GemmArgs& a, bool narrow, int* smem) {
   } while (0)
   if (a.kind == kAffine && a.bits == 4) {
     if (narrow) {
-      if (a.group_size == 32) GQMM_PICK(CfgNarrow, FmtA4g32);
-      if (a.group_size == 128) GQMM_PICK(CfgNarrow, FmtA4g128);
-      GQMM_PICK(CfgNarrow, FmtA4g64);
+      if (a.group_size == 32) GQMM_PICK(CfgSwap, FmtA4g32);
+      if (a.group_size == 128) GQMM_PICK(CfgSwap, FmtA4g128);
+      GQMM_PICK(CfgSwap, FmtA4g64);
+    }
+    if (mid) {
+      if (a.group_size == 32) GQMM_PICK(CfgSwapMid, FmtA4g32);
+      if (a.group_size == 128) GQMM_PICK(CfgSwapMid, FmtA4g128);
+      GQMM_PICK(CfgSwapMid, FmtA4g64);
     }
     if (a.group_size == 32) GQMM_PICK(CfgWide, FmtA4g32);
     if (a.group_size == 128) GQMM_PICK(CfgWide, FmtA4g128);
@@ -997,44 +1013,44 @@ GemmKernel pick_instance(const GemmArgs& a, bool narrow, int* smem) {
   }
   if (a.kind == kAffineNn) {
     if (narrow) {
-      if (a.group_size == 32) GQMM_PICK(CfgNarrow, FmtNn32);
-      if (a.group_size == 128) GQMM_PICK(CfgNarrow, FmtNn128);
-      GQMM_PICK(CfgNarrow, FmtNn64);
+      if (a.group_size == 32) GQMM_PICK(CfgSwap, FmtNn32);
+      if (a.group_size == 128) GQMM_PICK(CfgSwap, FmtNn128);
+      GQMM_PICK(CfgSwap, FmtNn64);
     }
     if (a.group_size == 32) GQMM_PICK(CfgWide, FmtNn32);
     if (a.group_size == 128) GQMM_PICK(CfgWide, FmtNn128);
     GQMM_PICK(CfgWide, FmtNn64);
   }
   if (a.kind == kAffine && a.bits == 2) {
-    if (narrow) GQMM_PICK(CfgNarrow16, FmtA2);
+    if (narrow) GQMM_PICK(CfgSwap16, FmtA2);
     GQMM_PICK(CfgWide16, FmtA2);
   }
   if (a.kind == kMxfp4) {
-    if (narrow) GQMM_PICK(CfgNarrow, FmtMxfp4);
+    if (narrow) GQMM_PICK(CfgSwap, FmtMxfp4);
     GQMM_PICK(CfgWide, FmtMxfp4);
   }
   if (a.kind == kNvfp4) {
-    if (narrow) GQMM_PICK(CfgNarrow, FmtNv);
+    if (narrow) GQMM_PICK(CfgSwap, FmtNv);
     GQMM_PICK(CfgWide, FmtNv);
   }
   if (a.kind == kMxfp8) {
-    if (narrow) GQMM_PICK(CfgNarrow64, FmtMxfp8);
+    if (narrow) GQMM_PICK(CfgSwap64, FmtMxfp8);
     GQMM_PICK(CfgWide64, FmtMxfp8);
   }
   if (a.kind == kAffine && a.bits == 8) {
-    if (narrow) GQMM_PICK(CfgNarrow64, FmtA8);
+    if (narrow) GQMM_PICK(CfgSwap64, FmtA8);
     GQMM_PICK(CfgWide64, FmtA8);
   }
   if (a.kind == kAffine && a.bits == 3) {
-    if (narrow) GQMM_PICK(CfgNarrow48, FmtA3);
+    if (narrow) GQMM_PICK(CfgSwap48, FmtA3);
     GQMM_PICK(CfgWide48, FmtA3);
   }
   if (a.kind == kAffine && a.bits == 5) {
-    if (narrow) GQMM_PICK(CfgNarrow48, FmtA5);
+    if (narrow) GQMM_PICK(CfgSwap48, FmtA5);
     GQMM_PICK(CfgWide48, FmtA5);
   }
   if (a.kind == kAffine && a.bits == 6) {
-    if (narrow) GQMM_PICK(CfgNarrow48, FmtA6);
+    if (narrow) GQMM_PICK(CfgSwap48, FmtA6);
     GQMM_PICK(CfgWide48, FmtA6);
   }
 #undef GQMM_PICK
@@ -1081,8 +1097,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
     encode = reinterpret_cast<decltype(&cuTensorMapEncodeTiled)>(fn);
   }
   const bool narrow = a.chunk_rows <= kChunkRowsNarrow;
+  const bool mid = !narrow && a.chunk_rows <= kChunkRowsMid;
   int smem = 0;
-  GemmKernel kern = pick_instance(a, narrow, &smem);
+  GemmKernel kern = pick_instance(a, narrow, mid, &smem);
   if (kern == nullptr) return cudaErrorInvalidValue;
   // Packed codes as an [E*F, row bytes] byte matrix; one box = the unit's 256 rows x one k-block's
   // code window (W bytes: formats.cuh), 32-byte swizzled when W is 32 so the dequant threads read

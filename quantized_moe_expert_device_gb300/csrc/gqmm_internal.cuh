@@ -48,6 +48,8 @@ inline int route_tile(int64_t n) {
 constexpr int64_t kSmallMaxN = 4096;          // unsorted calls up to this size: one route block
 constexpr int64_t kTinyMaxN = 256;            // ... and up to this size: one entry per thread
 constexpr int kChunkRowsWide = 256;           // tokens per work unit, wide GEMM variant
+constexpr int kChunkRowsMid = 128;            // tokens per work unit, mid GEMM variant
+constexpr int kMidMaxAvgRows = 64;            // ... taken up to this many rows per expert on average
 constexpr int kChunkRowsNarrow = 32;          // tokens per work unit, narrow GEMM variant
 constexpr int kMaxExperts = GQMM_MAX_EXPERTS;
 constexpr int kUnitRows = 256;                // weight rows per work unit (two 128-row tiles)
@@ -64,7 +66,8 @@ constexpr int kStreamMoeRows = 2;             // or a routed call in chunks of <
 // so the workspace size (which depends on it) is known before any device work:
 //   up to 8 for decode-sized calls (the weight-streaming path: one dense call of n <= 8 rows,
 //   or at most 1.5 rows per hit expert on average in chunks of 2, so a second row of an expert
-//   does not stream its weights again), else 32 (narrow) or 256 (wide).
+//   does not stream its weights again), else 32 (narrow: at most 32 rows per expert on average),
+//   128 (mid: at most 64) or 256 (wide).
 inline int chunk_rows_for(int64_t n, int E) {
   const int64_t busy = n < E ? n : E;  // experts that can have rows
   if (busy <= 0) return kChunkRowsWide;
@@ -74,7 +77,7 @@ inline int chunk_rows_for(int64_t n, int E) {
     if (2 * n <= 3 * busy) return kStreamMoeRows;
   }
   const int64_t avg = (n + busy - 1) / busy;
-  return avg <= kChunkRowsNarrow ? kChunkRowsNarrow : kChunkRowsWide;
+  return avg <= kChunkRowsNarrow ? kChunkRowsNarrow : avg <= kMidMaxAvgRows ? kChunkRowsMid : kChunkRowsWide;
 }
 
 // How a call is split into work units.  A pure function of the sizes.
@@ -200,7 +203,8 @@ struct GemmArgs {
   float* acc;           // [ksplit, n, F] split-K partial sums (ks_cap > 1)
   const int32_t* offsets;  // [E + 1]; offsets[E] = valid sorted positions (split-K finalize)
   int H, F, E;
-  int chunk_rows;       // rows per chunk: <= kChunkRowsNarrow selects the narrow variant
+  int chunk_rows;       // rows per chunk: <= kChunkRowsNarrow selects the narrow variant, kChunkRowsMid
+                        // the mid one (4-bit affine codes; other formats run such chunks on the wide one)
   int ks_cap;           // > 1: the plan step may split K (header->ksplit) and the finalize runs
   int dense_plan;       // 1: idx is NULL, so the plan is the single chunk (expert 0, start 0, n rows)
   int group_size = 64;  // quantization group along H: 32, 64 or 128 (the streaming kernels: 64)
@@ -444,36 +448,6 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 }
 
 // Each thread of the warp reads 16 consecutive 32-bit columns of its own TMEM lane.
-// D[tmem] (+)= A[tmem] * B[smem desc]^T, bf16 inputs, f32 accumulate; A (M rows in lanes, K
-// along columns, two bf16 per 32-bit column) in tensor memory.
-__device__ __forceinline__ void tc_mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                               uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// 32 lanes x 32 columns of 32 bits from registers (thread i writes lane base + i; v[c] holds
-// columns 4c .. 4c + 3).  Warp-collective.
-__device__ __forceinline__ void tc_st_32x32b_x32(uint32_t taddr, const uint4 (&v)[8]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {"
-      "%1, %2, %3, %4, %5, %6, %7, %8, "
-      "%9, %10, %11, %12, %13, %14, %15, %16, "
-      "%17, %18, %19, %20, %21, %22, %23, %24, "
-      "%25, %26, %27, %28, %29, %30, %31, %32"
-      "};" ::"r"(taddr),
-        "r"(v[0].x), "r"(v[0].y), "r"(v[0].z), "r"(v[0].w), "r"(v[1].x), "r"(v[1].y), "r"(v[1].z), "r"(v[1].w),
-        "r"(v[2].x), "r"(v[2].y), "r"(v[2].z), "r"(v[2].w), "r"(v[3].x), "r"(v[3].y), "r"(v[3].z), "r"(v[3].w),
-        "r"(v[4].x), "r"(v[4].y), "r"(v[4].z), "r"(v[4].w), "r"(v[5].x), "r"(v[5].y), "r"(v[5].z), "r"(v[5].w),
-        "r"(v[6].x), "r"(v[6].y), "r"(v[6].z), "r"(v[6].w), "r"(v[7].x), "r"(v[7].y), "r"(v[7].z), "r"(v[7].w)
-      : "memory");
-}
-__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
 __device__ __forceinline__ void tc_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -545,6 +519,7 @@ __device__ __forceinline__ uint32_t umma_idesc_bf16(int M, int N) {
   return d;
 }
 constexpr uint32_t kIdescTransposeA = 1u << 15;  // A is MN-major
+constexpr uint32_t kIdescTransposeB = 1u << 16;  // B is MN-major
 
 #endif  // __CUDACC__
 
