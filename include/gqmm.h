@@ -222,7 +222,8 @@ GQMM_API int gqmm_gather_qmm(const void* x, const void* wq, const void* scales, 
  *           scales and tscale 4-byte aligned
  *  mode     GQMM_MODE_MXFP4, GQMM_MODE_NVFP4 (needs tscale) or GQMM_MODE_MXFP8
  *  the rest as for gqmm_gather_qmm (H a positive multiple of 64; the same workspace size).
- * mxfp4 and nvfp4 run on both tensor-core variants; mxfp8 on the narrow one.
+ * Every mode runs on the wide tensor-core variant and on the narrow one (at most 32 rows per
+ * expert on average).
  * Errors: as gqmm_gather_qmm.
  */
 GQMM_API int gqmm_gather_qmm_fp(const void* x, const void* wq, const void* scales, const float* tscale,
@@ -399,7 +400,7 @@ GQMM_API void gqmm_test_stall_next(int n);
 #define GQMM_VARIANT_ROUTE_UNSORTED 0 /* histogram + scatter route sort */
 #define GQMM_VARIANT_ROUTE_SORTED 1   /* segment boundaries from caller-sorted idx */
 #define GQMM_VARIANT_ROUTE_DENSE 2    /* idx == NULL, E == 1 */
-#define GQMM_VARIANT_GEMM_TC 3        /* tcgen05 grouped GEMM, chunks of up to 256 rows */
+#define GQMM_VARIANT_GEMM_TC 3        /* tcgen05 grouped GEMM, chunks of up to 256 rows (128: mid variant) */
 #define GQMM_VARIANT_GEMM_NARROW 4    /* tcgen05 grouped GEMM, chunks of up to 32 rows */
 #define GQMM_VARIANT_SPLIT_K 5        /* K split into slices, fp32 partial sums + finalize */
 #define GQMM_VARIANT_GEMV 6           /* weight-streaming CUDA-core kernel: routed chunks of 1-2 rows, dense 1 row */

@@ -223,7 +223,9 @@ int launch_projection(const GemmArgs& ga, const UnitShape& shape, int sms, cudaS
                  : route_variant == GQMM_VARIANT_ROUTE_SORTED ? "sorted"
                  : route_variant == GQMM_VARIANT_ROUTE_FUSED ? "in-kernel" : "unsorted",
                  shape.stream ? (stream_mma ? "stream-mma" : "stream")
-                 : shape.chunk_rows <= kChunkRowsNarrow ? "narrow" : "wide",
+                 : shape.chunk_rows <= kChunkRowsNarrow ? "narrow"
+                 : shape.chunk_rows <= kChunkRowsMid    ? "mid"
+                                                        : "wide",
                  ga.ks_cap);
   return GQMM_OK;
 }
