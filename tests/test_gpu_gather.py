@@ -68,6 +68,33 @@ def test_rows_per_expert_regimes(rows_per_expert):
     assert_parity(y, y_ref, f"r={rows_per_expert}")
 
 
+@pytest.mark.parametrize("gs", [32, 64, 128])
+def test_mid_variant_uneven_experts(gs):
+    """33-64 routed rows per expert on average run on the mid variant (operands swapped: the chunk's
+    tokens are the MMA's M rows, 256 weight rows its N; chunks of up to 128 tokens).  Experts of 150
+    down to 2 rows (so one chunk splits at 128), F = 400 (a partial second 256-row unit), every group
+    size, against the oracle; caller-sorted indices give the same bits as the unsorted call."""
+    import quantized_moe_expert_device_gb300 as g
+
+    E, F, H = 6, 400, 1024
+    sizes = [150, 100, 40, 30, 10, 2]  # 332 rows: 56 per expert on average
+    w = wl.normal_bf16((E, F, H), wl.SEED_W, chunk_rows=1)
+    host_w = oracle.quantize(w, group_size=gs)
+    dev_w = g.gqmm_quantize(w.cuda(), group_size=gs)
+    idx = np.random.default_rng(gs).permutation(np.repeat(np.arange(E, dtype=np.uint32), sizes)).reshape(-1, 1)
+    n = idx.shape[0]
+    x = wl.normal_bf16((n, 1, H), wl.SEED_X)
+    ws = g.new_workspace(n, F, E)
+    y = g.gqmm_gather_qmm(x.cuda(), *dev_w, to_dev_idx(idx), group_size=gs, ws=ws)
+    assert g.gqmm_device_status(ws) == 0
+    assert_parity(y.reshape(n, F), oracle.gather_qmm(x, *host_w, idx, E, group_size=gs), f"mid gs={gs}")
+    idx_s = np.sort(idx.reshape(-1)).reshape(-1, 1)
+    y_s = g.gqmm_gather_qmm(x.cuda(), *dev_w, to_dev_idx(idx_s), group_size=gs, sorted_indices=True)
+    y_u = g.gqmm_gather_qmm(x.cuda(), *dev_w, to_dev_idx(idx_s), group_size=gs, sorted_indices=False)
+    torch.cuda.synchronize()
+    assert torch.equal(y_s, y_u)
+
+
 def test_unaligned_78_row_batch_sorted_and_unsorted():
     E, F, H = 4, 128, 1024
     host_w, dev_w = _weights(E, F, H)
