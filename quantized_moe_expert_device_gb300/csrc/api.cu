@@ -216,17 +216,20 @@ int launch_projection(const GemmArgs& ga, const UnitShape& shape, int sms, cudaS
   count_variant(shape.stream ? (stream_mma ? GQMM_VARIANT_GEMV_MMA : GQMM_VARIANT_GEMV)
                 : shape.chunk_rows <= kChunkRowsNarrow ? GQMM_VARIANT_GEMM_NARROW : GQMM_VARIANT_GEMM_TC);
   if (ga.ks_cap > 1) count_variant(GQMM_VARIANT_SPLIT_K);
+  int workers = sms;
+  if (log_dispatch() && !shape.stream) (void)gemm_tc_workers(ga.kind, ga.bits, shape.chunk_rows, &workers);
   if (log_dispatch())
-    std::fprintf(stderr, "[gqmm] %s n=%lld H=%d F=%d E=%d route=%s gemm=%s ks_cap=%d\n", what, (long long)ga.n, ga.H,
-                 ga.F, ga.E,
+    std::fprintf(stderr, "[gqmm] %s n=%lld H=%d F=%d E=%d route=%s gemm=%s ks_cap=%d workers=%d\n", what,
+                 (long long)ga.n, ga.H, ga.F, ga.E,
                  route_variant == GQMM_VARIANT_ROUTE_DENSE ? "dense"
                  : route_variant == GQMM_VARIANT_ROUTE_SORTED ? "sorted"
                  : route_variant == GQMM_VARIANT_ROUTE_FUSED ? "in-kernel" : "unsorted",
                  shape.stream ? (stream_mma ? "stream-mma" : "stream")
                  : shape.chunk_rows <= kChunkRowsNarrow ? "narrow"
                  : shape.chunk_rows <= kChunkRowsMid    ? "mid"
+                 : shape.chunk_rows > kChunkRowsWide    ? "pair"
                                                         : "wide",
-                 ga.ks_cap);
+                 ga.ks_cap, workers);
   return GQMM_OK;
 }
 
@@ -256,6 +259,14 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
     return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
   rc = check_device(nullptr);
   if (rc) return rc;
+  // wide 4-bit affine calls of more than 256 rows per expert run on CTA pairs, in chunks of up to
+  // 512 rows, when the device holds any
+  if (!shape.stream) {
+    int cr = shape.chunk_rows;
+    cudaError_t ce = gemm_tc_chunk_rows(kind, kind == kAffine ? bits : 4, shape.chunk_rows, n, E, &cr);
+    if (ce != cudaSuccess) return fail(GQMM_ERR_CUDA, "device query: %s", cudaGetErrorString(ce));
+    shape.chunk_rows = cr;
+  }
   uint8_t* w = static_cast<uint8_t*>(ws);
   WsHeader* header = reinterpret_cast<WsHeader*>(w);
   if (clear_header) {
@@ -282,7 +293,13 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   int sms = 0;
   cudaError_t e = device_sm_count(&sms);
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
-  ra.sms = sms;
+  // the plan step starts the tensor-core GEMM's unit counter at its number of unit workers
+  int workers = sms;
+  if (!shape.stream) {
+    e = gemm_tc_workers(kind, kind == kAffine ? bits : 4, shape.chunk_rows, &workers);
+    if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+  }
+  ra.sms = workers;
   // Decode-sized calls on the weight-streaming path need no route kernel: a dense call's plan is
   // the single chunk, and an unsorted routed call of at most kFusedPlanMaxRows rows on the CUDA-core
   // streaming kernel is planned inside that kernel.  Such a call is one programmatic-dependent
@@ -388,7 +405,13 @@ int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, cons
   ra.chunk_rows = shape1.chunk_rows;
   ra.n_fpairs = (2 * I + kUnitRows - 1) / kUnitRows;
   ra.ks_cap = 1;
-  ra.sms = sms;
+  // unit workers of each projection's tensor-core GEMM (the plan step and the gating kernel
+  // start the unit counter at these)
+  int workers1 = sms, workers2 = sms;
+  if (!shape1.stream) e = gemm_tc_workers(kAffine, bits, shape1.chunk_rows, &workers1);
+  if (e == cudaSuccess && !shape2.stream) e = gemm_tc_workers(kAffine, bits, shape2.chunk_rows, &workers2);
+  if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "device query: %s", cudaGetErrorString(e));
+  ra.sms = workers1;
   const bool permuted = idx != nullptr && !sorted;
   int launched = 0;
   e = launch_route(ra, s, &launched);
@@ -422,7 +445,7 @@ int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, cons
   rc = launch_projection(g1, shape1, sms, s, "moe_mlp gate/up", route_variant);
   if (rc) return rc;
 
-  e = launch_glu(h1, hg, n, I, activation, header, sms, s);
+  e = launch_glu(h1, hg, n, I, activation, header, sms, workers2, s);
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "gating launch: %s", cudaGetErrorString(e));
   g_launches.fetch_add(1);
 

@@ -68,11 +68,9 @@ constexpr int UM = BM * NT;              // weight rows per unit
 static_assert(UM == kUnitRows, "unit height");
 constexpr int BK = 64;                   // K per stage = one quantization group
 constexpr int A_TILE_BYTES = BM * BK * 2;      // 16 KB bf16
-constexpr int A_BYTES = NT * A_TILE_BYTES;     // 32 KB
 constexpr int EPI_WARP_BYTES = 16 * 32 * 2;
 
 constexpr int kThreads = 1024;
-constexpr int kDeqGroup = UM;            // threads per dequant group (one per weight row)
 constexpr uint32_t kTmemCols = 512;      // the whole tensor memory of the SM
 
 // A work unit as the scheduler hands it to the CTA's roles (one entry of the unit queue), or
@@ -88,31 +86,38 @@ constexpr int kUnitQ = 8;  // queue depth: how far the scheduler may run ahead o
 
 // Variant: largest chunk (UMMA N), code ring depth, and the warp roles: DEQ_GROUPS groups of 8
 // dequant warps (warps 0 ..), EPI_WARPS epilogue warps, then the scheduler/TMA warp, the MMA
-// warp and the gather warps.
+// warp and the gather warps.  PAIR: a cluster of two CTAs computes each unit with cta_group::2
+// MMAs of M = 256 and units of up to 512 tokens (see the pair notes at the top of the kernel).
 // SWAP: the operands trade places: the chunk's x rows are the MMA's A (M = 128 token rows; rows
 // past the chunk's end are never stored) and the unit's 256 dequantized weight rows its B (N = 256),
 // so a k-block takes 4 MMAs of 128 x 256 x 16 instead of 8 of 128 x NMAX x 16, and each unit's
 // accumulator (token lanes x 256 weight-row columns) takes 256 columns: two fit in tensor memory,
 // so the epilogue of one unit overlaps the MMAs of the next.
 template <int NMAX_, int NIB_STAGES_, int DEQ_GROUPS_, int EPI_WARPS_, int AB_STAGES_, int W_ = 32,
-          bool SWAP_ = false>
+          bool SWAP_ = false, bool PAIR_ = false>
 struct Cfg {
   static constexpr bool SWAP = SWAP_;
+  static constexpr bool PAIR = PAIR_;
   static constexpr int NMAX = NMAX_;              // rows per chunk = largest UMMA N (SWAP: at most M)
   static constexpr int NIB_STAGES = NIB_STAGES_;  // code ring depth
   static constexpr int W = W_;                    // bytes of a weight row's code window per k-block
-  static constexpr int NIB_BYTES = UM * W;        // one code stage: the unit's rows' windows
+  static constexpr int ROWS = PAIR ? BM : UM;     // weight rows of a unit this CTA dequantizes
+  static constexpr int CT = PAIR ? 1 : NT;        // A tiles of a stage in this CTA
+  static constexpr int A_BYTES = CT * A_TILE_BYTES;
+  static constexpr int NIB_BYTES = ROWS * W;      // one code stage: this CTA's rows' windows
   // AB_STAGES = depth of the A (dequantized weights) / x ring.  Tensor memory: accumulators of
   // NMAX columns per tile at column tile * ACC_COLS (SWAP: one accumulator of 256 columns per
-  // unit, in one of two slots).
+  // unit, in one of two slots; PAIR: this CTA's 128 weight rows x the unit's up to 512 tokens,
+  // column = token).
   static constexpr int AB_STAGES = AB_STAGES_;
   static constexpr int ACC_COLS = SWAP ? UM : NMAX;
   static constexpr int SLOTS = SWAP ? 2 : 1;
-  static_assert((SWAP ? SLOTS : NT) * ACC_COLS <= (int)kTmemCols, "accumulators fit in tensor memory");
+  static_assert((SWAP ? SLOTS : PAIR ? 1 : NT) * ACC_COLS <= (int)kTmemCols, "accumulators fit in tensor memory");
   static_assert(!SWAP || NMAX <= BM, "SWAP: chunks of at most M rows");
-  static constexpr int DEQ_GROUPS = DEQ_GROUPS_;  // dequant groups of kDeqGroup threads, alternate steps
+  static_assert(!PAIR || (!SWAP && NMAX == 2 * UM), "PAIR: units of up to 512 tokens, two N tiles of 256");
+  static constexpr int DEQ_GROUPS = DEQ_GROUPS_;  // dequant groups of ROWS threads, alternate steps
   static constexpr int EPI_WARPS = EPI_WARPS_;    // 4 * NT (one tile each) or 4 (both tiles each)
-  static constexpr int EPI_WARP0 = DEQ_GROUPS * kDeqGroup / 32;
+  static constexpr int EPI_WARP0 = DEQ_GROUPS * ROWS / 32;
   static constexpr int TMA_WARP = EPI_WARP0 + EPI_WARPS;
   static constexpr int MMA_WARP = TMA_WARP + 1;
   static constexpr int GATHER_WARP0 = MMA_WARP + 1;
@@ -121,9 +126,14 @@ struct Cfg {
   // warps that pop every unit: all but the scheduler's
   static constexpr int UNIT_CONSUMER_WARPS = EPI_WARP0 + EPI_WARPS + GATHER_WARPS + 1;
   static_assert(GATHER_WARPS >= 1 && UNIT_CONSUMER_WARPS == kThreads / 32 - 1, "warp roles fill the block");
+  // releases of a unit-queue entry the scheduler waits for (PAIR: the odd CTA's warps too, its
+  // scheduler warp among them, which loads that CTA's codes)
+  static constexpr int UQ_RELEASES = PAIR ? UNIT_CONSUMER_WARPS + kThreads / 32 : UNIT_CONSUMER_WARPS;
   static_assert(EPI_WARPS % 4 == 0 && (NT * 4) % EPI_WARPS == 0, "epilogue warps cover the TMEM lane quarters");
   static_assert(NIB_STAGES > DEQ_GROUPS && AB_STAGES >= DEQ_GROUPS, "a step advances the rings by DEQ_GROUPS");
-  static constexpr int B_BYTES = NMAX * BK * 2;
+  // x rows of a stage in this CTA (PAIR: its halves of the two N tiles, 128 rows apart)
+  static constexpr int B_ROWS = PAIR ? NMAX / 2 : NMAX;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
   // SWAP: the x stages come first: the MMA reads 128 rows (16 KB) from an x stage's start, past its
   // NMAX written rows into the following stages (rows whose results are never stored), which keeps
   // every read inside the block's shared memory
@@ -173,6 +183,9 @@ using CfgSwap48 = Cfg<kChunkRowsNarrow, 4, 3, 4, 4, 48, true>;
 using CfgSwap64 = Cfg<kChunkRowsNarrow, 4, 3, 4, 4, 64, true>;
 // mid (SWAP, 4-bit affine codes): the same with 16 KB x stages and a 3-deep ring
 using CfgSwapMid = Cfg<kChunkRowsMid, 9, 3, 4, 3, 32, true>;
+// CTA pairs (4-bit affine, chunks of up to 512 rows): per CTA 128 weight rows and up to 256 x rows a
+// unit, so a stage is 16 + 32 KB: a 4-deep ring, a 5-deep code ring, four dequant groups of 128
+using CfgPair = Cfg<kChunkRowsPair, 5, 4, 8, 4, 32, false, true>;
 
 __device__ __forceinline__ UnitEntry decode_unit(const Chunk* chunks, int u, int n_fpairs, int ksplit, int num_kb) {
   const int ks = u % ksplit;
@@ -235,24 +248,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sbase + C::OFF_BAR + 8u * (uint32_t)i; };
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // CTA pairs: rank 0 (the even CTA) schedules the units and issues the MMAs; rank 1 holds weight
+  // rows 128.. of each unit and the second half of each N tile's x rows.  The unit queue's entries
+  // are written into the odd CTA by the even one, so its barriers are released and acquired at
+  // cluster scope; the per-stage and per-accumulator handshakes are plain remote arrivals.
+  constexpr bool PAIR = C::PAIR;
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = crank == 0;
+  const int rbase = PAIR ? (int)crank * BM : 0;  // first weight row of the unit in this CTA
+  auto peer_bar = [&](int i) -> uint32_t { return mapa_shared(bar(i), crank ^ 1u); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NIB_STAGES; ++s) {
       mbar_init(bar(C::nib_full(s)), 1);
-      mbar_init(bar(C::nib_empty(s)), kDeqGroup / 32);  // one arrival per warp of the group that consumed it
+      mbar_init(bar(C::nib_empty(s)), C::ROWS / 32);  // one arrival per warp of the group that consumed it
     }
     for (int s = 0; s < C::AB_STAGES; ++s) {
-      // one arrival per warp of the dequant group that wrote A and per gather warp
-      mbar_init(bar(C::ab_full(s)), kDeqGroup / 32 + C::GATHER_WARPS);
+      // one arrival per warp of the dequant group that wrote A and per gather warp (PAIR, even
+      // CTA: and one from the odd CTA when its A and x of the stage are written)
+      mbar_init(bar(C::ab_full(s)), C::ROWS / 32 + C::GATHER_WARPS + (PAIR && leader ? 1 : 0));
       mbar_init(bar(C::ab_empty(s)), 1);
     }
     for (int q = 0; q < kUnitQ; ++q) {
       mbar_init(bar(C::uq_full(q)), 1);
-      mbar_init(bar(C::uq_empty(q)), C::UNIT_CONSUMER_WARPS);
+      mbar_init(bar(C::uq_empty(q)), C::UQ_RELEASES);
     }
     for (int slot = 0; slot < 2; ++slot) {
       mbar_init(bar(C::tmem_full(slot)), 1);
-      mbar_init(bar(C::tmem_empty(slot)), C::EPI_WARPS);  // one arrival per epilogue warp
+      // one arrival per epilogue warp (PAIR: of both CTAs)
+      mbar_init(bar(C::tmem_empty(slot)), PAIR ? 2 * C::EPI_WARPS : C::EPI_WARPS);
     }
     mbar_init(bar(C::unwind()), 1);
     *abort_flag = 0;
@@ -261,11 +285,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == C::TMA_WARP && lane == 0) prefetch_tensormap(&tmap_wq);
   if (warp == C::GATHER_WARP0 && lane == 0) prefetch_tensormap(&tmap_x);
   if (warp == C::MMA_WARP) {
-    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  // PAIR: neither CTA touches the other's barriers before both have initialized them
+  if constexpr (PAIR) cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   grid_dependents_launch();  // the split-K finalize may be scheduled; it waits for this grid
@@ -286,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // each entry in order and releases it once its lanes hold a copy.
   auto pop = [&](uint32_t qi, UnitEntry& U) -> bool {
     const uint32_t slot = qi % kUnitQ;
-    if (!mbar_wait(bar(C::uq_full(slot)), (qi / kUnitQ) & 1u, abort_flag, status)) return false;
+    if (!mbar_wait<PAIR>(bar(C::uq_full(slot)), (qi / kUnitQ) & 1u, abort_flag, status)) return false;
     U.expert = uq[slot].expert;
     U.start = uq[slot].start;
     U.rows = uq[slot].rows;
@@ -297,9 +328,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     U.valid = uq[slot].valid;
     return true;
   };
+  // one release of entry qi (PAIR: the odd CTA's releases go to the even CTA's scheduler; the
+  // entry was read into registers before, and the slot is rewritten kUnitQ entries later)
+  auto release_one = [&](uint32_t qi) {
+    if (PAIR && !leader)
+      mbar_arrive_remote(peer_bar(C::uq_empty(qi % kUnitQ)));
+    else
+      mbar_arrive(bar(C::uq_empty(qi % kUnitQ)));
+  };
   auto release_warp = [&](uint32_t qi) {  // all 32 lanes of the warp call this
     __syncwarp();
-    if (lane == 0) mbar_arrive(bar(C::uq_empty(qi % kUnitQ)));
+    if (lane == 0) release_one(qi);
   };
 
   if (warp == C::TMA_WARP) {
@@ -312,55 +351,77 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The kernel may start while the route step that wrote the plan is still running
       // (programmatic dependent launch).  Only this thread reads the plan directly; every
       // other read of routing output (perm) follows a pop from the unit queue, so it comes
-      // after this wait.
+      // after this wait.  (PAIR: the odd CTA's scheduler warp only pops the units, in the
+      // even CTA's order, and loads its own rows' codes.)
       grid_dependency_wait();
       const int ksplit = p.header->ksplit;
       const int n_fpairs = (F + UM - 1) / UM;
       const int n_units = p.header->n_chunks * n_fpairs * ksplit;
+      // the first unit of a CTA (PAIR: of a pair) is its own index (the counter starts at the
+      // number of CTAs, or pairs), which saves the counter's round trip on the way to the first MMA
+      const int first_unit = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
       uint32_t itn = 0, qi = 0;
       bool ok = true;
       for (;;) {
         const uint32_t slot = qi % kUnitQ;
-        if (!mbar_wait(bar(C::uq_empty(slot)), ((qi / kUnitQ) & 1u) ^ 1u, abort_flag, status)) {
-          ok = false;
-          break;
-        }
-        // the first unit is the CTA's own (the counter starts at the grid size), which saves
-        // the counter's round trip on the way to the first MMA
-        const int u = qi == 0 ? (int)blockIdx.x : atomicAdd(&p.header->next_unit, 1);
         UnitEntry U;
-        U.valid = u < n_units ? 1 : 0;
-        if (U.valid) {
-          U = decode_unit(p.chunks, u, n_fpairs, ksplit, num_kb);
+        if (PAIR && !leader) {
+          if (!pop(qi, U)) {
+            ok = false;
+            break;
+          }
+          release_one(qi);
         } else {
-          U.expert = U.start = U.rows = U.f0 = U.kb0 = U.kb1 = 0;
-          U.ks = -1;
+          if (!mbar_wait<PAIR>(bar(C::uq_empty(slot)), ((qi / kUnitQ) & 1u) ^ 1u, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          const int u = qi == 0 ? first_unit : atomicAdd(&p.header->next_unit, 1);
+          U.valid = u < n_units ? 1 : 0;
+          if (U.valid) {
+            U = decode_unit(p.chunks, u, n_fpairs, ksplit, num_kb);
+          } else {
+            U.expert = U.start = U.rows = U.f0 = U.kb0 = U.kb1 = 0;
+            U.ks = -1;
+          }
+          uq[slot].expert = U.expert;
+          uq[slot].start = U.start;
+          uq[slot].rows = U.rows;
+          uq[slot].f0 = U.f0;
+          uq[slot].kb0 = U.kb0;
+          uq[slot].kb1 = U.kb1;
+          uq[slot].ks = U.ks;
+          uq[slot].valid = U.valid;
+          mbar_arrive(bar(C::uq_full(slot)));  // release: the entry is visible to the waiters
+          if constexpr (PAIR) {
+            // the same entry into the odd CTA's queue, then its full barrier (release at cluster
+            // scope orders the remote stores before the arrival)
+            const uint32_t e0 = mapa_shared(smem_u32(const_cast<UnitEntry*>(&uq[slot])), crank ^ 1u);
+            const int vals[8] = {U.expert, U.start, U.rows, U.f0, U.kb0, U.kb1, U.ks, U.valid};
+#pragma unroll
+            for (int j = 0; j < 8; ++j) st_cluster_u32(e0 + 4u * (uint32_t)j, (uint32_t)vals[j]);
+            mbar_arrive_cluster(peer_bar(C::uq_full(slot)));
+          }
         }
-        uq[slot].expert = U.expert;
-        uq[slot].start = U.start;
-        uq[slot].rows = U.rows;
-        uq[slot].f0 = U.f0;
-        uq[slot].kb0 = U.kb0;
-        uq[slot].kb1 = U.kb1;
-        uq[slot].ks = U.ks;
-        uq[slot].valid = U.valid;
-        mbar_arrive(bar(C::uq_full(slot)));  // release: the entry is visible to the waiters
         ++qi;
         if (!U.valid) break;
+        const int urows = F - U.f0 < UM ? F - U.f0 : UM;  // the unit's weight rows (a multiple of 16)
+        const int crows = min(C::ROWS, urows - rbase);    // this CTA's (none: past F)
         if constexpr (FMT::KIND == kAffine) {
           // The unit's scales and biases (its rows are contiguous, rows x H/GS bf16 each) are
           // pulled into L2 now, so the dequant threads' loads a step ahead hit L2 rather
           // than HBM when they reach this unit.  (The other formats' scales are fetched on
           // demand: their scale arrays are only 4-byte aligned, and bulk prefetches want 16.)
-          const int rows = F - U.f0 < UM ? F - U.f0 : UM;  // a multiple of 16 (F is)
-          const int64_t off = ((int64_t)U.expert * F + U.f0) * G;
-          prefetch_l2_bulk(p.scales + off, (uint32_t)(rows * G * 2));
-          prefetch_l2_bulk(p.biases + off, (uint32_t)(rows * G * 2));
+          if (crows > 0) {
+            const int64_t off = ((int64_t)U.expert * F + U.f0 + rbase) * G;
+            prefetch_l2_bulk(p.scales + off, (uint32_t)(crows * G * 2));
+            prefetch_l2_bulk(p.biases + off, (uint32_t)(crows * G * 2));
+          }
         }
         // codes of k-block kb: rows row0.. of the [E*F, row bytes] code matrix at byte
         // code_window_x(kb); transpose=False: k-rows U.expert*H + 64 kb.. of the [E*K, N/2]
         // code matrix at byte U.f0 / 2
-        const int row0 = U.expert * F + U.f0;
+        const int row0 = U.expert * F + U.f0 + rbase;
         for (int kb = U.kb0; kb < U.kb1; ++kb) {
           const uint32_t s = itn % NIB_STAGES, ph = (itn / NIB_STAGES) & 1u;
           if (!mbar_wait(bar(C::nib_empty(s)), ph ^ 1u, abort_flag, status)) {
@@ -390,16 +451,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == C::MMA_WARP) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0) {
+    // (PAIR: the even CTA's thread issues the pair's MMAs once both CTAs' A and x of a stage are
+    // written, and its commits release the stage and signal the accumulator in both CTAs; the
+    // odd CTA's thread forwards the completion of each of its own stages to the even CTA's
+    // barrier of that stage, whose phase then completes with the even CTA's own arrivals.)
+    if (lane == 0 && PAIR && !leader) {
+      uint32_t it = 0, qi = 0;
+      bool ok = true;
+      for (;;) {
+        UnitEntry U;
+        if (!pop(qi, U)) break;
+        release_one(qi);
+        ++qi;
+        if (!U.valid) break;
+        for (int kb = U.kb0; kb < U.kb1; ++kb, ++it) {
+          const uint32_t s = it % C::AB_STAGES, ph = (it / C::AB_STAGES) & 1u;
+          if (!mbar_wait(bar(C::ab_full(s)), ph, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_remote(peer_bar(C::ab_full(s)));
+        }
+        if (!ok) break;
+      }
+      // the even CTA's stage-release commits of the last stages have landed here
+      const uint32_t first = it > C::AB_STAGES ? it - C::AB_STAGES : 0;
+      for (uint32_t j = first; j < it; ++j)
+        mbar_wait_unwind(bar(C::ab_empty(j % C::AB_STAGES)), (j / C::AB_STAGES) & 1u, 100000000ull);
+    } else if (lane == 0) {
       uint32_t it = 0, lu = 0, qi = 0;
       bool ok = true;
       for (;; ++lu) {
         UnitEntry U;
         if (!pop(qi, U)) break;
-        mbar_arrive(bar(C::uq_empty(qi % kUnitQ)));  // the only lane of this role
+        release_one(qi);  // the only lane of this role
         ++qi;
         if (!U.valid) break;
         const int N = (U.rows + 15) & ~15;
+        // PAIR: M = 256 (both CTAs' weight rows) x the chunk's tokens in N tiles of up to 256
+        const int N0 = N < UM ? N : UM, N1 = N - N0;
         // SWAP: M = 128 token rows x N = 256 weight rows, the weights (B) MN-major for transpose=False
         const uint32_t idesc = C::SWAP ? umma_idesc_bf16(BM, UM) | (kAmn ? kIdescTransposeB : 0u)
                                        : umma_idesc_bf16(BM, N) | (kAmn ? kIdescTransposeA : 0u);
@@ -414,9 +504,25 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_after();
           const uint64_t bdesc = umma_desc_sw128(sbase + C::OFF_B + s * C::B_BYTES);
-          if constexpr (C::SWAP) {
+          if constexpr (PAIR) {
+            // N tile t: accumulator columns 256 t.. (column = token), x rows 128 t.. of each CTA's
+            // stage (its half of the tile's tokens)
+            const uint64_t adesc = umma_desc_kmajor_interleave(sbase + C::OFF_A + s * C::A_BYTES);
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int Nt = t == 0 ? N0 : N1;
+              if (Nt == 0) break;
+              const uint32_t idt = umma_idesc_bf16(2 * BM, Nt);
+              const uint64_t bdt = bdesc + (uint64_t)((t * BM * BK * 2) >> 4);
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k)
+                tc_mma_bf16_pair(tmem_base + (uint32_t)(t * UM), adesc + (256u >> 4) * k, bdt + 2u * k, idt,
+                                 (kb > U.kb0 || k > 0) ? 1u : 0u);
+            }
+            tc_commit_pair_mc(bar(C::ab_empty(s)), 0x3);
+          } else if constexpr (C::SWAP) {
             // A = the x tile (128-byte-swizzled K-major), B = the 256 weight rows of the stage
-            const uint32_t w_addr = sbase + C::OFF_A + s * A_BYTES;
+            const uint32_t w_addr = sbase + C::OFF_A + s * C::A_BYTES;
             const uint64_t wdesc =
                 kAmn ? umma_desc_sw128_mn(w_addr, kAmnAtomPitch, 1024u) : umma_desc_kmajor_interleave(w_addr);
             const uint32_t wstep = kAmn ? 2048u >> 4 : 256u >> 4;
@@ -428,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
               const uint32_t d_tmem = tmem_base + (uint32_t)(t * C::ACC_COLS);
-              const uint32_t a_addr = sbase + C::OFF_A + s * A_BYTES + t * A_TILE_BYTES;
+              const uint32_t a_addr = sbase + C::OFF_A + s * C::A_BYTES + t * A_TILE_BYTES;
               // K-major (unswizzled): 16 elements = two 16-byte chunks, 256 bytes on; MN-major: two
               // 8-row atoms (2048 bytes)
               const uint64_t adesc =
@@ -439,14 +545,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_mma_bf16(d_tmem, adesc + astep * k, bdesc + 2u * k, idesc, (kb > U.kb0 || k > 0) ? 1u : 0u);
             }
           }
-          tc_commit(bar(C::ab_empty(s)));
+          if constexpr (!PAIR) tc_commit(bar(C::ab_empty(s)));
           ++it;
         }
         if (!ok) break;
-        tc_commit(bar(C::tmem_full(slot)));
+        if constexpr (PAIR)
+          tc_commit_pair_mc(bar(C::tmem_full(slot)), 0x3);
+        else
+          tc_commit(bar(C::tmem_full(slot)));
       }
       // every MMA issued above completes before this barrier's phase 0 completes
-      tc_commit(bar(C::unwind()));
+      if constexpr (PAIR)
+        tc_commit_pair(bar(C::unwind()));
+      else
+        tc_commit(bar(C::unwind()));
       mbar_wait_unwind(bar(C::unwind()), 0, 100000000ull);
       // and the stage-release arrivals of the last stages have landed
       const uint32_t first = it > C::AB_STAGES ? it - C::AB_STAGES : 0;
@@ -473,12 +585,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       release_warp(qi);
       ++qi;
       if (!U.valid) break;
-      const int nops = ((U.rows + 15) & ~15) / 4;
+      // PAIR: this CTA's half of each N tile (tile 0: tokens 0 .. N0-1, tile 1: 256 .. N-1; the odd
+      // CTA takes the second half of each), tile 1's rows 128 rows into the stage
+      const int N = (U.rows + 15) & ~15;
+      const int N0 = N < UM ? N : UM;
+      const int ops0 = PAIR ? N0 / 8 : N / 4;
+      const int nops = PAIR ? ops0 + (N - N0) / 8 : ops0;
       const bool mine = g < nops;
+      const bool t1 = PAIR && g >= ops0;
+      const int tok0 = !PAIR ? 4 * g
+                       : t1 ? UM + (int)crank * ((N - N0) / 2) + 4 * (g - ops0)
+                            : (int)crank * (N0 / 2) + 4 * g;
+      const uint32_t soff = t1 ? (uint32_t)(BM * BK * 2) + (uint32_t)(g - ops0) * 512u : (uint32_t)g * 512u;
       int rr[4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int pos = 4 * g + j < U.rows ? 4 * g + j : 0;
+        const int pos = tok0 + j < U.rows ? tok0 + j : 0;
         rr[j] = mine ? (p.perm ? __ldg(p.perm + U.start + pos) : U.start + pos) : 0;
         if (p.x_div != 1) rr[j] /= p.x_div;  // a token's A rows share one x row
       }
@@ -493,8 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive_expect_tx(bar(C::ab_full(s)), (uint32_t)wops * 512u);
         __syncwarp();
         if (mine)
-          tma_gather4(sbase + C::OFF_B + s * C::B_BYTES + (uint32_t)g * 512u, &tmap_x, bar(C::ab_full(s)), kb * BK,
-                      rr[0], rr[1], rr[2], rr[3]);
+          tma_gather4(sbase + C::OFF_B + s * C::B_BYTES + soff, &tmap_x, bar(C::ab_full(s)), kb * BK, rr[0], rr[1],
+                      rr[2], rr[3]);
       }
     }
     if (!ok && lane == 0) {  // unwinding: let this warp's copies of the last stages land
@@ -563,16 +685,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-      } else
-      for (int tt = 0; tt < C::TILES_PER_EPI_WARP; ++tt) {
-        const int tile = (ew >> 2) * C::TILES_PER_EPI_WARP + tt;  // accumulator (weight-row tile)
+      } else {
+      // PAIR: one accumulator of this CTA's 128 weight rows x the unit's tokens (column = token); the
+      // two warps of a lane quarter take alternate 16-column blocks
+      constexpr int kTiles = PAIR ? 1 : C::TILES_PER_EPI_WARP;
+      const int half = ew >> 2;
+      for (int tt = 0; tt < kTiles; ++tt) {
+        const int tile = PAIR ? 0 : (ew >> 2) * C::TILES_PER_EPI_WARP + tt;  // accumulator (weight-row tile)
         const uint32_t trow = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(tile * C::ACC_COLS);
+        const int frow = U.f0 + rbase + tile * BM + quarter * 32;  // weight row of the warp's lane 0
         if (U.ks >= 0) {
           // partial sums of this K slice into its own plane: thread = weight row f, 16 tokens
           // per TMEM load; a warp's stores for one token are 32 consecutive f (128 bytes)
-          const int f = U.f0 + tile * BM + quarter * 32 + lane;
+          const int f = frow + lane;
           float* plane = p.acc + (int64_t)U.ks * p.n * F;
-          for (int c0 = 0; c0 < N; c0 += 16) {
+          for (int c0 = PAIR ? 16 * half : 0; c0 < N; c0 += PAIR ? 32 : 16) {
             uint32_t v[16];
             tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
             tc_wait_ld_regs(v);
@@ -584,10 +711,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         } else {
           const int q = lane & 3;
-          const int fcol = U.f0 + tile * BM + quarter * 32 + q * 8;
+          const int fcol = frow + q * 8;
 #pragma unroll
           for (int c0 = 0; c0 < C::NMAX; c0 += 16) {
             if (c0 >= N) break;
+            if (PAIR && ((c0 >> 4) & 1) != half) continue;
             uint32_t v[16];
             tc_ld_32x32b_x16(trow + (uint32_t)c0, v);
             tc_wait_ld_regs(v);
@@ -613,16 +741,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::tmem_empty(slot)));
+      if (lane == 0) {
+        if (PAIR && !leader)
+          mbar_arrive_remote(peer_bar(C::tmem_empty(slot)));
+        else
+          mbar_arrive(bar(C::tmem_empty(slot)));
+      }
     }
   } else {
     // ---------------------------------------------------------------- dequant
-    const int t = threadIdx.x;                   // 0 .. DEQ_GROUPS * UM - 1
-    const int r = t % UM;                        // weight row within the unit
-    const uint32_t grp = (uint32_t)(t / UM);     // handles the steps with it % DEQ_GROUPS == grp
-    const int tile = r >> 7, rr = r & (BM - 1);
+    static_assert(!PAIR || (FMT::KIND == kAffine && FMT::BITS == 4), "pairs: 4-bit affine codes");
+    const int t = threadIdx.x;                     // 0 .. DEQ_GROUPS * ROWS - 1
+    const int r = t % C::ROWS;                     // weight row within this CTA's rows of the unit
+    const uint32_t grp = (uint32_t)(t / C::ROWS);  // handles the steps with it % DEQ_GROUPS == grp
+    const int tile = PAIR ? 0 : r >> 7, rr = r & (BM - 1);
     // code tile rows are W bytes; 32-byte rows are TMA-swizzled in 32-byte mode (16-byte chunk c
     // of row r at chunk position c ^ ((r >> 2) & 1)), other widths are not swizzled
     const uint32_t nib_row = sbase + C::OFF_NIB + (uint32_t)(r * C::W);
@@ -689,11 +824,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         return;
       }
-      if (!U.valid || U.f0 + r >= F) {
+      if (!U.valid || U.f0 + rbase + r >= F) {
         sblk = bblk = make_uint4(0, 0, 0, 0);
         return;
       }
-      const int64_t row = (int64_t)(U.expert * F + U.f0) + r;  // E * F fits in int
+      const int64_t row = (int64_t)(U.expert * F + U.f0 + rbase) + r;  // E * F fits in int
       if constexpr (FMT::KIND != kAffine) {
         const uint8_t* sc8 = reinterpret_cast<const uint8_t*>(p.scales);
         if constexpr (FMT::KIND == kNvfp4) {
@@ -786,7 +921,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sa2 = splat16(nn_s), ba2 = splat16(nn_b);
         const uint32_t sb2 = GS == 32 ? splat16(nn_s2) : sa2, bb2 = GS == 32 ? splat16(nn_b2) : ba2;
         if (!__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
-        const uint32_t a_row = a_nn0 + sa * A_BYTES;
+        const uint32_t a_row = a_nn0 + sa * C::A_BYTES;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint4 v = deq8(cw[c], c < 4 ? sa2 : sb2, c < 4 ? ba2 : bb2);
@@ -808,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // wait for the A stage first and store each 8-weight piece as soon as it is computed, so
         // the row's 64 bf16 are never all live in registers at once
         if (!__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
-        const uint32_t a_row = a_row0 + sa * A_BYTES;
+        const uint32_t a_row = a_row0 + sa * C::A_BYTES;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
           const uint4 v = deq8(cw[c], c < 4 ? s2 : s2b, c < 4 ? b2 : b2b);
@@ -846,7 +981,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr bool kStored = (FMT::KIND == kAffine && FMT::BITS == 4) || FMT::KIND == kAffineNn;
       if (!kStored && !__all_sync(0xffffffffu, mbar_wait(bar(C::ab_empty(sa)), pha ^ 1u, abort_flag, status))) break;
       if (!kStored) {
-        const uint32_t a_row = a_row0 + sa * A_BYTES;
+        const uint32_t a_row = a_row0 + sa * C::A_BYTES;
 #pragma unroll
         for (int c = 0; c < 8; ++c)
           asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a_row + (uint32_t)(c * 128)), "r"(o[c].x),
@@ -880,8 +1015,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  if (warp == C::MMA_WARP) tmem_dealloc(tmem_base, kTmemCols);
+  if constexpr (PAIR) {
+    // neither CTA leaves (or frees the pair's tensor memory) while the other may still read its
+    // shared memory through the MMAs or arrive on its barriers
+    cluster_sync();
+    tc_fence_after();
+    if (warp == C::MMA_WARP) tmem_dealloc_pair(tmem_base, kTmemCols);
+  } else {
+    tc_fence_after();
+    if (warp == C::MMA_WARP) tmem_dealloc(tmem_base, kTmemCols);
+  }
 }
 
 // Split-K epilogue: y[row(p), f] = bf16(sum over slices ks of acc[ks, p, f]), added in slice
@@ -923,6 +1066,7 @@ __global__ void __launch_bounds__(256) splitk_finalize(const GemmArgs p) {
 
 struct DeviceInfo {
   int sms = 0;
+  int pairs = 0;  // CTA pairs of the pair instances resident at once (0: those are not used)
   bool configured = false;
 };
 
@@ -969,7 +1113,61 @@ cudaError_t configure_all() {
   need(set_smem<CfgSwap, FmtNn<32>>());
   need(set_smem<CfgSwap, FmtNn<64>>());
   need(set_smem<CfgSwap, FmtNn<128>>());
+  need(set_smem<CfgPair, FmtAffine<32, 4>>());
+  need(set_smem<CfgPair, FmtAffine<64, 4>>());
+  need(set_smem<CfgPair, FmtAffine<128, 4>>());
   return e;
+}
+
+// Launch attribute of the pair instances: clusters of two CTAs.
+cudaLaunchAttribute pair_cluster_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeClusterDimension;
+  a.val.clusterDim.x = 2;
+  a.val.clusterDim.y = 1;
+  a.val.clusterDim.z = 1;
+  return a;
+}
+
+// How many CTA pairs of the pair instances the device holds at once (one CTA per SM); 0 if the
+// occupancy query fails, and the single-CTA wide instances are used instead.
+int query_pairs(int sms) {
+  cudaLaunchAttribute ca[1] = {pair_cluster_attr()};
+  cudaLaunchConfig_t qc = {};
+  qc.gridDim = dim3((unsigned)(sms - sms % 2));
+  qc.blockDim = dim3(kThreads);
+  qc.dynamicSmemBytes = (size_t)CfgPair::SMEM_DYN;
+  qc.attrs = ca;
+  qc.numAttrs = 1;
+  int nc = 0;
+  if (cudaOccupancyMaxActiveClusters(&nc, gemm_tc_kernel<CfgPair, FmtAffine<64, 4>>, &qc) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  return nc < sms / 2 ? nc : sms / 2;
+}
+
+// The device's info, configuring the kernel instances on first use.
+cudaError_t device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  DeviceInfo& di = g_dev[dev];
+  if (!di.configured) {
+    e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if ((e = configure_all()) != cudaSuccess) return e;
+    di.pairs = query_pairs(di.sms);
+    di.configured = true;
+  }
+  *out = &di;
+  return cudaSuccess;
+}
+
+// Calls whose plan has chunks of up to 512 rows (4-bit affine) run on CTA pairs.
+bool uses_pairs(const DeviceInfo& di, int kind, int bits, int chunk_rows) {
+  return di.pairs > 0 && kind == kAffine && bits == 4 && chunk_rows == kChunkRowsPair;
 }
 
 using GemmKernel = decltype(&gemm_tc_kernel<CfgWide, FmtAffine<64, 4>>);
@@ -990,13 +1188,18 @@ using FmtNn32 = FmtNn<32>;
 using FmtNn64 = FmtNn<64>;
 using FmtNn128 = FmtNn<128>;
 
-GemmKernel pick_instance(const GemmArgs& a, bool narrow, bool mid, int* smem) {
+GemmKernel pick_instance(const GemmArgs& a, bool narrow, bool mid, bool pair, int* smem) {
 #define GQMM_PICK(CFG, FMT)      \
   do {                           \
     *smem = CFG::SMEM_DYN;       \
     return gemm_tc_kernel<CFG, FMT>; \
   } while (0)
   if (a.kind == kAffine && a.bits == 4) {
+    if (pair) {
+      if (a.group_size == 32) GQMM_PICK(CfgPair, FmtA4g32);
+      if (a.group_size == 128) GQMM_PICK(CfgPair, FmtA4g128);
+      GQMM_PICK(CfgPair, FmtA4g64);
+    }
     if (narrow) {
       if (a.group_size == 32) GQMM_PICK(CfgSwap, FmtA4g32);
       if (a.group_size == 128) GQMM_PICK(CfgSwap, FmtA4g128);
@@ -1059,6 +1262,25 @@ GemmKernel pick_instance(const GemmArgs& a, bool narrow, bool mid, int* smem) {
 
 }  // namespace
 
+cudaError_t gemm_tc_workers(int kind, int bits, int chunk_rows, int* workers) {
+  DeviceInfo* di = nullptr;
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  *workers = uses_pairs(*di, kind, bits, chunk_rows) ? di->pairs : di->sms;
+  return cudaSuccess;
+}
+
+cudaError_t gemm_tc_chunk_rows(int kind, int bits, int chunk_rows, int64_t n, int E, int* out) {
+  DeviceInfo* di = nullptr;
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  const int64_t busy = n < E ? n : E;  // experts that can have rows
+  const bool big = busy > 0 && n > busy * kChunkRowsWide;
+  *out = di->pairs > 0 && kind == kAffine && bits == 4 && chunk_rows == kChunkRowsWide && big ? kChunkRowsPair
+                                                                                            : chunk_rows;
+  return cudaSuccess;
+}
+
 cudaError_t device_sm_count(int* sms) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -1075,17 +1297,10 @@ cudaError_t device_sm_count(int* sms) {
 
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   *launched = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  DeviceInfo* dip = nullptr;
+  cudaError_t e = device_info(&dip);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  DeviceInfo& di = g_dev[dev];
-  if (!di.configured) {
-    e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return e;
-    if ((e = configure_all()) != cudaSuccess) return e;
-    di.configured = true;
-  }
+  const DeviceInfo& di = *dip;
 
   static decltype(&cuTensorMapEncodeTiled) encode = nullptr;
   if (!encode) {
@@ -1098,8 +1313,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   }
   const bool narrow = a.chunk_rows <= kChunkRowsNarrow;
   const bool mid = !narrow && a.chunk_rows <= kChunkRowsMid;
+  const bool pair = uses_pairs(di, a.kind, a.bits, a.chunk_rows);
   int smem = 0;
-  GemmKernel kern = pick_instance(a, narrow, mid, &smem);
+  GemmKernel kern = pick_instance(a, narrow, mid, pair, &smem);
   if (kern == nullptr) return cudaErrorInvalidValue;
   // Packed codes as an [E*F, row bytes] byte matrix; one box = the unit's 256 rows x one k-block's
   // code window (W bytes: formats.cuh), 32-byte swizzled when W is 32 so the dequant threads read
@@ -1114,7 +1330,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   CUtensorMap map_wq;
   const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)code_rows};
   const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
-  const cuuint32_t box[2] = {nn ? (cuuint32_t)(UM / 2) : (cuuint32_t)W, nn ? (cuuint32_t)BK : (cuuint32_t)UM};
+  const cuuint32_t box[2] = {nn ? (cuuint32_t)(UM / 2) : (cuuint32_t)W,
+                             nn ? (cuuint32_t)BK : (cuuint32_t)(pair ? CfgPair::ROWS : UM)};
   const cuuint32_t estr[2] = {1, 1};
   const CUtensorMapSwizzle swz = nn ? CU_TENSOR_MAP_SWIZZLE_128B
                                 : W == 32 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_NONE;
@@ -1135,15 +1352,17 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
   // Both kernels are launched with programmatic stream serialization: the GEMM's prologue
   // (barriers, TMEM, tensor maps) overlaps the route step, and the finalize's launch the
   // GEMM's tail.  Each waits (griddepcontrol.wait) before reading its predecessor's output.
-  cudaLaunchAttribute pdl[1];
+  // The pair instances are launched as clusters of two CTAs, one pair per unit worker.
+  cudaLaunchAttribute pdl[2];
   pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  pdl[1] = pair_cluster_attr();
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)di.sms);
+  cfg.gridDim = dim3((unsigned)(pair ? 2 * di.pairs : di.sms));
   cfg.blockDim = dim3(kThreads);
   cfg.stream = s;
   cfg.attrs = pdl;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pair ? 2 : 1;
   cfg.dynamicSmemBytes = (size_t)smem;
   e = cudaLaunchKernelEx(&cfg, kern, map_wq, map_x, a);
   if (e != cudaSuccess) return e;
@@ -1154,6 +1373,7 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched) {
     cfg.gridDim = dim3((unsigned)(blocks < 4 * di.sms ? blocks : 4 * di.sms));
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = 0;
+    cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, splitk_finalize, a);
     if (e != cudaSuccess) return e;
     *launched = 2;

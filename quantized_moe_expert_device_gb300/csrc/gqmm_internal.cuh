@@ -26,7 +26,7 @@ struct WsHeader {
   int32_t n_chunks;   // number of valid entries in the chunk list (written by the plan step)
   int32_t ksplit;     // K slices per (chunk, F pair) chosen by the plan step (1 = no split)
   int32_t next_unit;  // work counter of the grouped GEMM's schedulers; the plan step sets it to
-                      // the grid size (CTA b takes unit b first)
+                      // the number of unit workers (worker b, a CTA or a CTA pair, takes unit b first)
   int32_t pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
@@ -48,6 +48,7 @@ inline int route_tile(int64_t n) {
 constexpr int64_t kSmallMaxN = 4096;          // unsorted calls up to this size: one route block
 constexpr int64_t kTinyMaxN = 256;            // ... and up to this size: one entry per thread
 constexpr int kChunkRowsWide = 256;           // tokens per work unit, wide GEMM variant
+constexpr int kChunkRowsPair = 512;           // tokens per work unit, wide GEMM on CTA pairs
 constexpr int kChunkRowsMid = 128;            // tokens per work unit, mid GEMM variant
 constexpr int kMidMaxAvgRows = 64;            // ... taken up to this many rows per expert on average
 constexpr int kChunkRowsNarrow = 32;          // tokens per work unit, narrow GEMM variant
@@ -184,7 +185,7 @@ struct RouteArgs {
   int chunk_rows;       // longest chunk of the work list
   int n_fpairs;         // 256-row output tiles per expert (work units per chunk and K slice)
   int ks_cap;           // largest K split the workspace and H allow (1: never split)
-  int sms;              // streaming multiprocessors = CTAs of the grouped GEMM
+  int sms;              // unit workers of the grouped GEMM (its CTAs, or CTA pairs: gemm_tc_workers)
 };
 // Unsorted: histogram kernel + scan/scatter/plan kernel.  Sorted or dense: one plan kernel.
 cudaError_t launch_route(const RouteArgs& a, cudaStream_t s, int* kernels_launched);
@@ -223,6 +224,15 @@ struct GemmArgs {
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t s, int* launched);
 // Streaming multiprocessors of the current device (queried once per device).
 cudaError_t device_sm_count(int* sms);
+// Unit workers of the grouped GEMM instance a call of this format and chunk size runs on: the
+// CTAs (one per SM), or the CTA pairs of the 4-bit affine pair instance.  The plan step starts
+// the GEMM's unit counter (WsHeader::next_unit) at this number.
+cudaError_t gemm_tc_workers(int kind, int bits, int chunk_rows, int* workers);
+// The chunk size a gather call of n routed rows over E experts uses: kChunkRowsPair for wide 4-bit
+// affine calls with more than kChunkRowsWide rows per expert on average (whose experts would
+// otherwise be split into several chunks, each dequantizing the expert's weights again) when the
+// device runs the pair instance, else chunk_rows.
+cudaError_t gemm_tc_chunk_rows(int kind, int bits, int chunk_rows, int64_t n, int E, int* out);
 
 // The weight-streaming kernels for chunks of at most `rows` rows: the CUDA-core kernel (two blocks
 // per SM) for routed chunks of 1 or 2 rows and single-row dense calls, the MMA kernel (one block
@@ -267,15 +277,28 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                : "memory");
 }
 
+// kCluster: acquire at cluster scope, for barriers that threads of the other CTA of a pair
+// arrive on after writing data the waiter reads.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (kCluster) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
@@ -286,12 +309,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 // Bounded wait for the phase of parity `parity` of barrier `bar` to complete.  Returns
 // false if the CTA-wide abort flag is raised or the limit passes (which raises the flag and
 // records GQMM_STATUS_TIMEOUT).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           uint32_t* status) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kCluster>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kCluster>(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -445,6 +469,74 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    bar)
                : "memory");
+}
+
+// ---- CTA pairs (a cluster of two CTAs on two SMs sharing one MMA: cta_group::2) ----
+// The pair's tensor memory is allocated, used and freed with .cta_group::2 throughout: one warp
+// of each CTA allocates (collectively), the even CTA issues the MMAs, whose M = 256 rows are the
+// even CTA's 128 A rows then the odd CTA's 128, and whose N columns of B are split in halves, the
+// first half in the even CTA's shared memory; each CTA's tensor memory holds its own 128 rows of
+// the accumulator.  Both CTAs keep operands, barriers and the TMEM address at the same offsets.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The shared::cluster address of this CTA's shared-memory location `addr` in CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive on a barrier of another CTA of the cluster; this thread's earlier writes (including
+// remote ones) are released to the barrier's waiters at cluster scope.  (Costly: the release waits
+// for the thread's outstanding writes; used once per work unit.)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+// Arrive on a barrier of another CTA of the cluster with the default (CTA-scope) semantics: a
+// signal that the data it guards is complete, for data the tensor core or the tensor memory
+// holds (per-stage and per-accumulator handshakes of a CTA pair).
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t cluster_addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr), "r"(v) : "memory");
+}
+// Every thread of both CTAs: barrier.cluster (arrive with release, wait with acquire).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T over the pair (M = 256), bf16 in, f32 accumulate.
+__device__ __forceinline__ void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive once on the barrier at offset `bar` in each CTA of `cta_mask` when every tcgen05
+// operation this thread issued so far has completed.
+__device__ __forceinline__ void tc_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"(cta_mask)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // Each thread of the warp reads 16 consecutive 32-bit columns of its own TMEM lane.

@@ -36,13 +36,14 @@ __device__ __forceinline__ float glu(float g, float u) {
 
 // h[j, i] = bf16(act(h1[j, i]) * h1[j, I + i]) for the n sorted rows of the gate/up output,
 // eight columns per thread and step.  Block 0 also resets the work counter that the second
-// projection's tensor-core GEMM takes units from (this kernel starts after the first has ended).
+// projection's tensor-core GEMM takes units from to that GEMM's number of unit workers (this
+// kernel starts after the first projection has ended).
 template <int ACT>
 __global__ void __launch_bounds__(kGateThreads) glu_kernel(const __nv_bfloat16* __restrict__ h1,
                                                            __nv_bfloat16* __restrict__ h, int64_t n, int I,
-                                                           WsHeader* header, int sms) {
+                                                           WsHeader* header, int workers) {
   grid_dependents_launch();  // the second projection may start its prologue
-  if (blockIdx.x == 0 && threadIdx.x == 0) header->next_unit = sms;
+  if (blockIdx.x == 0 && threadIdx.x == 0) header->next_unit = workers;
   const int64_t per_row = I / 8;
   const int64_t total = n * per_row;
   for (int64_t v = (int64_t)blockIdx.x * kGateThreads + threadIdx.x; v < total; v += (int64_t)gridDim.x * kGateThreads) {
@@ -61,16 +62,16 @@ __global__ void __launch_bounds__(kGateThreads) glu_kernel(const __nv_bfloat16* 
 }  // namespace
 
 cudaError_t launch_glu(const __nv_bfloat16* h1, __nv_bfloat16* h, int64_t n, int I, int activation,
-                       WsHeader* header, int sms, cudaStream_t s) {
+                       WsHeader* header, int sms, int workers, cudaStream_t s) {
   const int64_t total = n * (I / 8);
   int64_t blocks = (total + kGateThreads - 1) / kGateThreads;
   if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
   if (blocks < 1) blocks = 1;
   switch (activation) {
-    case GQMM_ACT_SILU: glu_kernel<GQMM_ACT_SILU><<<(unsigned)blocks, kGateThreads, 0, s>>>(h1, h, n, I, header, sms); break;
-    case GQMM_ACT_GELU: glu_kernel<GQMM_ACT_GELU><<<(unsigned)blocks, kGateThreads, 0, s>>>(h1, h, n, I, header, sms); break;
+    case GQMM_ACT_SILU: glu_kernel<GQMM_ACT_SILU><<<(unsigned)blocks, kGateThreads, 0, s>>>(h1, h, n, I, header, workers); break;
+    case GQMM_ACT_GELU: glu_kernel<GQMM_ACT_GELU><<<(unsigned)blocks, kGateThreads, 0, s>>>(h1, h, n, I, header, workers); break;
     case GQMM_ACT_GELU_TANH:
-      glu_kernel<GQMM_ACT_GELU_TANH><<<(unsigned)blocks, kGateThreads, 0, s>>>(h1, h, n, I, header, sms);
+      glu_kernel<GQMM_ACT_GELU_TANH><<<(unsigned)blocks, kGateThreads, 0, s>>>(h1, h, n, I, header, workers);
       break;
     default: return cudaErrorInvalidValue;
   }

@@ -30,9 +30,10 @@ int moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, const void
                  size_t ws_bytes, cudaStream_t s);
 
 // Gating of the MLP's gate/up output (n sorted rows of [g | u]) by a GQMM_ACT_* activation into
-// h [n, I]; also resets header->next_unit to `sms` for the down projection's tensor-core GEMM
-// (it starts after the gate/up projection has ended).
+// h [n, I] (grid sized for `sms` SMs); also resets header->next_unit to `workers`, the unit
+// workers of the down projection's tensor-core GEMM (it starts after the gate/up projection has
+// ended).
 cudaError_t launch_glu(const __nv_bfloat16* h1, __nv_bfloat16* h, int64_t n, int I, int activation,
-                       WsHeader* header, int sms, cudaStream_t s);
+                       WsHeader* header, int sms, int workers, cudaStream_t s);
 
 }  // namespace gqmm

@@ -61,8 +61,9 @@ __device__ __forceinline__ int64_t block_exclusive_scan(int64_t v, int64_t* warp
   return warp_prefix + inc - v;
 }
 
-// K slices per (chunk, F pair) for n_units0 = chunks x F pairs work units on `sms` CTAs:
-// the split (at most ks_cap) that minimises the waves of units per CTA per unit of work,
+// K slices per (chunk, F pair) for n_units0 = chunks x F pairs work units on `sms` unit workers
+// (CTAs or CTA pairs): the split (at most ks_cap) that minimises the waves of units per worker per
+// unit of work,
 // ceil(n_units0 * ks / sms) / ks, taken only when it saves at least a tenth.
 __device__ __forceinline__ int choose_ksplit(int64_t n_units0, int ks_cap, int sms) {
   if (n_units0 <= 0 || ks_cap <= 1 || sms <= 0) return 1;
@@ -89,7 +90,11 @@ template <int NT>
 __device__ void write_plan(const int32_t* seg_start, const int32_t* seg_len, int E, int max_rows, Chunk* chunks,
                            WsHeader* header, int64_t* warp_tot, int n_fpairs, int ks_cap, int sms) {
   static_assert(NT >= kChunkRowsWide, "one thread per size bucket");
-  __shared__ int32_t bucket[kChunkRowsWide];  // chunks with max_rows - b rows, then cursors
+  // chunks with max_rows - b rows (with max_rows - 2b or - 2b - 1 rows for the CTA pairs' chunks of
+  // up to 512 rows), then cursors
+  __shared__ int32_t bucket[kChunkRowsWide];
+  const int sh = max_rows > kChunkRowsWide ? 1 : 0;
+  const int nb = ((max_rows - 1) >> sh) + 1;
   for (int b = threadIdx.x; b < kChunkRowsWide; b += NT) bucket[b] = 0;
   __syncthreads();
   const int per = (E + NT - 1) / NT;
@@ -100,13 +105,13 @@ __device__ void write_plan(const int32_t* seg_start, const int32_t* seg_len, int
     const int nch = (len + max_rows - 1) / max_rows;
     if (nch == 0) continue;
     const int base = len / nch, rem = len % nch;  // rem chunks of base + 1 rows, the rest base
-    if (rem) atomicAdd(&bucket[max_rows - (base + 1)], rem);
-    if (nch > rem) atomicAdd(&bucket[max_rows - base], nch - rem);
+    if (rem) atomicAdd(&bucket[(max_rows - (base + 1)) >> sh], rem);
+    if (nch > rem) atomicAdd(&bucket[(max_rows - base) >> sh], nch - rem);
   }
   __syncthreads();
   int64_t total;
-  const int64_t at = block_exclusive_scan<NT>(threadIdx.x < max_rows ? bucket[threadIdx.x] : 0, warp_tot, &total);
-  if (threadIdx.x < max_rows) bucket[threadIdx.x] = (int32_t)at;
+  const int64_t at = block_exclusive_scan<NT>(threadIdx.x < nb ? bucket[threadIdx.x] : 0, warp_tot, &total);
+  if (threadIdx.x < nb) bucket[threadIdx.x] = (int32_t)at;
   __syncthreads();
   for (int e = e0; e < e1; ++e) {
     const int len = seg_len[e];
@@ -119,13 +124,13 @@ __device__ void write_plan(const int32_t* seg_start, const int32_t* seg_len, int
       c.start = seg_start[e] + k * base + min(k, rem);
       c.rows = base + (k < rem ? 1 : 0);
       c.pad = 0;
-      chunks[atomicAdd(&bucket[max_rows - c.rows], 1)] = c;
+      chunks[atomicAdd(&bucket[(max_rows - c.rows) >> sh], 1)] = c;
     }
   }
   if (threadIdx.x == 0) {
     header->n_chunks = (int32_t)total;
     header->ksplit = choose_ksplit(total * (int64_t)n_fpairs, ks_cap, sms);
-    header->next_unit = sms;  // units below the grid size go to the CTA of that index first
+    header->next_unit = sms;  // units below the worker count go to the worker of that index first
   }
 }
 
