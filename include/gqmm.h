@@ -400,7 +400,8 @@ GQMM_API void gqmm_test_stall_next(int n);
 #define GQMM_VARIANT_ROUTE_UNSORTED 0 /* histogram + scatter route sort */
 #define GQMM_VARIANT_ROUTE_SORTED 1   /* segment boundaries from caller-sorted idx */
 #define GQMM_VARIANT_ROUTE_DENSE 2    /* idx == NULL, E == 1 */
-#define GQMM_VARIANT_GEMM_TC 3        /* tcgen05 grouped GEMM, chunks of up to 256 rows (128: mid variant) */
+#define GQMM_VARIANT_GEMM_TC 3        /* tcgen05 grouped GEMM, chunks of up to 256 rows (mid variant: 128;
+                                         CTA pairs, above 256 rows per expert: 512) */
 #define GQMM_VARIANT_GEMM_NARROW 4    /* tcgen05 grouped GEMM, chunks of up to 32 rows */
 #define GQMM_VARIANT_SPLIT_K 5        /* K split into slices, fp32 partial sums + finalize */
 #define GQMM_VARIANT_GEMV 6           /* weight-streaming CUDA-core kernel: routed chunks of 1-2 rows, dense 1 row */
