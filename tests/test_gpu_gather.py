@@ -95,6 +95,36 @@ def test_mid_variant_uneven_experts(gs):
     assert torch.equal(y_s, y_u)
 
 
+@pytest.mark.parametrize("H", [1024, 384])
+@pytest.mark.parametrize("gs", [32, 64, 128])
+def test_pair_variant_uneven_experts(gs, H):
+    """More than 256 routed rows per expert on average run on CTA pairs (chunks of up to 512 tokens,
+    each CTA of the pair dequantizing 128 of the unit's 256 weight rows).  Experts of 600, 300 and 10
+    rows (one chunk splits at 512), F = 384 (the second unit has 128 weight rows, so the odd CTA of
+    its pair has none), every group size, H/gs a multiple of 8 (one 16-byte scale load covers eight
+    groups) and not (H = 384), against the oracle; caller-sorted indices give the same bits as the
+    unsorted call."""
+    import quantized_moe_expert_device_gb300 as g
+
+    E, F = 3, 384
+    sizes = [600, 300, 10]  # 910 rows: 303 per expert on average
+    w = wl.normal_bf16((E, F, H), wl.SEED_W, chunk_rows=1)
+    host_w = oracle.quantize(w, group_size=gs)
+    dev_w = g.gqmm_quantize(w.cuda(), group_size=gs)
+    idx = np.random.default_rng(gs + H).permutation(np.repeat(np.arange(E, dtype=np.uint32), sizes)).reshape(-1, 1)
+    n = idx.shape[0]
+    x = wl.normal_bf16((n, 1, H), wl.SEED_X)
+    ws = g.new_workspace(n, F, E)
+    y = g.gqmm_gather_qmm(x.cuda(), *dev_w, to_dev_idx(idx), group_size=gs, ws=ws)
+    assert g.gqmm_device_status(ws) == 0
+    assert_parity(y.reshape(n, F), oracle.gather_qmm(x, *host_w, idx, E, group_size=gs), f"pair gs={gs} H={H}")
+    idx_s = np.sort(idx.reshape(-1)).reshape(-1, 1)
+    y_s = g.gqmm_gather_qmm(x.cuda(), *dev_w, to_dev_idx(idx_s), group_size=gs, sorted_indices=True)
+    y_u = g.gqmm_gather_qmm(x.cuda(), *dev_w, to_dev_idx(idx_s), group_size=gs, sorted_indices=False)
+    torch.cuda.synchronize()
+    assert torch.equal(y_s, y_u)
+
+
 def test_unaligned_78_row_batch_sorted_and_unsorted():
     E, F, H = 4, 128, 1024
     host_w, dev_w = _weights(E, F, H)
