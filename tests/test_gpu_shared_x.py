@@ -25,7 +25,8 @@ def _weights(shape, gs, seed, std=1.0):
                                           (16, 4, 512, 256, 8, 64),      # narrow
                                           (4, 8, 2048, 768, 64, 64),     # weight streaming (chunks of 2 rows)
                                           (4, 2, 2048, 768, 16, 32),     # narrow with split K
-                                          (130, 2, 512, 256, 4, 128)])   # wide, ragged
+                                          (130, 2, 512, 256, 4, 128),    # wide, ragged
+                                          (160, 8, 1024, 384, 4, 64)])   # CTA pairs (320 rows per expert)
 def test_shared_x_equals_repeated_x(T, A, H, F, E, gs):
     import quantized_moe_expert_device_gb300 as g
 
