@@ -229,3 +229,52 @@ def test_fp_mode_validation_rejects_bad_arguments_without_a_gpu(lib):
     assert q(fake, 8, 100, 8, 1, fake, fake, None, None) == 2   # H a multiple of 64
     assert q(fake, 8, 256, 3, 2, fake, fake, fake, None) == 2   # nvfp4: rows a multiple of rows_per_tensor
     assert q(fake, 8, 256, 8, 2, fake, fake, None, None) == 1   # nvfp4 needs tscale
+
+
+def declared_prototypes():
+    """name -> (return type, [parameter types]) for every GQMM_API function of gqmm.h, types with
+    qualifiers and parameter names stripped (e.g. "void*", "int64_t", "gqmm_stream_t")."""
+    text = open(os.path.join(ROOT, "include", "gqmm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    protos = {}
+    for ret, name, params in re.findall(r"GQMM_API\s+([\w \*]+?)\s*\b(gqmm_\w+)\s*\(([^)]*)\)\s*;", text):
+        types = []
+        for prm in [q.strip() for q in params.split(",") if q.strip() and q.strip() != "void"]:
+            prm = re.sub(r"\bconst\b", "", prm)
+            stars = prm.count("*")
+            words = prm.replace("*", " ").split()
+            base = words[0] if stars or len(words) == 1 else " ".join(words[:-1])
+            types.append(base + "*" * stars)
+        protos[name] = (re.sub(r"\bconst\b", "", ret).replace(" ", ""), types)
+    return protos
+
+
+def _ctype_of(c_type):
+    P, I, I64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    table = {"int": I, "int64_t": I64, "size_t": SZ, "gqmm_stream_t": P, "void": None, "char*": ctypes.c_char_p,
+             "int64_t*": ctypes.POINTER(I64), "double*": ctypes.POINTER(ctypes.c_double)}
+    if c_type in table:
+        return table[c_type]
+    assert c_type.endswith("*"), f"unmapped C type {c_type}"
+    return P  # data pointers (void*, uint32_t*, int32_t*, float*) travel as void*
+
+
+def test_binding_signatures_match_the_header():
+    """Every function the binding declares to ctypes has the header's parameter count and types
+    (an int where the C side takes int64_t, or a missing stream argument, would be undefined
+    behaviour at the call), and the header's return type."""
+    import quantized_moe_expert_device_gb300 as g
+
+    protos = declared_prototypes()
+    assert set(declared_functions()) == set(protos), "every declaration parsed"
+    lib = g.load_library()
+    checked = 0
+    for name, (ret, params) in protos.items():
+        fn = getattr(lib, name)
+        if fn.argtypes is None:  # not marshalled by the binding (called directly through ctypes)
+            continue
+        want = [_ctype_of(t) for t in params]
+        assert list(fn.argtypes) == want, f"{name}: binding {fn.argtypes} vs header {params}"
+        assert fn.restype == _ctype_of(ret), f"{name}: binding returns {fn.restype}, header {ret}"
+        checked += 1
+    assert checked >= 19
