@@ -41,12 +41,11 @@ int ok() {
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 bool log_dispatch() {
-  static int v = -1;
-  if (v < 0) {
+  static const bool on = [] {
     const char* e = std::getenv("GQMM_LOG_DISPATCH");
-    v = (e && e[0] && e[0] != '0') ? 1 : 0;
-  }
-  return v == 1;
+    return e && e[0] && e[0] != '0';
+  }();
+  return on;
 }
 
 void count_variant(int v) {
@@ -54,19 +53,18 @@ void count_variant(int v) {
 }
 
 // Device check: the library is built for sm_103a only.
-int check_device(int* sms) {
+int check_device() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail(GQMM_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
-  static int cached_ok[64] = {0};
-  if (dev >= 0 && dev < 64 && cached_ok[dev] == 1) return GQMM_OK;
+  static std::atomic<int> cached_ok[64];  // zero-initialized; set once a device has passed the check
+  if (dev >= 0 && dev < 64 && cached_ok[dev].load(std::memory_order_relaxed) == 1) return GQMM_OK;
   int major = 0, minor = 0;
   cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
   cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
   if (!(major == 10 && minor == 3))
     return fail(GQMM_ERR_DEVICE, "device %d is sm_%d%d; libgqmm is built for sm_103a only", dev, major, minor);
-  if (sms) cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
-  if (dev >= 0 && dev < 64) cached_ok[dev] = 1;
+  if (dev >= 0 && dev < 64) cached_ok[dev].store(1, std::memory_order_relaxed);
   return GQMM_OK;
 }
 
@@ -252,12 +250,12 @@ int gqmm::gather_qmm_impl(const void* x, const void* wq, const void* scales, con
   const WsLayout L = ws_layout(n, F, E, allow_split);
   UnitShape shape = unit_shape(n, H, F, E);
   if (!allow_split) shape.ksplit = 1;
-  const bool affine4 = kind == 0 && bits == 4;
+  const bool affine4 = kind == kAffine && bits == 4;
   // the weight-streaming kernels take 4-bit affine codes in 64-wide groups
   if (group_size != 64 || !affine4) shape.stream = false;
   if (!aligned(ws, 256) || ws_bytes < L.total)
     return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
-  rc = check_device(nullptr);
+  rc = check_device();
   if (rc) return rc;
   // wide 4-bit affine calls of more than 256 rows per expert run on CTA pairs, in chunks of up to
   // 512 rows, when the device holds any
@@ -375,7 +373,7 @@ int gqmm::moe_mlp_impl(const void* x, const void* wq_gu, const void* sc_gu, cons
   const WsLayout& L = M.route;
   if (!aligned(ws, 256) || ws_bytes < M.total)
     return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", M.total, ws_bytes);
-  rc = check_device(nullptr);
+  rc = check_device();
   if (rc) return rc;
   UnitShape shape1 = unit_shape(n, H, 2 * I, E);
   UnitShape shape2 = unit_shape(n, I, H, E);
@@ -477,7 +475,7 @@ int gqmm_quantize(const void* w, int64_t rows, int64_t H, int group_size, int bi
     return fail(GQMM_ERR_SHAPE, "need rows >= 0 and H a positive multiple of group_size");
   if (!aligned(w, 16) || !aligned(wq, 16)) return fail(GQMM_ERR_ALIGN, "w and wq must be 16-byte aligned");
   if (!aligned(scales, 2) || !aligned(biases, 2)) return fail(GQMM_ERR_ALIGN, "scales and biases must be 2-byte aligned");
-  int rc = check_device(nullptr);
+  int rc = check_device();
   if (rc) return rc;
   cudaError_t e = launch_quantize(static_cast<const __nv_bfloat16*>(w), rows, H, group_size, bits, static_cast<uint8_t*>(wq),
                                   static_cast<__nv_bfloat16*>(scales), static_cast<__nv_bfloat16*>(biases),
@@ -501,7 +499,7 @@ int gqmm_route_sort(const uint32_t* idx, int64_t n, int E, int32_t* perm, int32_
   const WsLayout L = ws_layout(n, 1, E);
   if (!aligned(ws, 256) || ws_bytes < L.total)
     return fail(GQMM_ERR_WORKSPACE, "workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total, ws_bytes);
-  int rc = check_device(nullptr);
+  int rc = check_device();
   if (rc) return rc;
   uint8_t* w = static_cast<uint8_t*>(ws);
   RouteArgs a;
@@ -550,7 +548,7 @@ int gqmm_quantize_fp(const void* w, int64_t rows, int64_t H, int64_t rows_per_te
   }
   if (!aligned(w, 16) || !aligned(wq, 16) || (tscale && !aligned(tscale, 4)))
     return fail(GQMM_ERR_ALIGN, "w and wq must be 16-byte aligned, tscale 4-byte aligned");
-  int rc = check_device(nullptr);
+  int rc = check_device();
   if (rc) return rc;
   cudaError_t e = launch_quantize_fp(static_cast<const __nv_bfloat16*>(w), rows, H, rows_per_tensor, mode,
                                      static_cast<uint8_t*>(wq), static_cast<uint8_t*>(scales), tscale,
@@ -610,7 +608,7 @@ int gqmm_gather_qmm_nn_simt(const void* x, const void* wq, const void* scales, c
   if (!aligned(x, 2) || !aligned(wq, 16) || !aligned(scales, 2) || !aligned(biases, 2) || !aligned(y, 16))
     return fail(GQMM_ERR_ALIGN, "wq and y must be 16-byte aligned, x, scales and biases 2-byte aligned");
   if (idx && !aligned(idx, 4)) return fail(GQMM_ERR_ALIGN, "idx must be 4-byte aligned");
-  rc = check_device(nullptr);
+  rc = check_device();
   if (rc) return rc;
   size_t slot = 0;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -633,7 +631,7 @@ int gqmm_gather_qmm_simt(const void* x, const void* wq, const void* scales, cons
   if (rc) return rc;
   rc = validate_shared(x_shared, idx);
   if (rc) return rc;
-  rc = check_device(nullptr);
+  rc = check_device();
   if (rc) return rc;
   cudaError_t e = launch_gemm_simt(static_cast<const __nv_bfloat16*>(x), static_cast<const uint8_t*>(wq),
                                    static_cast<const __nv_bfloat16*>(scales), static_cast<const __nv_bfloat16*>(biases),
